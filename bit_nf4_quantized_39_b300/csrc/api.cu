@@ -1,0 +1,517 @@
+// api.cu -- the C ABI of libqlora_nf4 (see include/qlora_nf4.h): argument
+// checks, workspace carving, launch configuration and the LoftQ host loop.
+// The whole library is one translation unit: the kernel headers are included
+// here.
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+#include "nf4_codec.cuh"
+#include "qlora_simt.cuh"
+#include "qlora_tc.cuh"
+#include "loftq.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+qn_status fail(qn_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+qn_status fail(qn_status st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+qn_status cuda_check(cudaError_t e, const char *what) {
+  if (e == cudaSuccess) return QN_OK;
+  return fail(QN_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define QN_TRY(expr)                 \
+  do {                               \
+    const qn_status st_ = (expr);    \
+    if (st_ != QN_OK) return st_;    \
+  } while (0)
+
+// With QN_DEBUG_SYNC=1 in the environment every launch is followed by a
+// device synchronisation, so that an asynchronous fault is reported with the
+// name of the kernel that raised it.
+bool debug_sync() {
+  static const bool on = [] {
+    const char *e = std::getenv("QN_DEBUG_SYNC");
+    return e && e[0] == '1';
+  }();
+  return on;
+}
+
+qn_status launch_check(const char *what) {
+  QN_TRY(cuda_check(cudaGetLastError(), what));
+  if (debug_sync()) QN_TRY(cuda_check(cudaDeviceSynchronize(), what));
+  return QN_OK;
+}
+
+#define QN_LAUNCH_CHECK(what) QN_TRY(launch_check(what))
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int sm_count() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static int cached[64] = {0};
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+  int n = 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+// Checks the threshold table against the level table: t_i must be the largest
+// fp32 not above the exact midpoint of levels i and i+1.
+bool tables_consistent() {
+  for (int i = 0; i < 15; ++i) {
+    const double mid = (static_cast<double>(kNF4Levels[i]) + static_cast<double>(kNF4Levels[i + 1])) * 0.5;
+    const float t = kNF4Thresholds[i];
+    if (static_cast<double>(t) > mid) return false;
+    const float up = std::nextafter(t, INFINITY);
+    if (static_cast<double>(up) <= mid) return false;
+  }
+  return true;
+}
+
+struct Span {  // bump allocator over the caller's workspace
+  char *base;
+  size_t size, used;
+  template <typename T> T *take(size_t count) {
+    const size_t off = (used + 255) & ~static_cast<size_t>(255);
+    used = off + count * sizeof(T);
+    return reinterpret_cast<T *>(base + off);
+  }
+};
+
+size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+qn_status check_nf4(const qn_nf4 *Q, bool need_dq_ptrs) {
+  if (!Q) return fail(QN_EINVAL, "Q is NULL");
+  if (Q->block != 64) return fail(QN_EUNSUPPORTED, "block must be 64 (got %d)", Q->block);
+  if (Q->dq && Q->dq_block != 256) return fail(QN_EUNSUPPORTED, "dq_block must be 256 (got %d)", Q->dq_block);
+  if (Q->d <= 0 || Q->k <= 0) return fail(QN_ESHAPE, "d and k must be positive");
+  if (Q->d > (int64_t(1) << 40) / Q->k) return fail(QN_ESHAPE, "d*k too large");
+  if (!Q->codes || !Q->absmax) return fail(QN_EINVAL, "codes/absmax NULL");
+  if (!aligned(Q->codes, 16) || !aligned(Q->absmax, 16)) return fail(QN_EALIGN, "codes/absmax not 16-byte aligned");
+  if (Q->dq && need_dq_ptrs) {
+    if (!Q->absmax_q || !Q->absmax_scale || !Q->absmax_mean) return fail(QN_EINVAL, "dq pointers NULL");
+    if (!aligned(Q->absmax_scale, 4) || !aligned(Q->absmax_mean, 4)) return fail(QN_EALIGN, "dq scale/mean misaligned");
+  }
+  return QN_OK;
+}
+
+QnNF4View view_of(const qn_nf4 *Q) {
+  QnNF4View v;
+  v.codes = Q->codes;
+  v.absmax = Q->absmax;
+  v.absmax_q = Q->absmax_q;
+  v.absmax_scale = Q->absmax_scale;
+  v.absmax_mean = Q->absmax_mean;
+  v.d = Q->d;
+  v.k = Q->k;
+  v.dq = Q->dq ? 1 : 0;
+  return v;
+}
+
+constexpr size_t kQuantWs = qn::kNumBins * sizeof(unsigned long long);
+
+// Quantise n elements (internal; arguments already checked).
+qn_status launch_quantize(const void *W, qn_dtype wdt, const qn_nf4 *Q, unsigned long long *bins,
+                          cudaStream_t st) {
+  const int64_t n = Q->d * Q->k;
+  const int64_t nfull = n / 64;
+  const int64_t nblk = qn_ceil_div(n, 64);
+  unsigned long long *b = Q->dq ? bins : nullptr;
+  if (b) QN_TRY(cuda_check(cudaMemsetAsync(b, 0, kQuantWs, st), "memset bins"));
+  const int sms = sm_count();
+  if (nfull > 0) {
+    const int64_t bpc = (qn::kQuantThreads / 32) * (wdt == QN_F32 ? 2 : 4);  // blocks per CTA-iteration
+    int64_t grid = qn_ceil_div(nfull, bpc);
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    if (grid > cap) grid = cap;
+    if (wdt == QN_F32)
+      qn::nf4_quant_kernel<float><<<static_cast<unsigned>(grid), qn::kQuantThreads, 0, st>>>(
+          static_cast<const float *>(W), nfull, Q->codes, Q->absmax, b);
+    else
+      qn::nf4_quant_kernel<__nv_bfloat16><<<static_cast<unsigned>(grid), qn::kQuantThreads, 0, st>>>(
+          static_cast<const __nv_bfloat16 *>(W), nfull, Q->codes, Q->absmax, b);
+    QN_LAUNCH_CHECK("nf4_quant_kernel");
+  }
+  if (nblk > nfull) {
+    if (wdt == QN_F32)
+      qn::nf4_quant_tail_kernel<float><<<1, 32, 0, st>>>(static_cast<const float *>(W), n, nfull, Q->codes,
+                                                         Q->absmax, b);
+    else
+      qn::nf4_quant_tail_kernel<__nv_bfloat16><<<1, 32, 0, st>>>(static_cast<const __nv_bfloat16 *>(W), n, nfull,
+                                                                 Q->codes, Q->absmax, b);
+    QN_LAUNCH_CHECK("nf4_quant_tail_kernel");
+  }
+  if (Q->dq) {
+    const int64_t ngrp = qn_ceil_div(nblk, 256);
+    int64_t grid = qn_ceil_div(ngrp, qn::kDqWarps);
+    const int64_t cap = static_cast<int64_t>(sms) * 4;
+    if (grid > cap) grid = cap;
+    qn::nf4_dq_kernel<<<static_cast<unsigned>(grid), qn::kDqWarps * 32, 0, st>>>(
+        Q->absmax, nblk, b, Q->absmax_q, Q->absmax_scale, Q->absmax_mean);
+    QN_LAUNCH_CHECK("nf4_dq_kernel");
+  }
+  return QN_OK;
+}
+
+qn_status launch_dequantize(const qn_nf4 *Q, void *out, qn_dtype odt, cudaStream_t st) {
+  const int64_t n = Q->d * Q->k;
+  const int64_t nchunk = n / 32;
+  int64_t grid = qn_ceil_div(nchunk > 0 ? nchunk : 1, 256);
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
+  if (grid > cap) grid = cap;
+  if (odt == QN_BF16)
+    qn::nf4_dequant_kernel<true><<<static_cast<unsigned>(grid), 256, 0, st>>>(view_of(Q), n, out);
+  else
+    qn::nf4_dequant_kernel<false><<<static_cast<unsigned>(grid), 256, 0, st>>>(view_of(Q), n, out);
+  QN_LAUNCH_CHECK("nf4_dequant_kernel");
+  return QN_OK;
+}
+
+// ----------------------------------------------------------------- the layer
+struct GemvPlan {
+  int splits;
+  int64_t chunks_per_split;
+  int64_t row_groups;
+};
+
+GemvPlan gemv_plan(int64_t d, int64_t k) {
+  GemvPlan p;
+  p.row_groups = qn_ceil_div(d, qn::kGemvWarps);
+  const int64_t chunks = k / 32;
+  const int64_t want = 4 * static_cast<int64_t>(sm_count());
+  int64_t splits = qn_ceil_div(want, p.row_groups);
+  const int64_t max_splits = chunks / 32 > 0 ? chunks / 32 : 1;  // >= 32 chunks (one per lane) per split
+  if (splits > max_splits) splits = max_splits;
+  if (splits > 16) splits = 16;
+  if (splits < 1) splits = 1;
+  p.chunks_per_split = qn_ceil_div(chunks, splits);
+  p.splits = static_cast<int>(qn_ceil_div(chunks, p.chunks_per_split));
+  return p;
+}
+
+size_t fwd_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
+  size_t b = round256(static_cast<size_t>(M) * r * sizeof(float));  // u
+  if (M <= qn::kGemvMaxM) {
+    const GemvPlan p = gemv_plan(d, k);
+    if (p.splits > 1) {
+      b += round256(static_cast<size_t>(p.splits) * M * d * sizeof(float));
+      b += round256(static_cast<size_t>(p.row_groups) * sizeof(unsigned int));
+    }
+  }
+  b += qn::tc_ws_bytes(M, d, k, r);
+  return b;
+}
+
+size_t bwd_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
+  return round256(static_cast<size_t>(M) * r * sizeof(float)) + qn::tc_ws_bytes(M, k, d, r);
+}
+
+qn_status check_layer(const qn_nf4 *Q, const void *in, int64_t M, const void *A, const void *B, int32_t r,
+                      float alpha, const void *out) {
+  QN_TRY(check_nf4(Q, true));
+  if (Q->k % 64) return fail(QN_ESHAPE, "k must be a multiple of 64 (got %lld)", (long long)Q->k);
+  if (M < 1) return fail(QN_ESHAPE, "M must be >= 1");
+  if (r < 1 || r > 256) return fail(QN_ESHAPE, "r must be in [1, 256] (got %d)", r);
+  if (!std::isfinite(alpha)) return fail(QN_EINVAL, "alpha must be finite");
+  if (!in || !A || !B || !out) return fail(QN_EINVAL, "NULL tensor pointer");
+  if (!aligned(in, 16) || !aligned(A, 16) || !aligned(B, 16) || !aligned(out, 16))
+    return fail(QN_EALIGN, "tensor pointers must be 16-byte aligned");
+  return QN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qn_abi_version(void) { return QN_ABI_VERSION; }
+
+const char *qn_last_error(void) { return g_last_error.c_str(); }
+
+void qn_nf4_tables(float codebook[16], float thresholds[15]) {
+  if (codebook) std::memcpy(codebook, kNF4Levels, sizeof(kNF4Levels));
+  if (thresholds) std::memcpy(thresholds, kNF4Thresholds, sizeof(kNF4Thresholds));
+}
+
+size_t qn_workspace_bytes(qn_op op, int64_t M, int64_t d, int64_t k, int32_t r) {
+  switch (op) {
+    case QN_OP_QUANTIZE: return kQuantWs;
+    case QN_OP_DEQUANTIZE: return 0;
+    case QN_OP_LINEAR_FWD: return (M < 1 || d < 1 || k < 1 || r < 1) ? 0 : fwd_ws_bytes(M, d, k, r);
+    case QN_OP_LINEAR_BWD_DX: return (M < 1 || d < 1 || k < 1 || r < 1) ? 0 : bwd_ws_bytes(M, d, k, r);
+    case QN_OP_LOFTQ: {
+      if (d < 1 || k < 1) return 0;
+      const size_t P = qn::kLqMaxP;
+      size_t b = round256(static_cast<size_t>(d) * k * sizeof(float));       // target / residual
+      b += round256(static_cast<size_t>(d) * P * sizeof(float));            // Y
+      b += 2 * round256(static_cast<size_t>(k) * P * sizeof(float));        // Zt, Omega
+      b += round256(P * P * sizeof(double)) + round256(P * P * sizeof(float)) + round256(P * sizeof(float));  // G, V, lam
+      b += round256(P * P * sizeof(float));                                  // Linv
+      b += round256(1024 * sizeof(double)) + round256(sizeof(double));       // partials, norm
+      b += round256(kQuantWs);
+      return b;
+    }
+  }
+  return 0;
+}
+
+qn_status nf4_quantize(const void *W, qn_dtype wdt, const qn_nf4 *Q, void *ws, size_t ws_bytes, void *stream) {
+  g_last_error.clear();
+  if (!tables_consistent()) return fail(QN_EUNSUPPORTED, "internal NF4 tables inconsistent");
+  QN_TRY(check_nf4(Q, true));
+  if (!W) return fail(QN_EINVAL, "W is NULL");
+  if (wdt != QN_F32 && wdt != QN_BF16) return fail(QN_EINVAL, "bad input dtype %d", (int)wdt);
+  if (!aligned(W, 16)) return fail(QN_EALIGN, "W not 16-byte aligned");
+  if (Q->dq) {
+    if (!ws) return fail(QN_EINVAL, "workspace NULL");
+    if (ws_bytes < kQuantWs) return fail(QN_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, kQuantWs);
+    if (!aligned(ws, 16)) return fail(QN_EALIGN, "workspace not 16-byte aligned");
+  }
+  return launch_quantize(W, wdt, Q, static_cast<unsigned long long *>(ws), static_cast<cudaStream_t>(stream));
+}
+
+qn_status nf4_dequantize(const qn_nf4 *Q, void *Wout, qn_dtype odt, void *stream) {
+  g_last_error.clear();
+  QN_TRY(check_nf4(Q, true));
+  if (!Wout) return fail(QN_EINVAL, "Wout is NULL");
+  if (odt != QN_F32 && odt != QN_BF16) return fail(QN_EINVAL, "bad output dtype %d", (int)odt);
+  if (!aligned(Wout, 16)) return fail(QN_EALIGN, "Wout not 16-byte aligned");
+  return launch_dequantize(Q, Wout, odt, static_cast<cudaStream_t>(stream));
+}
+
+qn_status qlora_linear_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M, const uint16_t *A, const uint16_t *B,
+                           int32_t r, float alpha, uint16_t *Y, void *ws, size_t ws_bytes, void *stream) {
+  g_last_error.clear();
+  QN_TRY(check_layer(Q, X, M, A, B, r, alpha, Y));
+  const int64_t d = Q->d, k = Q->k;
+  const size_t need = fwd_ws_bytes(M, d, k, r);
+  if (!ws) return fail(QN_EINVAL, "workspace NULL");
+  if (ws_bytes < need) return fail(QN_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (!aligned(ws, 256)) return fail(QN_EALIGN, "workspace not 256-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Span sp{static_cast<char *>(ws), ws_bytes, 0};
+  const float s = alpha / static_cast<float>(r);
+  float *u = sp.take<float>(static_cast<size_t>(M) * r);
+  if (M <= qn::kGemvMaxM) {
+    {
+      dim3 grid(static_cast<unsigned>(qn_ceil_div(M, qn::kProjTM)), static_cast<unsigned>(qn_ceil_div(r, qn::kProjTN)));
+      qn::lora_proj_kernel<<<grid, 256, 0, st>>>(X, M, k, A, r, k, 1, s, u);
+      QN_LAUNCH_CHECK("lora_proj_kernel");
+    }
+    const GemvPlan p = gemv_plan(d, k);
+    float *part = nullptr;
+    unsigned int *counters = nullptr;
+    if (p.splits > 1) {
+      part = sp.take<float>(static_cast<size_t>(p.splits) * M * d);
+      counters = sp.take<unsigned int>(p.row_groups);
+      QN_TRY(cuda_check(cudaMemsetAsync(counters, 0, p.row_groups * sizeof(unsigned int), st), "memset counters"));
+    }
+    dim3 grid(static_cast<unsigned>(p.row_groups), static_cast<unsigned>(p.splits));
+    const QnNF4View v = view_of(Q);
+    const int Mi = static_cast<int>(M);
+#define QN_GEMV(MT) qn::qlora_fwd_gemv_kernel<MT><<<grid, qn::kGemvThreads, 0, st>>>(v, X, Mi, u, B, r, Y, part, counters, p.splits, p.chunks_per_split)
+    if (M == 1) QN_GEMV(1);
+    else if (M <= 2) QN_GEMV(2);
+    else if (M <= 4) QN_GEMV(4);
+    else if (M <= 8) QN_GEMV(8);
+    else QN_GEMV(16);
+#undef QN_GEMV
+    QN_LAUNCH_CHECK("qlora_fwd_gemv_kernel");
+    return QN_OK;
+  }
+  {
+    dim3 grid(static_cast<unsigned>(qn_ceil_div(M, qn::kProjTM)), static_cast<unsigned>(qn_ceil_div(r, qn::kProjTN)));
+    qn::lora_proj_kernel<<<grid, 256, 0, st>>>(X, M, k, A, r, k, 1, s, u);
+    QN_LAUNCH_CHECK("lora_proj_kernel");
+  }
+  if (qn::tc_supported(M, d, k, r)) {
+    return qn::launch_tc_fwd(view_of(Q), X, M, u, B, r, Y, sp, st) == 0 ? QN_OK
+                                                                        : fail(QN_ECUDA, "tcgen05 forward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  }
+  dim3 grid(static_cast<unsigned>(qn_ceil_div(d, qn::kTileN)), static_cast<unsigned>(qn_ceil_div(M, qn::kTileM)));
+  qn::qlora_gemm_simt_kernel<false><<<grid, 256, 0, st>>>(view_of(Q), X, M, u, B, r, Y);
+  QN_LAUNCH_CHECK("qlora_gemm_simt_kernel<fwd>");
+  return QN_OK;
+}
+
+qn_status qlora_linear_bwd_dx(const qn_nf4 *Q, const uint16_t *dY, int64_t M, const uint16_t *A, const uint16_t *B,
+                              int32_t r, float alpha, uint16_t *dX, void *ws, size_t ws_bytes, void *stream) {
+  g_last_error.clear();
+  QN_TRY(check_layer(Q, dY, M, A, B, r, alpha, dX));
+  const int64_t d = Q->d, k = Q->k;
+  const size_t need = bwd_ws_bytes(M, d, k, r);
+  if (!ws) return fail(QN_EINVAL, "workspace NULL");
+  if (ws_bytes < need) return fail(QN_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (!aligned(ws, 256)) return fail(QN_EALIGN, "workspace not 256-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Span sp{static_cast<char *>(ws), ws_bytes, 0};
+  const float s = alpha / static_cast<float>(r);
+  float *v = sp.take<float>(static_cast<size_t>(M) * r);
+  {
+    // v[m, q] = s * sum_i dY[m, i] B[i, q]: Qop(n=q, kk=i) = B[i * r + q].
+    dim3 grid(static_cast<unsigned>(qn_ceil_div(M, qn::kProjTM)), static_cast<unsigned>(qn_ceil_div(r, qn::kProjTN)));
+    qn::lora_proj_kernel<<<grid, 256, 0, st>>>(dY, M, d, B, r, 1, r, s, v);
+    QN_LAUNCH_CHECK("lora_proj_kernel(dY B)");
+  }
+  if (qn::tc_bwd_supported(M, d, k, r)) {
+    return qn::launch_tc_bwd(view_of(Q), dY, M, v, A, r, dX, sp, st) == 0 ? QN_OK
+                                                                          : fail(QN_ECUDA, "tcgen05 backward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  }
+  dim3 grid(static_cast<unsigned>(qn_ceil_div(k, qn::kTileN)), static_cast<unsigned>(qn_ceil_div(M, qn::kTileM)));
+  qn::qlora_gemm_simt_kernel<true><<<grid, 256, 0, st>>>(view_of(Q), dY, M, v, A, r, dX);
+  QN_LAUNCH_CHECK("qlora_gemm_simt_kernel<bwd>");
+  return QN_OK;
+}
+
+qn_status qn_device_status(void *stream) {
+  g_last_error.clear();
+  QN_TRY(cuda_check(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream synchronize"));
+  unsigned int h = 0, zero = 0;
+  QN_TRY(cuda_check(cudaMemcpyFromSymbol(&h, g_qn_status, sizeof(h)), "read status word"));
+  QN_TRY(cuda_check(cudaMemcpyToSymbol(g_qn_status, &zero, sizeof(zero)), "clear status word"));
+  if (h & QN_DEV_TIMEOUT) return fail(QN_ETIMEOUT, "a bounded device wait expired");
+  return QN_OK;
+}
+
+qn_status loftq_init(const float *W, int64_t d, int64_t k, int32_t r, float alpha, int32_t T, uint64_t seed,
+                     int32_t oversample, int32_t power_iters, const qn_nf4 *Q, float *A, float *B, double *resid,
+                     void *ws, size_t ws_bytes, void *stream) {
+  g_last_error.clear();
+  if (!W || !A || !B || !resid || !Q) return fail(QN_EINVAL, "NULL pointer");
+  QN_TRY(check_nf4(Q, true));
+  if (Q->d != d || Q->k != k) return fail(QN_ESHAPE, "Q shape %lldx%lld != W shape", (long long)Q->d, (long long)Q->k);
+  if (d % 64 || k % 64) return fail(QN_ESHAPE, "d and k must be multiples of 64");
+  const int p = r + oversample;
+  if (r < 1 || oversample < 0 || p > qn::kLqMaxP) return fail(QN_ESHAPE, "need 1 <= r and r + oversample <= 32");
+  if (p > d || p > k) return fail(QN_ESHAPE, "r + oversample exceeds a matrix dimension");
+  if (T < 0 || T > 64) return fail(QN_ESHAPE, "T must be in [0, 64]");
+  if (power_iters < 0 || power_iters > 32) return fail(QN_ESHAPE, "power_iters must be in [0, 32]");
+  if (!std::isfinite(alpha) || alpha == 0.f) return fail(QN_EINVAL, "alpha must be finite and non-zero");
+  if (!aligned(W, 16) || !aligned(A, 16) || !aligned(B, 16)) return fail(QN_EALIGN, "W/A/B not 16-byte aligned");
+  const size_t need = qn_workspace_bytes(QN_OP_LOFTQ, 0, d, k, r);
+  if (!ws) return fail(QN_EINVAL, "workspace NULL");
+  if (ws_bytes < need) return fail(QN_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (!aligned(ws, 256)) return fail(QN_EALIGN, "workspace not 256-byte aligned");
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  constexpr int P = qn::kLqMaxP;
+  Span sp{static_cast<char *>(ws), ws_bytes, 0};
+  float *Tbuf = sp.take<float>(static_cast<size_t>(d) * k);
+  float *Y = sp.take<float>(static_cast<size_t>(d) * P);
+  float *Zt = sp.take<float>(static_cast<size_t>(k) * P);
+  float *Om = sp.take<float>(static_cast<size_t>(k) * P);
+  double *G = sp.take<double>(P * P);
+  float *V = sp.take<float>(P * P);
+  float *lam = sp.take<float>(P);
+  float *Linv = sp.take<float>(P * P);
+  double *partial = sp.take<double>(1024);
+  double *norm2 = sp.take<double>(1);
+  unsigned long long *bins = sp.take<unsigned long long>(qn::kNumBins);
+
+  const float s = alpha / static_cast<float>(r);
+  const int sms = sm_count();
+  const int64_t n = d * k;
+  const QnNF4View qv = view_of(Q);
+  const int red_blocks = sms * 4 < 1024 ? sms * 4 : 1024;
+
+  QN_TRY(cuda_check(cudaMemsetAsync(A, 0, sizeof(float) * r * k, st), "memset A"));
+  QN_TRY(cuda_check(cudaMemsetAsync(B, 0, sizeof(float) * d * r, st), "memset B"));
+
+  auto residual_norm = [&](int rr, double *outp) -> qn_status {
+    qn::resid_norm_kernel<<<red_blocks, 256, 0, st>>>(Tbuf, B, A, d, k, rr, s, partial);
+    QN_LAUNCH_CHECK("resid_norm_kernel");
+    qn::sum_partials_kernel<<<1, 256, 0, st>>>(partial, red_blocks, norm2);
+    QN_LAUNCH_CHECK("sum_partials_kernel");
+    QN_TRY(cuda_check(cudaMemcpyAsync(outp, norm2, sizeof(double), cudaMemcpyDeviceToHost, st), "copy norm"));
+    QN_TRY(cuda_check(cudaStreamSynchronize(st), "synchronize"));
+    *outp = std::sqrt(*outp);
+    return QN_OK;
+  };
+  auto orth = [&](float *Ym, int64_t rows) -> qn_status {
+    for (int rep = 0; rep < 2; ++rep) {
+      QN_TRY(cuda_check(cudaMemsetAsync(G, 0, sizeof(double) * P * P, st), "memset G"));
+      const int64_t rpb = 256;
+      qn::gram_kernel<P><<<static_cast<unsigned>(qn_ceil_div(rows, rpb)), P * P, 0, st>>>(Ym, rows, rpb, G);
+      QN_LAUNCH_CHECK("gram_kernel");
+      qn::chol_inv_kernel<P><<<1, P, 0, st>>>(G, p, Linv);
+      QN_LAUNCH_CHECK("chol_inv_kernel");
+      qn::apply_linv_kernel<P><<<static_cast<unsigned>(qn_ceil_div(rows, 8)), 256, 0, st>>>(Ym, rows, Linv, p);
+      QN_LAUNCH_CHECK("apply_linv_kernel");
+    }
+    return QN_OK;
+  };
+  auto r_times = [&](const float *Z, float *Yo) -> qn_status {  // Yo = R Z   (d x P)
+    qn::rz_kernel<P><<<static_cast<unsigned>(qn_ceil_div(d, 8)), 256, 0, st>>>(Tbuf, d, k, Z, p, Yo);
+    QN_LAUNCH_CHECK("rz_kernel");
+    return QN_OK;
+  };
+  auto rt_times = [&](const float *Ym, float *Zo) -> qn_status {  // Zo = R^T Y  (k x P)
+    QN_TRY(cuda_check(cudaMemsetAsync(Zo, 0, sizeof(float) * k * P, st), "memset Zt"));
+    const int64_t slices = 8;
+    dim3 grid(static_cast<unsigned>(qn_ceil_div(k, 128)), static_cast<unsigned>(slices));
+    qn::rty_kernel<P><<<grid, 128, 0, st>>>(Tbuf, d, k, Ym, qn_ceil_div(d, slices), Zo);
+    QN_LAUNCH_CHECK("rty_kernel");
+    return QN_OK;
+  };
+
+  // t = 0: Q_0 = NF4(W), residual without adapter.
+  QN_TRY(launch_quantize(W, QN_F32, Q, bins, st));
+  qn::residual_kernel<<<sms * 8, 256, 0, st>>>(qv, W, Tbuf, n);
+  QN_LAUNCH_CHECK("residual_kernel");
+  QN_TRY(residual_norm(0, &resid[0]));
+
+  for (int t = 1; t <= T; ++t) {
+    if (t > 1) {  // Q-step: Q_t = NF4(W - s B A)
+      qn::lowrank_sub_kernel<<<sms * 8, 256, 0, st>>>(W, B, A, d, k, r, s, Tbuf);
+      QN_LAUNCH_CHECK("lowrank_sub_kernel");
+      QN_TRY(launch_quantize(Tbuf, QN_F32, Q, bins, st));
+      qn::residual_kernel<<<sms * 8, 256, 0, st>>>(qv, W, Tbuf, n);
+      QN_LAUNCH_CHECK("residual_kernel");
+    }
+    // Delta-step on R = W - deq(Q_t) (in Tbuf).
+    qn::omega_kernel<<<static_cast<unsigned>(qn_ceil_div(k * P, 256)), 256, 0, st>>>(
+        Om, k, p, P, seed ^ (0x9E3779B97F4A7C15ull * static_cast<uint64_t>(t)));
+    QN_LAUNCH_CHECK("omega_kernel");
+    QN_TRY(r_times(Om, Y));
+    QN_TRY(orth(Y, d));
+    for (int it = 0; it < power_iters; ++it) {
+      QN_TRY(rt_times(Y, Zt));
+      QN_TRY(orth(Zt, k));
+      QN_TRY(r_times(Zt, Y));
+      QN_TRY(orth(Y, d));
+    }
+    QN_TRY(rt_times(Y, Zt));  // Zt = R^T Y, i.e. (Y^T R)^T
+    QN_TRY(cuda_check(cudaMemsetAsync(G, 0, sizeof(double) * P * P, st), "memset G"));
+    qn::gram_kernel<P><<<static_cast<unsigned>(qn_ceil_div(k, 256)), P * P, 0, st>>>(Zt, k, 256, G);
+    QN_LAUNCH_CHECK("gram_kernel");
+    qn::jacobi_eig_kernel<P><<<1, P, 0, st>>>(G, p, lam, V);
+    QN_LAUNCH_CHECK("jacobi_eig_kernel");
+    qn::project_kernel<P><<<static_cast<unsigned>(qn_ceil_div(d, 256)), 256, 0, st>>>(Y, d, V, lam, r, s, 0, B, 0);
+    QN_LAUNCH_CHECK("project_kernel(B)");
+    qn::project_kernel<P><<<static_cast<unsigned>(qn_ceil_div(k, 256)), 256, 0, st>>>(Zt, k, V, lam, r, s, 1, A, 1);
+    QN_LAUNCH_CHECK("project_kernel(A)");
+    QN_TRY(residual_norm(r, &resid[t]));
+  }
+  return QN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,352 @@
+// nf4_codec.cuh -- blockwise NF4 quantise / double-quantise / dequantise kernels.
+//
+// Method ("QLoRA technical analysis" §2.1; "QLoRA paper summary", NF4 and
+// double-quantisation bullets): per 64-element block divide by the block
+// absmax and replace each value by its nearest NF4 level; pack two 4-bit codes
+// per byte; quantise the fp32 absmax constants again to int8 in groups of 256
+// after subtracting their mean.
+//
+// Kernels
+//   nf4_quant_kernel      full 64-blocks: 128-bit loads, shuffle absmax,
+//                         IEEE division, threshold count, packed stores,
+//                         exact exponent-binned sum of the absmax constants.
+//   nf4_quant_tail_kernel the final partial block (n % 64 != 0).
+//   nf4_dq_kernel         per 256-group: exact mean from the bins, int8 codes.
+//   nf4_dequant_kernel    codes + constants -> fp32 / bf16, 128-bit stores.
+#pragma once
+
+#include "common.cuh"
+
+namespace qn {
+
+constexpr int kQuantThreads = 256;
+constexpr int kNumBins = 256;  // one bin per fp32 exponent field value
+
+// Adds a block absmax to the exponent-binned exact sum: bin e' = max(e, 1)
+// accumulates the integer significand (implicit bit included), so that
+// sum = sum_e bins[e] * 2^(e - 150).
+__device__ __forceinline__ void bin_add_shared(unsigned long long *s_bins, float m) {
+  const uint32_t b = __float_as_uint(m);
+  const uint32_t e = (b >> 23) & 0xFFu;
+  const uint32_t sig = (b & 0x7FFFFFu) | (e ? 0x800000u : 0u);
+  if (sig) atomicAdd(&s_bins[e ? e : 1u], static_cast<unsigned long long>(sig));
+}
+
+template <typename T> struct QuantVec;
+template <> struct QuantVec<float> { static constexpr int kVec = 4; };
+template <> struct QuantVec<__nv_bfloat16> { static constexpr int kVec = 8; };
+
+// Loads kVec consecutive elements (16 bytes) as fp32.
+__device__ __forceinline__ void load_vec(const float *p, float (&v)[4]) {
+  const float4 t = __ldcs(reinterpret_cast<const float4 *>(p));
+  v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+}
+__device__ __forceinline__ void load_vec(const __nv_bfloat16 *p, float (&v)[8]) {
+  const uint4 t = __ldcs(reinterpret_cast<const uint4 *>(p));
+  const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// One group of G = 64 / kVec lanes owns one 64-element block per iteration.
+template <typename T>
+__global__ void __launch_bounds__(kQuantThreads)
+nf4_quant_kernel(const T *__restrict__ x, int64_t nfull, uint8_t *__restrict__ codes,
+                 float *__restrict__ absmax, unsigned long long *__restrict__ bins) {
+  constexpr int V = QuantVec<T>::kVec;
+  constexpr int G = 64 / V;        // lanes per block
+  constexpr int BPW = 32 / G;      // blocks per warp-iteration
+  __shared__ unsigned long long s_bins[kNumBins];
+  if (bins) {
+    for (int i = threadIdx.x; i < kNumBins; i += blockDim.x) s_bins[i] = 0ull;
+    __syncthreads();
+  }
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / G;
+  const int li = lane % G;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+
+  for (int64_t b0 = warp * BPW; b0 < nfull; b0 += nwarps * BPW) {
+    const int64_t blk = b0 + sub;
+    const bool valid = blk < nfull;
+    float v[V];
+    if (valid) {
+      load_vec(x + blk * 64 + li * V, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < V; ++i) v[i] = 0.f;
+    }
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) m = fmaxf(m, fabsf(v[i]));
+#pragma unroll
+    for (int off = G / 2; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+
+    uint32_t packed = 0;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const float q = (m > 0.f) ? __fdiv_rn(v[i], m) : 0.f;
+      packed |= nf4_code_of(q) << (4 * i);
+    }
+    if (valid) {
+      if constexpr (V == 4) {
+        reinterpret_cast<uint16_t *>(codes + blk * 32)[li] = static_cast<uint16_t>(packed);
+      } else {
+        reinterpret_cast<uint32_t *>(codes + blk * 32)[li] = packed;
+      }
+      if (li == 0) {
+        absmax[blk] = m;
+        if (bins) bin_add_shared(s_bins, m);
+      }
+    }
+  }
+  if (bins) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < kNumBins; i += blockDim.x)
+      if (s_bins[i]) atomicAdd(&bins[i], s_bins[i]);
+  }
+}
+
+// The final partial block: one warp, scalar loads.
+template <typename T>
+__global__ void nf4_quant_tail_kernel(const T *__restrict__ x, int64_t n, int64_t blk,
+                                      uint8_t *__restrict__ codes, float *__restrict__ absmax,
+                                      unsigned long long *__restrict__ bins) {
+  const int lane = threadIdx.x;
+  const int64_t base = blk * 64;
+  const int cnt = static_cast<int>(n - base);  // 1..63
+  float v0 = 0.f, v1 = 0.f;
+  const int e0 = 2 * lane, e1 = 2 * lane + 1;
+  if (e0 < cnt) v0 = static_cast<float>(x[base + e0]);
+  if (e1 < cnt) v1 = static_cast<float>(x[base + e1]);
+  float m = fmaxf(fabsf(v0), fabsf(v1));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  const uint32_t c0 = nf4_code_of(m > 0.f ? __fdiv_rn(v0, m) : 0.f);
+  const uint32_t c1 = nf4_code_of(m > 0.f ? __fdiv_rn(v1, m) : 0.f);
+  if (e0 < cnt) codes[blk * 32 + lane] = static_cast<uint8_t>(c0 | ((e1 < cnt) ? (c1 << 4) : 0u));
+  if (lane == 0) {
+    absmax[blk] = m;
+    if (bins) {
+      const uint32_t b = __float_as_uint(m);
+      const uint32_t e = (b >> 23) & 0xFFu;
+      const uint32_t sig = (b & 0x7FFFFFu) | (e ? 0x800000u : 0u);
+      if (sig) atomicAdd(&bins[e ? e : 1u], static_cast<unsigned long long>(sig));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Exact mean of the absmax constants, rounded once to fp32 (ties to even).
+// bins[e] holds sum of significands with exponent field e (bin 1 also holds
+// subnormals); the exact sum in units of 2^-149 is sum_e bins[e] << (e - 1),
+// a number below 2^320 kept in ten 32-bit limbs.
+// ---------------------------------------------------------------------------
+constexpr int kLimbs = 10;
+
+__device__ __forceinline__ void limbs_add(uint32_t (&acc)[kLimbs], const uint32_t (&add)[kLimbs]) {
+  uint64_t carry = 0;
+#pragma unroll
+  for (int i = 0; i < kLimbs; ++i) {
+    const uint64_t s = static_cast<uint64_t>(acc[i]) + add[i] + carry;
+    acc[i] = static_cast<uint32_t>(s);
+    carry = s >> 32;
+  }
+}
+
+// Adds value << shift (value < 2^64, shift <= 253) into the accumulator.
+__device__ __forceinline__ void limbs_add_shifted(uint32_t (&acc)[kLimbs], uint64_t value, int shift) {
+  const int ls = shift >> 5, bs = shift & 31;
+  const uint64_t lo64 = value << bs;                                          // bits 0..63
+  const uint32_t hi32 = bs ? static_cast<uint32_t>(value >> (64 - bs)) : 0u;  // bits 64..95
+  uint32_t add[kLimbs];
+#pragma unroll
+  for (int i = 0; i < kLimbs; ++i) {
+    uint32_t w = 0;
+    if (i == ls) w = static_cast<uint32_t>(lo64);
+    else if (i == ls + 1) w = static_cast<uint32_t>(lo64 >> 32);
+    else if (i == ls + 2) w = hi32;
+    add[i] = w;
+  }
+  limbs_add(acc, add);
+}
+
+// Warp-cooperative exact mean; every lane returns the same fp32.
+__device__ float exact_mean_from_bins(const unsigned long long *__restrict__ bins, uint64_t count) {
+  const int lane = threadIdx.x & 31;
+  uint32_t acc[kLimbs];
+#pragma unroll
+  for (int i = 0; i < kLimbs; ++i) acc[i] = 0u;
+  for (int j = 0; j < kNumBins / 32; ++j) {
+    const int e = lane * (kNumBins / 32) + j;
+    const unsigned long long s = bins[e];
+    if (e >= 1 && s) limbs_add_shifted(acc, s, e - 1);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    uint32_t other[kLimbs];
+#pragma unroll
+    for (int i = 0; i < kLimbs; ++i) other[i] = __shfl_xor_sync(0xffffffffu, acc[i], off);
+    limbs_add(acc, other);
+  }
+  if (count == 0) return 0.f;
+  // Long division by count, most significant limb first.  count < 2^32 uses
+  // 64-bit steps; larger counts fall back to bit-serial division.
+  uint32_t quo[kLimbs];
+  uint64_t rem = 0;
+  if (count < (1ull << 32)) {
+    for (int i = kLimbs - 1; i >= 0; --i) {
+      const uint64_t cur = (rem << 32) | acc[i];
+      quo[i] = static_cast<uint32_t>(cur / count);
+      rem = cur % count;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kLimbs; ++i) quo[i] = 0u;
+    for (int bit = 32 * kLimbs - 1; bit >= 0; --bit) {
+      const uint32_t in = (acc[bit >> 5] >> (bit & 31)) & 1u;
+      const bool top = (rem >> 63) != 0;  // rem < count < 2^64; 2*rem may need 65 bits
+      rem = (rem << 1) | in;
+      if (top || rem >= count) {
+        rem -= count;
+        quo[bit >> 5] |= 1u << (bit & 31);
+      }
+    }
+  }
+  // Position of the quotient's top set bit.
+  int p = -1;
+  for (int i = kLimbs - 1; i >= 0 && p < 0; --i)
+    if (quo[i]) p = 32 * i + 31 - __clz(quo[i]);
+  // Significand = quotient >> shift, shift = max(p - 23, 0) (2^-149 units).
+  const int shift = p > 23 ? p - 23 : 0;
+  auto qbit = [&](int b) -> uint32_t { return (b < 0) ? 0u : (quo[b >> 5] >> (b & 31)) & 1u; };
+  uint32_t mant = 0;
+  for (int b = 0; b < 24; ++b) mant |= qbit(shift + b) << b;
+  bool round_up;
+  const bool odd = mant & 1u;
+  if (shift == 0) {
+    // The remainder alone decides: compare 2 * rem with count.
+    const bool gt = (rem > count - rem);
+    const bool eq = (rem == count - rem);
+    round_up = gt || (eq && odd);
+  } else {
+    const bool guard = qbit(shift - 1);
+    bool sticky = rem != 0;
+    for (int b = 0; b < shift - 1 && !sticky; ++b) sticky = qbit(b);
+    round_up = guard && (sticky || odd);
+  }
+  int sh = shift;
+  mant += round_up ? 1u : 0u;
+  if (mant == (1u << 24)) { mant = 1u << 23; sh += 1; }
+  uint32_t bits;
+  if (mant >= (1u << 23)) bits = (static_cast<uint32_t>(sh + 1) << 23) | (mant - (1u << 23));
+  else bits = mant;  // subnormal (only reachable with sh == 0)
+  return __uint_as_float(bits);
+}
+
+constexpr int kDqWarps = 8;
+
+// One warp per group of 256 constants.  Every CTA first derives the mean
+// (identical in every CTA); CTA 0 stores it.
+__global__ void __launch_bounds__(kDqWarps * 32)
+nf4_dq_kernel(const float *__restrict__ absmax, int64_t nblk, const unsigned long long *__restrict__ bins,
+              int8_t *__restrict__ absmax_q, float *__restrict__ absmax_scale, float *__restrict__ absmax_mean) {
+  __shared__ float s_mu;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0) {
+    const float mu = exact_mean_from_bins(bins, static_cast<uint64_t>(nblk));
+    if (lane == 0) {
+      s_mu = mu;
+      if (blockIdx.x == 0) *absmax_mean = mu;
+    }
+  }
+  __syncthreads();
+  const float mu = s_mu;
+  const int64_t ngrp = qn_ceil_div(nblk, 256);
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * kDqWarps + warp; g < ngrp;
+       g += static_cast<int64_t>(gridDim.x) * kDqWarps) {
+    const int64_t base = g * 256 + lane * 8;
+    float c[8];
+    float S = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int64_t j = base + i;
+      c[i] = (j < nblk) ? __fsub_rn(absmax[j], mu) : 0.f;
+      S = fmaxf(S, fabsf(c[i]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) S = fmaxf(S, __shfl_xor_sync(0xffffffffu, S, off));
+    const float sigma = __fdiv_rn(S, 127.f);
+    if (lane == 0) absmax_scale[g] = sigma;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int64_t j = base + i;
+      if (j < nblk) {
+        int q = 0;
+        if (sigma > 0.f) {
+          q = __float2int_rn(__fdiv_rn(c[i], sigma));
+          q = q > 127 ? 127 : (q < -127 ? -127 : q);
+        }
+        absmax_q[j] = static_cast<int8_t>(q);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Dequantisation: one thread per 32 elements (16 code bytes, one 128-bit load).
+// ---------------------------------------------------------------------------
+template <bool kBf16Out>
+__global__ void __launch_bounds__(256)
+nf4_dequant_kernel(QnNF4View q, int64_t n, void *__restrict__ out) {
+  __shared__ float s_lut[16];
+  if (threadIdx.x < 16) s_lut[threadIdx.x] = c_nf4_levels[threadIdx.x];
+  __syncthreads();
+  const int64_t nchunk = n / 32;
+  for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < nchunk;
+       c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint4 w4 = __ldcs(reinterpret_cast<const uint4 *>(q.codes) + c);
+    const float m = block_scale(q, c >> 1);
+    const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+    if constexpr (kBf16Out) {
+      uint32_t o[16];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t byte = (w[i] >> (8 * j)) & 0xFFu;
+          o[4 * i + j] = pack_bf16x2(__fmul_rn(s_lut[byte & 15u], m), __fmul_rn(s_lut[byte >> 4], m));
+        }
+      uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + c * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) __stcs(dst + i, make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]));
+    } else {
+      float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(out) + c * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float f[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = __fmul_rn(s_lut[(w[i] >> (4 * j)) & 15u], m);
+        __stcs(dst + 2 * i, make_float4(f[0], f[1], f[2], f[3]));
+        __stcs(dst + 2 * i + 1, make_float4(f[4], f[5], f[6], f[7]));
+      }
+    }
+  }
+  // Tail: elements [nchunk*32, n), one thread each.
+  const int64_t t0 = nchunk * 32;
+  if (blockIdx.x == 0) {
+    for (int64_t e = t0 + threadIdx.x; e < n; e += blockDim.x) {
+      const uint32_t byte = q.codes[e >> 1];
+      const uint32_t code = (e & 1) ? (byte >> 4) : (byte & 15u);
+      const float wv = __fmul_rn(s_lut[code], block_scale(q, e >> 6));
+      if constexpr (kBf16Out) static_cast<uint16_t *>(out)[e] = f32_to_bf16_bits(wv);
+      else static_cast<float *>(out)[e] = wv;
+    }
+  }
+}
+
+}  // namespace qn

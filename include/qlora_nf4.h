@@ -1,0 +1,205 @@
+/*
+ * qlora_nf4.h -- C ABI of the B300 (sm_103a) QLoRA NF4 library.
+ *
+ * The hot path of QLoRA over NF4 4-bit weights, as the method's pages state it:
+ *
+ *   nf4_quantize / nf4_dequantize
+ *       Blockwise NF4: every 64 consecutive elements share one absmax; each
+ *       element is divided by it and replaced by the index of the nearest of
+ *       16 normal-quantile levels with an exact zero; two indices are packed
+ *       per byte; the absmax constants are quantised a second time ("double
+ *       quantisation").  Sources: "QLoRA technical analysis" (xdnf.cn) §2.1
+ *       (absmax normalisation and argmin search), "QLoRA paper summary"
+ *       (blog.csdn.net, QLoRA论文概述: NF4 from normal quantiles, double
+ *       quantisation), "PEFT course notes" (demo.tomabc.com) §4.2.
+ *
+ *   qlora_linear_fwd
+ *       Y = X deq(Q)^T + (alpha/r) (X A^T) B^T with W in R^{d x k},
+ *       B in R^{d x r}, A in R^{r x k} ("PEFT course notes" §2.2: h = Wx + BAx;
+ *       "PEFT quantization guide" (huggingface docs, 量化): bf16 compute dtype).
+ *
+ *   qlora_linear_bwd_dx
+ *       dX = dY deq(Q) + (alpha/r) (dY B) A: the gradient flowing through the
+ *       frozen 4-bit weight into the inputs ("QLoRA paper summary", abstract).
+ *
+ *   loftq_init
+ *       T alternations of Q_t = NF4(W - s B A) and a rank-r approximation of
+ *       W - deq(Q_t) ("LoftQ explainer" (mhpn.cn) §2.2 objective, §2.3 algorithm).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Memory: the caller owns every buffer.  Pointers documented "device" must
+ *   be device (or managed) memory on the current CUDA device and 16-byte
+ *   aligned; pointers documented "host" are ordinary host memory.  The library
+ *   allocates no device memory; scratch space is the caller's workspace `ws`
+ *   of at least qn_workspace_bytes(...) bytes (device, 256-byte aligned).
+ * - Layout: matrices are row-major.  W (d x k) element (i, j) is at i*k + j;
+ *   its flat element index e = i*k + j is what the 64-element blocks run over.
+ * - bf16 buffers are passed as `uint16_t *` holding IEEE bfloat16 bit patterns.
+ * - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  Every
+ *   call only enqueues work on it and returns, except loftq_init, which
+ *   synchronises the stream once per alternation to report residuals.
+ * - Errors: argument errors return before anything is enqueued and leave
+ *   outputs untouched.  A failed launch returns QN_ECUDA.  Kernels never trap:
+ *   a bounded wait that expires records QN_ETIMEOUT in a device status word
+ *   that qn_device_status() reads.  qn_last_error() gives a message for the
+ *   calling thread's last non-OK status.
+ */
+#ifndef QLORA_NF4_H
+#define QLORA_NF4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QN_ABI_VERSION 1
+
+typedef enum {
+  QN_OK = 0,
+  QN_EINVAL = 1,       /* null pointer, bad enum, non-finite alpha ...        */
+  QN_ESHAPE = 2,       /* sizes out of range or inconsistent                  */
+  QN_EALIGN = 3,       /* pointer not 16-byte aligned                          */
+  QN_ENOMEM = 4,       /* workspace smaller than qn_workspace_bytes()          */
+  QN_ECUDA = 5,        /* a CUDA runtime call or kernel launch failed          */
+  QN_ETIMEOUT = 6,     /* a bounded device-side wait expired                   */
+  QN_EUNSUPPORTED = 7  /* valid request this build does not implement          */
+} qn_status;
+
+typedef enum { QN_F32 = 0, QN_BF16 = 1 } qn_dtype;
+
+typedef enum {
+  QN_OP_QUANTIZE = 0,
+  QN_OP_DEQUANTIZE = 1,
+  QN_OP_LINEAR_FWD = 2,
+  QN_OP_LINEAR_BWD_DX = 3,
+  QN_OP_LOFTQ = 4
+} qn_op;
+
+/*
+ * Quantised state of one tensor of n = d*k elements (all pointers device,
+ * caller-owned).  Block size 64 and double-quantisation group 256 are the only
+ * supported values.
+ *   codes        uint8[ceil(n/2)]  element 2q in the low nibble of byte q,
+ *                                  element 2q+1 in the high nibble; an unused
+ *                                  high nibble (odd n) is 0.
+ *   absmax       fp32[nblk]        exact block absmax, nblk = ceil(n/64).
+ *                                  Always written by nf4_quantize; read by the
+ *                                  dequantiser only when dq == 0.
+ *   absmax_q     int8[nblk]        (dq) int8 code of absmax - mean.
+ *   absmax_scale fp32[ngrp]        (dq) per-256-block scale, ngrp = ceil(nblk/256).
+ *   absmax_mean  fp32[1]           (dq) exact mean of absmax rounded to fp32.
+ */
+typedef struct {
+  int64_t d;
+  int64_t k;
+  int32_t block;     /* must be 64                     */
+  int32_t dq;        /* 1 = double-quantised constants */
+  int32_t dq_block;  /* must be 256                    */
+  int32_t reserved;
+  uint8_t *codes;
+  float *absmax;
+  int8_t *absmax_q;
+  float *absmax_scale;
+  float *absmax_mean;
+} qn_nf4;
+
+/* ABI version of the loaded library (QN_ABI_VERSION at build time). */
+int qn_abi_version(void);
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+const char *qn_last_error(void);
+
+/*
+ * Host copies of the constant tables the kernels use: the 16 NF4 levels
+ * (ascending) and the 15 fp32 decision thresholds t_i, where t_i is the
+ * largest fp32 not above the exact midpoint (c_i + c_{i+1}) / 2, so that
+ * code(v) = #{ i : v > t_i } is the nearest level with ties to the lower
+ * index.  Either pointer may be NULL.
+ */
+void qn_nf4_tables(float codebook[16], float thresholds[15]);
+
+/*
+ * Workspace bytes the call `op` needs for the given sizes (0 if none).
+ * M: rows of X / dY; d, k: W is d x k; r: LoRA rank (LoftQ: rank r and
+ * oversampling are taken at their maximum supported value, 256 + 32).
+ */
+size_t qn_workspace_bytes(qn_op op, int64_t M, int64_t d, int64_t k, int32_t r);
+
+/*
+ * nf4_quantize -- blockwise NF4 quantisation of W (d x k, flat n = d*k).
+ *   W      device, n elements of dtype wdt (QN_F32 or QN_BF16).
+ *   Q      host struct; Q->d, Q->k, Q->block (64), Q->dq, Q->dq_block (256)
+ *          and its device output pointers must be set (absmax_q, absmax_scale,
+ *          absmax_mean may be NULL when dq == 0).
+ *   ws     device workspace of ws_bytes >= qn_workspace_bytes(QN_OP_QUANTIZE,..)
+ * Per block j: m_j = max |x|; codes = nearest level of fp32(x / m_j) (IEEE
+ * division; a block with m_j = 0 gets code 7, the exact zero).  With dq:
+ * mu = nearest fp32 to the exact mean of all m_j; per group g of 256 blocks
+ * sigma_g = fp32(max_j |fp32(m_j - mu)| / 127) and
+ * q_j = clamp(rint_half_even(fp32(fp32(m_j - mu) / sigma_g)), -127, 127)
+ * (q_j = 0 when sigma_g = 0).  Results are bit-identical for any launch shape.
+ */
+qn_status nf4_quantize(const void *W, qn_dtype wdt, const qn_nf4 *Q,
+                       void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * nf4_dequantize -- W'[e] = fp32(c[code_e] * m'_{block(e)}), written as fp32
+ * or rounded to bf16 (nearest even).  m' = fp32(fp32(q_j * sigma_g) + mu) when
+ * Q->dq, else the exact absmax.  Wout: device, n elements of dtype odt.
+ */
+qn_status nf4_dequantize(const qn_nf4 *Q, void *Wout, qn_dtype odt, void *stream);
+
+/*
+ * qlora_linear_fwd -- Y = X deq(Q)^T + (alpha/r) (X A^T) B^T.
+ *   Q     quantised weight, d x k with k % 64 == 0.
+ *   X     device bf16 [M x k];  A device bf16 [r x k];  B device bf16 [d x r].
+ *   Y     device bf16 [M x d] (written).
+ *   1 <= M, 1 <= r <= 256.  Accumulation is fp32; the weight enters the
+ *   tensor-core path as bf16(deq(Q)).  ws: qn_workspace_bytes(QN_OP_LINEAR_FWD).
+ */
+qn_status qlora_linear_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M,
+                           const uint16_t *A, const uint16_t *B, int32_t r,
+                           float alpha, uint16_t *Y,
+                           void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * qlora_linear_bwd_dx -- dX = dY deq(Q) + (alpha/r) (dY B) A.
+ *   dY device bf16 [M x d]; A, B as in the forward; dX device bf16 [M x k].
+ *   Same size rules and workspace query (QN_OP_LINEAR_BWD_DX).
+ */
+qn_status qlora_linear_bwd_dx(const qn_nf4 *Q, const uint16_t *dY, int64_t M,
+                              const uint16_t *A, const uint16_t *B, int32_t r,
+                              float alpha, uint16_t *dX,
+                              void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * loftq_init -- LoftQ initialisation of one fp32 matrix W (d x k, device).
+ *   For t = 1..T: Q_t = NF4(W - s B_{t-1} A_{t-1}) (B_0 A_0 = 0, s = alpha/r);
+ *   R_t = W - deq(Q_t); the rank-r part of R_t by randomised subspace
+ *   iteration (oversample columns, power_iters passes, Gaussian test matrix
+ *   from `seed`); B_t = U_r sqrt(S_r)/sqrt(s), A_t = sqrt(S_r) V_r^T/sqrt(s).
+ *   Outputs: Q (as nf4_quantize, holding Q_T; Q_0 = NF4(W) when T == 0),
+ *   A device fp32 [r x k], B device fp32 [d x r],
+ *   resid host fp64[T+1]: resid[t] = ||W - deq(Q_t) - s B_t A_t||_F, with
+ *   resid[0] the plain QLoRA residual ||W - deq(NF4(W))||_F.
+ *   1 <= r, r + oversample <= 32, 0 <= T <= 64, d, k multiples of 64 and >= r + oversample.
+ */
+qn_status loftq_init(const float *W, int64_t d, int64_t k, int32_t r, float alpha,
+                     int32_t T, uint64_t seed, int32_t oversample, int32_t power_iters,
+                     const qn_nf4 *Q, float *A, float *B, double *resid,
+                     void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word that
+ * bounded waits write.  Returns QN_OK, QN_ETIMEOUT, or QN_ECUDA.
+ */
+qn_status qn_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QLORA_NF4_H */

@@ -125,7 +125,8 @@ def adversarial_block_values(seed: int, cb: np.ndarray, nblocks: int) -> np.ndar
             idx[0] = 0
             v = (cb[idx] * scale).astype(np.float32)
             ulps = g.integers(-3, 4, 64).astype(np.int32)
-            bits = v.view(np.int32) + ulps
+            ulps[v == 0] = 0                      # keep exact zeros (no sign crossing)
+            bits = v.view(np.int32) + ulps        # same-sign neighbours of the level multiples
             v = bits.view(np.float32)
             v[0] = -scale
             out.append(v)

@@ -1,0 +1,110 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every
+function include/qlora_nf4.h declares, its constant tables match the
+oracle's independent construction, and argument errors come back as status
+codes before anything is launched."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qlora_nf4.h")
+
+
+@pytest.fixture(scope="module")
+def qn():
+    import __graft_entry__ as ge
+    ge._build_module().build()      # no-op when the library is up to date
+    import bit_nf4_quantized_39_b300 as mod
+    return mod
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*([a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "return")))
+
+
+def test_header_declares_the_entry_points():
+    names = header_functions()
+    for n in ("nf4_quantize", "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd_dx", "loftq_init"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(qn):
+    raw = ctypes.CDLL(qn.LIB_PATH)
+    for n in header_functions():
+        assert hasattr(raw, n), n
+    assert set(header_functions()) <= set(qn.EXPORTS)
+    assert qn.lib.qn_abi_version() == 1
+
+
+def test_tables_match_oracle_codebook_and_thresholds(qn):
+    from fractions import Fraction
+    from oracle import nf4
+    cb, th = qn.tables()
+    ocb = nf4.codebook()
+    assert np.array_equal(np.array(cb, dtype=np.float32).view(np.uint32), ocb.view(np.uint32))
+    for i, t in enumerate(th):
+        mid = (Fraction(float(ocb[i])) + Fraction(float(ocb[i + 1]))) / 2
+        t32 = np.float32(t)
+        assert Fraction(float(t32)) <= mid
+        assert Fraction(float(np.nextafter(t32, np.float32(np.inf)))) > mid
+
+
+def test_workspace_queries(qn):
+    assert qn.workspace_bytes(qn.QN_OP_QUANTIZE, 0, 1024, 1024, 0) == 2048
+    assert qn.workspace_bytes(qn.QN_OP_DEQUANTIZE, 0, 1024, 1024, 0) == 0
+    assert qn.workspace_bytes(qn.QN_OP_LINEAR_FWD, 1, 4096, 4096, 64) >= 4 * 64
+    assert qn.workspace_bytes(qn.QN_OP_LINEAR_FWD, 0, 4096, 4096, 64) == 0
+    lq = qn.workspace_bytes(qn.QN_OP_LOFTQ, 0, 4096, 4096, 16)
+    assert lq >= 4096 * 4096 * 4
+
+
+def _struct(qn, d=128, k=128, block=64, dq=1, dq_block=256, ptr=0x10000):
+    return qn.qn_nf4(d, k, block, dq, dq_block, 0, ptr, ptr, ptr, ptr, ptr)
+
+
+def _err(qn, status):
+    return status, qn.lib.qn_last_error().decode()
+
+
+def test_argument_errors_return_before_launch(qn):
+    L = qn.lib
+    P = 0x10000  # never dereferenced: every call below fails validation first
+    st = _struct(qn)
+    assert L.nf4_quantize(P, 0, None, P, 4096, None) == qn.QN_EINVAL
+    bad_block = _struct(qn, block=32)
+    assert L.nf4_quantize(P, 0, ctypes.byref(bad_block), P, 4096, None) == qn.QN_EUNSUPPORTED
+    bad_dq = _struct(qn, dq_block=128)
+    assert L.nf4_quantize(P, 0, ctypes.byref(bad_dq), P, 4096, None) == qn.QN_EUNSUPPORTED
+    assert L.nf4_quantize(P, 7, ctypes.byref(st), P, 4096, None) == qn.QN_EINVAL
+    assert L.nf4_quantize(P + 4, 0, ctypes.byref(st), P, 4096, None) == qn.QN_EALIGN
+    assert L.nf4_quantize(P, 0, ctypes.byref(st), P, 16, None) == qn.QN_ENOMEM
+    neg = _struct(qn, d=-1)
+    assert L.nf4_quantize(P, 0, ctypes.byref(neg), P, 4096, None) == qn.QN_ESHAPE
+    assert L.nf4_dequantize(ctypes.byref(st), None, 0, None) == qn.QN_EINVAL
+    # layer: k % 64, r range, M range, alignment, workspace size
+    odd_k = _struct(qn, k=100)
+    assert L.qlora_linear_fwd(ctypes.byref(odd_k), P, 1, P, P, 8, 16.0, P, P, 1 << 20, None) == qn.QN_ESHAPE
+    assert L.qlora_linear_fwd(ctypes.byref(st), P, 1, P, P, 0, 16.0, P, P, 1 << 20, None) == qn.QN_ESHAPE
+    assert L.qlora_linear_fwd(ctypes.byref(st), P, 1, P, P, 300, 16.0, P, P, 1 << 20, None) == qn.QN_ESHAPE
+    assert L.qlora_linear_fwd(ctypes.byref(st), P, 0, P, P, 8, 16.0, P, P, 1 << 20, None) == qn.QN_ESHAPE
+    assert L.qlora_linear_fwd(ctypes.byref(st), P + 2, 1, P, P, 8, 16.0, P, P, 1 << 20, None) == qn.QN_EALIGN
+    assert L.qlora_linear_fwd(ctypes.byref(st), P, 1, P, P, 8, float("nan"), P, P, 1 << 20, None) == qn.QN_EINVAL
+    assert L.qlora_linear_fwd(ctypes.byref(st), P, 1, P, P, 8, 16.0, P, P, 4, None) == qn.QN_ENOMEM
+    assert L.qlora_linear_bwd_dx(ctypes.byref(st), P, 1, P, P, 8, 16.0, P, None, 1 << 20, None) == qn.QN_EINVAL
+    msg = _err(qn, L.qlora_linear_bwd_dx(ctypes.byref(st), P, 1, P, P, 8, 16.0, P, P, 4, None))[1]
+    assert "workspace" in msg
+    # LoftQ: rank + oversample bound, T bound, shape agreement
+    res = (ctypes.c_double * 8)()
+    assert L.loftq_init(P, 128, 128, 30, 16.0, 5, 0, 8, 4, ctypes.byref(st), P, P, ctypes.addressof(res), P,
+                        1 << 30, None) == qn.QN_ESHAPE
+    assert L.loftq_init(P, 128, 128, 8, 16.0, 99, 0, 8, 4, ctypes.byref(st), P, P, ctypes.addressof(res), P,
+                        1 << 30, None) == qn.QN_ESHAPE
+    assert L.loftq_init(P, 64, 128, 8, 16.0, 5, 0, 8, 4, ctypes.byref(st), P, P, ctypes.addressof(res), P,
+                        1 << 30, None) == qn.QN_ESHAPE

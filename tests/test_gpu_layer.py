@@ -1,0 +1,113 @@
+"""GPU parity of the fused QLoRA layer (forward Y and backward dX) against the
+float64 oracle.  Tolerance: relative Frobenius error <= 5e-3, the bound the
+method's target fixes for layer outputs; the CUDA path rounds the dequantised
+weight and the outputs to bf16 and accumulates in fp32, which stays well
+inside it (typically ~2e-3)."""
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import layer, nf4
+
+pytestmark = pytest.mark.gpu
+
+TOL = 5e-3
+
+
+@pytest.fixture(scope="module")
+def qn():
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    import bit_nf4_quantized_39_b300 as mod
+    return mod
+
+
+def _f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def _run(qn, W, X, A, B, alpha, dY=None):
+    q = qn.nf4_quantize(torch.from_numpy(W).cuda(), dq=True)
+    ref = nf4.quantize(W, 64, dq=True)
+    Wd = nf4.dequantize(ref).reshape(W.shape)
+    Y = qn.qlora_linear_fwd(q, X.cuda(), A.cuda(), B.cuda(), alpha)
+    out = {"Y": Y, "Yref": layer.linear_fwd(_f64(X), Wd, _f64(A), _f64(B), alpha, A.shape[0])}
+    if dY is not None:
+        dX = qn.qlora_linear_bwd_dx(q, dY.cuda(), A.cuda(), B.cuda(), alpha)
+        out["dX"] = dX
+        out["dXref"] = layer.linear_bwd_dx(_f64(dY), Wd, _f64(A), _f64(B), alpha, A.shape[0])
+    qn.device_status()
+    return out
+
+
+def test_layer_case(qn):
+    c = synth.layer_case(seed=0)
+    o = _run(qn, c["W"], c["X"], c["A"], c["B"], c["alpha"], c["dY"])
+    assert layer.rel_fro(_f64(o["Y"]), o["Yref"]) < TOL
+    assert layer.rel_fro(_f64(o["dX"]), o["dXref"]) < TOL
+
+
+@pytest.mark.parametrize("M,d,k,r", [
+    (1, 256, 512, 8), (2, 200, 192, 3), (5, 384, 1024, 64), (16, 320, 256, 16),
+    (17, 192, 320, 8), (100, 330, 256, 24), (300, 128, 640, 64), (129, 1000, 128, 1),
+])
+def test_shapes_with_ragged_tails(qn, M, d, k, r):
+    c = synth.layer_case(seed=M * 7 + d, d=d, k=k, M=M, r=r, alpha=2.0 * r)
+    o = _run(qn, c["W"], c["X"], c["A"], c["B"], c["alpha"], c["dY"])
+    assert layer.rel_fro(_f64(o["Y"]), o["Yref"]) < TOL, (M, d, k, r)
+    assert layer.rel_fro(_f64(o["dX"]), o["dXref"]) < TOL, (M, d, k, r)
+
+
+def test_degenerate_adapter_and_weight(qn):
+    c = synth.layer_case(seed=9, d=256, k=256, M=24, r=8)
+    zB = torch.zeros_like(c["B"])
+    o = _run(qn, c["W"], c["X"], c["A"], zB, c["alpha"], c["dY"])          # B = 0: plain GEMM
+    assert layer.rel_fro(_f64(o["Y"]), o["Yref"]) < TOL
+    Wz = np.zeros((256, 256), np.float32)                                    # deq(Q) = 0: pure adapter
+    o = _run(qn, Wz, c["X"], c["A"], c["B"], c["alpha"], c["dY"])
+    assert layer.rel_fro(_f64(o["Y"]), o["Yref"]) < TOL
+    assert layer.rel_fro(_f64(o["dX"]), o["dXref"]) < TOL
+
+
+@pytest.mark.parametrize("shape", [(4096, 4096), (11008, 4096), (4096, 11008)])
+@pytest.mark.parametrize("M", [1, 16])
+def test_decode_shapes(qn, shape, M):
+    d, k = shape
+    m = synth.decode_matrix(seed=1, d=d, k=k, r=64, M=M)
+    o = _run(qn, m["W"], m["X"], m["A"], m["B"], m["alpha"])
+    assert layer.rel_fro(_f64(o["Y"]), o["Yref"]) < TOL
+
+
+def test_prefill_full_size_sampled_rows(qn):
+    """M=4096, d=11008, k=4096, r=16: full Y and dX on the GPU; the oracle
+    checks 48 sampled rows of each (the full float64 product is 0.7 TFLOP)."""
+    c = synth.prefill_case(seed=2)
+    W = c["W"]
+    q = qn.nf4_quantize(torch.from_numpy(W).cuda(), dq=True)
+    Y = qn.qlora_linear_fwd(q, c["X"].cuda(), c["A"].cuda(), c["B"].cuda(), c["alpha"])
+    dX = qn.qlora_linear_bwd_dx(q, c["dY"].cuda(), c["A"].cuda(), c["B"].cuda(), c["alpha"])
+    qn.device_status()
+    ref = nf4.quantize(W, 64, dq=True)
+    Wd = nf4.dequantize(ref).reshape(W.shape)
+    g = np.random.default_rng(2)
+    rows = np.sort(g.choice(c["M"], 48, replace=False))
+    A, B = _f64(c["A"]), _f64(c["B"])
+    Yref = layer.linear_fwd(_f64(c["X"])[rows], Wd, A, B, c["alpha"], c["r"])
+    dXref = layer.linear_bwd_dx(_f64(c["dY"])[rows], Wd, A, B, c["alpha"], c["r"])
+    assert layer.rel_fro(_f64(Y)[rows], Yref) < TOL
+    assert layer.rel_fro(_f64(dX)[rows], dXref) < TOL
+    # every output finite and of the right scale
+    assert torch.isfinite(Y.float()).all() and torch.isfinite(dX.float()).all()
+
+
+def test_host_buffers_round_trip(qn):
+    """The host-buffer path copies X in and Y out around the same kernels."""
+    c = synth.layer_case(seed=4, d=512, k=512, M=1, r=8)
+    q = qn.nf4_quantize(torch.from_numpy(c["W"]).cuda())
+    Xh = c["X"].pin_memory()
+    Yh = qn.qlora_linear_fwd(q, Xh, c["A"].cuda(), c["B"].cuda(), c["alpha"])
+    torch.cuda.synchronize()
+    Yd = qn.qlora_linear_fwd(q, c["X"].cuda(), c["A"].cuda(), c["B"].cuda(), c["alpha"])
+    assert not Yh.is_cuda
+    assert torch.equal(Yh, Yd.cpu())
