@@ -68,6 +68,7 @@ def _load():
         "loftq_init": (ctypes.c_int, [vp, i64, i64, i32, f32, i32, ctypes.c_uint64, i32, i32,
                                       P(qn_nf4), vp, vp, vp, vp, sz, vp]),
         "qn_device_status": (ctypes.c_int, [vp]),
+        "nf4_quantize_noalloc": (ctypes.c_int, [vp, ctypes.c_int, P(qn_nf4), vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -78,7 +79,8 @@ def _load():
 
 lib = _load()
 EXPORTS = ("qn_abi_version", "qn_last_error", "qn_nf4_tables", "qn_workspace_bytes", "nf4_quantize",
-           "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd_dx", "loftq_init", "qn_device_status")
+           "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd_dx", "loftq_init", "qn_device_status",
+           "nf4_quantize_noalloc")
 
 
 def _check(status: int):

@@ -241,6 +241,46 @@ qn_status check_layer(const qn_nf4 *Q, const void *in, int64_t M, const void *A,
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Scratch for nf4_quantize_noalloc.  Some callers cannot call cudaMalloc:
+// code that runs while another allocator owns all free device memory (a
+// framework's pre-reserved pool), or a latency-bound loop that must not pay
+// the implicit device-wide synchronisation of an allocation.  For them the
+// 2 KiB of exponent bins the quantiser needs live in this file-scope device
+// array.  Every GPU that loads the library holds it until the process exits.
+// In host code the name is only a host-side stand-in: the device address is
+// obtained once per device with cudaGetSymbolAddress and passed to the kernels.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned long long g_noalloc_bins[qn::kNumBins];
+
+namespace {
+
+constexpr int kNoallocMaxDevices = 64;
+// Largest tensor nf4_quantize_noalloc accepts: 2^40 elements keeps every
+// 64-bit bin of the fixed 2 KiB scratch exact (at most 2^34 block constants,
+// each adding a significand below 2^24).
+constexpr int64_t kNoallocMaxElements = int64_t(1) << 40;
+std::mutex g_noalloc_mutex;
+unsigned long long *g_noalloc_dev_ptr[kNoallocMaxDevices] = {};
+
+// Device address of g_noalloc_bins on the current device; looked up on the
+// first call per device.
+qn_status noalloc_bins(unsigned long long **out) {
+  int dev = 0;
+  QN_TRY(cuda_check(cudaGetDevice(&dev), "cudaGetDevice"));
+  if (dev < 0 || dev >= kNoallocMaxDevices) return fail(QN_EUNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_dev_ptr[dev]) {
+    void *p = nullptr;
+    QN_TRY(cuda_check(cudaGetSymbolAddress(&p, g_noalloc_bins), "cudaGetSymbolAddress(scratch)"));
+    g_noalloc_dev_ptr[dev] = static_cast<unsigned long long *>(p);
+  }
+  *out = g_noalloc_dev_ptr[dev];
+  return QN_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int qn_abi_version(void) { return QN_ABI_VERSION; }
@@ -380,6 +420,21 @@ qn_status qlora_linear_bwd_dx(const qn_nf4 *Q, const uint16_t *dY, int64_t M, co
   qn::qlora_gemm_simt_kernel<true><<<grid, 256, 0, st>>>(view_of(Q), dY, M, v, A, r, dX);
   QN_LAUNCH_CHECK("qlora_gemm_simt_kernel<bwd>");
   return QN_OK;
+}
+
+qn_status nf4_quantize_noalloc(const void *W, qn_dtype wdt, const qn_nf4 *Q, void *stream) {
+  g_last_error.clear();
+  if (!tables_consistent()) return fail(QN_EUNSUPPORTED, "internal NF4 tables inconsistent");
+  QN_TRY(check_nf4(Q, true));
+  if (!W) return fail(QN_EINVAL, "W is NULL");
+  if (wdt != QN_F32 && wdt != QN_BF16) return fail(QN_EINVAL, "bad input dtype %d", (int)wdt);
+  if (!aligned(W, 16)) return fail(QN_EALIGN, "W not 16-byte aligned");
+  if (Q->d * Q->k > kNoallocMaxElements)
+    return fail(QN_ESHAPE, "nf4_quantize_noalloc: %lld elements exceed the maximum of 2^40 its static scratch covers",
+                (long long)(Q->d * Q->k));
+  unsigned long long *bins = nullptr;
+  QN_TRY(noalloc_bins(&bins));
+  return launch_quantize(W, wdt, Q, bins, static_cast<cudaStream_t>(stream));
 }
 
 qn_status qn_device_status(void *stream) {

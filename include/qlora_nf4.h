@@ -193,6 +193,27 @@ qn_status loftq_init(const float *W, int64_t d, int64_t k, int32_t r, float alph
                      void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * nf4_quantize_noalloc -- nf4_quantize without a caller workspace.  The
+ * method's pages have no counterpart to this entry point: it exists for
+ * callers that cannot call cudaMalloc (code running while another allocator
+ * owns the free device memory, or loops that cannot afford the device-wide
+ * synchronisation an allocation implies).  Arguments, results and errors are
+ * those of nf4_quantize; the 2 KiB of scratch the double-quantisation mean
+ * needs is a static device array inside the library, which every GPU that
+ * loads the library keeps until the process exits.
+ *   - The first call on each device looks up that array's device address
+ *     (cudaGetSymbolAddress) with the device current; make that first call
+ *     before any stream capture.
+ *   - The call clears the scratch itself on `stream` before using it.
+ *   - All calls share the one array: calls that overlap on the GPU (on
+ *     different streams, or from different host threads) race and may
+ *     return wrong constants.  Serialise them.
+ *   - Tensors above 2^40 elements are rejected with QN_ESHAPE.
+ *   - No device memory is allocated or freed.
+ */
+qn_status nf4_quantize_noalloc(const void *W, qn_dtype wdt, const qn_nf4 *Q, void *stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word that
  * bounded waits write.  Returns QN_OK, QN_ETIMEOUT, or QN_ECUDA.
  */

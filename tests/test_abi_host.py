@@ -108,3 +108,14 @@ def test_argument_errors_return_before_launch(qn):
                         1 << 30, None) == qn.QN_ESHAPE
     assert L.loftq_init(P, 64, 128, 8, 16.0, 5, 0, 8, 4, ctypes.byref(st), P, P, ctypes.addressof(res), P,
                         1 << 30, None) == qn.QN_ESHAPE
+
+
+def test_noalloc_quantize_argument_errors(qn):
+    L = qn.lib
+    P = 0x10000
+    assert L.nf4_quantize_noalloc(P, 0, None, None) == qn.QN_EINVAL
+    st = _struct(qn)
+    assert L.nf4_quantize_noalloc(P, 9, ctypes.byref(st), None) == qn.QN_EINVAL
+    assert L.nf4_quantize_noalloc(P + 8, 0, ctypes.byref(st), None) == qn.QN_EALIGN
+    huge = _struct(qn, d=1 << 21, k=1 << 20)          # 2^41 elements
+    assert L.nf4_quantize_noalloc(P, 0, ctypes.byref(huge), None) == qn.QN_ESHAPE
