@@ -39,7 +39,8 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 METRIC = "QLoRA NF4 linear GB/s (M=1) & TFLOP/s (M=4096); NF4 quantize GB/s"
-WORKLOAD = "llama7b-decode-set M=1: 32 layers x 7 NF4+DQ matrices (q,k,v,o 4096x4096; gate,up 11008x4096; down 4096x11008), LoRA r=64 alpha=16"
+WORKLOAD = ("llama7b-decode-set M=1: 32 layers x 7 NF4+DQ matrices (q,k,v,o 4096x4096; gate,up 11008x4096; "
+            "down 4096x11008), LoRA r=64 alpha=16; per layer 4 calls: grouped q/k/v, o, grouped gate/up, down")
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -144,62 +145,104 @@ def build_decode_set(qn, device, layers: int, r: int, seed: int):
     return mats
 
 
-def time_decode(qn, mats, M, steps, warmup, ws, device, alpha=16.0):
-    """Timed region: `steps` replays of a CUDA graph holding one pass over all
-    matrices (two kernel launches per matrix).  Also times, per matrix shape,
-    a graph of that shape's calls alone to get the mean duration of one call."""
+GROUPS = [("qkv", ["q_proj", "k_proj", "v_proj"]), ("o", ["o_proj"]), ("gate_up", ["gate_proj", "up_proj"]),
+          ("down", ["down_proj"])]
+
+
+def decode_plan(mats, layers, M, device, seed=101):
+    """Calls of one decode step: per layer, the projections that share an
+    input run as one grouped call (q/k/v, gate/up), o and down alone.  Every
+    call reads its input from one packed X buffer and writes into one packed
+    Y buffer, so a step's host<->device traffic is one copy each way."""
+    by = {}
+    for i, (name, q, A, B) in enumerate(mats):
+        by.setdefault(i // 7, {})[name] = (q, A, B)
+    calls, xoff, yoff = [], 0, 0
+    for layer in range(layers):
+        for gname, names in GROUPS:
+            members = [by[layer][n] for n in names]
+            k = members[0][0].k
+            calls.append(dict(kind=gname, qs=[m[0] for m in members], As=[m[1] for m in members],
+                              Bs=[m[2] for m in members], k=k, xoff=xoff,
+                              youts=[(yoff + sum(mm[0].d for mm in members[:j]), m[0].d) for j, m in enumerate(members)]))
+            xoff += M * k
+            yoff += sum(m[0].d for m in members)
     gen = torch.Generator(device=device)
-    gen.manual_seed(101)
-    xs = {}
-    for _, q, _, _ in mats:
-        if q.k not in xs:
-            xs[q.k] = torch.randn((M, q.k), device=device, generator=gen).to(torch.bfloat16)
-    outs = [torch.empty((M, q.d), dtype=torch.bfloat16, device=device) for _, q, _, _ in mats]
+    gen.manual_seed(seed)
+    Xall = torch.randn(xoff, device=device, generator=gen).to(torch.bfloat16)
+    Yall = torch.empty(yoff * M, dtype=torch.bfloat16, device=device)
+    return calls, Xall, Yall
 
-    def calls(sel):
-        for i in sel:
-            _, q, A, B = mats[i]
-            qn.qlora_linear_fwd(q, xs[q.k], A, B, alpha, out=outs[i])
 
-    def capture(sel):
-        s = torch.cuda.Stream(device)
-        s.wait_stream(torch.cuda.current_stream(device))
-        with torch.cuda.stream(s):
-            calls(sel)                      # warm-up outside the graph
-        torch.cuda.current_stream(device).wait_stream(s)
-        torch.cuda.synchronize(device)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            calls(sel)
-        return g
+def run_calls(qn, calls, Xall, Yall, M, alpha=16.0, sel=None):
+    for c in (calls if sel is None else [calls[i] for i in sel]):
+        X = Xall[c["xoff"]:c["xoff"] + M * c["k"]].view(M, c["k"])
+        outs = [Yall[o * M:(o + d) * M].view(M, d) for o, d in c["youts"]]
+        qn.qlora_linear_fwd_group(c["qs"], X, c["As"], c["Bs"], [alpha] * len(c["qs"]), outs=outs)
 
-    def timed(g, reps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(device)
-        e0.record()
-        for _ in range(reps):
-            g.replay()
-        e1.record()
-        torch.cuda.synchronize(device)
-        return e0.elapsed_time(e1)
 
-    g_all = capture(range(len(mats)))
+def capture(device, fn):
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        fn()                      # warm-up outside the graph
+    torch.cuda.current_stream(device).wait_stream(s)
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def timed_replays(device, g, reps, pre=None, post=None):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    e0.record()
+    for _ in range(reps):
+        if pre is not None:
+            pre()
+        g.replay()
+        if post is not None:
+            post()
+    e1.record()
+    torch.cuda.synchronize(device)
+    return e0.elapsed_time(e1)
+
+
+def time_decode(qn, mats, layers, M, steps, warmup, ws, device):
+    """Timed region: `steps` replays of a CUDA graph holding one decode step.
+    Also times, per kind of call, a graph of that kind's calls alone to get
+    the mean duration of one launch."""
+    calls, Xall, Yall = decode_plan(mats, layers, M, device)
+    g_all = capture(device, lambda: run_calls(qn, calls, Xall, Yall, M))
     for _ in range(warmup):
         g_all.replay()
     torch.cuda.synchronize(device)
     barrier(ws)
-    total_ms = timed(g_all, steps)
-    call_ms = {}
-    by_shape = {}
-    for i, (_, q, _, _) in enumerate(mats):
-        by_shape.setdefault((q.d, q.k), []).append(i)
-    for shp, sel in by_shape.items():
-        g = capture(sel)
+    total_ms = timed_replays(device, g_all, steps)
+    per_kind = {}
+    for kind, _ in GROUPS:
+        sel = [i for i, c in enumerate(calls) if c["kind"] == kind]
+        g = capture(device, lambda: run_calls(qn, calls, Xall, Yall, M, sel=sel))
         g.replay()
         reps = max(2, steps // 2)
-        call_ms[shp] = (timed(g, reps) / (reps * len(sel)), len(sel))
+        ms = timed_replays(device, g, reps) / (reps * len(sel))
+        c0 = calls[sel[0]]
+        w4 = sum(q.nbytes() for q in c0["qs"])
+        byt = w4 + sum(2 * A.shape[0] * (q.d + q.k) for q, A in zip(c0["qs"], c0["As"])) \
+            + 2 * M * c0["k"] + sum(2 * M * q.d for q in c0["qs"])
+        per_kind[kind] = {"us": ms * 1e3, "bytes": byt, "weight_bytes": w4, "gbs": byt / (ms * 1e-3) / 1e9,
+                          "launches": len(sel)}
         del g
-    return {"total_ms": total_ms, "call_ms": call_ms}
+    # end to end: host inputs in, host outputs out, every step
+    Xh = torch.empty(Xall.shape, dtype=Xall.dtype, pin_memory=True).copy_(Xall.cpu())
+    Yh = torch.empty(Yall.shape, dtype=Yall.dtype, pin_memory=True)
+    e2e_steps = max(2, steps // 2)
+    e2e_ms = timed_replays(device, g_all, e2e_steps, pre=lambda: Xall.copy_(Xh, non_blocking=True),
+                           post=lambda: Yh.copy_(Yall, non_blocking=True))
+    h2d, d2h = Xall.numel() * 2, Yall.numel() * 2
+    return {"total_ms": total_ms, "per_kind": per_kind, "e2e_ms": e2e_ms, "e2e_steps": e2e_steps, "h2d": h2d,
+            "d2h": d2h, "launches_per_step": len(calls)}
 
 
 def decode_bytes(mats, M, r):
@@ -207,34 +250,6 @@ def decode_bytes(mats, M, r):
     lora = sum(2 * r * (q.d + q.k) for _, q, _, _ in mats)
     act = sum(2 * M * (q.d + q.k) for _, q, _, _ in mats)
     return w4, lora, act
-
-
-def time_e2e_decode(qn, mats, M, steps, warmup, device, alpha=16.0):
-    """The same step through the public API with HOST buffers: X is copied
-    from pinned host memory and Y read back to the host for every matrix."""
-    xs = {}
-    for _, q, _, _ in mats:
-        if q.k not in xs:
-            xs[q.k] = torch.randn((M, q.k)).to(torch.bfloat16).pin_memory()
-    youts = [torch.empty((M, q.d), dtype=torch.bfloat16).pin_memory() for _, q, _, _ in mats]
-
-    def one_step():
-        for i, (_, q, A, B) in enumerate(mats):
-            qn.qlora_linear_fwd(q, xs[q.k], A, B, alpha, out=youts[i])
-
-    for _ in range(warmup):
-        one_step()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(steps):
-        one_step()
-    t1.record()
-    torch.cuda.synchronize()
-    h2d = sum(2 * M * q.k for _, q, _, _ in mats)
-    d2h = sum(2 * M * q.d for _, q, _, _ in mats)
-    return t0.elapsed_time(t1), h2d, d2h
 
 
 def secondary(qn, device, pk, quick: bool):
@@ -284,22 +299,36 @@ def secondary(qn, device, pk, quick: bool):
     deq = [torch.empty_like(t) for t in srcs]
     n_params = sum(t.numel() for t in srcs)
     qbytes = sum(2 * t.numel() + qq.nbytes() for t, qq in zip(srcs, qs))
+    def graph_of(fn):
+        st = torch.cuda.Stream(device)
+        st.wait_stream(torch.cuda.current_stream(device))
+        with torch.cuda.stream(st):
+            fn()
+        torch.cuda.current_stream(device).wait_stream(st)
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return g
+
     for name, fn, nbytes in (
             ("quantize", lambda: [qn.nf4_quantize(t, True, out=qq) for t, qq in zip(srcs, qs)], qbytes),
             ("dequantize", lambda: [qn.nf4_dequantize(qq, torch.bfloat16, out=o) for qq, o in zip(qs, deq)], qbytes)):
-        fn()
+        g = graph_of(fn)
+        g.replay()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps = 2
+        reps = 3
         e0.record()
         for _ in range(reps):
-            fn()
+            g.replay()
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / reps
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[name] = {"ms": ms, "gbs": gbs, "frac_of_hbm": gbs / pk["hbm_gbs"], "params": n_params,
-                     "bytes": nbytes, "workload": f"{layers} layers x 7 bf16 matrices, NF4+DQ"}
+                     "bytes": nbytes, "workload": f"{layers} layers x 7 bf16 matrices, NF4+DQ, one CUDA graph"}
+        del g
     del srcs, qs, deq
 
     # LoftQ
@@ -404,36 +433,30 @@ def main():
     mats = build_decode_set(qn, device, args.layers, r, seed=1 + rank)
 
     with ClockSampler(local) as clk:
-        res = time_decode(qn, mats, 1, args.steps, args.warmup, ws, device)
+        res = time_decode(qn, mats, args.layers, 1, args.steps, args.warmup, ws, device)
     clocks = clk.summary()
     total_ms = max_over_ranks(res["total_ms"], ws)
     w4, lora, act = decode_bytes(mats, 1, r)
     value = w4 * args.steps * ws / (total_ms * 1e-3) / 1e9
 
-    # roofline of the dominant call (the fused M=1 forward of one matrix),
-    # per shape: algorithmic bytes / mean CUDA-event duration of one call
-    # (from graphs of that shape's calls back to back).
-    shapes, tot_bytes, tot_ms = {}, 0.0, 0.0
-    for (d, k), (ms, cnt) in res["call_ms"].items():
-        q0 = next(q for _, q, _, _ in mats if (q.d, q.k) == (d, k))
-        byt = q0.nbytes() + 2 * r * (d + k) + 2 * (d + k) + 4 * r
-        shapes[f"{d}x{k}"] = {"us": ms * 1e3, "bytes": byt, "gbs": byt / (ms * 1e-3) / 1e9, "calls": cnt}
-        tot_bytes += byt * cnt
-        tot_ms += ms * cnt
-    achieved = tot_bytes / (tot_ms * 1e-3) / 1e9
+    # roofline of the dominant kernel (qlora_decode_kernel, one launch per
+    # call): algorithmic bytes per launch / mean CUDA-event launch duration,
+    # weighted over the four kinds of call of a decode step.
+    tot_bytes = sum(v["bytes"] * v["launches"] for v in res["per_kind"].values())
+    tot_s = sum(v["us"] * 1e-6 * v["launches"] for v in res["per_kind"].values())
+    achieved = tot_bytes / tot_s / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"], "traffic": None,
-                "kernel": "qlora_linear_fwd at M=1 (lora_proj + fused NF4 GEMV), per call",
-                "peak_source": pk["source"], "per_shape": shapes}
-
-    e2e_ms, h2d, d2h = time_e2e_decode(qn, mats, 1, max(2, args.steps // 2), 2, device)
-    e2e_steps = max(2, args.steps // 2)
-    e2e = {"value": w4 * e2e_steps / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h}
+                "kernel": "qlora_decode_kernel (M=1; 4-bit weight + LoRA A, B + x + y bytes per launch)",
+                "peak_source": pk["source"], "per_call": res["per_kind"]}
+    e2e = {"value": w4 * res["e2e_steps"] / (res["e2e_ms"] * 1e-3) / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+           "how": "per step: one pinned-host->device copy of all inputs, the graph of public-API calls, "
+                  "one device->pinned-host copy of all outputs"}
 
     extra = {}
     if rank == 0:
-        r16 = time_decode(qn, mats, 16, max(3, args.steps // 2), 2, 1, device)
+        r16 = time_decode(qn, mats, args.layers, 16, max(3, args.steps // 2), 2, 1, device)
         extra["decode_M16"] = {"gbs": w4 * max(3, args.steps // 2) / (r16["total_ms"] * 1e-3) / 1e9,
                                "unit": "GB/s of 4-bit weight bytes"}
     del mats
@@ -458,7 +481,7 @@ def main():
                            "l2": "no flush: 3.34 GB weight set per step >> 126 MB L2",
                            "parallelism": f"replica x{ws}"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": 2 * 7 * args.layers * args.steps, "clocks": clocks, "secondary": extra}
+                "gpu_launches": res["launches_per_step"] * args.steps, "clocks": clocks, "secondary": extra}
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()

@@ -69,6 +69,8 @@ def _load():
                                       P(qn_nf4), vp, vp, vp, vp, sz, vp]),
         "qn_device_status": (ctypes.c_int, [vp]),
         "nf4_quantize_noalloc": (ctypes.c_int, [vp, ctypes.c_int, P(qn_nf4), vp]),
+        "qlora_linear_fwd_group": (ctypes.c_int, [i32, P(P(qn_nf4)), vp, i64, P(vp), P(vp), P(i32), P(f32), P(vp),
+                                                  vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -80,7 +82,7 @@ def _load():
 lib = _load()
 EXPORTS = ("qn_abi_version", "qn_last_error", "qn_nf4_tables", "qn_workspace_bytes", "nf4_quantize",
            "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd_dx", "loftq_init", "qn_device_status",
-           "nf4_quantize_noalloc")
+           "nf4_quantize_noalloc", "qlora_linear_fwd_group")
 
 
 def _check(status: int):
@@ -115,7 +117,7 @@ def _workspace(nbytes: int, device) -> torch.Tensor | None:
     key = (str(device), torch.cuda.current_stream(device).cuda_stream)
     ws = _WS.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+        ws = torch.zeros(nbytes + 512, dtype=torch.uint8, device=device)  # semaphore area starts at zero
         _WS[key] = ws
     return ws
 
@@ -236,6 +238,29 @@ def qlora_linear_fwd(q: NF4Tensor, X: torch.Tensor, A: torch.Tensor, B: torch.Te
         Yh.copy_(Y, non_blocking=True)
         return Yh
     return Y
+
+
+def qlora_linear_fwd_group(qs, X: torch.Tensor, As, Bs, alphas, outs=None, stream=None):
+    """Several projections of one input: Y[g] = X deq(Q[g])^T + (alpha[g]/r[g]) (X A[g]^T) B[g]^T."""
+    n = len(qs)
+    k = qs[0].k
+    Xd = _dev_bf16(X, "X").reshape(-1, k)
+    M = Xd.shape[0]
+    As = [_dev_bf16(a, "A") for a in As]
+    Bs = [_dev_bf16(b, "B") for b in Bs]
+    rs = [a.shape[0] for a in As]
+    Ys = list(outs) if outs is not None else [torch.empty((M, q.d), dtype=torch.bfloat16, device=q.device) for q in qs]
+    structs = [q.c_struct() for q in qs]
+    QP = (ctypes.POINTER(qn_nf4) * n)(*[ctypes.pointer(st) for st in structs])
+    AP = (ctypes.c_void_p * n)(*[a.data_ptr() for a in As])
+    BP = (ctypes.c_void_p * n)(*[b.data_ptr() for b in Bs])
+    YP = (ctypes.c_void_p * n)(*[y.data_ptr() for y in Ys])
+    RP = (ctypes.c_int32 * n)(*rs)
+    FP = (ctypes.c_float * n)(*[float(a) for a in alphas])
+    ws = _workspace(workspace_bytes(QN_OP_LINEAR_FWD, M, sum(q.d for q in qs), k, sum(rs)), qs[0].device)
+    wp, wn = _ws_ptr(ws)
+    _check(lib.qlora_linear_fwd_group(n, QP, Xd.data_ptr(), M, AP, BP, RP, FP, YP, wp, wn, _stream_ptr(stream)))
+    return Ys
 
 
 def qlora_linear_bwd_dx(q: NF4Tensor, dY: torch.Tensor, A: torch.Tensor, B: torch.Tensor, alpha: float,

@@ -14,6 +14,7 @@
 #include "common.cuh"
 #include "nf4_codec.cuh"
 #include "qlora_simt.cuh"
+#include "qlora_decode.cuh"
 #include "qlora_tc.cuh"
 #include "loftq.cuh"
 
@@ -100,6 +101,12 @@ struct Span {  // bump allocator over the caller's workspace
 
 size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
+// The first kSemBytes of every workspace are a zero area: semaphores
+// (grid-wide counters) and accumulators that must be zero before the first
+// call on that workspace; every kernel that uses them returns them to zero
+// before it exits.  Every other scratch buffer lives after it.
+constexpr size_t kSemBytes = 256 * 1024;
+
 qn_status check_nf4(const qn_nf4 *Q, bool need_dq_ptrs) {
   if (!Q) return fail(QN_EINVAL, "Q is NULL");
   if (Q->block != 64) return fail(QN_EUNSUPPORTED, "block must be 64 (got %d)", Q->block);
@@ -128,30 +135,20 @@ QnNF4View view_of(const qn_nf4 *Q) {
   return v;
 }
 
-constexpr size_t kQuantWs = qn::kNumBins * sizeof(unsigned long long);
+constexpr size_t kQuantWs = kSemBytes + qn::kNumBins * sizeof(unsigned long long);
 
-// Quantise n elements (internal; arguments already checked).
+// Quantise n elements (internal; arguments already checked).  `bins` (2 KiB)
+// and `ticket` (one word, zero on entry, zero again on exit) are scratch.
 qn_status launch_quantize(const void *W, qn_dtype wdt, const qn_nf4 *Q, unsigned long long *bins,
-                          cudaStream_t st) {
+                          unsigned int *ticket, cudaStream_t st) {
   const int64_t n = Q->d * Q->k;
   const int64_t nfull = n / 64;
   const int64_t nblk = qn_ceil_div(n, 64);
   unsigned long long *b = Q->dq ? bins : nullptr;
-  if (b) QN_TRY(cuda_check(cudaMemsetAsync(b, 0, kQuantWs, st), "memset bins"));
+  if (b) QN_TRY(cuda_check(cudaMemsetAsync(b, 0, qn::kNumBins * sizeof(unsigned long long), st), "memset bins"));
   const int sms = sm_count();
-  if (nfull > 0) {
-    const int64_t bpc = (qn::kQuantThreads / 32) * (wdt == QN_F32 ? 2 : 4);  // blocks per CTA-iteration
-    int64_t grid = qn_ceil_div(nfull, bpc);
-    const int64_t cap = static_cast<int64_t>(sms) * 8;
-    if (grid > cap) grid = cap;
-    if (wdt == QN_F32)
-      qn::nf4_quant_kernel<float><<<static_cast<unsigned>(grid), qn::kQuantThreads, 0, st>>>(
-          static_cast<const float *>(W), nfull, Q->codes, Q->absmax, b);
-    else
-      qn::nf4_quant_kernel<__nv_bfloat16><<<static_cast<unsigned>(grid), qn::kQuantThreads, 0, st>>>(
-          static_cast<const __nv_bfloat16 *>(W), nfull, Q->codes, Q->absmax, b);
-    QN_LAUNCH_CHECK("nf4_quant_kernel");
-  }
+  // The partial last block goes first: its constant must be in the bins
+  // before the main kernel's last CTA forms the mean.
   if (nblk > nfull) {
     if (wdt == QN_F32)
       qn::nf4_quant_tail_kernel<float><<<1, 32, 0, st>>>(static_cast<const float *>(W), n, nfull, Q->codes,
@@ -161,13 +158,27 @@ qn_status launch_quantize(const void *W, qn_dtype wdt, const qn_nf4 *Q, unsigned
                                                                  Q->codes, Q->absmax, b);
     QN_LAUNCH_CHECK("nf4_quant_tail_kernel");
   }
+  {
+    const int64_t bpc = (qn::kQuantThreads / 32) * (wdt == QN_F32 ? 4 : 8);  // blocks per CTA-iteration
+    int64_t grid = qn_ceil_div(nfull, bpc);
+    const int64_t cap = static_cast<int64_t>(sms) * 4;  // resident CTAs (registers, 31 KB of shared tables)
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    if (wdt == QN_F32)
+      qn::nf4_quant_kernel<float><<<static_cast<unsigned>(grid), qn::kQuantThreads, 0, st>>>(
+          static_cast<const float *>(W), nfull, nblk, Q->codes, Q->absmax, b, ticket, Q->absmax_mean);
+    else
+      qn::nf4_quant_kernel<__nv_bfloat16><<<static_cast<unsigned>(grid), qn::kQuantThreads, 0, st>>>(
+          static_cast<const __nv_bfloat16 *>(W), nfull, nblk, Q->codes, Q->absmax, b, ticket, Q->absmax_mean);
+    QN_LAUNCH_CHECK("nf4_quant_kernel");
+  }
   if (Q->dq) {
     const int64_t ngrp = qn_ceil_div(nblk, 256);
     int64_t grid = qn_ceil_div(ngrp, qn::kDqWarps);
     const int64_t cap = static_cast<int64_t>(sms) * 4;
     if (grid > cap) grid = cap;
     qn::nf4_dq_kernel<<<static_cast<unsigned>(grid), qn::kDqWarps * 32, 0, st>>>(
-        Q->absmax, nblk, b, Q->absmax_q, Q->absmax_scale, Q->absmax_mean);
+        Q->absmax, nblk, Q->absmax_mean, Q->absmax_q, Q->absmax_scale);
     QN_LAUNCH_CHECK("nf4_dq_kernel");
   }
   return QN_OK;
@@ -209,21 +220,116 @@ GemvPlan gemv_plan(int64_t d, int64_t k) {
   return p;
 }
 
+bool use_decode(int64_t M, int64_t d, int64_t k) { return M == 1 && k <= qn::kDecMaxK && d <= qn::kDecMaxD; }
+
+// r: sum of the ranks of a group.
+size_t decode_ws_bytes(int64_t, int64_t k, int32_t r) {
+  return round256(static_cast<size_t>(r) * static_cast<size_t>(qn_ceil_div(k, qn::kDecPiece)) * sizeof(float)) +
+         round256(static_cast<size_t>(r) * sizeof(float));
+}
+
 size_t fwd_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
-  size_t b = round256(static_cast<size_t>(M) * r * sizeof(float));  // u
+  if (use_decode(M, d, k)) return kSemBytes + decode_ws_bytes(d, k, r);
+  size_t b = kSemBytes + round256(static_cast<size_t>(M) * r * sizeof(float));  // u
   if (M <= qn::kGemvMaxM) {
-    const GemvPlan p = gemv_plan(d, k);
-    if (p.splits > 1) {
-      b += round256(static_cast<size_t>(p.splits) * M * d * sizeof(float));
-      b += round256(static_cast<size_t>(p.row_groups) * sizeof(unsigned int));
-    }
+    // sized for the largest split count, so that the size grows with d (a
+    // group's query with the summed d covers each member)
+    b += round256(static_cast<size_t>(16) * M * d * sizeof(float));
+    b += round256(static_cast<size_t>(qn_ceil_div(d, qn::kGemvWarps)) * sizeof(unsigned int));
   }
   b += qn::tc_ws_bytes(M, d, k, r);
   return b;
 }
 
 size_t bwd_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
-  return round256(static_cast<size_t>(M) * r * sizeof(float)) + qn::tc_ws_bytes(M, k, d, r);
+  return kSemBytes + round256(static_cast<size_t>(M) * r * sizeof(float)) + qn::tc_ws_bytes(M, k, d, r);
+}
+
+// Launch with programmatic stream serialisation (PDL): the kernel may start
+// before the previous kernel on the stream has finished; the kernels
+// themselves call griddepcontrol.wait before touching anything that the
+// previous kernel may write.
+template <typename... KArgs, typename... Args>
+qn_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     const char *what, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  QN_TRY(cuda_check(cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...), what));
+  QN_LAUNCH_CHECK(what);
+  return QN_OK;
+}
+
+// Single-token forward of a group of projections of one input: one
+// persistent kernel (every CTA resident, at least one per SM); its counters
+// and row accumulators live in the zero area.
+qn_status launch_decode_group(int n, const qn_nf4 *const *Q, const uint16_t *X, const uint16_t *const *A,
+                              const uint16_t *const *B, const int32_t *r, const float *alpha, uint16_t *const *Y,
+                              unsigned int *zero_area, Span &sp, cudaStream_t st) {
+  const int64_t k = Q[0]->k;
+  const size_t smem = qn::dec_smem_bytes(k);
+  static int attr_set[64] = {0};
+  int dev = 0;
+  QN_TRY(cuda_check(cudaGetDevice(&dev), "cudaGetDevice"));
+  if (dev < 0 || dev >= 64) return fail(QN_EUNSUPPORTED, "device ordinal out of range");
+  if (!attr_set[dev]) {
+    QN_TRY(cuda_check(cudaFuncSetAttribute(qn::qlora_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(qn::dec_smem_bytes(qn::kDecMaxK))),
+                      "cudaFuncSetAttribute(decode smem)"));
+    attr_set[dev] = 1;
+  }
+  int per_sm = 0;
+  QN_TRY(cuda_check(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qn::qlora_decode_kernel, qn::kDecThreads,
+                                                                  smem), "occupancy query"));
+  if (per_sm < 1) return fail(QN_EUNSUPPORTED, "decode kernel does not fit on an SM");
+  const int64_t nsteps = qn_ceil_div(k / 32, 32);
+  const int64_t nparts = qn_ceil_div(nsteps, qn::kDecUnitSteps);
+  const int64_t KC = qn_ceil_div(k, qn::kDecPiece);
+  qn::DecGroup g = {};
+  g.n = n;
+  g.k = k;
+  g.X = X;
+  int64_t units = 0, adapters = 0, quads = 0, rows = 0, us = 0;
+  for (int i = 0; i < n; ++i) {
+    qn::DecProj &p = g.p[i];
+    p.q = view_of(Q[i]);
+    p.A = A[i];
+    p.B = B[i];
+    p.Y = Y[i];
+    p.r = r[i];
+    p.s = alpha[i] / static_cast<float>(r[i]);
+    p.unit_off = units;
+    p.adapter_off = adapters;
+    p.quad_off = quads;
+    p.row_off = rows;
+    p.u_off = us;
+    const int64_t nq = qn_ceil_div(Q[i]->d, qn::kDecRows);
+    units += nq * nparts;
+    adapters += static_cast<int64_t>(r[i]) * KC;
+    quads += nq;
+    rows += Q[i]->d;
+    us += r[i];
+  }
+  g.nunits = units;
+  g.nadapter = adapters;
+  const int64_t sms = sm_count();
+  int64_t grid = qn_ceil_div(units, qn::kDecWarps);
+  if (grid < sms) grid = sms;
+  if (grid > sms * per_sm) grid = sms * per_sm;
+  if (units > grid * qn::kDecWarps * qn::kDecMaxSlots)
+    return fail(QN_EUNSUPPORTED, "decode kernel: too many weight units for the resident grid");
+  float *upart = sp.take<float>(static_cast<size_t>(adapters));
+  float *u = sp.take<float>(static_cast<size_t>(us));
+  qn::qlora_decode_kernel<<<static_cast<unsigned>(grid), qn::kDecThreads, smem, st>>>(g, zero_area, upart, u);
+  QN_LAUNCH_CHECK("qlora_decode_kernel");
+  return QN_OK;
 }
 
 qn_status check_layer(const qn_nf4 *Q, const void *in, int64_t M, const void *A, const void *B, int32_t r,
@@ -246,18 +352,18 @@ qn_status check_layer(const qn_nf4 *Q, const void *in, int64_t M, const void *A,
 // code that runs while another allocator owns all free device memory (a
 // framework's pre-reserved pool), or a latency-bound loop that must not pay
 // the implicit device-wide synchronisation of an allocation.  For them the
-// 2 KiB of exponent bins the quantiser needs live in this file-scope device
-// array.  Every GPU that loads the library holds it until the process exits.
+// exponent bins and the ticket word the quantiser needs (2 KiB + 256 B) live
+// in this file-scope device array.  Every GPU that loads the library holds it until the process exits.
 // In host code the name is only a host-side stand-in: the device address is
 // obtained once per device with cudaGetSymbolAddress and passed to the kernels.
 // ---------------------------------------------------------------------------
-static __device__ __align__(256) unsigned long long g_noalloc_bins[qn::kNumBins];
+static __device__ __align__(256) unsigned long long g_noalloc_bins[qn::kNumBins + 32];  // bins, then a ticket word
 
 namespace {
 
 constexpr int kNoallocMaxDevices = 64;
 // Largest tensor nf4_quantize_noalloc accepts: 2^40 elements keeps every
-// 64-bit bin of the fixed 2 KiB scratch exact (at most 2^34 block constants,
+// 64-bit bin of the fixed scratch exact (at most 2^34 block constants,
 // each adding a significand below 2^24).
 constexpr int64_t kNoallocMaxElements = int64_t(1) << 40;
 std::mutex g_noalloc_mutex;
@@ -301,7 +407,7 @@ size_t qn_workspace_bytes(qn_op op, int64_t M, int64_t d, int64_t k, int32_t r) 
     case QN_OP_LOFTQ: {
       if (d < 1 || k < 1) return 0;
       const size_t P = qn::kLqMaxP;
-      size_t b = round256(static_cast<size_t>(d) * k * sizeof(float));       // target / residual
+      size_t b = kSemBytes + round256(static_cast<size_t>(d) * k * sizeof(float));  // target / residual
       b += round256(static_cast<size_t>(d) * P * sizeof(float));            // Y
       b += 2 * round256(static_cast<size_t>(k) * P * sizeof(float));        // Zt, Omega
       b += round256(P * P * sizeof(double)) + round256(P * P * sizeof(float)) + round256(P * sizeof(float));  // G, V, lam
@@ -326,7 +432,8 @@ qn_status nf4_quantize(const void *W, qn_dtype wdt, const qn_nf4 *Q, void *ws, s
     if (ws_bytes < kQuantWs) return fail(QN_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, kQuantWs);
     if (!aligned(ws, 16)) return fail(QN_EALIGN, "workspace not 16-byte aligned");
   }
-  return launch_quantize(W, wdt, Q, static_cast<unsigned long long *>(ws), static_cast<cudaStream_t>(stream));
+  return launch_quantize(W, wdt, Q, reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kSemBytes),
+                         static_cast<unsigned int *>(ws), static_cast<cudaStream_t>(stream));
 }
 
 qn_status nf4_dequantize(const qn_nf4 *Q, void *Wout, qn_dtype odt, void *stream) {
@@ -349,7 +456,9 @@ qn_status qlora_linear_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M, const 
   if (!aligned(ws, 256)) return fail(QN_EALIGN, "workspace not 256-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Span sp{static_cast<char *>(ws), ws_bytes, 0};
+  unsigned int *sem = sp.take<unsigned int>(kSemBytes / sizeof(unsigned int));
   const float s = alpha / static_cast<float>(r);
+  if (use_decode(M, d, k)) return launch_decode_group(1, &Q, X, &A, &B, &r, &alpha, &Y, sem, sp, st);
   float *u = sp.take<float>(static_cast<size_t>(M) * r);
   if (M <= qn::kGemvMaxM) {
     {
@@ -393,6 +502,35 @@ qn_status qlora_linear_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M, const 
   return QN_OK;
 }
 
+qn_status qlora_linear_fwd_group(int32_t n, const qn_nf4 *const *Q, const uint16_t *X, int64_t M,
+                                 const uint16_t *const *A, const uint16_t *const *B, const int32_t *r,
+                                 const float *alpha, uint16_t *const *Y, void *ws, size_t ws_bytes, void *stream) {
+  g_last_error.clear();
+  if (n < 1 || n > qn::kDecMaxGroup) return fail(QN_ESHAPE, "group size must be in [1, %d]", qn::kDecMaxGroup);
+  if (!Q || !A || !B || !r || !alpha || !Y) return fail(QN_EINVAL, "NULL array");
+  int64_t dsum = 0, rsum = 0;
+  for (int i = 0; i < n; ++i) {
+    QN_TRY(check_layer(Q[i], X, M, A[i], B[i], r[i], alpha[i], Y[i]));
+    if (Q[i]->k != Q[0]->k) return fail(QN_ESHAPE, "all projections of a group share k");
+    dsum += Q[i]->d;
+    rsum += r[i];
+  }
+  const int64_t k = Q[0]->k;
+  const size_t need = qn_workspace_bytes(QN_OP_LINEAR_FWD, M, dsum, k, static_cast<int32_t>(rsum));
+  if (!ws) return fail(QN_EINVAL, "workspace NULL");
+  if (ws_bytes < need) return fail(QN_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (!aligned(ws, 256)) return fail(QN_EALIGN, "workspace not 256-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (use_decode(M, dsum, k)) {
+    Span sp{static_cast<char *>(ws), ws_bytes, 0};
+    unsigned int *sem = sp.take<unsigned int>(kSemBytes / sizeof(unsigned int));
+    return launch_decode_group(n, Q, X, A, B, r, alpha, Y, sem, sp, st);
+  }
+  for (int i = 0; i < n; ++i)
+    QN_TRY(qlora_linear_fwd(Q[i], X, M, A[i], B[i], r[i], alpha[i], Y[i], ws, ws_bytes, stream));
+  return QN_OK;
+}
+
 qn_status qlora_linear_bwd_dx(const qn_nf4 *Q, const uint16_t *dY, int64_t M, const uint16_t *A, const uint16_t *B,
                               int32_t r, float alpha, uint16_t *dX, void *ws, size_t ws_bytes, void *stream) {
   g_last_error.clear();
@@ -404,6 +542,7 @@ qn_status qlora_linear_bwd_dx(const qn_nf4 *Q, const uint16_t *dY, int64_t M, co
   if (!aligned(ws, 256)) return fail(QN_EALIGN, "workspace not 256-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Span sp{static_cast<char *>(ws), ws_bytes, 0};
+  (void)sp.take<unsigned int>(kSemBytes / sizeof(unsigned int));
   const float s = alpha / static_cast<float>(r);
   float *v = sp.take<float>(static_cast<size_t>(M) * r);
   {
@@ -434,7 +573,10 @@ qn_status nf4_quantize_noalloc(const void *W, qn_dtype wdt, const qn_nf4 *Q, voi
                 (long long)(Q->d * Q->k));
   unsigned long long *bins = nullptr;
   QN_TRY(noalloc_bins(&bins));
-  return launch_quantize(W, wdt, Q, bins, static_cast<cudaStream_t>(stream));
+  unsigned int *ticket = reinterpret_cast<unsigned int *>(bins + qn::kNumBins);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  QN_TRY(cuda_check(cudaMemsetAsync(ticket, 0, sizeof(unsigned int), st), "clear scratch ticket"));
+  return launch_quantize(W, wdt, Q, bins, ticket, st);
 }
 
 qn_status qn_device_status(void *stream) {
@@ -470,6 +612,7 @@ qn_status loftq_init(const float *W, int64_t d, int64_t k, int32_t r, float alph
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   constexpr int P = qn::kLqMaxP;
   Span sp{static_cast<char *>(ws), ws_bytes, 0};
+  unsigned int *sem = sp.take<unsigned int>(kSemBytes / sizeof(unsigned int));  // zero on entry and exit
   float *Tbuf = sp.take<float>(static_cast<size_t>(d) * k);
   float *Y = sp.take<float>(static_cast<size_t>(d) * P);
   float *Zt = sp.take<float>(static_cast<size_t>(k) * P);
@@ -529,7 +672,7 @@ qn_status loftq_init(const float *W, int64_t d, int64_t k, int32_t r, float alph
   };
 
   // t = 0: Q_0 = NF4(W), residual without adapter.
-  QN_TRY(launch_quantize(W, QN_F32, Q, bins, st));
+  QN_TRY(launch_quantize(W, QN_F32, Q, bins, sem, st));
   qn::residual_kernel<<<sms * 8, 256, 0, st>>>(qv, W, Tbuf, n);
   QN_LAUNCH_CHECK("residual_kernel");
   QN_TRY(residual_norm(0, &resid[0]));
@@ -538,7 +681,7 @@ qn_status loftq_init(const float *W, int64_t d, int64_t k, int32_t r, float alph
     if (t > 1) {  // Q-step: Q_t = NF4(W - s B A)
       qn::lowrank_sub_kernel<<<sms * 8, 256, 0, st>>>(W, B, A, d, k, r, s, Tbuf);
       QN_LAUNCH_CHECK("lowrank_sub_kernel");
-      QN_TRY(launch_quantize(Tbuf, QN_F32, Q, bins, st));
+      QN_TRY(launch_quantize(Tbuf, QN_F32, Q, bins, sem, st));
       qn::residual_kernel<<<sms * 8, 256, 0, st>>>(qv, W, Tbuf, n);
       QN_LAUNCH_CHECK("residual_kernel");
     }

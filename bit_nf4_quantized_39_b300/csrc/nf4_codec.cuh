@@ -32,114 +32,6 @@ __device__ __forceinline__ void bin_add_shared(unsigned long long *s_bins, float
   if (sig) atomicAdd(&s_bins[e ? e : 1u], static_cast<unsigned long long>(sig));
 }
 
-template <typename T> struct QuantVec;
-template <> struct QuantVec<float> { static constexpr int kVec = 4; };
-template <> struct QuantVec<__nv_bfloat16> { static constexpr int kVec = 8; };
-
-// Loads kVec consecutive elements (16 bytes) as fp32.
-__device__ __forceinline__ void load_vec(const float *p, float (&v)[4]) {
-  const float4 t = __ldcs(reinterpret_cast<const float4 *>(p));
-  v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-}
-__device__ __forceinline__ void load_vec(const __nv_bfloat16 *p, float (&v)[8]) {
-  const uint4 t = __ldcs(reinterpret_cast<const uint4 *>(p));
-  const uint32_t w[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = __uint_as_float(w[i] << 16);
-    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
-// One group of G = 64 / kVec lanes owns one 64-element block per iteration.
-template <typename T>
-__global__ void __launch_bounds__(kQuantThreads)
-nf4_quant_kernel(const T *__restrict__ x, int64_t nfull, uint8_t *__restrict__ codes,
-                 float *__restrict__ absmax, unsigned long long *__restrict__ bins) {
-  constexpr int V = QuantVec<T>::kVec;
-  constexpr int G = 64 / V;        // lanes per block
-  constexpr int BPW = 32 / G;      // blocks per warp-iteration
-  __shared__ unsigned long long s_bins[kNumBins];
-  if (bins) {
-    for (int i = threadIdx.x; i < kNumBins; i += blockDim.x) s_bins[i] = 0ull;
-    __syncthreads();
-  }
-  const int lane = threadIdx.x & 31;
-  const int sub = lane / G;
-  const int li = lane % G;
-  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-
-  for (int64_t b0 = warp * BPW; b0 < nfull; b0 += nwarps * BPW) {
-    const int64_t blk = b0 + sub;
-    const bool valid = blk < nfull;
-    float v[V];
-    if (valid) {
-      load_vec(x + blk * 64 + li * V, v);
-    } else {
-#pragma unroll
-      for (int i = 0; i < V; ++i) v[i] = 0.f;
-    }
-    float m = 0.f;
-#pragma unroll
-    for (int i = 0; i < V; ++i) m = fmaxf(m, fabsf(v[i]));
-#pragma unroll
-    for (int off = G / 2; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-
-    uint32_t packed = 0;
-#pragma unroll
-    for (int i = 0; i < V; ++i) {
-      const float q = (m > 0.f) ? __fdiv_rn(v[i], m) : 0.f;
-      packed |= nf4_code_of(q) << (4 * i);
-    }
-    if (valid) {
-      if constexpr (V == 4) {
-        reinterpret_cast<uint16_t *>(codes + blk * 32)[li] = static_cast<uint16_t>(packed);
-      } else {
-        reinterpret_cast<uint32_t *>(codes + blk * 32)[li] = packed;
-      }
-      if (li == 0) {
-        absmax[blk] = m;
-        if (bins) bin_add_shared(s_bins, m);
-      }
-    }
-  }
-  if (bins) {
-    __syncthreads();
-    for (int i = threadIdx.x; i < kNumBins; i += blockDim.x)
-      if (s_bins[i]) atomicAdd(&bins[i], s_bins[i]);
-  }
-}
-
-// The final partial block: one warp, scalar loads.
-template <typename T>
-__global__ void nf4_quant_tail_kernel(const T *__restrict__ x, int64_t n, int64_t blk,
-                                      uint8_t *__restrict__ codes, float *__restrict__ absmax,
-                                      unsigned long long *__restrict__ bins) {
-  const int lane = threadIdx.x;
-  const int64_t base = blk * 64;
-  const int cnt = static_cast<int>(n - base);  // 1..63
-  float v0 = 0.f, v1 = 0.f;
-  const int e0 = 2 * lane, e1 = 2 * lane + 1;
-  if (e0 < cnt) v0 = static_cast<float>(x[base + e0]);
-  if (e1 < cnt) v1 = static_cast<float>(x[base + e1]);
-  float m = fmaxf(fabsf(v0), fabsf(v1));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  const uint32_t c0 = nf4_code_of(m > 0.f ? __fdiv_rn(v0, m) : 0.f);
-  const uint32_t c1 = nf4_code_of(m > 0.f ? __fdiv_rn(v1, m) : 0.f);
-  if (e0 < cnt) codes[blk * 32 + lane] = static_cast<uint8_t>(c0 | ((e1 < cnt) ? (c1 << 4) : 0u));
-  if (lane == 0) {
-    absmax[blk] = m;
-    if (bins) {
-      const uint32_t b = __float_as_uint(m);
-      const uint32_t e = (b >> 23) & 0xFFu;
-      const uint32_t sig = (b & 0x7FFFFFu) | (e ? 0x800000u : 0u);
-      if (sig) atomicAdd(&bins[e ? e : 1u], static_cast<unsigned long long>(sig));
-    }
-  }
-}
-
 // ---------------------------------------------------------------------------
 // Exact mean of the absmax constants, rounded once to fp32 (ties to even).
 // bins[e] holds sum of significands with exponent field e (bin 1 also holds
@@ -183,7 +75,7 @@ __device__ float exact_mean_from_bins(const unsigned long long *__restrict__ bin
   for (int i = 0; i < kLimbs; ++i) acc[i] = 0u;
   for (int j = 0; j < kNumBins / 32; ++j) {
     const int e = lane * (kNumBins / 32) + j;
-    const unsigned long long s = bins[e];
+    const unsigned long long s = __ldcg(bins + e);
     if (e >= 1 && s) limbs_add_shifted(acc, s, e - 1);
   }
 #pragma unroll
@@ -223,9 +115,14 @@ __device__ float exact_mean_from_bins(const unsigned long long *__restrict__ bin
     if (quo[i]) p = 32 * i + 31 - __clz(quo[i]);
   // Significand = quotient >> shift, shift = max(p - 23, 0) (2^-149 units).
   const int shift = p > 23 ? p - 23 : 0;
-  auto qbit = [&](int b) -> uint32_t { return (b < 0) ? 0u : (quo[b >> 5] >> (b & 31)) & 1u; };
-  uint32_t mant = 0;
-  for (int b = 0; b < 24; ++b) mant |= qbit(shift + b) << b;
+  // 24 quotient bits starting at bit `pos` (they span at most two limbs).
+  auto bits_at = [&](int pos) -> uint64_t {
+    const int li = pos >> 5, bi = pos & 31;
+    const uint64_t lo = quo[li];
+    const uint64_t hi = (li + 1 < kLimbs) ? quo[li + 1] : 0u;
+    return ((hi << 32) | lo) >> bi;
+  };
+  uint32_t mant = static_cast<uint32_t>(bits_at(shift) & 0xFFFFFFu);
   bool round_up;
   const bool odd = mant & 1u;
   if (shift == 0) {
@@ -234,9 +131,12 @@ __device__ float exact_mean_from_bins(const unsigned long long *__restrict__ bin
     const bool eq = (rem == count - rem);
     round_up = gt || (eq && odd);
   } else {
-    const bool guard = qbit(shift - 1);
+    const int gpos = shift - 1;
+    const bool guard = (quo[gpos >> 5] >> (gpos & 31)) & 1u;
     bool sticky = rem != 0;
-    for (int b = 0; b < shift - 1 && !sticky; ++b) sticky = qbit(b);
+    // bits strictly below gpos: whole limbs below, then a partial limb
+    for (int i = 0; i < (gpos >> 5) && !sticky; ++i) sticky = quo[i] != 0u;
+    if (!sticky && (gpos & 31)) sticky = (quo[gpos >> 5] & ((1u << (gpos & 31)) - 1u)) != 0u;
     round_up = guard && (sticky || odd);
   }
   int sh = shift;
@@ -248,24 +148,231 @@ __device__ float exact_mean_from_bins(const unsigned long long *__restrict__ bin
   return __uint_as_float(bits);
 }
 
-constexpr int kDqWarps = 8;
+// Each lane owns 32 input bytes of one block per iteration: 16 bf16 or 8 fp32.
+template <typename T> struct QuantVec;
+template <> struct QuantVec<float> { static constexpr int kVec = 8; };
+template <> struct QuantVec<__nv_bfloat16> { static constexpr int kVec = 16; };
 
-// One warp per group of 256 constants.  Every CTA first derives the mean
-// (identical in every CTA); CTA 0 stores it.
-__global__ void __launch_bounds__(kDqWarps * 32)
-nf4_dq_kernel(const float *__restrict__ absmax, int64_t nblk, const unsigned long long *__restrict__ bins,
-              int8_t *__restrict__ absmax_q, float *__restrict__ absmax_scale, float *__restrict__ absmax_mean) {
-  __shared__ float s_mu;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp == 0) {
-    const float mu = exact_mean_from_bins(bins, static_cast<uint64_t>(nblk));
-    if (lane == 0) {
-      s_mu = mu;
-      if (blockIdx.x == 0) *absmax_mean = mu;
+// Loads kVec consecutive elements (32 bytes) as fp32.
+__device__ __forceinline__ void load_vec(const float *p, float (&v)[8]) {
+  const float4 a = __ldcs(reinterpret_cast<const float4 *>(p));
+  const float4 b = __ldcs(reinterpret_cast<const float4 *>(p) + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load_vec(const __nv_bfloat16 *p, float (&v)[16]) {
+  const uint4 a = __ldcs(reinterpret_cast<const uint4 *>(p));
+  const uint4 b = __ldcs(reinterpret_cast<const uint4 *>(p) + 1);
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Nearest-level decision by bucket lookup.  A normalised value v in [-1, 1]
+// is bucketed by its sign, its exponent clamped below at 2^-6 and the top 3
+// bits of its significand (112 buckets).  Every bucket contains at most one
+// decision threshold, so code(v) = base[b] + (v > thr[b]) with thr[b] = +inf
+// when the bucket holds none.  Values below 2^-5 in magnitude are all code 7
+// (the smallest threshold magnitude is 0.0398), which is why the clamp at
+// 2^-6 is exact.  The table is rebuilt from the threshold constants by every
+// CTA (one entry per thread).
+// ---------------------------------------------------------------------------
+constexpr int kBuckets = 112;
+constexpr uint32_t kBucketKeyMin = 121u << 3;   // exponent 121 (2^-6), 3 significand bits
+
+struct BucketEntry { float thr; uint32_t base; };
+
+__device__ __forceinline__ void build_bucket_entry(int idx, BucketEntry *tab) {
+  const int neg = idx >= 56;
+  const int key = idx % 56;
+  const int e = 121 + (key >> 3), m3 = key & 7;
+  // |v| range of the bucket: [L, H) = [(8 + m3), (9 + m3)) * 2^(e - 130)
+  const float L = ldexpf(static_cast<float>(8 + m3), e - 130);
+  const float H = ldexpf(static_cast<float>(9 + m3), e - 130);
+  uint32_t base = 0;
+  float thr = __int_as_float(0x7f800000);  // +inf: no threshold inside
+  if (!neg) {       // v in [L, H): count thresholds below L, pick the one in [L, H)
+    for (int i = 0; i < 15; ++i) {
+      const float t = c_nf4_thresholds[i];
+      if (t < L) ++base;
+      else if (t < H) thr = t;
+    }
+  } else {          // v in (-H, -L]: count thresholds <= -H, pick the one in (-H, -L]
+    for (int i = 0; i < 15; ++i) {
+      const float t = c_nf4_thresholds[i];
+      if (t <= -H) ++base;
+      else if (t <= -L) thr = t;
     }
   }
+  tab[idx].thr = thr;
+  tab[idx].base = base;
+}
+
+// `tab` is the lane's column of the per-lane replicated table: entry b of
+// lane l sits at tab[b * 32 + l], so the 32 lanes of a warp never conflict on
+// a bank whatever buckets they hit.
+__device__ __forceinline__ uint32_t bucket_code(float v, const BucketEntry *tab) {
+  const uint32_t bits = __float_as_uint(v);
+  // |v| <= 1 gives key <= 48; the upper clamp only keeps non-finite inputs
+  // (outside the method's domain) inside the table.
+  const uint32_t key = min(max((bits & 0x7FFFFFFFu) >> 20, kBucketKeyMin) - kBucketKeyMin, 55u);
+  const BucketEntry en = tab[(key + (bits >> 31) * 56u) * 32u];
+  return en.base + ((v > en.thr) ? 1u : 0u);
+}
+
+// IEEE-correct x / m for |x| <= m with m in [2^-125, 2^125], from the
+// correctly rounded reciprocal rcp = RN(1/m): q0 = RN(x * rcp) is within one
+// ulp of x/m, the residual x - q0 * m is exact under one fused multiply-add,
+// and q0 + residual * rcp rounded once is RN(x/m) (Markstein's correction
+// theorem, P. Markstein, IBM J. Res. Dev. 34(1), 1990).  Two quotients at a
+// time with the packed fp32x2 operations of sm_100+.  Checked bit-exact
+// against the oracle's IEEE division on near-threshold inputs.
+__device__ __forceinline__ void div_pair_by_scale(float &x0, float &x1, unsigned long long m2,
+                                                  unsigned long long rcp2, unsigned long long nm2) {
+  unsigned long long x, q, res;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q) : "l"(x), "l"(rcp2));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(res) : "l"(q), "l"(nm2), "l"(x));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(res), "l"(rcp2), "l"(q));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(q));
+  (void)m2;
+}
+
+// Lanes in groups of G = 64 / kVec own one 64-element block each per
+// iteration; the last CTA to finish derives the double-quantisation mean
+// from the exact exponent-binned sum and resets the ticket counter.
+template <typename T>
+__global__ void __launch_bounds__(kQuantThreads)
+nf4_quant_kernel(const T *__restrict__ x, int64_t nfull, int64_t nblk, uint8_t *__restrict__ codes,
+                 float *__restrict__ absmax, unsigned long long *__restrict__ bins,
+                 unsigned int *__restrict__ ticket, float *__restrict__ absmax_mean) {
+  constexpr int V = QuantVec<T>::kVec;
+  constexpr int G = 64 / V;        // lanes per block
+  constexpr int BPW = 32 / G;      // blocks per warp-iteration
+  __shared__ unsigned long long s_bins[kNumBins];
+  __shared__ BucketEntry s_one[kBuckets];
+  __shared__ BucketEntry s_tab[kBuckets * 32];
+  __shared__ bool s_last;
+  for (int i = threadIdx.x; i < kNumBins; i += blockDim.x) s_bins[i] = 0ull;
+  if (threadIdx.x < kBuckets) build_bucket_entry(threadIdx.x, s_one);
   __syncthreads();
-  const float mu = s_mu;
+  for (int i = threadIdx.x; i < kBuckets * 32; i += blockDim.x) s_tab[i] = s_one[i >> 5];
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const BucketEntry *my_tab = s_tab + lane;
+  const int sub = lane / G;
+  const int li = lane % G;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+
+  for (int64_t b0 = warp * BPW; b0 < nfull; b0 += nwarps * BPW) {
+    const int64_t blk = b0 + sub;
+    const bool valid = blk < nfull;
+    float v[V];
+    if (valid) {
+      load_vec(x + blk * 64 + li * V, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < V; ++i) v[i] = 0.f;
+    }
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) m = fmaxf(m, fabsf(v[i]));
+#pragma unroll
+    for (int off = G / 2; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+
+    if (m >= 0x1.0p-125f && m <= 0x1.0p+125f) {
+      const float rcp = __frcp_rn(m);
+      unsigned long long rcp2, nm2;
+      asm("mov.b64 %0, {%1, %1};" : "=l"(rcp2) : "f"(rcp));
+      asm("mov.b64 %0, {%1, %1};" : "=l"(nm2) : "f"(-m));
+#pragma unroll
+      for (int i = 0; i < V; i += 2) div_pair_by_scale(v[i], v[i + 1], 0ull, rcp2, nm2);
+    } else {
+#pragma unroll
+      for (int i = 0; i < V; ++i) v[i] = (m > 0.f) ? __fdiv_rn(v[i], m) : 0.f;
+    }
+    if (valid) {
+      if constexpr (V == 8) {
+        uint32_t packed = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) packed |= bucket_code(v[i], my_tab) << (4 * i);
+        reinterpret_cast<uint32_t *>(codes + blk * 32)[li] = packed;
+      } else {
+        uint32_t p0 = 0, p1 = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) p0 |= bucket_code(v[i], my_tab) << (4 * i);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) p1 |= bucket_code(v[8 + i], my_tab) << (4 * i);
+        reinterpret_cast<uint2 *>(codes + blk * 32)[li] = make_uint2(p0, p1);
+      }
+      if (li == 0) {
+        absmax[blk] = m;
+        if (bins) bin_add_shared(s_bins, m);
+      }
+    }
+  }
+  if (!bins) return;
+  __syncthreads();
+  for (int i = threadIdx.x; i < kNumBins; i += blockDim.x)
+    if (s_bins[i]) atomicAdd(&bins[i], s_bins[i]);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(ticket, 1u) == gridDim.x - 1u);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (threadIdx.x < 32) {
+    const float mu = exact_mean_from_bins(bins, static_cast<uint64_t>(nblk));
+    if (threadIdx.x == 0) {
+      *absmax_mean = mu;
+      *ticket = 0u;
+    }
+  }
+}
+
+// The final partial block: one warp, scalar loads.
+template <typename T>
+__global__ void nf4_quant_tail_kernel(const T *__restrict__ x, int64_t n, int64_t blk,
+                                      uint8_t *__restrict__ codes, float *__restrict__ absmax,
+                                      unsigned long long *__restrict__ bins) {
+  const int lane = threadIdx.x;
+  const int64_t base = blk * 64;
+  const int cnt = static_cast<int>(n - base);  // 1..63
+  float v0 = 0.f, v1 = 0.f;
+  const int e0 = 2 * lane, e1 = 2 * lane + 1;
+  if (e0 < cnt) v0 = static_cast<float>(x[base + e0]);
+  if (e1 < cnt) v1 = static_cast<float>(x[base + e1]);
+  float m = fmaxf(fabsf(v0), fabsf(v1));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  const uint32_t c0 = nf4_code_of(m > 0.f ? __fdiv_rn(v0, m) : 0.f);
+  const uint32_t c1 = nf4_code_of(m > 0.f ? __fdiv_rn(v1, m) : 0.f);
+  if (e0 < cnt) codes[blk * 32 + lane] = static_cast<uint8_t>(c0 | ((e1 < cnt) ? (c1 << 4) : 0u));
+  if (lane == 0) {
+    absmax[blk] = m;
+    if (bins) {
+      const uint32_t b = __float_as_uint(m);
+      const uint32_t e = (b >> 23) & 0xFFu;
+      const uint32_t sig = (b & 0x7FFFFFu) | (e ? 0x800000u : 0u);
+      if (sig) atomicAdd(&bins[e ? e : 1u], static_cast<unsigned long long>(sig));
+    }
+  }
+}
+
+constexpr int kDqWarps = 8;
+
+// One warp per group of 256 constants; the mean was stored by the last CTA
+// of nf4_quant_kernel.
+__global__ void __launch_bounds__(kDqWarps * 32)
+nf4_dq_kernel(const float *__restrict__ absmax, int64_t nblk, const float *__restrict__ absmax_mean,
+              int8_t *__restrict__ absmax_q, float *__restrict__ absmax_scale) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float mu = __ldcg(absmax_mean);
   const int64_t ngrp = qn_ceil_div(nblk, 256);
   for (int64_t g = static_cast<int64_t>(blockIdx.x) * kDqWarps + warp; g < ngrp;
        g += static_cast<int64_t>(gridDim.x) * kDqWarps) {

@@ -1,0 +1,459 @@
+// qlora_decode.cuh -- single-token (M = 1) fused QLoRA forward of a group of
+// projections of one input, in one kernel:
+//
+//   Y_g = x deq(Q_g)^T + s_g (x A_g^T) B_g^T      x: 1 x k bf16, Q_g: d_g x k NF4
+//
+// ("PEFT course notes" §2.2, h = Wx + BAx; "QLoRA paper summary": the frozen
+// weight is 4-bit NF4.)  A single projection is the group of one; several
+// projections of the same activation (query/key/value, gate/up) share one
+// launch so that their memory round trips overlap.  The call is bound by the
+// bytes of the packed weights; at decode sizes (8-45 MB per launch) what
+// limits it is how many bytes each SM keeps in flight and how many dependent
+// round trips a warp makes, so:
+//
+// * persistent grid (every CTA resident, at least one per SM);
+// * every weight is cut into units of 4 rows x 2048 columns; the units of all
+//   projections form one list; unit u goes to warp slot u mod W with slots
+//   interleaved across CTAs, so every SM gets an equal share; a warp issues
+//   the loads of its next unit before it decodes the current one;
+// * decode: x is staged once per CTA in shared memory as fp32, lane-
+//   interleaved so that each lane's 32-element chunk is read with
+//   conflict-free 128-bit loads; two codes at a time are looked up in a
+//   byte-pair table of bf16 levels replicated per lane (entry b of lane l at
+//   word 32 b + l, so a warp never conflicts on a bank), widened to fp32 and
+//   multiplied into packed fp32x2 accumulators (fma.rn.f32x2); each
+//   32-element partial is scaled by its 64-block constant;
+// * the row sums of a unit are added into per-row fp32 accumulators; the
+//   warp that completes the last unit of a quad (per-quad counter) takes the
+//   sums with an atomic exchange (which also returns them to zero), adds
+//   u . B[row] and writes bf16 Y;
+// * the down-projections u_g = s_g A_g x are split into (row of A,
+//   256-column piece) units done by all warps first; the last CTA to finish
+//   them sums every u_g once and raises a flag that finishing warps wait on
+//   (bounded spin, no trap).
+//
+// Workspace: the counters and row accumulators live in the caller's zero
+// area (zero before the first call; every call leaves it zero); the adapter
+// partials and u live after it.
+#pragma once
+
+#include "common.cuh"
+
+namespace qn {
+
+constexpr int kDecThreads = 256;
+constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kDecRows = 4;            // weight rows per warp item
+constexpr int kDecDepth = 2;           // lane steps whose loads are in flight together
+constexpr int kDecLutWords = 256 * 32;
+constexpr int kDecMaxK = 16384;
+constexpr int kDecUnitSteps = 2;       // 1024-column lane steps per unit (2048 columns)
+constexpr int kDecPiece = 256;         // elements of an A row per adapter unit
+constexpr int kDecMaxUnitsPerWarp = 2;   // adapter units whose loads go out in the prologue
+constexpr int kDecMaxSlots = 16;         // weight units per warp (partials kept in shared memory)
+constexpr unsigned kDecSpinLimit = 1u << 22;
+// Zero area layout (32-bit words): flags, then per-quad counters, then row sums.
+constexpr int kDecFlagArrive = 0, kDecFlagUReady = 1, kDecFlagExit = 2;
+constexpr int64_t kDecQuadCtrOffset = 64;          // words
+constexpr int64_t kDecRowSumOffset = 16384;        // words (64 KiB)
+constexpr int64_t kDecMaxD = 32768;            // sum of d over a group
+constexpr int kDecMaxGroup = 8;
+
+// One projection of a group (device pointers; k is shared by the group).
+struct DecProj {
+  QnNF4View q;
+  const uint16_t *A;   // r x k bf16
+  const uint16_t *B;   // d x r bf16
+  uint16_t *Y;         // d bf16
+  int r;
+  float s;
+  int64_t unit_off;    // first unit of this projection in the group's list
+  int64_t adapter_off; // first adapter unit
+  int64_t quad_off;    // first per-quad counter
+  int64_t row_off;     // first row accumulator
+  int64_t u_off;       // first element of u
+};
+struct DecGroup {
+  DecProj p[kDecMaxGroup];
+  int n;
+  int64_t k;
+  int64_t nunits, nadapter;  // totals
+  const uint16_t *X;
+};
+
+// Staging covers whole 1024-element steps so that ragged tails read zeros.
+__host__ __device__ constexpr int64_t dec_xs_floats(int64_t k) { return qn_ceil_div(k, 1024) * 1024; }
+__host__ __device__ constexpr size_t dec_smem_bytes(int64_t k) {
+  return sizeof(uint32_t) * kDecLutWords + sizeof(float) * dec_xs_floats(k);
+}
+
+__device__ __forceinline__ unsigned long long pack_f2(float lo, float hi) {
+  unsigned long long v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));
+  return v;
+}
+__device__ __forceinline__ float sum_f2(unsigned long long v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo + hi;
+}
+// acc += a * b on both halves (packed fp32x2 FMA, sm_100+).
+__device__ __forceinline__ void ffma2(unsigned long long &acc, unsigned long long a, unsigned long long b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
+// Position of element e of x in the lane-interleaved staging buffer: the
+// 32-element chunk c = e/32 belongs to lane c % 32 at step c / 32; within a
+// step, float4 e4 of lane l sits at float4 index (step * 8 + e4) * 32 + l.
+__device__ __forceinline__ int64_t dec_xs_index(int64_t e) {
+  const int64_t c = e >> 5;
+  const int o = static_cast<int>(e & 31);
+  return ((((c >> 5) * 8 + (o >> 2)) * 32 + (c & 31)) << 2) + (o & 3);
+}
+
+// One lane step of 4 rows as loaded: code chunks plus the raw constants of
+// their 64-block (int8 code and group scale, or the exact absmax).  The
+// block constant is formed only when the step is decoded, so that no load
+// of a step waits on another.
+struct DecStep {
+  uint4 w[kDecRows];
+  float sc[kDecRows];   // group scale sigma (dq) or exact absmax
+  int qv[kDecRows];     // int8 code of the constant (dq)
+};
+
+// Loads lane step `st` of the 4 rows starting at row0 (codes and constants).
+__device__ __forceinline__ void dec_load_step(const QnNF4View &q, int64_t row0, int64_t st, int lane,
+                                              DecStep &out) {
+  const int64_t d = q.d, k = q.k;
+  const int64_t nchunk = k >> 5, kb = k >> 6;
+  const int64_t c = st * 32 + lane;
+#pragma unroll
+  for (int rr = 0; rr < kDecRows; ++rr) {
+    const int64_t row = row0 + rr;
+    if (row < d && c < nchunk) {
+      out.w[rr] = __ldcs(reinterpret_cast<const uint4 *>(q.codes + row * (k >> 1)) + c);
+      const int64_t blk = row * kb + (c >> 1);
+      if (q.dq) {
+        out.qv[rr] = __ldg(q.absmax_q + blk);
+        out.sc[rr] = __ldg(q.absmax_scale + (blk >> 8));
+      } else {
+        out.qv[rr] = 0;
+        out.sc[rr] = __ldg(q.absmax + blk);
+      }
+    } else {
+      out.w[rr] = make_uint4(0x77777777u, 0x77777777u, 0x77777777u, 0x77777777u);  // level 7 = 0.0
+      out.qv[rr] = 0;
+      out.sc[rr] = 0.f;
+    }
+  }
+}
+
+// Block constant of a loaded step: fp32(fp32(q * sigma) + mu) or the absmax.
+__device__ __forceinline__ float dec_step_scale(const DecStep &sp, int rr, bool dq, float mu) {
+  return dq ? dq_absmax(static_cast<int8_t>(sp.qv[rr]), sp.sc[rr], mu) : sp.sc[rr];
+}
+
+// Adds the dot products of one lane step of 4 rows with the staged x.
+__device__ __forceinline__ void dec_compute_step(const DecStep &sp, int64_t st, const float *__restrict__ xs,
+                                                 const uint32_t *__restrict__ lut, int lane, bool dq, float mu,
+                                                 float (&rsum)[kDecRows]) {
+  const float4 *xp = reinterpret_cast<const float4 *>(xs) + st * 8 * 32 + lane;
+  unsigned long long acc[kDecRows];
+#pragma unroll
+  for (int rr = 0; rr < kDecRows; ++rr) acc[rr] = pack_f2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 x0 = xp[(2 * i) * 32], x1 = xp[(2 * i + 1) * 32];
+    const unsigned long long xpair[4] = {pack_f2(x0.x, x0.y), pack_f2(x0.z, x0.w), pack_f2(x1.x, x1.y),
+                                         pack_f2(x1.z, x1.w)};
+#pragma unroll
+    for (int rr = 0; rr < kDecRows; ++rr) {
+      const uint32_t word = (i == 0) ? sp.w[rr].x : (i == 1) ? sp.w[rr].y : (i == 2) ? sp.w[rr].z : sp.w[rr].w;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const uint32_t v = lut[(((word >> (8 * b)) & 0xFFu) << 5) | lane];
+        ffma2(acc[rr], pack_f2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u)), xpair[b]);
+      }
+    }
+  }
+#pragma unroll
+  for (int rr = 0; rr < kDecRows; ++rr) rsum[rr] = fmaf(sum_f2(acc[rr]), dec_step_scale(sp, rr, dq, mu), rsum[rr]);
+}
+
+// s * A[j, piece] . x for one adapter unit (lane holds 8 A values in av).
+__device__ __forceinline__ float dec_adapter_unit(const uint4 &av, int64_t e0, const float *__restrict__ xs) {
+  const float4 x0 = *reinterpret_cast<const float4 *>(xs + dec_xs_index(e0));
+  const float4 x1 = *reinterpret_cast<const float4 *>(xs + dec_xs_index(e0 + 4));
+  float acc = 0.f;
+  acc = fmaf(__uint_as_float(av.x << 16), x0.x, acc);
+  acc = fmaf(__uint_as_float(av.x & 0xFFFF0000u), x0.y, acc);
+  acc = fmaf(__uint_as_float(av.y << 16), x0.z, acc);
+  acc = fmaf(__uint_as_float(av.y & 0xFFFF0000u), x0.w, acc);
+  acc = fmaf(__uint_as_float(av.z << 16), x1.x, acc);
+  acc = fmaf(__uint_as_float(av.z & 0xFFFF0000u), x1.y, acc);
+  acc = fmaf(__uint_as_float(av.w << 16), x1.z, acc);
+  acc = fmaf(__uint_as_float(av.w & 0xFFFF0000u), x1.w, acc);
+  return acc;
+}
+
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Index of the projection that owns list position `pos` given the
+// per-projection offsets `off` (ascending, off[0] = 0).
+template <typename F>
+__device__ __forceinline__ int dec_find(const DecGroup &g, int64_t pos, F off) {
+  int i = 0;
+#pragma unroll
+  for (int t = 1; t < kDecMaxGroup; ++t)
+    if (t < g.n && pos >= off(g.p[t])) i = t;
+  return i;
+}
+
+__global__ void __launch_bounds__(kDecThreads, 2)
+qlora_decode_kernel(const __grid_constant__ DecGroup g, unsigned int *__restrict__ zero_area,
+                    float *__restrict__ upart, float *__restrict__ u) {
+  extern __shared__ __align__(16) unsigned char dec_smem[];
+  uint32_t *lut = reinterpret_cast<uint32_t *>(dec_smem);
+  float *xs = reinterpret_cast<float *>(dec_smem + sizeof(uint32_t) * kDecLutWords);
+  unsigned int *flags = zero_area;
+  unsigned int *quad_ctr = zero_area + kDecQuadCtrOffset;
+  float *rowsum = reinterpret_cast<float *>(zero_area + kDecRowSumOffset);
+  const int64_t k = g.k;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x;
+  const int64_t nsteps = qn_ceil_div(k >> 5, 32);
+  const int64_t nparts = qn_ceil_div(nsteps, kDecUnitSteps);  // units per quad
+  const int64_t KC = qn_ceil_div(k, kDecPiece);
+  // warp slots interleaved across CTAs: slot = warp * G + cta
+  const int64_t wslot = static_cast<int64_t>(warp) * G + blockIdx.x;
+  const int64_t W = static_cast<int64_t>(G) * kDecWarps;
+  auto unit_of = [](const DecProj &p) { return p.unit_off; };
+  auto adapter_of = [](const DecProj &p) { return p.adapter_off; };
+
+  auto load_unit = [&](int64_t unit, DecStep (&pp)[kDecUnitSteps]) {
+    const DecProj &p = g.p[dec_find(g, unit, unit_of)];
+    const int64_t local = unit - p.unit_off;
+    const int64_t quad = local / nparts, part = local % nparts;
+#pragma unroll
+    for (int t = 0; t < kDecUnitSteps; ++t)
+      dec_load_step(p.q, quad * kDecRows, part * kDecUnitSteps + t, lane, pp[t]);
+  };
+  auto adapter_load = [&](int64_t unit) -> uint4 {
+    const DecProj &p = g.p[dec_find(g, unit, adapter_of)];
+    const int64_t local = unit - p.adapter_off;
+    const int64_t j = local / KC, e0 = (local % KC) * kDecPiece + lane * 8;
+    return (e0 < k) ? __ldg(reinterpret_cast<const uint4 *>(p.A + j * k + e0)) : make_uint4(0u, 0u, 0u, 0u);
+  };
+
+  // ---- prologue: independent loads first ------------------------------------
+  DecStep pipe[kDecUnitSteps];
+  if (warp != 0 && wslot < g.nunits) load_unit(wslot, pipe);
+  uint4 av[kDecMaxUnitsPerWarp];
+#pragma unroll
+  for (int i = 0; i < kDecMaxUnitsPerWarp; ++i) {
+    const int64_t unit = wslot + i * W;
+    av[i] = (unit < g.nadapter) ? adapter_load(unit) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  __shared__ uint32_t s_lv[16];
+  if (tid < 16) s_lv[tid] = f32_to_bf16_bits(c_nf4_levels[tid]);
+  {
+    constexpr int kPer = 8;  // 16-byte x loads in flight per thread per round
+    const int64_t nvec = dec_xs_floats(k) / 8;
+    for (int64_t base = 0; base < nvec; base += static_cast<int64_t>(kDecThreads) * kPer) {
+      uint4 t[kPer];
+#pragma unroll
+      for (int v = 0; v < kPer; ++v) {
+        const int64_t vi = base + v * kDecThreads + tid;
+        t[v] = (vi * 8 < k) ? __ldg(reinterpret_cast<const uint4 *>(g.X) + vi) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int v = 0; v < kPer; ++v) {
+        const int64_t vi = base + v * kDecThreads + tid;
+        if (vi < nvec) {
+          const int64_t e = vi * 8;  // 8 consecutive elements: two float4 groups of one lane
+          *reinterpret_cast<float4 *>(xs + dec_xs_index(e)) =
+              make_float4(__uint_as_float(t[v].x << 16), __uint_as_float(t[v].x & 0xFFFF0000u),
+                          __uint_as_float(t[v].y << 16), __uint_as_float(t[v].y & 0xFFFF0000u));
+          *reinterpret_cast<float4 *>(xs + dec_xs_index(e + 4)) =
+              make_float4(__uint_as_float(t[v].z << 16), __uint_as_float(t[v].z & 0xFFFF0000u),
+                          __uint_as_float(t[v].w << 16), __uint_as_float(t[v].w & 0xFFFF0000u));
+        }
+      }
+    }
+  }
+  __syncthreads();  // s_lv and xs ready
+  for (int i = tid; i < kDecLutWords; i += kDecThreads) {
+    const int b = i >> 5;
+    lut[i] = (s_lv[b >> 4] << 16) | s_lv[b & 15];
+  }
+
+  // ---- adapter partials: upart[adapter unit] = s * A[j, piece] . x ---------
+  for (int64_t unit = wslot, i = 0; unit < g.nadapter; unit += W, ++i) {
+    const DecProj &p = g.p[dec_find(g, unit, adapter_of)];
+    const int64_t local = unit - p.adapter_off;
+    const int64_t e0 = (local % KC) * kDecPiece + lane * 8;
+    uint4 a;
+    if (i < kDecMaxUnitsPerWarp) a = (i == 0) ? av[0] : av[kDecMaxUnitsPerWarp - 1];
+    else a = adapter_load(unit);
+    float acc = (e0 < k) ? dec_adapter_unit(a, e0, xs) : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) upart[unit] = p.s * acc;
+  }
+  __syncthreads();  // lut ready; this CTA's adapter partials written
+  // Arrival: warp 0 alone (the other warps go straight to the weights).  The
+  // last CTA to arrive forms every u_g with warp 0 and raises the flag.
+  if (warp == 0) {
+    int last = 0;
+    if (lane == 0) {
+      __threadfence();
+      last = (atomicAdd(&flags[kDecFlagArrive], 1u) == static_cast<unsigned>(G) - 1u);
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+      __threadfence();
+      // lane j sums the KC partials of u_g[j]; loads in batches of 8
+      for (int pi = 0; pi < g.n; ++pi) {
+        const DecProj &p = g.p[pi];
+        for (int j = lane; j < p.r; j += 32) {
+          const float *src = upart + p.adapter_off + static_cast<int64_t>(j) * KC;
+          float acc = 0.f;
+          for (int64_t kc0 = 0; kc0 < KC; kc0 += 8) {
+            float t[8];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) t[v] = (kc0 + v < KC) ? __ldcg(src + kc0 + v) : 0.f;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) acc += t[v];
+          }
+          u[p.u_off + j] = acc;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        atomicExch(&flags[kDecFlagUReady], 1u);
+      }
+    }
+  }
+
+  if (warp == 0 && wslot < g.nunits) load_unit(wslot, pipe);
+
+  // ---- main loop over units: decode only, partial row sums to shared memory --
+  // (No fence or returning atomic here: either would wait for the loads of
+  // the next unit that are already in flight.)
+  __shared__ float s_part[kDecWarps][kDecMaxSlots][kDecRows];
+  int nslot = 0;
+  for (int64_t unit = wslot; unit < g.nunits; unit += W, ++nslot) {
+    DecStep cur[kDecUnitSteps];
+#pragma unroll
+    for (int t = 0; t < kDecUnitSteps; ++t) cur[t] = pipe[t];
+    if (unit + W < g.nunits) load_unit(unit + W, pipe);
+    const DecProj &p = g.p[dec_find(g, unit, unit_of)];
+    const int64_t local = unit - p.unit_off;
+    const int64_t part = local % nparts;
+    const float mu = p.q.dq ? __ldg(p.q.absmax_mean) : 0.f;
+    float rsum[kDecRows] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int t = 0; t < kDecUnitSteps; ++t) {
+      const int64_t st = part * kDecUnitSteps + t;
+      if (st < nsteps) dec_compute_step(cur[t], st, xs, lut, lane, p.q.dq != 0, mu, rsum);
+    }
+#pragma unroll
+    for (int rr = 0; rr < kDecRows; ++rr) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) rsum[rr] += __shfl_xor_sync(0xffffffffu, rsum[rr], off);
+    }
+    if (lane < kDecRows && nslot < kDecMaxSlots) {
+      float v = rsum[0];
+#pragma unroll
+      for (int rr = 1; rr < kDecRows; ++rr) if (lane == rr) v = rsum[rr];
+      s_part[warp][nslot][lane] = v;
+    }
+  }
+  __syncwarp();
+
+  // ---- combine: add partials, then one fence, then count arrivals per quad --
+  if (nparts > 1) {
+    int sl = 0;
+    for (int64_t unit = wslot; unit < g.nunits && sl < kDecMaxSlots; unit += W, ++sl) {
+      const DecProj &p = g.p[dec_find(g, unit, unit_of)];
+      const int64_t quad = (unit - p.unit_off) / nparts;
+      const int64_t row = quad * kDecRows + lane;
+      if (lane < kDecRows && row < p.q.d) atomicAdd(&rowsum[p.row_off + row], s_part[warp][sl][lane]);
+    }
+    __threadfence();
+    __syncwarp();
+  }
+  bool have_u = false;
+  {
+    int sl = 0;
+    for (int64_t unit = wslot; unit < g.nunits && sl < kDecMaxSlots; unit += W, ++sl) {
+      const DecProj &p = g.p[dec_find(g, unit, unit_of)];
+      const int64_t d = p.q.d;
+      const int64_t quad = (unit - p.unit_off) / nparts;
+      const int64_t row0 = quad * kDecRows;
+      float total = 0.f;  // lane rr < 4: final row sum of row0 + rr
+      if (nparts == 1) {
+        if (lane < kDecRows) total = s_part[warp][sl][lane];
+      } else {
+        unsigned int prev = 0;
+        if (lane == 0) prev = atomicAdd(&quad_ctr[p.quad_off + quad], 1u);
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev != static_cast<unsigned>(nparts) - 1u) continue;  // another warp finishes this quad
+        __threadfence();
+        if (lane < kDecRows && row0 + lane < d) total = atomicExch(&rowsum[p.row_off + row0 + lane], 0.f);
+        if (lane == 0) quad_ctr[p.quad_off + quad] = 0u;
+      }
+      // ---- finish the quad: y = row sum + u . B[row] ------------------------
+      if (!have_u) {
+        if (lane == 0) {
+          unsigned int spins = 0;
+          while (ld_acquire_u32(&flags[kDecFlagUReady]) == 0u) {
+            if (++spins > kDecSpinLimit) { qn_flag_timeout(); break; }
+            __nanosleep(20);
+          }
+        }
+        __syncwarp();
+        have_u = true;
+      }
+      float acc[kDecRows];
+#pragma unroll
+      for (int rr = 0; rr < kDecRows; ++rr) {
+        const int64_t row = row0 + rr;
+        float a = 0.f;
+        if (row < d)
+          for (int j = lane; j < p.r; j += 32)
+            a = fmaf(__ldcg(u + p.u_off + j), bf16_bits_to_f32(p.B[row * p.r + j]), a);
+        acc[rr] = a;
+      }
+#pragma unroll
+      for (int rr = 0; rr < kDecRows; ++rr) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc[rr] += __shfl_xor_sync(0xffffffffu, acc[rr], off);
+      }
+      if (lane < kDecRows && row0 + lane < d) {
+        float a = acc[0];
+#pragma unroll
+        for (int rr = 1; rr < kDecRows; ++rr) if (lane == rr) a = acc[rr];
+        p.Y[row0 + lane] = f32_to_bf16_bits(total + a);
+      }
+    }
+  }
+
+  // ---- exit: the last CTA returns the flags to zero ---------------------------
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned int prev = atomicAdd(&flags[kDecFlagExit], 1u);
+    if (prev == static_cast<unsigned>(G) - 1u) {
+      atomicExch(&flags[kDecFlagArrive], 0u);
+      atomicExch(&flags[kDecFlagUReady], 0u);
+      atomicExch(&flags[kDecFlagExit], 0u);
+    }
+  }
+}
+
+}  // namespace qn

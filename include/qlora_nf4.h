@@ -33,6 +33,10 @@
  *   aligned; pointers documented "host" are ordinary host memory.  The library
  *   allocates no device memory; scratch space is the caller's workspace `ws`
  *   of at least qn_workspace_bytes(...) bytes (device, 256-byte aligned).
+ *   The first 256 KiB of a workspace are a zero area (semaphores and
+ *   accumulators for grid-wide hand-offs): zero them once when the
+ *   workspace is allocated; every call leaves them zero again when its
+ *   kernels finish.  qn_workspace_bytes() includes them.
  * - Layout: matrices are row-major.  W (d x k) element (i, j) is at i*k + j;
  *   its flat element index e = i*k + j is what the 64-element blocks run over.
  * - bf16 buffers are passed as `uint16_t *` holding IEEE bfloat16 bit patterns.
@@ -166,6 +170,24 @@ qn_status qlora_linear_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M,
                            void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * qlora_linear_fwd_group -- several projections of one input in one call:
+ *   Y[g] = X deq(Q[g])^T + (alpha[g]/r[g]) (X A[g]^T) B[g]^T,  g < n,
+ * the layer of "PEFT course notes" §2.2 applied to a shared activation (the
+ * query/key/value or gate/up projections of a transformer block).
+ *   n      1..8 projections; Q, A, B, r, alpha, Y are host arrays of n entries
+ *          (each as in qlora_linear_fwd); every Q[g] has the same k.
+ *   X      device bf16 [M x k], shared.
+ *   ws     qn_workspace_bytes(QN_OP_LINEAR_FWD, M, sum of d, k, sum of r).
+ * With M == 1 (and sum of d <= 32768) the group runs as one kernel whose
+ * memory round trips overlap across projections; otherwise it is the n
+ * single calls in order.  Results equal those of n qlora_linear_fwd calls.
+ */
+qn_status qlora_linear_fwd_group(int32_t n, const qn_nf4 *const *Q, const uint16_t *X, int64_t M,
+                                 const uint16_t *const *A, const uint16_t *const *B, const int32_t *r,
+                                 const float *alpha, uint16_t *const *Y,
+                                 void *ws, size_t ws_bytes, void *stream);
+
+/*
  * qlora_linear_bwd_dx -- dX = dY deq(Q) + (alpha/r) (dY B) A.
  *   dY device bf16 [M x d]; A, B as in the forward; dX device bf16 [M x k].
  *   Same size rules and workspace query (QN_OP_LINEAR_BWD_DX).
@@ -198,7 +220,7 @@ qn_status loftq_init(const float *W, int64_t d, int64_t k, int32_t r, float alph
  * callers that cannot call cudaMalloc (code running while another allocator
  * owns the free device memory, or loops that cannot afford the device-wide
  * synchronisation an allocation implies).  Arguments, results and errors are
- * those of nf4_quantize; the 2 KiB of scratch the double-quantisation mean
+ * those of nf4_quantize; the 2.25 KiB of scratch the double-quantisation mean
  * needs is a static device array inside the library, which every GPU that
  * loads the library keeps until the process exits.
  *   - The first call on each device looks up that array's device address

@@ -141,6 +141,29 @@ def adversarial_block_values(seed: int, cb: np.ndarray, nblocks: int) -> np.ndar
     return np.concatenate(out)
 
 
+def near_point_blocks(seed: int, points: np.ndarray, nblocks: int, max_ulps: int = 4) -> np.ndarray:
+    """Blocks whose normalised values sit on or a few ulps around given points.
+
+    Each 64-element block gets a random scale m; element 0 is +-m (so the
+    block absmax is m) and the others are fp32(p * m) moved by up to
+    ``max_ulps`` ulps, for points p drawn from ``points`` (the caller passes
+    the decision boundaries it wants exercised)."""
+    g = rng(seed)
+    pts = np.asarray(points, dtype=np.float32)
+    out = []
+    for _ in range(nblocks):
+        m = np.float32(10.0 ** g.uniform(-5, 2))
+        p = pts[g.integers(0, pts.size, 64)]
+        v = (p * m).astype(np.float32)
+        ulps = g.integers(-max_ulps, max_ulps + 1, 64).astype(np.int32)
+        ulps[v == 0] = 0
+        v = (v.view(np.int32) + ulps).view(np.float32)
+        v = np.clip(v, -m, m).astype(np.float32)
+        v[0] = m if g.integers(0, 2) else -m
+        out.append(v)
+    return np.concatenate(out)
+
+
 # ---- device-side generators for the multi-gigabyte bench sets ----------------
 
 def device_normal_(t: torch.Tensor, std: float, gen: torch.Generator) -> torch.Tensor:

@@ -57,7 +57,7 @@ def test_tables_match_oracle_codebook_and_thresholds(qn):
 
 
 def test_workspace_queries(qn):
-    assert qn.workspace_bytes(qn.QN_OP_QUANTIZE, 0, 1024, 1024, 0) == 2048
+    assert qn.workspace_bytes(qn.QN_OP_QUANTIZE, 0, 1024, 1024, 0) == 256 * 1024 + 2048
     assert qn.workspace_bytes(qn.QN_OP_DEQUANTIZE, 0, 1024, 1024, 0) == 0
     assert qn.workspace_bytes(qn.QN_OP_LINEAR_FWD, 1, 4096, 4096, 64) >= 4 * 64
     assert qn.workspace_bytes(qn.QN_OP_LINEAR_FWD, 0, 4096, 4096, 64) == 0

@@ -68,6 +68,29 @@ def test_adversarial_blocks(qn, dq):
     assert np.array_equal(w.view(np.uint32), nf4.dequantize(ref).view(np.uint32))
 
 
+def _oracle_thresholds():
+    """Decision points of the oracle's codebook: exact midpoints, rounded to
+    fp32 both ways (the values a division lands on or next to)."""
+    from fractions import Fraction
+    cb = nf4.codebook()
+    pts = []
+    for i in range(15):
+        mid = (Fraction(float(cb[i])) + Fraction(float(cb[i + 1]))) / 2
+        f = np.float32(float(mid))
+        pts += [f, np.nextafter(f, np.float32(-1)), np.nextafter(f, np.float32(1))]
+    return np.array(pts + list(cb), dtype=np.float32)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_near_threshold_values(qn, dtype):
+    """Quotients x/m on and around every decision threshold: the GPU's
+    division and nearest-level decision must agree with IEEE division and the
+    brute-force argmin bit for bit."""
+    v = synth.near_point_blocks(seed=17, points=_oracle_thresholds(), nblocks=4000)
+    q, ref, _ = _quant_both(qn, v.reshape(250, -1), bf16=(dtype == "bf16"))
+    _check_state(q, ref)
+
+
 @pytest.mark.parametrize("n", [1, 2, 63, 64, 65, 127, 64 * 257 + 5, 1_000_003])
 def test_ragged_lengths(qn, n):
     g = np.random.default_rng(n)

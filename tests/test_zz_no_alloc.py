@@ -2,7 +2,7 @@
 
 It serves callers that cannot call cudaMalloc (another allocator owns the
 free device memory, or the caller's loop cannot take the device-wide
-synchronisation an allocation implies): its 2 KiB of scratch is a static
+synchronisation an allocation implies): its 2.25 KiB of scratch is a static
 device array inside the library.  This test calls it through the C ABI and
 checks every output against the allocating entry point nf4_quantize (the
 codec's tolerance: bit-exact), on two calls in a row with different inputs,
