@@ -345,6 +345,30 @@ qn_status check_layer(const qn_nf4 *Q, const void *in, int64_t M, const void *A,
   return QN_OK;
 }
 
+// Large-M forward on the tensor cores: split u into bf16 hi/lo halves, then
+// one CTA per 128 weight rows x 256 tokens (qlora_fwd_tc_kernel).
+qn_status launch_tc_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M, const float *u, const uint16_t *B, int32_t r,
+                        uint16_t *Y, Span &sp, cudaStream_t st) {
+  const int R = qn::tc_pad_r(r);
+  uint16_t *u2 = sp.take<uint16_t>(static_cast<size_t>(M) * 2 * R);
+  {
+    const int64_t n = M * R;
+    qn::u_split_kernel<<<static_cast<unsigned>(qn_ceil_div(n, 256)), 256, 0, st>>>(u, M, r, R, u2);
+    QN_LAUNCH_CHECK("u_split_kernel");
+  }
+  CUtensorMap xmap;
+  if (const char *e = qn::make_bf16_tile_map(&xmap, X, static_cast<uint64_t>(Q->k), static_cast<uint64_t>(M), qn::kTcBM))
+    return fail(QN_ECUDA, "tcgen05 forward: %s", e);
+  const size_t smem = qn::tc_smem_bytes(R);
+  QN_TRY(cuda_check(cudaFuncSetAttribute(qn::qlora_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(qn::tc_smem_bytes(qn::kTcMaxR))),
+                    "tcgen05 forward shared-memory limit"));
+  dim3 grid(static_cast<unsigned>(qn_ceil_div(Q->d, qn::kTcBN)), static_cast<unsigned>(qn_ceil_div(M, qn::kTcBM)));
+  qn::qlora_fwd_tc_kernel<<<grid, qn::kTcThreads, smem, st>>>(xmap, view_of(Q), M, B, r, R, u2, Y);
+  QN_LAUNCH_CHECK("qlora_fwd_tc_kernel");
+  return QN_OK;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -492,10 +516,7 @@ qn_status qlora_linear_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M, const 
     qn::lora_proj_kernel<<<grid, 256, 0, st>>>(X, M, k, A, r, k, 1, s, u);
     QN_LAUNCH_CHECK("lora_proj_kernel");
   }
-  if (qn::tc_supported(M, d, k, r)) {
-    return qn::launch_tc_fwd(view_of(Q), X, M, u, B, r, Y, sp, st) == 0 ? QN_OK
-                                                                        : fail(QN_ECUDA, "tcgen05 forward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
-  }
+  if (qn::tc_supported(M, d, k, r)) return launch_tc_fwd(Q, X, M, u, B, r, Y, sp, st);
   dim3 grid(static_cast<unsigned>(qn_ceil_div(d, qn::kTileN)), static_cast<unsigned>(qn_ceil_div(M, qn::kTileM)));
   qn::qlora_gemm_simt_kernel<false><<<grid, 256, 0, st>>>(view_of(Q), X, M, u, B, r, Y);
   QN_LAUNCH_CHECK("qlora_gemm_simt_kernel<fwd>");
@@ -550,10 +571,6 @@ qn_status qlora_linear_bwd_dx(const qn_nf4 *Q, const uint16_t *dY, int64_t M, co
     dim3 grid(static_cast<unsigned>(qn_ceil_div(M, qn::kProjTM)), static_cast<unsigned>(qn_ceil_div(r, qn::kProjTN)));
     qn::lora_proj_kernel<<<grid, 256, 0, st>>>(dY, M, d, B, r, 1, r, s, v);
     QN_LAUNCH_CHECK("lora_proj_kernel(dY B)");
-  }
-  if (qn::tc_bwd_supported(M, d, k, r)) {
-    return qn::launch_tc_bwd(view_of(Q), dY, M, v, A, r, dX, sp, st) == 0 ? QN_OK
-                                                                          : fail(QN_ECUDA, "tcgen05 backward launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   }
   dim3 grid(static_cast<unsigned>(qn_ceil_div(k, qn::kTileN)), static_cast<unsigned>(qn_ceil_div(M, qn::kTileM)));
   qn::qlora_gemm_simt_kernel<true><<<grid, 256, 0, st>>>(view_of(Q), dY, M, v, A, r, dX);

@@ -1,20 +1,413 @@
-// qlora_tc.cuh -- tensor-core (tcgen05) fused layer kernels.  Placeholder
-// interface: the tcgen05 path is not enabled in this build yet, so every
-// shape takes the CUDA-core kernels.
+// qlora_tc.cuh -- fused QLoRA forward on the 5th-generation tensor cores
+// (tcgen05, sm_100 family):
+//
+//   Y^T tile [128 weight rows x 256 tokens] = deq(Q) tile . X tile^T + B . U2^T
+//
+// Per CTA: one output tile, 192 threads in three roles.
+//   warps 0-3  dequantisers, then epilogue.  Thread i owns weight row
+//              n0 + i, which is tensor-memory lane i: per 64-column stage it
+//              loads its 32 code bytes, builds the 16 levels scaled by the
+//              block constant as bf16 (exactly bf16(fp32(c * m')), the value
+//              nf4_dequantize writes), selects them with byte permutes and
+//              writes the 64 bf16 weights straight into tensor memory with
+//              tcgen05.st -- the weight operand never touches shared memory.
+//   warp 4     TMA producer: X tiles (256 tokens x 64, 128-byte swizzle)
+//              into a 4-stage shared-memory ring.
+//   warp 5     allocates tensor memory and issues the MMAs (one elected
+//              thread): A = dequantised weights from tensor memory, B = X from
+//              shared memory, D = fp32 accumulator in tensor memory.
+// The adapter term s (X A^T) B^T enters as one more MMA with K = 2R: A holds
+// [B | B] (bf16, in tensor memory) and the shared-memory operand holds
+// U2 = [hi | lo] with hi = bf16(u), lo = bf16(u - hi), u = s X A^T, so the
+// product keeps about 16 significant bits of u.
+//
+// Tensor-memory columns: [0, 256) accumulator, [256, 384) four 32-column
+// weight stages, [384, 384 + R) the adapter operand.
 #pragma once
 
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace qn {
 
-inline size_t tc_ws_bytes(int64_t, int64_t, int64_t, int32_t) { return 0; }
-inline bool tc_supported(int64_t, int64_t, int64_t, int32_t) { return false; }
+constexpr int kTcBN = 128;   // weight rows per tile  (MMA M)
+constexpr int kTcBM = 256;   // tokens per tile       (MMA N)
+constexpr int kTcBK = 64;    // K per stage
+constexpr int kTcXStages = 4;
+constexpr int kTcAStages = 4;
+constexpr int kTcMaxR = 64;  // padded adapter rank R (multiple of 8)
+constexpr int kTcThreads = 192;
+constexpr uint32_t kTcXStageBytes = kTcBM * kTcBK * 2;  // 32 KiB
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCol = 0, kACol = 256, kLoraCol = 384;
+
+__host__ __device__ constexpr int tc_pad_r(int r) { return (r + 7) & ~7; }
+__host__ __device__ constexpr size_t tc_u_bytes(int R) { return static_cast<size_t>(kTcBM) * 2 * R * 2; }
+__host__ __device__ constexpr size_t tc_smem_bytes(int R) {
+  // 1024 alignment slack + X ring + U2 tile + barriers / bookkeeping
+  return 1024 + static_cast<size_t>(kTcXStages) * kTcXStageBytes + tc_u_bytes(R) + 256;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// Byte tables of the 16 scaled levels: L[i] / H[i] hold the low / high bytes
+// of the bf16 values of levels 4i .. 4i+3.
+struct ScaledLevels {
+  uint32_t L[4], H[4];
+};
+
+__device__ __forceinline__ ScaledLevels scaled_levels(float m) {
+  uint32_t P[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    P[j] = pack_bf16x2(__fmul_rn(c_nf4_levels[2 * j], m), __fmul_rn(c_nf4_levels[2 * j + 1], m));
+  ScaledLevels t;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    t.L[i] = prmt(P[2 * i], P[2 * i + 1], 0x6420u);
+    t.H[i] = prmt(P[2 * i], P[2 * i + 1], 0x7531u);
+  }
+  return t;
+}
+
+// Eight 4-bit codes (element 0 in the low nibble) -> four bf16x2 words.
+__device__ __forceinline__ void decode_word(uint32_t w, const ScaledLevels &t, uint32_t *out) {
+  const uint32_t sel = w & 0x77777777u;   // level index within its half of the table
+  const uint32_t w4 = w << 4;
+  // byte masks: 0xFF where the code's bit 3 is set (upper half of the table)
+  const uint32_t m_lo = prmt(w4, w, 0xD9C8u);
+  const uint32_t m_hi = prmt(w4, w, 0xFBEAu);
+  const uint32_t s_hi = sel >> 16;
+  {
+    const uint32_t la = prmt(t.L[0], t.L[1], sel), lb = prmt(t.L[2], t.L[3], sel);
+    const uint32_t ha = prmt(t.H[0], t.H[1], sel), hb = prmt(t.H[2], t.H[3], sel);
+    const uint32_t lo = (la & ~m_lo) | (lb & m_lo), hi = (ha & ~m_lo) | (hb & m_lo);
+    out[0] = prmt(lo, hi, 0x5140u);
+    out[1] = prmt(lo, hi, 0x7362u);
+  }
+  {
+    const uint32_t la = prmt(t.L[0], t.L[1], s_hi), lb = prmt(t.L[2], t.L[3], s_hi);
+    const uint32_t ha = prmt(t.H[0], t.H[1], s_hi), hb = prmt(t.H[2], t.H[3], s_hi);
+    const uint32_t lo = (la & ~m_hi) | (lb & m_hi), hi = (ha & ~m_hi) | (hb & m_hi);
+    out[2] = prmt(lo, hi, 0x5140u);
+    out[3] = prmt(lo, hi, 0x7362u);
+  }
+}
+
+struct TcBars {
+  uint64_t x_full[kTcXStages], x_empty[kTcXStages];
+  uint64_t a_full[kTcAStages], a_empty[kTcAStages];
+  uint64_t lora_full, acc_full, done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// u2[t, :] = [bf16(u) | bf16(u - bf16(u))] for t < M, zero-padded to R columns
+// each; u is the fp32 s X A^T of lora_proj_kernel.
+__global__ void u_split_kernel(const float *__restrict__ u, int64_t M, int r, int R, uint16_t *__restrict__ u2) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= M * R) return;
+  const int64_t t = i / R;
+  const int j = static_cast<int>(i % R);
+  const float v = (j < r) ? u[t * r + j] : 0.f;
+  const uint16_t hi = f32_to_bf16_bits(v);
+  const uint16_t lo = f32_to_bf16_bits(v - bf16_bits_to_f32(hi));
+  u2[t * 2 * R + j] = hi;
+  u2[t * 2 * R + R + j] = lo;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+qlora_fwd_tc_kernel(const __grid_constant__ CUtensorMap xmap, QnNF4View q, int64_t M,
+                    const uint16_t *__restrict__ Bm, int r, int R, const uint16_t *__restrict__ u2,
+                    uint16_t *__restrict__ Y) {
+  extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
+  unsigned char *base = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char *xring = base;
+  unsigned char *utile = base + kTcXStages * kTcXStageBytes;
+  TcBars *bars = reinterpret_cast<TcBars *>(utile + tc_u_bytes(R));
+  volatile int *abort = &bars->abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t d = q.d, k = q.k;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kTcBN;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kTcBM;
+  const int nk = static_cast<int>(k / kTcBK);
+
+  if (tid == 0) {
+    for (int i = 0; i < kTcXStages; ++i) {
+      mbar_init(smem_u32(&bars->x_full[i]), 1);
+      mbar_init(smem_u32(&bars->x_empty[i]), 1);
+    }
+    for (int i = 0; i < kTcAStages; ++i) {
+      mbar_init(smem_u32(&bars->a_full[i]), 4);  // one arrival per dequantiser warp
+      mbar_init(smem_u32(&bars->a_empty[i]), 1);
+    }
+    mbar_init(smem_u32(&bars->lora_full), 4);
+    mbar_init(smem_u32(&bars->acc_full), 1);
+    mbar_init(smem_u32(&bars->done), 1);
+    bars->abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) tma_prefetch_desc(&xmap);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp < 4) {
+    // ======================= dequantisers, then epilogue =======================
+    const int64_t n = n0 + tid;           // this thread's weight row = TMEM lane tid
+    const bool row_ok = n < d;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float mu = (q.dq && row_ok) ? __ldg(q.absmax_mean) : 0.f;
+    const int64_t kb = k >> 6;
+
+    // U2 tile into shared memory, canonical K-major layout without swizzle:
+    // 8-row x 16-byte core matrices, K-adjacent cores 128 B apart, row groups
+    // (2R/8) * 128 B apart.
+    {
+      const int kgroups = (2 * R) / 8;
+      for (int tt = tid; tt < kTcBM; tt += 128) {
+        const int64_t t = m0 + tt;
+        for (int g = 0; g < kgroups; ++g) {
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (t < M) v = __ldg(reinterpret_cast<const uint4 *>(u2 + t * 2 * R) + g);
+          const uint32_t off = ((tt >> 3) * kgroups + g) * 128 + (tt & 7) * 16;
+          *reinterpret_cast<uint4 *>(utile + off) = v;
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    // Adapter operand [B | B] of this row into tensor memory.
+    {
+      uint32_t v[32];
+      const int half = R / 2;  // words per copy
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const int j = 2 * (c % half);
+        uint32_t w = 0;
+        if (row_ok && c < 2 * half) {
+          const uint32_t lo = (j < r) ? Bm[n * r + j] : 0u;
+          const uint32_t hi = (j + 1 < r) ? Bm[n * r + j + 1] : 0u;
+          w = lo | (hi << 16);
+        }
+        v[c] = w;
+      }
+      tmem_st_x32(lane_addr + kLoraCol, v);
+      if (R > 32) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int cc = 32 + c;
+          const int j = 2 * (cc % half);
+          uint32_t w = 0;
+          if (row_ok && cc < 2 * half) {
+            const uint32_t lo = (j < r) ? Bm[n * r + j] : 0u;
+            const uint32_t hi = (j + 1 < r) ? Bm[n * r + j + 1] : 0u;
+            w = lo | (hi << 16);
+          }
+          v[c] = w;
+        }
+        tmem_st_x32(lane_addr + kLoraCol + 32, v);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->lora_full));
+    }
+
+    // Main dequantisation loop; codes and block constants run two stages
+    // ahead in a register pipeline (f0: stage s, f1: stage s + 1).
+    const uint4 *crow = reinterpret_cast<const uint4 *>(q.codes + (row_ok ? n : 0) * (k >> 1));
+    struct Fetch {
+      uint4 c0, c1;
+      float sc;
+      int qv;
+    };
+    auto fetch = [&](int s) {
+      Fetch f{make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), 0.f, 0};
+      if (row_ok && s < nk) {
+        f.c0 = __ldg(crow + 2 * s);
+        f.c1 = __ldg(crow + 2 * s + 1);
+        const int64_t blk = n * kb + s;
+        if (q.dq) {
+          f.qv = __ldg(q.absmax_q + blk);
+          f.sc = __ldg(q.absmax_scale + (blk >> 8));
+        } else {
+          f.sc = __ldg(q.absmax + blk);
+        }
+      }
+      return f;
+    };
+    Fetch f0 = fetch(0), f1 = fetch(1);
+    bool ok = true;
+    for (int s = 0; s < nk && ok; ++s) {
+      const uint4 c0 = f0.c0, c1 = f0.c1;
+      const float m = q.dq ? dq_absmax(static_cast<int8_t>(f0.qv), f0.sc, mu) : f0.sc;
+      f0 = f1;
+      f1 = fetch(s + 2);
+      const int st = s % kTcAStages;
+      if (s >= kTcAStages) ok = mbar_wait(smem_u32(&bars->a_empty[st]), ((s / kTcAStages) - 1) & 1, abort);
+      ok = __all_sync(0xffffffffu, ok);  // tcgen05.st is warp-collective: leave together
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t v[32];
+      if (row_ok) {
+        const ScaledLevels t = scaled_levels(m);
+        decode_word(c0.x, t, v + 0);
+        decode_word(c0.y, t, v + 4);
+        decode_word(c0.z, t, v + 8);
+        decode_word(c0.w, t, v + 12);
+        decode_word(c1.x, t, v + 16);
+        decode_word(c1.y, t, v + 20);
+        decode_word(c1.z, t, v + 24);
+        decode_word(c1.w, t, v + 28);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) v[c] = 0u;
+      }
+      tmem_st_x32(lane_addr + kACol + st * 32, v);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->a_full[st]));
+    }
+
+    // Epilogue: accumulator lane = this row, columns = tokens.
+    if (ok) ok = mbar_wait(smem_u32(&bars->acc_full), 0, abort);
+    if (__all_sync(0xffffffffu, ok)) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < kTcBM / 32; ++c) {
+        uint32_t acc[32];
+        tmem_ld_x32(lane_addr + kAccCol + c * 32, acc);
+        tmem_ld_wait();
+        if (row_ok) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int64_t t = m0 + c * 32 + j;
+            if (t < M) Y[t * d + n] = f32_to_bf16_bits(__uint_as_float(acc[j]));
+          }
+        }
+      }
+    }
+  } else if (warp == 4) {
+    // =============================== TMA producer ===============================
+    if (lane == 0) {
+      int issued = 0;
+      for (int s = 0; s < nk; ++s) {
+        const int st = s % kTcXStages;
+        if (s >= kTcXStages && !mbar_wait(smem_u32(&bars->x_empty[st]), ((s / kTcXStages) - 1) & 1, abort)) break;
+        const uint32_t full = smem_u32(&bars->x_full[st]);
+        mbar_arrive_expect_tx(full, kTcXStageBytes);
+        tma_load_2d(smem_u32(xring + st * kTcXStageBytes), &xmap, s * kTcBK, static_cast<int32_t>(m0), full);
+        ++issued;
+      }
+      // Before the CTA can retire, every copy it started must have landed.
+      for (int s = (issued > kTcXStages ? issued - kTcXStages : 0); s < issued; ++s)
+        mbar_wait(smem_u32(&bars->x_full[s % kTcXStages]), (s / kTcXStages) & 1, abort);
+    }
+  } else {
+    // ================================ MMA issuer ================================
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kTcBN, kTcBM);
+      const uint32_t d_tmem = tmem + kAccCol;
+      bool ok = mbar_wait(smem_u32(&bars->lora_full), 0, abort);
+      if (ok) {
+        // The U2 tile was written by the dequantiser warps (generic proxy,
+        // fenced); it is complete once all four arrived on lora_full.
+        tc_fence_after();
+        const uint32_t ubase = smem_u32(utile);
+        const uint32_t sbo = static_cast<uint32_t>((2 * R) / 8) * 128u;
+        for (int kc = 0; kc < (2 * R) / 16; ++kc) {
+          const uint64_t bdesc = smem_desc(ubase + kc * 256, 128, sbo, 0);
+          tc_mma_tmem_a(d_tmem, tmem + kLoraCol + kc * 8, bdesc, idesc, kc > 0 ? 1u : 0u);
+        }
+      }
+      for (int s = 0; s < nk && ok; ++s) {
+        const int sx = s % kTcXStages, sa = s % kTcAStages;
+        ok = mbar_wait(smem_u32(&bars->x_full[sx]), (s / kTcXStages) & 1, abort) &&
+             mbar_wait(smem_u32(&bars->a_full[sa]), (s / kTcAStages) & 1, abort);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t xbase = smem_u32(xring + sx * kTcXStageBytes);
+#pragma unroll
+        for (int kk = 0; kk < kTcBK / 16; ++kk) {
+          const uint64_t bdesc = smem_desc(xbase + kk * 32, 16, 1024, 2);
+          tc_mma_tmem_a(d_tmem, tmem + kACol + sa * 32 + kk * 8, bdesc, idesc, 1u);
+        }
+        tc_commit(smem_u32(&bars->x_empty[sx]));
+        tc_commit(smem_u32(&bars->a_empty[sa]));
+      }
+      if (ok) tc_commit(smem_u32(&bars->acc_full));
+      // Every MMA issued must be complete before tensor memory is released.
+      tc_commit(smem_u32(&bars->done));
+      mbar_wait(smem_u32(&bars->done), 0, abort);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+inline bool tc_supported(int64_t M, int64_t d, int64_t k, int32_t r) {
+  (void)d;
+  return M > 16 && r <= kTcMaxR && (k % kTcBK) == 0 && k >= kTcBK;
+}
 inline bool tc_bwd_supported(int64_t, int64_t, int64_t, int32_t) { return false; }
-template <typename SpanT>
-inline int launch_tc_fwd(const QnNF4View &, const uint16_t *, int64_t, const float *, const uint16_t *, int,
-                         uint16_t *, SpanT &, cudaStream_t) { return -1; }
-template <typename SpanT>
-inline int launch_tc_bwd(const QnNF4View &, const uint16_t *, int64_t, const float *, const uint16_t *, int,
-                         uint16_t *, SpanT &, cudaStream_t) { return -1; }
+inline size_t tc_ws_bytes(int64_t M, int64_t, int64_t, int32_t r) {
+  const int R = tc_pad_r(r);
+  return ((static_cast<size_t>(M) * 2 * R * sizeof(uint16_t)) + 255) & ~static_cast<size_t>(255);
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (the library links only the runtime).
+inline EncodeTiledFn encode_tiled_fn() {
+  static const EncodeTiledFn fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// Tensor map of a row-major bf16 matrix [rows x cols] read in boxes of
+// box_rows rows x 64 columns (128 bytes, the swizzle span) with the 128-byte
+// swizzle; rows beyond the matrix read as zero.
+inline const char *make_bf16_tile_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
+                                      uint32_t box_rows) {
+  const EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return "cuTensorMapEncodeTiled unavailable";
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? nullptr : "cuTensorMapEncodeTiled rejected the operand";
+}
 
 }  // namespace qn

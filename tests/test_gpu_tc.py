@@ -1,0 +1,62 @@
+"""GPU parity of the tensor-core forward (M > 16, r <= 64, the tcgen05 kernel)
+against the float64 oracle, relative Frobenius error <= 5e-3.
+
+The shapes put ragged edges on every tile boundary of that kernel: weight
+rows not a multiple of 128, token counts below, at and above one 256-token
+tile, a single 64-column stage, padded adapter ranks (r = 1, 33, 40) and the
+largest rank it takes (64); r = 65 checks the CUDA-core kernel that takes
+over above that rank."""
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import layer, nf4
+
+pytestmark = pytest.mark.gpu
+
+TOL = 5e-3
+
+
+@pytest.fixture(scope="module")
+def qn():
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    import bit_nf4_quantized_39_b300 as mod
+    return mod
+
+
+def _f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def _fwd(qn, W, X, A, B, alpha, dq=True):
+    q = qn.nf4_quantize(torch.from_numpy(W).cuda(), dq=dq)
+    Wd = nf4.dequantize(nf4.quantize(W, 64, dq=dq)).reshape(W.shape)
+    Y = qn.qlora_linear_fwd(q, X.cuda(), A.cuda(), B.cuda(), alpha)
+    qn.device_status()
+    return _f64(Y), layer.linear_fwd(_f64(X), Wd, _f64(A), _f64(B), alpha, A.shape[0])
+
+
+@pytest.mark.parametrize("M,d,k,r", [
+    (17, 128, 64, 8), (256, 256, 128, 16), (257, 384, 192, 1), (300, 200, 576, 33),
+    (600, 1000, 256, 64), (1024, 512, 1024, 40), (40, 130, 64, 65),
+])
+def test_tc_forward_shapes(qn, M, d, k, r):
+    c = synth.layer_case(seed=M + 3 * d + k, d=d, k=k, M=M, r=r, alpha=2.0 * r)
+    Y, ref = _fwd(qn, c["W"], c["X"], c["A"], c["B"], c["alpha"])
+    assert layer.rel_fro(Y, ref) < TOL, (M, d, k, r)
+
+
+def test_tc_forward_exact_absmax(qn):
+    c = synth.layer_case(seed=5, d=384, k=320, M=200, r=16)
+    Y, ref = _fwd(qn, c["W"], c["X"], c["A"], c["B"], c["alpha"], dq=False)
+    assert layer.rel_fro(Y, ref) < TOL
+
+
+def test_tc_forward_degenerate_terms(qn):
+    c = synth.layer_case(seed=6, d=256, k=256, M=300, r=8)
+    Y, ref = _fwd(qn, c["W"], c["X"], c["A"], torch.zeros_like(c["B"]), c["alpha"])  # no adapter
+    assert layer.rel_fro(Y, ref) < TOL
+    Y, ref = _fwd(qn, np.zeros((256, 256), np.float32), c["X"], c["A"], c["B"], c["alpha"])  # adapter only
+    assert layer.rel_fro(Y, ref) < TOL
