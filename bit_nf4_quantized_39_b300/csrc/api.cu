@@ -15,6 +15,7 @@
 #include "nf4_codec.cuh"
 #include "qlora_simt.cuh"
 #include "qlora_decode.cuh"
+#include "qlora_skinny.cuh"
 #include "qlora_tc.cuh"
 #include "loftq.cuh"
 
@@ -199,45 +200,12 @@ qn_status launch_dequantize(const qn_nf4 *Q, void *out, qn_dtype odt, cudaStream
 }
 
 // ----------------------------------------------------------------- the layer
-struct GemvPlan {
-  int splits;
-  int64_t chunks_per_split;
-  int64_t row_groups;
-};
-
-GemvPlan gemv_plan(int64_t d, int64_t k) {
-  GemvPlan p;
-  p.row_groups = qn_ceil_div(d, qn::kGemvWarps);
-  const int64_t chunks = k / 32;
-  const int64_t want = 4 * static_cast<int64_t>(sm_count());
-  int64_t splits = qn_ceil_div(want, p.row_groups);
-  const int64_t max_splits = chunks / 32 > 0 ? chunks / 32 : 1;  // >= 32 chunks (one per lane) per split
-  if (splits > max_splits) splits = max_splits;
-  if (splits > 16) splits = 16;
-  if (splits < 1) splits = 1;
-  p.chunks_per_split = qn_ceil_div(chunks, splits);
-  p.splits = static_cast<int>(qn_ceil_div(chunks, p.chunks_per_split));
-  return p;
-}
-
-bool use_decode(int64_t M, int64_t d, int64_t k) { return M == 1 && k <= qn::kDecMaxK && d <= qn::kDecMaxD; }
-
-// r: sum of the ranks of a group.
-size_t decode_ws_bytes(int64_t, int64_t k, int32_t r) {
-  return round256(static_cast<size_t>(r) * static_cast<size_t>(qn_ceil_div(k, qn::kDecPiece)) * sizeof(float)) +
-         round256(static_cast<size_t>(r) * sizeof(float));
-}
+bool use_decode(int64_t M, int64_t k) { return M == 1 && k <= qn::kDecMaxK; }
+bool use_skinny(int64_t M, int64_t k) { return M <= qn::kSkMaxM && k <= 64 * qn::kSkMaxNb; }
 
 size_t fwd_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
-  if (use_decode(M, d, k)) return kSemBytes + decode_ws_bytes(d, k, r);
   size_t b = kSemBytes + round256(static_cast<size_t>(M) * r * sizeof(float));  // u
-  if (M <= qn::kGemvMaxM) {
-    // sized for the largest split count, so that the size grows with d (a
-    // group's query with the summed d covers each member)
-    b += round256(static_cast<size_t>(16) * M * d * sizeof(float));
-    b += round256(static_cast<size_t>(qn_ceil_div(d, qn::kGemvWarps)) * sizeof(unsigned int));
-  }
-  b += qn::tc_ws_bytes(M, d, k, r);
+  if (!use_skinny(M, k)) b += qn::tc_ws_bytes(M, d, k, r);
   return b;
 }
 
@@ -268,8 +236,8 @@ qn_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 // Single-token forward of a group of projections of one input: one
-// persistent kernel (every CTA resident, at least one per SM); its counters
-// and row accumulators live in the zero area.
+// persistent kernel (every CTA resident, at least one per SM); its two
+// counters live in the zero area.
 qn_status launch_decode_group(int n, const qn_nf4 *const *Q, const uint16_t *X, const uint16_t *const *A,
                               const uint16_t *const *B, const int32_t *r, const float *alpha, uint16_t *const *Y,
                               unsigned int *zero_area, Span &sp, cudaStream_t st) {
@@ -289,14 +257,11 @@ qn_status launch_decode_group(int n, const qn_nf4 *const *Q, const uint16_t *X, 
   QN_TRY(cuda_check(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qn::qlora_decode_kernel, qn::kDecThreads,
                                                                   smem), "occupancy query"));
   if (per_sm < 1) return fail(QN_EUNSUPPORTED, "decode kernel does not fit on an SM");
-  const int64_t nsteps = qn_ceil_div(k / 32, 32);
-  const int64_t nparts = qn_ceil_div(nsteps, qn::kDecUnitSteps);
-  const int64_t KC = qn_ceil_div(k, qn::kDecPiece);
   qn::DecGroup g = {};
   g.n = n;
   g.k = k;
   g.X = X;
-  int64_t units = 0, adapters = 0, quads = 0, rows = 0, us = 0;
+  int64_t units = 0, us = 0;
   for (int i = 0; i < n; ++i) {
     qn::DecProj &p = g.p[i];
     p.q = view_of(Q[i]);
@@ -306,30 +271,80 @@ qn_status launch_decode_group(int n, const qn_nf4 *const *Q, const uint16_t *X, 
     p.r = r[i];
     p.s = alpha[i] / static_cast<float>(r[i]);
     p.unit_off = units;
-    p.adapter_off = adapters;
-    p.quad_off = quads;
-    p.row_off = rows;
     p.u_off = us;
-    const int64_t nq = qn_ceil_div(Q[i]->d, qn::kDecRows);
-    units += nq * nparts;
-    adapters += static_cast<int64_t>(r[i]) * KC;
-    quads += nq;
-    rows += Q[i]->d;
+    units += qn_ceil_div(Q[i]->d, qn::kDecRows);
     us += r[i];
   }
   g.nunits = units;
-  g.nadapter = adapters;
+  g.nadapter = us;
   const int64_t sms = sm_count();
   int64_t grid = qn_ceil_div(units, qn::kDecWarps);
   if (grid < sms) grid = sms;
   if (grid > sms * per_sm) grid = sms * per_sm;
-  if (units > grid * qn::kDecWarps * qn::kDecMaxSlots)
-    return fail(QN_EUNSUPPORTED, "decode kernel: too many weight units for the resident grid");
-  float *upart = sp.take<float>(static_cast<size_t>(adapters));
   float *u = sp.take<float>(static_cast<size_t>(us));
-  qn::qlora_decode_kernel<<<static_cast<unsigned>(grid), qn::kDecThreads, smem, st>>>(g, zero_area, upart, u);
+  qn::qlora_decode_kernel<<<static_cast<unsigned>(grid), qn::kDecThreads, smem, st>>>(g, zero_area, u);
   QN_LAUNCH_CHECK("qlora_decode_kernel");
   return QN_OK;
+}
+
+template <int MT, bool XS>
+qn_status launch_skinny_variant(const qn::SkGroup &g, size_t smem, cudaStream_t st) {
+  auto kern = qn::skinny_kernel<MT, XS>;
+  static int attr_set[64] = {0};
+  int dev = 0;
+  QN_TRY(cuda_check(cudaGetDevice(&dev), "cudaGetDevice"));
+  if (dev < 0 || dev >= 64) return fail(QN_EUNSUPPORTED, "device ordinal out of range");
+  if (!attr_set[dev]) {
+    QN_TRY(cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024),
+                      "cudaFuncSetAttribute(skinny smem)"));
+    attr_set[dev] = 1;
+  }
+  int64_t grid = sm_count();
+  if (grid > g.ngroups) grid = g.ngroups;
+  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(qn::kSkThreads), smem, st, "skinny_kernel", g);
+}
+
+// Forward of a group of projections of one input with M <= 16 tokens: the
+// adapter down-projection u, then the weights (both kernels PDL-launched).
+qn_status launch_skinny_group(int n, const qn_nf4 *const *Q, const uint16_t *X, int64_t M,
+                              const uint16_t *const *A, const uint16_t *const *B, const int32_t *r,
+                              const float *alpha, uint16_t *const *Y, Span &sp, cudaStream_t st) {
+  const int64_t k = Q[0]->k;
+  qn::SkGroup g = {};
+  g.n = n;
+  g.M = static_cast<int>(M);
+  g.k = k;
+  g.X = X;
+  int64_t groups = 0, us = 0;
+  for (int i = 0; i < n; ++i) {
+    qn::SkProj &p = g.p[i];
+    p.q = view_of(Q[i]);
+    p.A = A[i];
+    p.B = B[i];
+    p.Y = Y[i];
+    p.r = r[i];
+    p.s = alpha[i] / static_cast<float>(r[i]);
+    p.group_off = groups;
+    p.u_off = us;
+    // codes as uint32 [d][k / 8]: one box = 16 rows x 128 bytes (4 blocks)
+    if (const char *e = qn::make_tile_map(&p.tmap, Q[i]->codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4,
+                                          static_cast<uint64_t>(k / 8), static_cast<uint64_t>(Q[i]->d),
+                                          qn::kSkBoxBytes / 4, qn::kSkRows, CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(QN_ECUDA, "few-token forward: %s", e);
+    groups += qn_ceil_div(Q[i]->d, qn::kSkRows);
+    us += r[i];
+  }
+  if (groups > (int64_t{1} << 30)) return fail(QN_ESHAPE, "too many rows for the few-token kernel");
+  g.ngroups = groups;
+  g.rtot = us;
+  g.u = sp.take<float>(static_cast<size_t>(M) * us);
+  QN_TRY(launch_pdl(qn::skinny_u_kernel, dim3(static_cast<unsigned>(us), static_cast<unsigned>(M)),
+                    dim3(qn::kSkUThreads), 0, st, "skinny_u_kernel", g));
+  const int MT = M <= 8 ? 1 : 2;
+  const bool xs = qn::sk_smem_bytes(MT, g.M, k, true) <= 227 * 1024;
+  const size_t smem = qn::sk_smem_bytes(MT, g.M, k, xs);
+  if (MT == 1) return xs ? launch_skinny_variant<1, true>(g, smem, st) : launch_skinny_variant<1, false>(g, smem, st);
+  return xs ? launch_skinny_variant<2, true>(g, smem, st) : launch_skinny_variant<2, false>(g, smem, st);
 }
 
 qn_status check_layer(const qn_nf4 *Q, const void *in, int64_t M, const void *A, const void *B, int32_t r,
@@ -482,35 +497,9 @@ qn_status qlora_linear_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M, const 
   Span sp{static_cast<char *>(ws), ws_bytes, 0};
   unsigned int *sem = sp.take<unsigned int>(kSemBytes / sizeof(unsigned int));
   const float s = alpha / static_cast<float>(r);
-  if (use_decode(M, d, k)) return launch_decode_group(1, &Q, X, &A, &B, &r, &alpha, &Y, sem, sp, st);
+  if (use_decode(M, k)) return launch_decode_group(1, &Q, X, &A, &B, &r, &alpha, &Y, sem, sp, st);
+  if (use_skinny(M, k)) return launch_skinny_group(1, &Q, X, M, &A, &B, &r, &alpha, &Y, sp, st);
   float *u = sp.take<float>(static_cast<size_t>(M) * r);
-  if (M <= qn::kGemvMaxM) {
-    {
-      dim3 grid(static_cast<unsigned>(qn_ceil_div(M, qn::kProjTM)), static_cast<unsigned>(qn_ceil_div(r, qn::kProjTN)));
-      qn::lora_proj_kernel<<<grid, 256, 0, st>>>(X, M, k, A, r, k, 1, s, u);
-      QN_LAUNCH_CHECK("lora_proj_kernel");
-    }
-    const GemvPlan p = gemv_plan(d, k);
-    float *part = nullptr;
-    unsigned int *counters = nullptr;
-    if (p.splits > 1) {
-      part = sp.take<float>(static_cast<size_t>(p.splits) * M * d);
-      counters = sp.take<unsigned int>(p.row_groups);
-      QN_TRY(cuda_check(cudaMemsetAsync(counters, 0, p.row_groups * sizeof(unsigned int), st), "memset counters"));
-    }
-    dim3 grid(static_cast<unsigned>(p.row_groups), static_cast<unsigned>(p.splits));
-    const QnNF4View v = view_of(Q);
-    const int Mi = static_cast<int>(M);
-#define QN_GEMV(MT) qn::qlora_fwd_gemv_kernel<MT><<<grid, qn::kGemvThreads, 0, st>>>(v, X, Mi, u, B, r, Y, part, counters, p.splits, p.chunks_per_split)
-    if (M == 1) QN_GEMV(1);
-    else if (M <= 2) QN_GEMV(2);
-    else if (M <= 4) QN_GEMV(4);
-    else if (M <= 8) QN_GEMV(8);
-    else QN_GEMV(16);
-#undef QN_GEMV
-    QN_LAUNCH_CHECK("qlora_fwd_gemv_kernel");
-    return QN_OK;
-  }
   {
     dim3 grid(static_cast<unsigned>(qn_ceil_div(M, qn::kProjTM)), static_cast<unsigned>(qn_ceil_div(r, qn::kProjTN)));
     qn::lora_proj_kernel<<<grid, 256, 0, st>>>(X, M, k, A, r, k, 1, s, u);
@@ -527,7 +516,7 @@ qn_status qlora_linear_fwd_group(int32_t n, const qn_nf4 *const *Q, const uint16
                                  const uint16_t *const *A, const uint16_t *const *B, const int32_t *r,
                                  const float *alpha, uint16_t *const *Y, void *ws, size_t ws_bytes, void *stream) {
   g_last_error.clear();
-  if (n < 1 || n > qn::kDecMaxGroup) return fail(QN_ESHAPE, "group size must be in [1, %d]", qn::kDecMaxGroup);
+  if (n < 1 || n > qn::kSkMaxGroup || n > qn::kDecMaxGroup) return fail(QN_ESHAPE, "group size must be in [1, %d]", qn::kSkMaxGroup);
   if (!Q || !A || !B || !r || !alpha || !Y) return fail(QN_EINVAL, "NULL array");
   int64_t dsum = 0, rsum = 0;
   for (int i = 0; i < n; ++i) {
@@ -542,10 +531,11 @@ qn_status qlora_linear_fwd_group(int32_t n, const qn_nf4 *const *Q, const uint16
   if (ws_bytes < need) return fail(QN_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, need);
   if (!aligned(ws, 256)) return fail(QN_EALIGN, "workspace not 256-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (use_decode(M, dsum, k)) {
+  if (use_decode(M, k) || use_skinny(M, k)) {
     Span sp{static_cast<char *>(ws), ws_bytes, 0};
     unsigned int *sem = sp.take<unsigned int>(kSemBytes / sizeof(unsigned int));
-    return launch_decode_group(n, Q, X, A, B, r, alpha, Y, sem, sp, st);
+    if (use_decode(M, k)) return launch_decode_group(n, Q, X, A, B, r, alpha, Y, sem, sp, st);
+    return launch_skinny_group(n, Q, X, M, A, B, r, alpha, Y, sp, st);
   }
   for (int i = 0; i < n; ++i)
     QN_TRY(qlora_linear_fwd(Q[i], X, M, A[i], B[i], r[i], alpha[i], Y[i], ws, ws_bytes, stream));

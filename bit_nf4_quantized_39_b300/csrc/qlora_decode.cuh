@@ -9,13 +9,15 @@
 // launch so that their memory round trips overlap.  The call is bound by the
 // bytes of the packed weights; at decode sizes (8-45 MB per launch) what
 // limits it is how many bytes each SM keeps in flight and how many dependent
-// round trips a warp makes, so:
+// round trips lie on the longest path, so:
 //
 // * persistent grid (every CTA resident, at least one per SM);
-// * every weight is cut into units of 4 rows x 2048 columns; the units of all
+// * every weight is cut into units of 2 whole rows; the units of all
 //   projections form one list; unit u goes to warp slot u mod W with slots
-//   interleaved across CTAs, so every SM gets an equal share; a warp issues
-//   the loads of its next unit before it decodes the current one;
+//   interleaved across CTAs, so every SM gets an equal share;
+// * a warp walks the 1024-column lane steps of its units as one flat
+//   sequence and keeps the loads of the next kDecDepth steps in flight, across
+//   unit boundaries, so a finishing unit never drains the pipeline;
 // * decode: x is staged once per CTA in shared memory as fp32, lane-
 //   interleaved so that each lane's 32-element chunk is read with
 //   conflict-free 128-bit loads; two codes at a time are looked up in a
@@ -23,18 +25,17 @@
 //   word 32 b + l, so a warp never conflicts on a bank), widened to fp32 and
 //   multiplied into packed fp32x2 accumulators (fma.rn.f32x2); each
 //   32-element partial is scaled by its 64-block constant;
-// * the row sums of a unit are added into per-row fp32 accumulators; the
-//   warp that completes the last unit of a quad (per-quad counter) takes the
-//   sums with an atomic exchange (which also returns them to zero), adds
-//   u . B[row] and writes bf16 Y;
-// * the down-projections u_g = s_g A_g x are split into (row of A,
-//   256-column piece) units done by all warps first; the last CTA to finish
-//   them sums every u_g once and raises a flag that finishing warps wait on
-//   (bounded spin, no trap).
+// * a unit is a whole row, so its sum is complete in one warp (no cross-warp
+//   combine, a fixed summation order): the warp adds u . B[row] and writes
+//   bf16 Y;
+// * the adapter rows u_g[j] = s_g A_g[j] . x are spread one per warp slot,
+//   done right after x is staged with all their loads in flight; each bumps a
+//   ready counter (release) that finishing warps wait on (acquire, bounded
+//   spin, no trap) before their first adapter term.
 //
-// Workspace: the counters and row accumulators live in the caller's zero
-// area (zero before the first call; every call leaves it zero); the adapter
-// partials and u live after it.
+// Workspace: the two counters live in the caller's zero area (zero before
+// the first call; the last CTA to leave returns them to zero); u lives after
+// it.
 #pragma once
 
 #include "common.cuh"
@@ -43,20 +44,13 @@ namespace qn {
 
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
-constexpr int kDecRows = 4;            // weight rows per warp item
-constexpr int kDecDepth = 2;           // lane steps whose loads are in flight together
+constexpr int kDecRows = 2;            // weight rows per unit (whole rows)
+constexpr int kDecDepth = 4;           // lane steps whose loads are in flight per warp
 constexpr int kDecLutWords = 256 * 32;
 constexpr int kDecMaxK = 16384;
-constexpr int kDecUnitSteps = 2;       // 1024-column lane steps per unit (2048 columns)
-constexpr int kDecPiece = 256;         // elements of an A row per adapter unit
-constexpr int kDecMaxUnitsPerWarp = 2;   // adapter units whose loads go out in the prologue
-constexpr int kDecMaxSlots = 16;         // weight units per warp (partials kept in shared memory)
 constexpr unsigned kDecSpinLimit = 1u << 22;
-// Zero area layout (32-bit words): flags, then per-quad counters, then row sums.
-constexpr int kDecFlagArrive = 0, kDecFlagUReady = 1, kDecFlagExit = 2;
-constexpr int64_t kDecQuadCtrOffset = 64;          // words
-constexpr int64_t kDecRowSumOffset = 16384;        // words (64 KiB)
-constexpr int64_t kDecMaxD = 32768;            // sum of d over a group
+// Zero-area words: adapter rows done, CTAs done.
+constexpr int kDecFlagReady = 0, kDecFlagExit = 1;
 constexpr int kDecMaxGroup = 8;
 
 // One projection of a group (device pointers; k is shared by the group).
@@ -68,16 +62,13 @@ struct DecProj {
   int r;
   float s;
   int64_t unit_off;    // first unit of this projection in the group's list
-  int64_t adapter_off; // first adapter unit
-  int64_t quad_off;    // first per-quad counter
-  int64_t row_off;     // first row accumulator
-  int64_t u_off;       // first element of u
+  int64_t u_off;       // first adapter row (element of u)
 };
 struct DecGroup {
   DecProj p[kDecMaxGroup];
   int n;
   int64_t k;
-  int64_t nunits, nadapter;  // totals
+  int64_t nunits, nadapter;  // totals: weight units, adapter rows
   const uint16_t *X;
 };
 
@@ -111,7 +102,7 @@ __device__ __forceinline__ int64_t dec_xs_index(int64_t e) {
   return ((((c >> 5) * 8 + (o >> 2)) * 32 + (c & 31)) << 2) + (o & 3);
 }
 
-// One lane step of 4 rows as loaded: code chunks plus the raw constants of
+// One lane step of a unit's rows as loaded: code chunks plus the raw constants of
 // their 64-block (int8 code and group scale, or the exact absmax).  The
 // block constant is formed only when the step is decoded, so that no load
 // of a step waits on another.
@@ -121,7 +112,7 @@ struct DecStep {
   int qv[kDecRows];     // int8 code of the constant (dq)
 };
 
-// Loads lane step `st` of the 4 rows starting at row0 (codes and constants).
+// Loads lane step `st` of the rows starting at row0 (codes and constants).
 __device__ __forceinline__ void dec_load_step(const QnNF4View &q, int64_t row0, int64_t st, int lane,
                                               DecStep &out) {
   const int64_t d = q.d, k = q.k;
@@ -153,7 +144,7 @@ __device__ __forceinline__ float dec_step_scale(const DecStep &sp, int rr, bool 
   return dq ? dq_absmax(static_cast<int8_t>(sp.qv[rr]), sp.sc[rr], mu) : sp.sc[rr];
 }
 
-// Adds the dot products of one lane step of 4 rows with the staged x.
+// Adds the dot products of one lane step of a unit's rows with the staged x.
 __device__ __forceinline__ void dec_compute_step(const DecStep &sp, int64_t st, const float *__restrict__ xs,
                                                  const uint32_t *__restrict__ lut, int lane, bool dq, float mu,
                                                  float (&rsum)[kDecRows]) {
@@ -180,7 +171,7 @@ __device__ __forceinline__ void dec_compute_step(const DecStep &sp, int64_t st, 
   for (int rr = 0; rr < kDecRows; ++rr) rsum[rr] = fmaf(sum_f2(acc[rr]), dec_step_scale(sp, rr, dq, mu), rsum[rr]);
 }
 
-// s * A[j, piece] . x for one adapter unit (lane holds 8 A values in av).
+// A[j, e0 .. e0 + 8) . x[e0 .. e0 + 8) (the lane's 8 A values in av).
 __device__ __forceinline__ float dec_adapter_unit(const uint4 &av, int64_t e0, const float *__restrict__ xs) {
   const float4 x0 = *reinterpret_cast<const float4 *>(xs + dec_xs_index(e0));
   const float4 x1 = *reinterpret_cast<const float4 *>(xs + dec_xs_index(e0 + 4));
@@ -214,50 +205,46 @@ __device__ __forceinline__ int dec_find(const DecGroup &g, int64_t pos, F off) {
 }
 
 __global__ void __launch_bounds__(kDecThreads, 2)
-qlora_decode_kernel(const __grid_constant__ DecGroup g, unsigned int *__restrict__ zero_area,
-                    float *__restrict__ upart, float *__restrict__ u) {
+qlora_decode_kernel(const __grid_constant__ DecGroup g, unsigned int *__restrict__ zero_area, float *__restrict__ u) {
   extern __shared__ __align__(16) unsigned char dec_smem[];
   uint32_t *lut = reinterpret_cast<uint32_t *>(dec_smem);
   float *xs = reinterpret_cast<float *>(dec_smem + sizeof(uint32_t) * kDecLutWords);
-  unsigned int *flags = zero_area;
-  unsigned int *quad_ctr = zero_area + kDecQuadCtrOffset;
-  float *rowsum = reinterpret_cast<float *>(zero_area + kDecRowSumOffset);
   const int64_t k = g.k;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x;
-  const int64_t nsteps = qn_ceil_div(k >> 5, 32);
-  const int64_t nparts = qn_ceil_div(nsteps, kDecUnitSteps);  // units per quad
-  const int64_t KC = qn_ceil_div(k, kDecPiece);
+  const int64_t nsteps = qn_ceil_div(k >> 5, 32);  // 1024-column lane steps per row
   // warp slots interleaved across CTAs: slot = warp * G + cta
   const int64_t wslot = static_cast<int64_t>(warp) * G + blockIdx.x;
   const int64_t W = static_cast<int64_t>(G) * kDecWarps;
+  const int64_t nunits = g.nunits;
   auto unit_of = [](const DecProj &p) { return p.unit_off; };
-  auto adapter_of = [](const DecProj &p) { return p.adapter_off; };
+  auto uoff_of = [](const DecProj &p) { return p.u_off; };
 
-  auto load_unit = [&](int64_t unit, DecStep (&pp)[kDecUnitSteps]) {
-    const DecProj &p = g.p[dec_find(g, unit, unit_of)];
-    const int64_t local = unit - p.unit_off;
-    const int64_t quad = local / nparts, part = local % nparts;
-#pragma unroll
-    for (int t = 0; t < kDecUnitSteps; ++t)
-      dec_load_step(p.q, quad * kDecRows, part * kDecUnitSteps + t, lane, pp[t]);
-  };
-  auto adapter_load = [&](int64_t unit) -> uint4 {
-    const DecProj &p = g.p[dec_find(g, unit, adapter_of)];
-    const int64_t local = unit - p.adapter_off;
-    const int64_t j = local / KC, e0 = (local % KC) * kDecPiece + lane * 8;
-    return (e0 < k) ? __ldg(reinterpret_cast<const uint4 *>(p.A + j * k + e0)) : make_uint4(0u, 0u, 0u, 0u);
-  };
-
-  // ---- prologue: independent loads first ------------------------------------
-  DecStep pipe[kDecUnitSteps];
-  if (warp != 0 && wslot < g.nunits) load_unit(wslot, pipe);
-  uint4 av[kDecMaxUnitsPerWarp];
-#pragma unroll
-  for (int i = 0; i < kDecMaxUnitsPerWarp; ++i) {
-    const int64_t unit = wslot + i * W;
-    av[i] = (unit < g.nadapter) ? adapter_load(unit) : make_uint4(0u, 0u, 0u, 0u);
+  // ---- load cursor: (unit, step) of the next step to load --------------------
+  int64_t l_unit = wslot, l_st = 0, l_row0 = 0;
+  int l_p = 0;
+  if (l_unit < nunits) {
+    l_p = dec_find(g, l_unit, unit_of);
+    l_row0 = (l_unit - g.p[l_p].unit_off) * kDecRows;
   }
+  auto load_next = [&](DecStep &dst) {
+    if (l_unit < nunits) {
+      dec_load_step(g.p[l_p].q, l_row0, l_st, lane, dst);
+      if (++l_st == nsteps) {
+        l_st = 0;
+        l_unit += W;
+        if (l_unit < nunits) {
+          l_p = dec_find(g, l_unit, unit_of);
+          l_row0 = (l_unit - g.p[l_p].unit_off) * kDecRows;
+        }
+      }
+    }
+  };
+
+  // ---- prologue: weight loads first, then x -----------------------------------
+  DecStep buf[kDecDepth];
+#pragma unroll
+  for (int i = 0; i < kDecDepth; ++i) load_next(buf[i]);
   __shared__ uint32_t s_lv[16];
   if (tid < 16) s_lv[tid] = f32_to_bf16_bits(c_nf4_levels[tid]);
   {
@@ -290,168 +277,124 @@ qlora_decode_kernel(const __grid_constant__ DecGroup g, unsigned int *__restrict
     const int b = i >> 5;
     lut[i] = (s_lv[b >> 4] << 16) | s_lv[b & 15];
   }
+  __syncthreads();  // lut ready
 
-  // ---- adapter partials: upart[adapter unit] = s * A[j, piece] . x ---------
-  for (int64_t unit = wslot, i = 0; unit < g.nadapter; unit += W, ++i) {
-    const DecProj &p = g.p[dec_find(g, unit, adapter_of)];
-    const int64_t local = unit - p.adapter_off;
-    const int64_t e0 = (local % KC) * kDecPiece + lane * 8;
-    uint4 a;
-    if (i < kDecMaxUnitsPerWarp) a = (i == 0) ? av[0] : av[kDecMaxUnitsPerWarp - 1];
-    else a = adapter_load(unit);
-    float acc = (e0 < k) ? dec_adapter_unit(a, e0, xs) : 0.f;
+  // ---- adapter rows: u[j] = s * A[j] . x, one warp slot per row ---------------
+  for (int64_t j = wslot; j < g.nadapter; j += W) {
+    const DecProj &p = g.p[dec_find(g, j, uoff_of)];
+    const uint16_t *arow = p.A + (j - p.u_off) * k;
+    float acc = 0.f;
+    for (int64_t base = 0; base < k; base += 8 * 256) {
+      uint4 t[8];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const int64_t e = base + v * 256 + lane * 8;
+        t[v] = (e < k) ? __ldg(reinterpret_cast<const uint4 *>(arow + e)) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const int64_t e = base + v * 256 + lane * 8;
+        if (e < k) acc += dec_adapter_unit(t[v], e, xs);
+      }
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) upart[unit] = p.s * acc;
-  }
-  __syncthreads();  // lut ready; this CTA's adapter partials written
-  // Arrival: warp 0 alone (the other warps go straight to the weights).  The
-  // last CTA to arrive forms every u_g with warp 0 and raises the flag.
-  if (warp == 0) {
-    int last = 0;
     if (lane == 0) {
+      u[j] = p.s * acc;
       __threadfence();
-      last = (atomicAdd(&flags[kDecFlagArrive], 1u) == static_cast<unsigned>(G) - 1u);
-    }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) {
-      __threadfence();
-      // lane j sums the KC partials of u_g[j]; loads in batches of 8
-      for (int pi = 0; pi < g.n; ++pi) {
-        const DecProj &p = g.p[pi];
-        for (int j = lane; j < p.r; j += 32) {
-          const float *src = upart + p.adapter_off + static_cast<int64_t>(j) * KC;
-          float acc = 0.f;
-          for (int64_t kc0 = 0; kc0 < KC; kc0 += 8) {
-            float t[8];
-#pragma unroll
-            for (int v = 0; v < 8; ++v) t[v] = (kc0 + v < KC) ? __ldcg(src + kc0 + v) : 0.f;
-#pragma unroll
-            for (int v = 0; v < 8; ++v) acc += t[v];
-          }
-          u[p.u_off + j] = acc;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence();
-        atomicExch(&flags[kDecFlagUReady], 1u);
-      }
+      atomicAdd(&zero_area[kDecFlagReady], 1u);
     }
   }
 
-  if (warp == 0 && wslot < g.nunits) load_unit(wslot, pipe);
-
-  // ---- main loop over units: decode only, partial row sums to shared memory --
-  // (No fence or returning atomic here: either would wait for the loads of
-  // the next unit that are already in flight.)
-  __shared__ float s_part[kDecWarps][kDecMaxSlots][kDecRows];
-  int nslot = 0;
-  for (int64_t unit = wslot; unit < g.nunits; unit += W, ++nslot) {
-    DecStep cur[kDecUnitSteps];
-#pragma unroll
-    for (int t = 0; t < kDecUnitSteps; ++t) cur[t] = pipe[t];
-    if (unit + W < g.nunits) load_unit(unit + W, pipe);
-    const DecProj &p = g.p[dec_find(g, unit, unit_of)];
-    const int64_t local = unit - p.unit_off;
-    const int64_t part = local % nparts;
-    const float mu = p.q.dq ? __ldg(p.q.absmax_mean) : 0.f;
-    float rsum[kDecRows] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int t = 0; t < kDecUnitSteps; ++t) {
-      const int64_t st = part * kDecUnitSteps + t;
-      if (st < nsteps) dec_compute_step(cur[t], st, xs, lut, lane, p.q.dq != 0, mu, rsum);
+  // ---- main loop: the warp's units as one flat sequence of lane steps --------
+  int64_t c_unit = wslot, c_st = 0, c_row0 = 0;
+  int c_p = 0;
+  float mu = 0.f;
+  bool c_dq = false;
+  auto enter_unit = [&]() {
+    if (c_unit < nunits) {
+      c_p = dec_find(g, c_unit, unit_of);
+      c_row0 = (c_unit - g.p[c_p].unit_off) * kDecRows;
+      c_dq = g.p[c_p].q.dq != 0;
+      mu = c_dq ? __ldg(g.p[c_p].q.absmax_mean) : 0.f;
     }
+  };
+  enter_unit();
+  bool have_u = false;
+  float rsum[kDecRows];
+#pragma unroll
+  for (int rr = 0; rr < kDecRows; ++rr) rsum[rr] = 0.f;
+
+  // y = row sum + u . B[row] for the rows of the current unit.
+  auto finish_unit = [&]() {
+    const DecProj &p = g.p[c_p];
+    const int64_t d = p.q.d;
 #pragma unroll
     for (int rr = 0; rr < kDecRows; ++rr) {
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) rsum[rr] += __shfl_xor_sync(0xffffffffu, rsum[rr], off);
     }
-    if (lane < kDecRows && nslot < kDecMaxSlots) {
-      float v = rsum[0];
-#pragma unroll
-      for (int rr = 1; rr < kDecRows; ++rr) if (lane == rr) v = rsum[rr];
-      s_part[warp][nslot][lane] = v;
-    }
-  }
-  __syncwarp();
-
-  // ---- combine: add partials, then one fence, then count arrivals per quad --
-  if (nparts > 1) {
-    int sl = 0;
-    for (int64_t unit = wslot; unit < g.nunits && sl < kDecMaxSlots; unit += W, ++sl) {
-      const DecProj &p = g.p[dec_find(g, unit, unit_of)];
-      const int64_t quad = (unit - p.unit_off) / nparts;
-      const int64_t row = quad * kDecRows + lane;
-      if (lane < kDecRows && row < p.q.d) atomicAdd(&rowsum[p.row_off + row], s_part[warp][sl][lane]);
-    }
-    __threadfence();
-    __syncwarp();
-  }
-  bool have_u = false;
-  {
-    int sl = 0;
-    for (int64_t unit = wslot; unit < g.nunits && sl < kDecMaxSlots; unit += W, ++sl) {
-      const DecProj &p = g.p[dec_find(g, unit, unit_of)];
-      const int64_t d = p.q.d;
-      const int64_t quad = (unit - p.unit_off) / nparts;
-      const int64_t row0 = quad * kDecRows;
-      float total = 0.f;  // lane rr < 4: final row sum of row0 + rr
-      if (nparts == 1) {
-        if (lane < kDecRows) total = s_part[warp][sl][lane];
-      } else {
-        unsigned int prev = 0;
-        if (lane == 0) prev = atomicAdd(&quad_ctr[p.quad_off + quad], 1u);
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        if (prev != static_cast<unsigned>(nparts) - 1u) continue;  // another warp finishes this quad
-        __threadfence();
-        if (lane < kDecRows && row0 + lane < d) total = atomicExch(&rowsum[p.row_off + row0 + lane], 0.f);
-        if (lane == 0) quad_ctr[p.quad_off + quad] = 0u;
-      }
-      // ---- finish the quad: y = row sum + u . B[row] ------------------------
-      if (!have_u) {
-        if (lane == 0) {
-          unsigned int spins = 0;
-          while (ld_acquire_u32(&flags[kDecFlagUReady]) == 0u) {
-            if (++spins > kDecSpinLimit) { qn_flag_timeout(); break; }
-            __nanosleep(20);
-          }
+    if (!have_u) {
+      if (lane == 0) {
+        unsigned int spins = 0;
+        while (ld_acquire_u32(&zero_area[kDecFlagReady]) < static_cast<unsigned>(g.nadapter)) {
+          if (++spins > kDecSpinLimit) { qn_flag_timeout(); break; }
+          __nanosleep(32);
         }
-        __syncwarp();
-        have_u = true;
       }
-      float acc[kDecRows];
+      __syncwarp();
+      have_u = true;
+    }
+    float acc[kDecRows];
 #pragma unroll
-      for (int rr = 0; rr < kDecRows; ++rr) {
-        const int64_t row = row0 + rr;
-        float a = 0.f;
-        if (row < d)
-          for (int j = lane; j < p.r; j += 32)
-            a = fmaf(__ldcg(u + p.u_off + j), bf16_bits_to_f32(p.B[row * p.r + j]), a);
-        acc[rr] = a;
-      }
+    for (int rr = 0; rr < kDecRows; ++rr) {
+      const int64_t row = c_row0 + rr;
+      float a = 0.f;
+      if (row < d)
+        for (int j = lane; j < p.r; j += 32)
+          a = fmaf(__ldcg(u + p.u_off + j), bf16_bits_to_f32(p.B[row * p.r + j]), a);
+      acc[rr] = a;
+    }
 #pragma unroll
-      for (int rr = 0; rr < kDecRows; ++rr) {
+    for (int rr = 0; rr < kDecRows; ++rr) {
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc[rr] += __shfl_xor_sync(0xffffffffu, acc[rr], off);
-      }
-      if (lane < kDecRows && row0 + lane < d) {
-        float a = acc[0];
+      for (int off = 16; off > 0; off >>= 1) acc[rr] += __shfl_xor_sync(0xffffffffu, acc[rr], off);
+    }
+    if (lane < kDecRows && c_row0 + lane < d) {
+      float y = rsum[0] + acc[0];
 #pragma unroll
-        for (int rr = 1; rr < kDecRows; ++rr) if (lane == rr) a = acc[rr];
-        p.Y[row0 + lane] = f32_to_bf16_bits(total + a);
+      for (int rr = 1; rr < kDecRows; ++rr)
+        if (lane == rr) y = rsum[rr] + acc[rr];
+      p.Y[c_row0 + lane] = f32_to_bf16_bits(y);
+    }
+#pragma unroll
+    for (int rr = 0; rr < kDecRows; ++rr) rsum[rr] = 0.f;
+  };
+
+  while (c_unit < nunits) {
+#pragma unroll
+    for (int i = 0; i < kDecDepth; ++i) {
+      if (c_unit < nunits) {
+        const DecStep cur = buf[i];
+        load_next(buf[i]);
+        dec_compute_step(cur, c_st, xs, lut, lane, c_dq, mu, rsum);
+        if (++c_st == nsteps) {
+          finish_unit();
+          c_st = 0;
+          c_unit += W;
+          enter_unit();
+        }
       }
     }
   }
 
-  // ---- exit: the last CTA returns the flags to zero ---------------------------
+  // ---- exit: the last CTA returns the counters to zero ------------------------
   __syncthreads();
   if (tid == 0) {
-    const unsigned int prev = atomicAdd(&flags[kDecFlagExit], 1u);
+    const unsigned int prev = atomicAdd(&zero_area[kDecFlagExit], 1u);
     if (prev == static_cast<unsigned>(G) - 1u) {
-      atomicExch(&flags[kDecFlagArrive], 0u);
-      atomicExch(&flags[kDecFlagUReady], 0u);
-      atomicExch(&flags[kDecFlagExit], 0u);
+      atomicExch(&zero_area[kDecFlagReady], 0u);
+      atomicExch(&zero_area[kDecFlagExit], 0u);
     }
   }
 }

@@ -1,7 +1,5 @@
 // qlora_simt.cuh -- CUDA-core kernels of the QLoRA layer:
 //   * the LoRA projections u = s X A^T (forward) and v = s dY B (backward);
-//   * the small-M fused forward (decode): split-K over the 4-bit weight,
-//     decoded in registers, bound by the bytes of the packed weight;
 //   * a tiled fused GEMM used for shapes the tensor-core kernel does not take.
 //
 // Layer ("PEFT course notes" §2.2, h = Wx + BAx with W in R^{d x k},
@@ -64,112 +62,6 @@ lora_proj_kernel(const uint16_t *__restrict__ P, int64_t M, int64_t K,
       const int64_t gm = m0 + tm + 32 * i, gn = n0 + tn + j;
       if (gm < M && gn < N) C[gm * N + gn] = s * acc[i][j];
     }
-}
-
-// ---------------------------------------------------------------------------
-// Small-M fused forward (M <= kGemvMaxM).  Grid: (row groups, k splits).
-// One warp owns one weight row per iteration; each lane streams 16-byte code
-// chunks (32 elements, half a 64-block), decodes through a shared LUT and
-// accumulates sum_e c[code_e] x[t, e] per token, scaled once per chunk by the
-// block constant.  Partial sums of the k splits go to `part` (fp32
-// [splits x M x d]); the last split to finish a row group reduces them in
-// order, adds the adapter term u B^T and writes bf16 Y.  Counters live in the
-// workspace and are returned to zero by the reducing CTA.
-// ---------------------------------------------------------------------------
-constexpr int kGemvMaxM = 16;
-constexpr int kGemvWarps = 8;           // rows per CTA
-constexpr int kGemvThreads = kGemvWarps * 32;
-
-template <int MT>
-__global__ void __launch_bounds__(kGemvThreads)
-qlora_fwd_gemv_kernel(QnNF4View q, const uint16_t *__restrict__ X, int M,
-                      const float *__restrict__ u, const uint16_t *__restrict__ Bm, int r,
-                      uint16_t *__restrict__ Y, float *__restrict__ part,
-                      unsigned int *__restrict__ counters, int splits, int64_t chunks_per_split) {
-  __shared__ float s_lut[16];
-  __shared__ bool s_last;
-  if (threadIdx.x < 16) s_lut[threadIdx.x] = c_nf4_levels[threadIdx.x];
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t d = q.d, k = q.k;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kGemvWarps + warp;
-  const int split = blockIdx.y;
-  const int64_t nchunk_row = k / 32;  // 16-byte chunks per row
-  const int64_t c_begin = split * chunks_per_split;
-  const int64_t c_end = (c_begin + chunks_per_split < nchunk_row) ? c_begin + chunks_per_split : nchunk_row;
-
-  float acc[MT];
-#pragma unroll
-  for (int t = 0; t < MT; ++t) acc[t] = 0.f;
-  if (row < d) {
-    const uint4 *wrow = reinterpret_cast<const uint4 *>(q.codes + row * (k / 2));
-    for (int64_t c = c_begin + lane; c < c_end; c += 32) {
-      const uint4 w4 = __ldcs(wrow + c);
-      const float m = block_scale(q, row * (k / 64) + (c >> 1));
-      const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-      float dec[32];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) dec[8 * i + j] = s_lut[(w[i] >> (4 * j)) & 15u];
-#pragma unroll
-      for (int t = 0; t < MT; ++t) {
-        if (t < M) {
-          const uint4 *xp = reinterpret_cast<const uint4 *>(X + t * k + c * 32);
-          float sum = 0.f;
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const uint4 xv = __ldg(xp + v);
-            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              sum = fmaf(dec[8 * v + 2 * h], __uint_as_float(xw[h] << 16), sum);
-              sum = fmaf(dec[8 * v + 2 * h + 1], __uint_as_float(xw[h] & 0xFFFF0000u), sum);
-            }
-          }
-          acc[t] = fmaf(sum, m, acc[t]);
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < MT; ++t) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], off);
-  }
-  if (splits == 1) {
-    if (row < d && lane < M) {
-      float y = 0.f;
-#pragma unroll
-      for (int t = 0; t < MT; ++t) if (t == lane) y = acc[t];
-      for (int j = 0; j < r; ++j) y = fmaf(u[lane * r + j], bf16_bits_to_f32(Bm[row * r + j]), y);
-      Y[lane * d + row] = f32_to_bf16_bits(y);
-    }
-    return;
-  }
-  // Split-K: publish partials, the last CTA of this row group reduces.
-  if (row < d && lane < M) {
-    float y = 0.f;
-#pragma unroll
-    for (int t = 0; t < MT; ++t) if (t == lane) y = acc[t];
-    part[(static_cast<int64_t>(split) * M + lane) * d + row] = y;
-  }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned int prev = atomicAdd(&counters[blockIdx.x], 1u);
-    s_last = (prev == static_cast<unsigned int>(splits - 1));
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (row < d && lane < M) {
-    float y = 0.f;
-    for (int sp = 0; sp < splits; ++sp) y += __ldcg(&part[(static_cast<int64_t>(sp) * M + lane) * d + row]);
-    for (int j = 0; j < r; ++j) y = fmaf(u[lane * r + j], bf16_bits_to_f32(Bm[row * r + j]), y);
-    Y[lane * d + row] = f32_to_bf16_bits(y);
-  }
-  if (threadIdx.x == 0) counters[blockIdx.x] = 0u;
 }
 
 // ---------------------------------------------------------------------------

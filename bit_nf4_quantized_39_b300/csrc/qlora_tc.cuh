@@ -375,39 +375,13 @@ inline size_t tc_ws_bytes(int64_t M, int64_t, int64_t, int32_t r) {
   return ((static_cast<size_t>(M) * 2 * R * sizeof(uint16_t)) + 255) & ~static_cast<size_t>(255);
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
-// (the library links only the runtime).
-inline EncodeTiledFn encode_tiled_fn() {
-  static const EncodeTiledFn fn = [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      p = nullptr;
-    return reinterpret_cast<EncodeTiledFn>(p);
-  }();
-  return fn;
-}
-
 // Tensor map of a row-major bf16 matrix [rows x cols] read in boxes of
 // box_rows rows x 64 columns (128 bytes, the swizzle span) with the 128-byte
 // swizzle; rows beyond the matrix read as zero.
 inline const char *make_bf16_tile_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
                                       uint32_t box_rows) {
-  const EncodeTiledFn enc = encode_tiled_fn();
-  if (!enc) return "cuTensorMapEncodeTiled unavailable";
-  const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
-  const cuuint32_t box[2] = {64, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? nullptr : "cuTensorMapEncodeTiled rejected the operand";
+  return make_tile_map(map, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, cols, rows, 64, box_rows,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace qn
