@@ -210,7 +210,7 @@ size_t fwd_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
 }
 
 size_t bwd_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
-  return kSemBytes + round256(static_cast<size_t>(M) * r * sizeof(float)) + qn::tc_ws_bytes(M, k, d, r);
+  return kSemBytes + round256(static_cast<size_t>(M) * r * sizeof(float)) + qn::tc_bwd_ws_bytes(M, d, k, r);
 }
 
 // Launch with programmatic stream serialisation (PDL): the kernel may start
@@ -357,6 +357,43 @@ qn_status check_layer(const qn_nf4 *Q, const void *in, int64_t M, const void *A,
   if (!in || !A || !B || !out) return fail(QN_EINVAL, "NULL tensor pointer");
   if (!aligned(in, 16) || !aligned(A, 16) || !aligned(B, 16) || !aligned(out, 16))
     return fail(QN_EALIGN, "tensor pointers must be 16-byte aligned");
+  return QN_OK;
+}
+
+// Large-M backward dX on the tensor cores: W^T dequantised into the
+// workspace, v = s dY B split into bf16 hi/lo halves, then one CTA per 128
+// columns of W x 256 tokens (qlora_bwd_tc_kernel).
+qn_status launch_tc_bwd(const qn_nf4 *Q, const uint16_t *dY, int64_t M, const float *v, const uint16_t *A, int32_t r,
+                        uint16_t *dX, Span &sp, cudaStream_t st) {
+  const int64_t d = Q->d, k = Q->k;
+  const int R = qn::tc_pad_r(r);
+  uint16_t *v2 = sp.take<uint16_t>(static_cast<size_t>(M) * 2 * R);
+  const int64_t ldw = qn::tb_ldw(d);
+  uint16_t *wt = sp.take<uint16_t>(static_cast<size_t>(ldw) * k);
+  {
+    const int64_t n = M * R;
+    qn::u_split_kernel<<<static_cast<unsigned>(qn_ceil_div(n, 256)), 256, 0, st>>>(v, M, r, R, v2);
+    QN_LAUNCH_CHECK("u_split_kernel(v)");
+  }
+  {
+    dim3 grid(static_cast<unsigned>(k / 64), static_cast<unsigned>(qn_ceil_div(d, 64)));
+    qn::nf4_dequant_t_kernel<<<grid, 256, 0, st>>>(view_of(Q), ldw, wt);
+    QN_LAUNCH_CHECK("nf4_dequant_t_kernel");
+  }
+  CUtensorMap amap, bmap;
+  if (const char *e = qn::make_tile_map(&amap, wt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(d),
+                                        static_cast<uint64_t>(k), 64, qn::kTcBN, CU_TENSOR_MAP_SWIZZLE_128B,
+                                        static_cast<uint64_t>(ldw) * 2))
+    return fail(QN_ECUDA, "tcgen05 backward: %s", e);
+  if (const char *e = qn::make_bf16_tile_map(&bmap, dY, static_cast<uint64_t>(d), static_cast<uint64_t>(M), qn::kTcBM))
+    return fail(QN_ECUDA, "tcgen05 backward: %s", e);
+  const size_t smem = qn::tb_smem_bytes(R);
+  QN_TRY(cuda_check(cudaFuncSetAttribute(qn::qlora_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(qn::tb_smem_bytes(qn::kTcMaxR))),
+                    "tcgen05 backward shared-memory limit"));
+  dim3 grid(static_cast<unsigned>(qn_ceil_div(k, qn::kTcBN)), static_cast<unsigned>(qn_ceil_div(M, qn::kTcBM)));
+  qn::qlora_bwd_tc_kernel<<<grid, qn::kTcThreads, smem, st>>>(amap, bmap, M, d, k, A, r, R, v2, dX);
+  QN_LAUNCH_CHECK("qlora_bwd_tc_kernel");
   return QN_OK;
 }
 
@@ -562,6 +599,7 @@ qn_status qlora_linear_bwd_dx(const qn_nf4 *Q, const uint16_t *dY, int64_t M, co
     qn::lora_proj_kernel<<<grid, 256, 0, st>>>(dY, M, d, B, r, 1, r, s, v);
     QN_LAUNCH_CHECK("lora_proj_kernel(dY B)");
   }
+  if (qn::tc_bwd_supported(M, d, k, r)) return launch_tc_bwd(Q, dY, M, v, A, r, dX, sp, st);
   dim3 grid(static_cast<unsigned>(qn_ceil_div(k, qn::kTileN)), static_cast<unsigned>(qn_ceil_div(M, qn::kTileM)));
   qn::qlora_gemm_simt_kernel<true><<<grid, 256, 0, st>>>(view_of(Q), dY, M, v, A, r, dX);
   QN_LAUNCH_CHECK("qlora_gemm_simt_kernel<bwd>");

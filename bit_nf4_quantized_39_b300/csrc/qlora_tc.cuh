@@ -363,16 +363,256 @@ qlora_fwd_tc_kernel(const __grid_constant__ CUtensorMap xmap, QnNF4View q, int64
 }
 
 // ---------------------------------------------------------------------------
+// Backward dX = dY deq(Q) + s (dY B) A on the tensor cores, as
+//   dX^T tile [128 columns of W x 256 tokens] = W^T tile . dY tile^T + A^T . V2^T
+// with W^T the dequantised weight transposed (bf16, written once per call by
+// nf4_dequant_t_kernel) so that both operands stream K-major (K = d) through
+// TMA, and the adapter term as one more MMA with K = 2R: A = [A^T | A^T] in
+// tensor memory, the column operand V2 = [bf16(v) | bf16(v - bf16(v))] with
+// v = s dY B.
+// Warps: 0-3 adapter operands then epilogue, 4 TMA producer, 5 MMA issuer.
+// ---------------------------------------------------------------------------
+constexpr int kTbStages = 3;
+constexpr uint32_t kTbAStageBytes = kTcBN * kTcBK * 2;  // 16 KiB
+constexpr uint32_t kTbStageBytes = kTbAStageBytes + kTcXStageBytes;  // 48 KiB
+__host__ __device__ constexpr size_t tb_smem_bytes(int R) {
+  return 1024 + static_cast<size_t>(kTbStages) * kTbStageBytes + tc_u_bytes(R) + 256;
+}
+
+// W^T[c, r] = bf16(level[code(r, c)] * m(r, c / 64)) for a 64 x 64 tile; W^T
+// has row stride ldw (d rounded up to a multiple of 8).
+__global__ void __launch_bounds__(256) nf4_dequant_t_kernel(QnNF4View q, int64_t ldw, uint16_t *__restrict__ wt) {
+  __shared__ float lv[16];
+  __shared__ uint16_t tile[64][64 + 2];  // [column of W][row of W]
+  const int tid = threadIdx.x;
+  if (tid < 16) lv[tid] = c_nf4_levels[tid];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64, c0 = static_cast<int64_t>(blockIdx.x) * 64;
+  const int rr = tid >> 2, part = tid & 3;  // row of the tile, 16-column quarter
+  const int64_t row = r0 + rr;
+  uint2 w = make_uint2(0u, 0u);
+  float m = 0.f;
+  if (row < q.d) {
+    w = __ldg(reinterpret_cast<const uint2 *>(q.codes + row * (q.k >> 1) + (c0 >> 1)) + part);
+    m = block_scale(q, row * (q.k >> 6) + (c0 >> 6));
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t word = (i < 8) ? w.x : w.y;
+    const uint32_t code = (word >> (4 * (i & 7))) & 15u;
+    tile[part * 16 + i][rr] = f32_to_bf16_bits(__fmul_rn(lv[code], m));
+  }
+  __syncthreads();
+  // 64 rows of W^T (columns c0 ..) x 64 entries (rows r0 ..): 16 threads per row, 4 entries each
+  const int oc = tid >> 2, seg = tid & 3;
+  const int64_t col = c0 + oc;
+  if (col < q.k) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int e0 = seg * 16 + h * 8;
+      if (r0 + e0 + 8 <= q.d) {
+        uint4 v;
+        v.x = tile[oc][e0] | (static_cast<uint32_t>(tile[oc][e0 + 1]) << 16);
+        v.y = tile[oc][e0 + 2] | (static_cast<uint32_t>(tile[oc][e0 + 3]) << 16);
+        v.z = tile[oc][e0 + 4] | (static_cast<uint32_t>(tile[oc][e0 + 5]) << 16);
+        v.w = tile[oc][e0 + 6] | (static_cast<uint32_t>(tile[oc][e0 + 7]) << 16);
+        *reinterpret_cast<uint4 *>(wt + col * ldw + r0 + e0) = v;
+      } else {
+        for (int e = e0; e < e0 + 8 && r0 + e < q.d; ++e) wt[col * ldw + r0 + e] = tile[oc][e];
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+qlora_bwd_tc_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap, int64_t M,
+                    int64_t d, int64_t k, const uint16_t *__restrict__ Am, int r, int R,
+                    const uint16_t *__restrict__ v2, uint16_t *__restrict__ dX) {
+  extern __shared__ __align__(1024) unsigned char tb_smem_raw[];
+  unsigned char *base = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(tb_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char *ring = base;  // stage s: A tile (16 KiB) then B tile (32 KiB)
+  unsigned char *utile = base + kTbStages * kTbStageBytes;
+  TcBars *bars = reinterpret_cast<TcBars *>(utile + tc_u_bytes(R));
+  volatile int *abort = &bars->abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kTcBN;  // columns of W (rows of the MMA)
+  const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kTcBM;  // tokens
+  const int nk = static_cast<int>((d + kTcBK - 1) / kTcBK);
+
+  if (tid == 0) {
+    for (int i = 0; i < kTbStages; ++i) {
+      mbar_init(smem_u32(&bars->x_full[i]), 1);
+      mbar_init(smem_u32(&bars->x_empty[i]), 1);
+    }
+    mbar_init(smem_u32(&bars->lora_full), 4);
+    mbar_init(smem_u32(&bars->acc_full), 1);
+    mbar_init(smem_u32(&bars->done), 1);
+    bars->abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&amap);
+    tma_prefetch_desc(&bmap);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp < 4) {
+    // ===================== adapter operands, then epilogue =====================
+    const int64_t c = c0 + tid;  // this thread's column of W = TMEM lane tid
+    const bool col_ok = c < k;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    // V2 tile into shared memory, canonical K-major layout without swizzle.
+    {
+      const int kgroups = (2 * R) / 8;
+      for (int tt = tid; tt < kTcBM; tt += 128) {
+        const int64_t t = m0 + tt;
+        for (int gi = 0; gi < kgroups; ++gi) {
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (t < M) v = __ldg(reinterpret_cast<const uint4 *>(v2 + t * 2 * R) + gi);
+          const uint32_t off = ((tt >> 3) * kgroups + gi) * 128 + (tt & 7) * 16;
+          *reinterpret_cast<uint4 *>(utile + off) = v;
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    // [A^T | A^T] of this column into tensor memory: element q is A[q, c].
+    {
+      uint32_t v[32];
+      const int half = R / 2;
+#pragma unroll
+      for (int cc = 0; cc < 32; ++cc) {
+        const int j = 2 * (cc % half);
+        uint32_t w = 0;
+        if (col_ok && cc < 2 * half) {
+          const uint32_t lo = (j < r) ? Am[static_cast<int64_t>(j) * k + c] : 0u;
+          const uint32_t hi = (j + 1 < r) ? Am[static_cast<int64_t>(j + 1) * k + c] : 0u;
+          w = lo | (hi << 16);
+        }
+        v[cc] = w;
+      }
+      tmem_st_x32(lane_addr + kLoraCol, v);
+      if (R > 32) {
+#pragma unroll
+        for (int cc0 = 0; cc0 < 32; ++cc0) {
+          const int cc = 32 + cc0;
+          const int j = 2 * (cc % half);
+          uint32_t w = 0;
+          if (col_ok && cc < 2 * half) {
+            const uint32_t lo = (j < r) ? Am[static_cast<int64_t>(j) * k + c] : 0u;
+            const uint32_t hi = (j + 1 < r) ? Am[static_cast<int64_t>(j + 1) * k + c] : 0u;
+            w = lo | (hi << 16);
+          }
+          v[cc0] = w;
+        }
+        tmem_st_x32(lane_addr + kLoraCol + 32, v);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->lora_full));
+    }
+    // Epilogue: accumulator lane = this column, columns = tokens.
+    bool ok = mbar_wait(smem_u32(&bars->acc_full), 0, abort);
+    if (__all_sync(0xffffffffu, ok)) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int cb = 0; cb < kTcBM / 32; ++cb) {
+        uint32_t acc[32];
+        tmem_ld_x32(lane_addr + kAccCol + cb * 32, acc);
+        tmem_ld_wait();
+        if (col_ok) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int64_t t = m0 + cb * 32 + j;
+            if (t < M) dX[t * k + c] = f32_to_bf16_bits(__uint_as_float(acc[j]));
+          }
+        }
+      }
+    }
+  } else if (warp == 4) {
+    // =============================== TMA producer ===============================
+    if (lane == 0) {
+      int issued = 0;
+      for (int s = 0; s < nk; ++s) {
+        const int st = s % kTbStages;
+        if (s >= kTbStages && !mbar_wait(smem_u32(&bars->x_empty[st]), ((s / kTbStages) - 1) & 1, abort)) break;
+        const uint32_t full = smem_u32(&bars->x_full[st]);
+        mbar_arrive_expect_tx(full, kTbStageBytes);
+        unsigned char *stage = ring + st * kTbStageBytes;
+        tma_load_2d(smem_u32(stage), &amap, s * kTcBK, static_cast<int32_t>(c0), full);
+        tma_load_2d(smem_u32(stage + kTbAStageBytes), &bmap, s * kTcBK, static_cast<int32_t>(m0), full);
+        ++issued;
+      }
+      for (int s = (issued > kTbStages ? issued - kTbStages : 0); s < issued; ++s)
+        mbar_wait(smem_u32(&bars->x_full[s % kTbStages]), (s / kTbStages) & 1, abort);
+    }
+  } else {
+    // ================================ MMA issuer ================================
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kTcBN, kTcBM);
+      const uint32_t d_tmem = tmem + kAccCol;
+      bool ok = mbar_wait(smem_u32(&bars->lora_full), 0, abort);
+      if (ok) {
+        tc_fence_after();
+        const uint32_t ubase = smem_u32(utile);
+        const uint32_t sbo = static_cast<uint32_t>((2 * R) / 8) * 128u;
+        for (int kc = 0; kc < (2 * R) / 16; ++kc) {
+          const uint64_t bdesc = smem_desc(ubase + kc * 256, 128, sbo, 0);
+          tc_mma_tmem_a(d_tmem, tmem + kLoraCol + kc * 8, bdesc, idesc, kc > 0 ? 1u : 0u);
+        }
+      }
+      for (int s = 0; s < nk && ok; ++s) {
+        const int st = s % kTbStages;
+        ok = mbar_wait(smem_u32(&bars->x_full[st]), (s / kTbStages) & 1, abort);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t abase = smem_u32(ring + st * kTbStageBytes);
+        const uint32_t bbase = abase + kTbAStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < kTcBK / 16; ++kk)
+          tc_mma_ss(d_tmem, smem_desc(abase + kk * 32, 16, 1024, 2), smem_desc(bbase + kk * 32, 16, 1024, 2), idesc, 1u);
+        tc_commit(smem_u32(&bars->x_empty[st]));
+      }
+      if (ok) tc_commit(smem_u32(&bars->acc_full));
+      tc_commit(smem_u32(&bars->done));
+      mbar_wait(smem_u32(&bars->done), 0, abort);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 inline bool tc_supported(int64_t M, int64_t d, int64_t k, int32_t r) {
   (void)d;
   return M > 16 && r <= kTcMaxR && (k % kTcBK) == 0 && k >= kTcBK;
 }
-inline bool tc_bwd_supported(int64_t, int64_t, int64_t, int32_t) { return false; }
+inline bool tc_bwd_supported(int64_t M, int64_t d, int64_t k, int32_t r) {
+  return M > 16 && r <= kTcMaxR && (d % 8) == 0 && k >= kTcBK;
+}
 inline size_t tc_ws_bytes(int64_t M, int64_t, int64_t, int32_t r) {
   const int R = tc_pad_r(r);
   return ((static_cast<size_t>(M) * 2 * R * sizeof(uint16_t)) + 255) & ~static_cast<size_t>(255);
+}
+inline int64_t tb_ldw(int64_t d) { return (d + 7) & ~int64_t{7}; }
+inline size_t tc_bwd_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
+  return tc_ws_bytes(M, d, k, r) + ((static_cast<size_t>(tb_ldw(d)) * k * 2 + 255) & ~static_cast<size_t>(255));
 }
 
 // Tensor map of a row-major bf16 matrix [rows x cols] read in boxes of

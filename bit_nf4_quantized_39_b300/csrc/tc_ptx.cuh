@@ -111,6 +111,15 @@ __device__ __forceinline__ void tc_mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, 
       ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[smem desc] * B[smem desc]; kind::f16 (bf16 inputs, fp32 accumulate).
+__device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrives on `bar` once every tcgen05 operation issued so far by this thread completes.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
@@ -185,15 +194,16 @@ inline EncodeTiledFn encode_tiled_fn() {
 }
 
 // 2-D tensor map of a row-major matrix [rows x cols] of `dtype` elements
-// (elem_bytes each, rows 16-byte aligned) read in boxes of box_rows x
-// box_cols with the given swizzle; out-of-range elements read as zero.
+// (elem_bytes each; row stride row_bytes, a multiple of 16, or cols *
+// elem_bytes when 0) read in boxes of box_rows x box_cols with the given
+// swizzle; out-of-range elements read as zero.
 inline const char *make_tile_map(CUtensorMap *map, const void *base, CUtensorMapDataType dtype, uint32_t elem_bytes,
                                  uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows,
-                                 CUtensorMapSwizzle swizzle) {
+                                 CUtensorMapSwizzle swizzle, uint64_t row_bytes = 0) {
   const EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return "cuTensorMapEncodeTiled unavailable";
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * elem_bytes};
+  const cuuint64_t strides[1] = {row_bytes ? row_bytes : cols * elem_bytes};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(map, dtype, 2, const_cast<void *>(base), dims, strides, box, estr,

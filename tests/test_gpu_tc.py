@@ -1,4 +1,4 @@
-"""GPU parity of the tensor-core forward (M > 16, r <= 64, the tcgen05 kernel)
+"""GPU parity of the tensor-core forward and backward (M > 16, r <= 64, the tcgen05 kernels)
 against the float64 oracle, relative Frobenius error <= 5e-3.
 
 The shapes put ragged edges on every tile boundary of that kernel: weight
@@ -60,3 +60,34 @@ def test_tc_forward_degenerate_terms(qn):
     assert layer.rel_fro(Y, ref) < TOL
     Y, ref = _fwd(qn, np.zeros((256, 256), np.float32), c["X"], c["A"], c["B"], c["alpha"])  # adapter only
     assert layer.rel_fro(Y, ref) < TOL
+
+
+def _bwd(qn, W, dY, A, B, alpha, dq=True):
+    q = qn.nf4_quantize(torch.from_numpy(W).cuda(), dq=dq)
+    Wd = nf4.dequantize(nf4.quantize(W, 64, dq=dq)).reshape(W.shape)
+    dX = qn.qlora_linear_bwd_dx(q, dY.cuda(), A.cuda(), B.cuda(), alpha)
+    qn.device_status()
+    return _f64(dX), layer.linear_bwd_dx(_f64(dY), Wd, _f64(A), _f64(B), alpha, A.shape[0])
+
+
+# The backward runs on the tensor cores for M > 16, r <= 64 and d a multiple
+# of 8 (dequantised W^T in the workspace, then a tcgen05 GEMM); the shapes put
+# ragged edges on its 128-column and 256-token tiles and on the K = d loop.
+@pytest.mark.parametrize("M,d,k,r", [
+    (17, 128, 64, 8), (256, 256, 128, 16), (257, 384, 192, 1), (300, 200, 576, 33),
+    (600, 1000, 256, 64), (1024, 520, 1024, 40), (40, 130, 64, 65),
+])
+def test_tc_backward_shapes(qn, M, d, k, r):
+    c = synth.layer_case(seed=M + 5 * d + k, d=d, k=k, M=M, r=r, alpha=2.0 * r)
+    dX, ref = _bwd(qn, c["W"], c["dY"], c["A"], c["B"], c["alpha"])
+    assert layer.rel_fro(dX, ref) < TOL, (M, d, k, r)
+
+
+def test_tc_backward_exact_absmax_and_degenerate(qn):
+    c = synth.layer_case(seed=7, d=384, k=320, M=200, r=16)
+    dX, ref = _bwd(qn, c["W"], c["dY"], c["A"], c["B"], c["alpha"], dq=False)
+    assert layer.rel_fro(dX, ref) < TOL
+    dX, ref = _bwd(qn, c["W"], c["dY"], torch.zeros_like(c["A"]), c["B"], c["alpha"])   # no adapter
+    assert layer.rel_fro(dX, ref) < TOL
+    dX, ref = _bwd(qn, np.zeros((384, 320), np.float32), c["dY"], c["A"], c["B"], c["alpha"])  # adapter only
+    assert layer.rel_fro(dX, ref) < TOL
