@@ -203,14 +203,20 @@ qn_status launch_dequantize(const qn_nf4 *Q, void *out, qn_dtype odt, cudaStream
 bool use_decode(int64_t M, int64_t k) { return M == 1 && k <= qn::kDecMaxK; }
 bool use_skinny(int64_t M, int64_t k) { return M <= qn::kSkMaxM && k <= 64 * qn::kSkMaxNb; }
 
+// Split-K partial sums of the adapter projection (large-M paths).
+size_t proj_ws_bytes(int64_t M, int32_t r) {
+  return round256(static_cast<size_t>(qn::kProjMaxSplit) * M * r * sizeof(float));
+}
+
 size_t fwd_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
   size_t b = kSemBytes + round256(static_cast<size_t>(M) * r * sizeof(float));  // u
-  if (!use_skinny(M, k)) b += qn::tc_ws_bytes(M, d, k, r);
+  if (!use_skinny(M, k)) b += proj_ws_bytes(M, r) + qn::tc_ws_bytes(M, d, k, r);
   return b;
 }
 
 size_t bwd_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
-  return kSemBytes + round256(static_cast<size_t>(M) * r * sizeof(float)) + qn::tc_bwd_ws_bytes(M, d, k, r);
+  return kSemBytes + round256(static_cast<size_t>(M) * r * sizeof(float)) + proj_ws_bytes(M, r) +
+         qn::tc_bwd_ws_bytes(M, d, k, r);
 }
 
 // Launch with programmatic stream serialisation (PDL): the kernel may start
@@ -360,21 +366,39 @@ qn_status check_layer(const qn_nf4 *Q, const void *in, int64_t M, const void *A,
   return QN_OK;
 }
 
+// Adapter projection C = s P Qop^T (M x N, K deep) split over K so that at
+// least two waves of CTAs run, then the splits summed in order into C32 (fp32)
+// or, with C2 set, its bf16 hi/lo split (each half padded to R columns).
+qn_status launch_lora_proj(const uint16_t *P, int64_t M, int64_t K, const uint16_t *Qm, int64_t N, int64_t qs_n,
+                           int64_t qs_k, float s, float *part, float *C32, int R, uint16_t *C2, cudaStream_t st) {
+  const int64_t tiles = qn_ceil_div(M, qn::kProjTM) * qn_ceil_div(N, qn::kProjTN);
+  int64_t S = qn_ceil_div(2 * static_cast<int64_t>(sm_count()), tiles);
+  const int64_t smax = qn_ceil_div(K, 256);
+  if (S > smax) S = smax;
+  if (S > qn::kProjMaxSplit) S = qn::kProjMaxSplit;
+  if (S < 1) S = 1;
+  const int64_t kchunk = qn_ceil_div(qn_ceil_div(K, S), qn::kProjTK) * qn::kProjTK;
+  S = qn_ceil_div(K, kchunk);
+  dim3 grid(static_cast<unsigned>(qn_ceil_div(M, qn::kProjTM)), static_cast<unsigned>(qn_ceil_div(N, qn::kProjTN)),
+            static_cast<unsigned>(S));
+  qn::lora_proj_kernel<<<grid, 256, 0, st>>>(P, M, K, Qm, N, qs_n, qs_k, s, kchunk, part);
+  QN_LAUNCH_CHECK("lora_proj_kernel");
+  const int64_t n = M * (C2 ? R : N);
+  qn::lora_reduce_kernel<<<static_cast<unsigned>(qn_ceil_div(n, 256)), 256, 0, st>>>(part, static_cast<int>(S), M, N,
+                                                                                      C32, R, C2);
+  QN_LAUNCH_CHECK("lora_reduce_kernel");
+  return QN_OK;
+}
+
 // Large-M backward dX on the tensor cores: W^T dequantised into the
-// workspace, v = s dY B split into bf16 hi/lo halves, then one CTA per 128
-// columns of W x 256 tokens (qlora_bwd_tc_kernel).
-qn_status launch_tc_bwd(const qn_nf4 *Q, const uint16_t *dY, int64_t M, const float *v, const uint16_t *A, int32_t r,
-                        uint16_t *dX, Span &sp, cudaStream_t st) {
+// workspace, then one CTA per 128 columns of W x 256 tokens
+// (qlora_bwd_tc_kernel); v2 is the bf16 hi/lo split of v = s dY B.
+qn_status launch_tc_bwd(const qn_nf4 *Q, const uint16_t *dY, int64_t M, const uint16_t *v2, const uint16_t *A,
+                        int32_t r, uint16_t *dX, Span &sp, cudaStream_t st) {
   const int64_t d = Q->d, k = Q->k;
   const int R = qn::tc_pad_r(r);
-  uint16_t *v2 = sp.take<uint16_t>(static_cast<size_t>(M) * 2 * R);
   const int64_t ldw = qn::tb_ldw(d);
   uint16_t *wt = sp.take<uint16_t>(static_cast<size_t>(ldw) * k);
-  {
-    const int64_t n = M * R;
-    qn::u_split_kernel<<<static_cast<unsigned>(qn_ceil_div(n, 256)), 256, 0, st>>>(v, M, r, R, v2);
-    QN_LAUNCH_CHECK("u_split_kernel(v)");
-  }
   {
     dim3 grid(static_cast<unsigned>(k / 64), static_cast<unsigned>(qn_ceil_div(d, 64)));
     qn::nf4_dequant_t_kernel<<<grid, 256, 0, st>>>(view_of(Q), ldw, wt);
@@ -397,17 +421,11 @@ qn_status launch_tc_bwd(const qn_nf4 *Q, const uint16_t *dY, int64_t M, const fl
   return QN_OK;
 }
 
-// Large-M forward on the tensor cores: split u into bf16 hi/lo halves, then
-// one CTA per 128 weight rows x 256 tokens (qlora_fwd_tc_kernel).
-qn_status launch_tc_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M, const float *u, const uint16_t *B, int32_t r,
-                        uint16_t *Y, Span &sp, cudaStream_t st) {
+// Large-M forward on the tensor cores: one CTA per 128 weight rows x 256
+// tokens (qlora_fwd_tc_kernel); u2 is the bf16 hi/lo split of u = s X A^T.
+qn_status launch_tc_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M, const uint16_t *u2, const uint16_t *B,
+                        int32_t r, uint16_t *Y, cudaStream_t st) {
   const int R = qn::tc_pad_r(r);
-  uint16_t *u2 = sp.take<uint16_t>(static_cast<size_t>(M) * 2 * R);
-  {
-    const int64_t n = M * R;
-    qn::u_split_kernel<<<static_cast<unsigned>(qn_ceil_div(n, 256)), 256, 0, st>>>(u, M, r, R, u2);
-    QN_LAUNCH_CHECK("u_split_kernel");
-  }
   CUtensorMap xmap;
   if (const char *e = qn::make_bf16_tile_map(&xmap, X, static_cast<uint64_t>(Q->k), static_cast<uint64_t>(M), qn::kTcBM))
     return fail(QN_ECUDA, "tcgen05 forward: %s", e);
@@ -537,12 +555,14 @@ qn_status qlora_linear_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M, const 
   if (use_decode(M, k)) return launch_decode_group(1, &Q, X, &A, &B, &r, &alpha, &Y, sem, sp, st);
   if (use_skinny(M, k)) return launch_skinny_group(1, &Q, X, M, &A, &B, &r, &alpha, &Y, sp, st);
   float *u = sp.take<float>(static_cast<size_t>(M) * r);
-  {
-    dim3 grid(static_cast<unsigned>(qn_ceil_div(M, qn::kProjTM)), static_cast<unsigned>(qn_ceil_div(r, qn::kProjTN)));
-    qn::lora_proj_kernel<<<grid, 256, 0, st>>>(X, M, k, A, r, k, 1, s, u);
-    QN_LAUNCH_CHECK("lora_proj_kernel");
+  float *part = sp.take<float>(static_cast<size_t>(qn::kProjMaxSplit) * M * r);
+  if (qn::tc_supported(M, d, k, r)) {
+    const int R = qn::tc_pad_r(r);
+    uint16_t *u2 = sp.take<uint16_t>(static_cast<size_t>(M) * 2 * R);
+    QN_TRY(launch_lora_proj(X, M, k, A, r, k, 1, s, part, nullptr, R, u2, st));
+    return launch_tc_fwd(Q, X, M, u2, B, r, Y, st);
   }
-  if (qn::tc_supported(M, d, k, r)) return launch_tc_fwd(Q, X, M, u, B, r, Y, sp, st);
+  QN_TRY(launch_lora_proj(X, M, k, A, r, k, 1, s, part, u, 0, nullptr, st));
   dim3 grid(static_cast<unsigned>(qn_ceil_div(d, qn::kTileN)), static_cast<unsigned>(qn_ceil_div(M, qn::kTileM)));
   qn::qlora_gemm_simt_kernel<false><<<grid, 256, 0, st>>>(view_of(Q), X, M, u, B, r, Y);
   QN_LAUNCH_CHECK("qlora_gemm_simt_kernel<fwd>");
@@ -593,13 +613,15 @@ qn_status qlora_linear_bwd_dx(const qn_nf4 *Q, const uint16_t *dY, int64_t M, co
   (void)sp.take<unsigned int>(kSemBytes / sizeof(unsigned int));
   const float s = alpha / static_cast<float>(r);
   float *v = sp.take<float>(static_cast<size_t>(M) * r);
-  {
-    // v[m, q] = s * sum_i dY[m, i] B[i, q]: Qop(n=q, kk=i) = B[i * r + q].
-    dim3 grid(static_cast<unsigned>(qn_ceil_div(M, qn::kProjTM)), static_cast<unsigned>(qn_ceil_div(r, qn::kProjTN)));
-    qn::lora_proj_kernel<<<grid, 256, 0, st>>>(dY, M, d, B, r, 1, r, s, v);
-    QN_LAUNCH_CHECK("lora_proj_kernel(dY B)");
+  float *part = sp.take<float>(static_cast<size_t>(qn::kProjMaxSplit) * M * r);
+  // v[m, q] = s * sum_i dY[m, i] B[i, q]: Qop(n = q, kk = i) = B[i * r + q].
+  if (qn::tc_bwd_supported(M, d, k, r)) {
+    const int R = qn::tc_pad_r(r);
+    uint16_t *v2 = sp.take<uint16_t>(static_cast<size_t>(M) * 2 * R);
+    QN_TRY(launch_lora_proj(dY, M, d, B, r, 1, r, s, part, nullptr, R, v2, st));
+    return launch_tc_bwd(Q, dY, M, v2, A, r, dX, sp, st);
   }
-  if (qn::tc_bwd_supported(M, d, k, r)) return launch_tc_bwd(Q, dY, M, v, A, r, dX, sp, st);
+  QN_TRY(launch_lora_proj(dY, M, d, B, r, 1, r, s, part, v, 0, nullptr, st));
   dim3 grid(static_cast<unsigned>(qn_ceil_div(k, qn::kTileN)), static_cast<unsigned>(qn_ceil_div(M, qn::kTileM)));
   qn::qlora_gemm_simt_kernel<true><<<grid, 256, 0, st>>>(view_of(Q), dY, M, v, A, r, dX);
   QN_LAUNCH_CHECK("qlora_gemm_simt_kernel<bwd>");

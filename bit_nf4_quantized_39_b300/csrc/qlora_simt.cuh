@@ -16,31 +16,37 @@ namespace qn {
 // Skinny projection  C[m, n] = s * sum_kk P[m, kk] * Qop(n, kk)   (fp32 out)
 // with Qop(n, kk) = Qm[n * qs_n + kk * qs_k].  P is bf16 [M x K] row-major.
 // 64 x 32 output tile, K chunks of 32, 256 threads, 8 outputs per thread.
+// K is split over gridDim.z CTAs of kchunk columns each (a multiple of 32);
+// split z writes its partial sums to part + z * M * N, and
+// lora_reduce_kernel adds the splits in order.
 // ---------------------------------------------------------------------------
 constexpr int kProjTM = 64, kProjTN = 32, kProjTK = 32;
+constexpr int kProjMaxSplit = 16;
 
 __global__ void __launch_bounds__(256)
 lora_proj_kernel(const uint16_t *__restrict__ P, int64_t M, int64_t K,
                  const uint16_t *__restrict__ Qm, int64_t N, int64_t qs_n, int64_t qs_k,
-                 float s, float *__restrict__ C) {
+                 float s, int64_t kchunk, float *__restrict__ part) {
   __shared__ float sP[kProjTK][kProjTM + 1];
   __shared__ float sQ[kProjTK][kProjTN + 1];
   const int tid = threadIdx.x;
   const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kProjTM;
   const int64_t n0 = static_cast<int64_t>(blockIdx.y) * kProjTN;
+  const int64_t kb = static_cast<int64_t>(blockIdx.z) * kchunk;
+  const int64_t ke = (kb + kchunk < K) ? kb + kchunk : K;
   const int tm = tid / 8;        // 0..31 -> rows tm and tm + 32
   const int tn = (tid % 8) * 4;  // 4 consecutive columns
   float acc[2][4] = {};
-  for (int64_t k0 = 0; k0 < K; k0 += kProjTK) {
+  for (int64_t k0 = kb; k0 < ke; k0 += kProjTK) {
     for (int i = tid; i < kProjTM * kProjTK; i += 256) {
       const int r = i / kProjTK, c = i % kProjTK;
       const int64_t gm = m0 + r, gk = k0 + c;
-      sP[c][r] = (gm < M && gk < K) ? bf16_bits_to_f32(P[gm * K + gk]) : 0.f;
+      sP[c][r] = (gm < M && gk < ke) ? bf16_bits_to_f32(P[gm * K + gk]) : 0.f;
     }
     for (int i = tid; i < kProjTN * kProjTK; i += 256) {
       const int r = i / kProjTK, c = i % kProjTK;
       const int64_t gn = n0 + r, gk = k0 + c;
-      sQ[c][r] = (gn < N && gk < K) ? bf16_bits_to_f32(Qm[gn * qs_n + gk * qs_k]) : 0.f;
+      sQ[c][r] = (gn < N && gk < ke) ? bf16_bits_to_f32(Qm[gn * qs_n + gk * qs_k]) : 0.f;
     }
     __syncthreads();
 #pragma unroll 8
@@ -55,6 +61,7 @@ lora_proj_kernel(const uint16_t *__restrict__ P, int64_t M, int64_t K,
     }
     __syncthreads();
   }
+  float *C = part + static_cast<int64_t>(blockIdx.z) * M * N;
 #pragma unroll
   for (int i = 0; i < 2; ++i)
 #pragma unroll
@@ -62,6 +69,26 @@ lora_proj_kernel(const uint16_t *__restrict__ P, int64_t M, int64_t K,
       const int64_t gm = m0 + tm + 32 * i, gn = n0 + tn + j;
       if (gm < M && gn < N) C[gm * N + gn] = s * acc[i][j];
     }
+}
+
+// C = sum over the S splits of part (in split order).  Writes the fp32 result
+// to C32 (if not null) and, if C2 is not null, its bf16 hi/lo split
+// C2[m, :] = [bf16(c) | bf16(c - bf16(c))], each half zero-padded to R columns.
+__global__ void lora_reduce_kernel(const float *__restrict__ part, int S, int64_t M, int64_t N,
+                                   float *__restrict__ C32, int R, uint16_t *__restrict__ C2) {
+  const int64_t cols = C2 ? R : N;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= M * cols) return;
+  const int64_t m = i / cols, j = i % cols;
+  float v = 0.f;
+  if (j < N)
+    for (int z = 0; z < S; ++z) v += part[(static_cast<int64_t>(z) * M + m) * N + j];
+  if (C32 && j < N) C32[m * N + j] = v;
+  if (C2) {
+    const uint16_t hi = f32_to_bf16_bits(v);
+    C2[m * 2 * R + j] = hi;
+    C2[m * 2 * R + R + j] = f32_to_bf16_bits(v - bf16_bits_to_f32(hi));
+  }
 }
 
 // ---------------------------------------------------------------------------

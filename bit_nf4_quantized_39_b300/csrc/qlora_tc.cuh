@@ -18,8 +18,8 @@
 //              shared memory, D = fp32 accumulator in tensor memory.
 // The adapter term s (X A^T) B^T enters as one more MMA with K = 2R: A holds
 // [B | B] (bf16, in tensor memory) and the shared-memory operand holds
-// U2 = [hi | lo] with hi = bf16(u), lo = bf16(u - hi), u = s X A^T, so the
-// product keeps about 16 significant bits of u.
+// U2 = [hi | lo] with hi = bf16(u), lo = bf16(u - hi), u = s X A^T (written by
+// lora_reduce_kernel), so the product keeps about 16 significant bits of u.
 //
 // Tensor-memory columns: [0, 256) accumulator, [256, 384) four 32-column
 // weight stages, [384, 384 + R) the adapter operand.
@@ -105,20 +105,6 @@ struct TcBars {
   uint32_t tmem_base;
   int abort;
 };
-
-// u2[t, :] = [bf16(u) | bf16(u - bf16(u))] for t < M, zero-padded to R columns
-// each; u is the fp32 s X A^T of lora_proj_kernel.
-__global__ void u_split_kernel(const float *__restrict__ u, int64_t M, int r, int R, uint16_t *__restrict__ u2) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= M * R) return;
-  const int64_t t = i / R;
-  const int j = static_cast<int>(i % R);
-  const float v = (j < r) ? u[t * r + j] : 0.f;
-  const uint16_t hi = f32_to_bf16_bits(v);
-  const uint16_t lo = f32_to_bf16_bits(v - bf16_bits_to_f32(hi));
-  u2[t * 2 * R + j] = hi;
-  u2[t * 2 * R + R + j] = lo;
-}
 
 __global__ void __launch_bounds__(kTcThreads, 1)
 qlora_fwd_tc_kernel(const __grid_constant__ CUtensorMap xmap, QnNF4View q, int64_t M,
