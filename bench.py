@@ -344,6 +344,51 @@ def secondary(qn, device, pk, quick: bool):
     return out
 
 
+# ------------------------------------------------------------ profiling cases
+
+def profile_case(case: str):
+    """Untimed runs for ncu: `decode` / `decode16` = one layer of the decode set
+    (4 calls: q/k/v, o, gate/up, down) at M = 1 / 16, three times; `prefill` =
+    the prefill layer forward and backward, three times; `quantize` = NF4+DQ
+    quantise and dequantise of one 11008 x 4096 bf16 matrix, three times."""
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    import bit_nf4_quantized_39_b300 as qn
+    if case in ("decode", "decode16"):
+        M = 1 if case == "decode" else 16
+        mats = build_decode_set(qn, device, 1, 64, seed=1)
+        calls, Xall, Yall = decode_plan(mats, 1, M, device)
+        for _ in range(3):
+            run_calls(qn, calls, Xall, Yall, M)
+    elif case == "prefill":
+        gen = torch.Generator(device=device)
+        gen.manual_seed(2)
+        c_d, c_k, M, r = 11008, 4096, 4096, 16
+        W = torch.empty((c_d, c_k), device=device).normal_(0, 0.02, generator=gen)
+        q = qn.nf4_quantize(W, dq=True)
+        X = torch.randn((M, c_k), device=device, generator=gen).to(torch.bfloat16)
+        dY = torch.randn((M, c_d), device=device, generator=gen).to(torch.bfloat16)
+        A = torch.empty((r, c_k), device=device).normal_(0, 1 / math.sqrt(c_k), generator=gen).to(torch.bfloat16)
+        B = torch.empty((c_d, r), device=device).normal_(0, 0.01, generator=gen).to(torch.bfloat16)
+        for _ in range(3):
+            qn.qlora_linear_fwd(q, X, A, B, 32.0)
+            qn.qlora_linear_bwd_dx(q, dY, A, B, 32.0)
+    else:
+        gen = torch.Generator(device=device)
+        gen.manual_seed(3)
+        t = torch.empty((11008, 4096), dtype=torch.bfloat16, device=device)
+        synth.device_normal_(t, 0.02, gen)
+        synth.device_outliers_bernoulli_(t, 0.001, 0.2, gen)
+        qq = qn.NF4Tensor.empty(t.shape[0], t.shape[1], True, device)
+        out = torch.empty_like(t)
+        for _ in range(3):
+            qn.nf4_quantize(t, True, out=qq)
+            qn.nf4_dequantize(qq, torch.bfloat16, out=out)
+    torch.cuda.synchronize()
+    qn.device_status()
+    print(json.dumps({"profile": case, "ok": True}))
+
+
 # ------------------------------------------------------------ oracle timing
 
 def oracle_decode_sample(seconds_budget: float = 15.0):
@@ -416,8 +461,14 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--quick", action="store_true", help="shorter secondary loops")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["decode", "decode16", "prefill", "quantize"],
+                    help="run one small case of a workload a few times, untimed (for ncu captures)")
     args = ap.parse_args()
     ws, rank, local = dist_env()
+
+    if args.profile:
+        profile_case(args.profile)
+        return
 
     if args.impl == "reference":
         run_reference(args, ws, rank)
@@ -474,11 +525,12 @@ def main():
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32",
                 "data": "synthetic (seeded device draws: N(0,0.02^2) weights with 0.1% N(0,0.2^2) outliers)",
                 "config": {"workload": WORKLOAD, "M": 1, "layers": args.layers, "matrices": 7 * args.layers,
                            "weight_bytes_per_step": w4, "lora_bytes_per_step": lora,
                            "l2": "no flush: 3.34 GB weight set per step >> 126 MB L2",
+                           "arith": "fp32 FMA of NF4 levels (fp32) with bf16 x, fp32 accumulation; bf16 y",
                            "parallelism": f"replica x{ws}"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": res["launches_per_step"] * args.steps, "clocks": clocks, "secondary": extra}

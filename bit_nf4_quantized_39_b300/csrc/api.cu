@@ -381,7 +381,7 @@ qn_status launch_lora_proj(const uint16_t *P, int64_t M, int64_t K, const uint16
   S = qn_ceil_div(K, kchunk);
   dim3 grid(static_cast<unsigned>(qn_ceil_div(M, qn::kProjTM)), static_cast<unsigned>(qn_ceil_div(N, qn::kProjTN)),
             static_cast<unsigned>(S));
-  qn::lora_proj_kernel<<<grid, 256, 0, st>>>(P, M, K, Qm, N, qs_n, qs_k, s, kchunk, part);
+  qn::lora_proj_kernel<<<grid, 128, 0, st>>>(P, M, K, Qm, N, qs_n, qs_k, s, kchunk, part);
   QN_LAUNCH_CHECK("lora_proj_kernel");
   const int64_t n = M * (C2 ? R : N);
   qn::lora_reduce_kernel<<<static_cast<unsigned>(qn_ceil_div(n, 256)), 256, 0, st>>>(part, static_cast<int>(S), M, N,

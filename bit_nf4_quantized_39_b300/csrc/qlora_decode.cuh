@@ -21,10 +21,11 @@
 // * decode: x is staged once per CTA in shared memory as fp32, lane-
 //   interleaved so that each lane's 32-element chunk is read with
 //   conflict-free 128-bit loads; two codes at a time are looked up in a
-//   byte-pair table of bf16 levels replicated per lane (entry b of lane l at
-//   word 32 b + l, so a warp never conflicts on a bank), widened to fp32 and
-//   multiplied into packed fp32x2 accumulators (fma.rn.f32x2); each
-//   32-element partial is scaled by its 64-block constant;
+//   byte-pair table of fp32 level pairs replicated per lane (entry b of lane
+//   l at byte 256 b + 8 l: one byte permute forms the address, and a warp
+//   never conflicts on a bank) and multiplied into packed fp32x2
+//   accumulators (fma.rn.f32x2); each 32-element partial is scaled by its
+//   64-block constant;
 // * a unit is a whole row, so its sum is complete in one warp (no cross-warp
 //   combine, a fixed summation order): the warp adds u . B[row] and writes
 //   bf16 Y;
@@ -46,7 +47,7 @@ constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kDecRows = 2;            // weight rows per unit (whole rows)
 constexpr int kDecDepth = 4;           // lane steps whose loads are in flight per warp
-constexpr int kDecLutWords = 256 * 32;
+constexpr int kDecLutBytes = 256 * 256;  // entry b of lane l: fp32 pair at byte 256 b + 8 l
 constexpr int kDecMaxK = 16384;
 constexpr unsigned kDecSpinLimit = 1u << 22;
 // Zero-area words: adapter rows done, CTAs done.
@@ -75,7 +76,7 @@ struct DecGroup {
 // Staging covers whole 1024-element steps so that ragged tails read zeros.
 __host__ __device__ constexpr int64_t dec_xs_floats(int64_t k) { return qn_ceil_div(k, 1024) * 1024; }
 __host__ __device__ constexpr size_t dec_smem_bytes(int64_t k) {
-  return sizeof(uint32_t) * kDecLutWords + sizeof(float) * dec_xs_floats(k);
+  return kDecLutBytes + sizeof(float) * dec_xs_floats(k);
 }
 
 __device__ __forceinline__ unsigned long long pack_f2(float lo, float hi) {
@@ -145,9 +146,12 @@ __device__ __forceinline__ float dec_step_scale(const DecStep &sp, int rr, bool 
 }
 
 // Adds the dot products of one lane step of a unit's rows with the staged x.
+// Each code byte (two elements) costs one byte permute (its table address,
+// (byte << 8) | (lane << 3)), one 64-bit shared load (the two fp32 levels)
+// and one packed fp32x2 FMA.
 __device__ __forceinline__ void dec_compute_step(const DecStep &sp, int64_t st, const float *__restrict__ xs,
-                                                 const uint32_t *__restrict__ lut, int lane, bool dq, float mu,
-                                                 float (&rsum)[kDecRows]) {
+                                                 const unsigned char *__restrict__ lut, uint32_t lane8, int lane,
+                                                 bool dq, float mu, float (&rsum)[kDecRows]) {
   const float4 *xp = reinterpret_cast<const float4 *>(xs) + st * 8 * 32 + lane;
   unsigned long long acc[kDecRows];
 #pragma unroll
@@ -162,8 +166,9 @@ __device__ __forceinline__ void dec_compute_step(const DecStep &sp, int64_t st, 
       const uint32_t word = (i == 0) ? sp.w[rr].x : (i == 1) ? sp.w[rr].y : (i == 2) ? sp.w[rr].z : sp.w[rr].w;
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        const uint32_t v = lut[(((word >> (8 * b)) & 0xFFu) << 5) | lane];
-        ffma2(acc[rr], pack_f2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u)), xpair[b]);
+        uint32_t off;
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(off) : "r"(word), "r"(lane8), "r"(0x5504u | (b << 4)));
+        ffma2(acc[rr], *reinterpret_cast<const unsigned long long *>(lut + off), xpair[b]);
       }
     }
   }
@@ -207,10 +212,11 @@ __device__ __forceinline__ int dec_find(const DecGroup &g, int64_t pos, F off) {
 __global__ void __launch_bounds__(kDecThreads, 2)
 qlora_decode_kernel(const __grid_constant__ DecGroup g, unsigned int *__restrict__ zero_area, float *__restrict__ u) {
   extern __shared__ __align__(16) unsigned char dec_smem[];
-  uint32_t *lut = reinterpret_cast<uint32_t *>(dec_smem);
-  float *xs = reinterpret_cast<float *>(dec_smem + sizeof(uint32_t) * kDecLutWords);
+  unsigned char *lut = dec_smem;
+  float *xs = reinterpret_cast<float *>(dec_smem + kDecLutBytes);
   const int64_t k = g.k;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t lane8 = static_cast<uint32_t>(lane) << 3;
   const int G = gridDim.x;
   const int64_t nsteps = qn_ceil_div(k >> 5, 32);  // 1024-column lane steps per row
   // warp slots interleaved across CTAs: slot = warp * G + cta
@@ -245,8 +251,8 @@ qlora_decode_kernel(const __grid_constant__ DecGroup g, unsigned int *__restrict
   DecStep buf[kDecDepth];
 #pragma unroll
   for (int i = 0; i < kDecDepth; ++i) load_next(buf[i]);
-  __shared__ uint32_t s_lv[16];
-  if (tid < 16) s_lv[tid] = f32_to_bf16_bits(c_nf4_levels[tid]);
+  __shared__ float s_lv[16];
+  if (tid < 16) s_lv[tid] = c_nf4_levels[tid];
   {
     constexpr int kPer = 8;  // 16-byte x loads in flight per thread per round
     const int64_t nvec = dec_xs_floats(k) / 8;
@@ -273,9 +279,9 @@ qlora_decode_kernel(const __grid_constant__ DecGroup g, unsigned int *__restrict
     }
   }
   __syncthreads();  // s_lv and xs ready
-  for (int i = tid; i < kDecLutWords; i += kDecThreads) {
-    const int b = i >> 5;
-    lut[i] = (s_lv[b >> 4] << 16) | s_lv[b & 15];
+  for (int i = tid; i < 256 * 32; i += kDecThreads) {
+    const int b = i >> 5, l = i & 31;  // entry b of lane l: (level[b & 15], level[b >> 4])
+    *reinterpret_cast<float2 *>(lut + 256 * b + 8 * l) = make_float2(s_lv[b & 15], s_lv[b >> 4]);
   }
   __syncthreads();  // lut ready
 
@@ -377,7 +383,7 @@ qlora_decode_kernel(const __grid_constant__ DecGroup g, unsigned int *__restrict
       if (c_unit < nunits) {
         const DecStep cur = buf[i];
         load_next(buf[i]);
-        dec_compute_step(cur, c_st, xs, lut, lane, c_dq, mu, rsum);
+        dec_compute_step(cur, c_st, xs, lut, lane8, lane, c_dq, mu, rsum);
         if (++c_st == nsteps) {
           finish_unit();
           c_st = 0;

@@ -13,62 +13,108 @@
 namespace qn {
 
 // ---------------------------------------------------------------------------
-// Skinny projection  C[m, n] = s * sum_kk P[m, kk] * Qop(n, kk)   (fp32 out)
-// with Qop(n, kk) = Qm[n * qs_n + kk * qs_k].  P is bf16 [M x K] row-major.
-// 64 x 32 output tile, K chunks of 32, 256 threads, 8 outputs per thread.
-// K is split over gridDim.z CTAs of kchunk columns each (a multiple of 32);
-// split z writes its partial sums to part + z * M * N, and
-// lora_reduce_kernel adds the splits in order.
+// Adapter projection  C[m, n] = s * sum_kk P[m, kk] * Qop(n, kk)   (fp32 out)
+// with Qop(n, kk) = Qm[n * qs_n + kk * qs_k] and P bf16 [M x K] row-major,
+// on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).
+// CTA tile 64 x 64 (4 warps of 16 rows x 8 n8-tiles), K staged 64 at a time
+// through padded shared-memory tiles (row stride 72 elements, so fragment
+// loads do not conflict).  K is split over gridDim.z CTAs of kchunk columns
+// each (a multiple of 64); split z writes its partial sums to
+// part + z * M * N, and lora_reduce_kernel adds the splits in order.
 // ---------------------------------------------------------------------------
-constexpr int kProjTM = 64, kProjTN = 32, kProjTK = 32;
+constexpr int kProjTM = 64, kProjTN = 64, kProjTK = 64, kProjStride = kProjTK + 8;
 constexpr int kProjMaxSplit = 16;
 
-__global__ void __launch_bounds__(256)
+__device__ __forceinline__ void mma_bf16_16816_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                   uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__global__ void __launch_bounds__(128)
 lora_proj_kernel(const uint16_t *__restrict__ P, int64_t M, int64_t K,
                  const uint16_t *__restrict__ Qm, int64_t N, int64_t qs_n, int64_t qs_k,
                  float s, int64_t kchunk, float *__restrict__ part) {
-  __shared__ float sP[kProjTK][kProjTM + 1];
-  __shared__ float sQ[kProjTK][kProjTN + 1];
-  const int tid = threadIdx.x;
+  __shared__ __align__(16) uint16_t sP[kProjTM][kProjStride];
+  __shared__ __align__(16) uint16_t sQ[kProjTN][kProjStride];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
   const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kProjTM;
   const int64_t n0 = static_cast<int64_t>(blockIdx.y) * kProjTN;
   const int64_t kb = static_cast<int64_t>(blockIdx.z) * kchunk;
   const int64_t ke = (kb + kchunk < K) ? kb + kchunk : K;
-  const int tm = tid / 8;        // 0..31 -> rows tm and tm + 32
-  const int tn = (tid % 8) * 4;  // 4 consecutive columns
-  float acc[2][4] = {};
+  const bool pvec = (K % 8) == 0;
+  const bool qvec = qs_k == 1 && (qs_n % 8) == 0;
+  float acc[8][4] = {};
   for (int64_t k0 = kb; k0 < ke; k0 += kProjTK) {
-    for (int i = tid; i < kProjTM * kProjTK; i += 256) {
-      const int r = i / kProjTK, c = i % kProjTK;
-      const int64_t gm = m0 + r, gk = k0 + c;
-      sP[c][r] = (gm < M && gk < ke) ? bf16_bits_to_f32(P[gm * K + gk]) : 0.f;
+    // P tile: 64 rows x 64 columns
+    if (pvec) {
+      for (int i = tid; i < kProjTM * kProjTK / 8; i += 128) {
+        const int r = i >> 3, c = (i & 7) * 8;
+        const int64_t gm = m0 + r, gk = k0 + c;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (gm < M && gk + 8 <= ke) v = __ldg(reinterpret_cast<const uint4 *>(P + gm * K + gk));
+        else if (gm < M)
+          for (int e = 0; e < 8; ++e)
+            if (gk + e < ke) reinterpret_cast<uint16_t *>(&v)[e] = P[gm * K + gk + e];
+        *reinterpret_cast<uint4 *>(&sP[r][c]) = v;
+      }
+    } else {
+      for (int i = tid; i < kProjTM * kProjTK; i += 128) {
+        const int r = i / kProjTK, c = i % kProjTK;
+        const int64_t gm = m0 + r, gk = k0 + c;
+        sP[r][c] = (gm < M && gk < ke) ? P[gm * K + gk] : static_cast<uint16_t>(0);
+      }
     }
-    for (int i = tid; i < kProjTN * kProjTK; i += 256) {
-      const int r = i / kProjTK, c = i % kProjTK;
-      const int64_t gn = n0 + r, gk = k0 + c;
-      sQ[c][r] = (gn < N && gk < ke) ? bf16_bits_to_f32(Qm[gn * qs_n + gk * qs_k]) : 0.f;
+    // Q tile: sQ[n][kk] = Qop(n0 + n, k0 + kk)
+    if (qvec) {
+      for (int i = tid; i < kProjTN * kProjTK / 8; i += 128) {
+        const int n = i >> 3, c = (i & 7) * 8;
+        const int64_t gn = n0 + n, gk = k0 + c;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (gn < N && gk + 8 <= ke) v = __ldg(reinterpret_cast<const uint4 *>(Qm + gn * qs_n + gk));
+        else if (gn < N)
+          for (int e = 0; e < 8; ++e)
+            if (gk + e < ke) reinterpret_cast<uint16_t *>(&v)[e] = Qm[gn * qs_n + gk + e];
+        *reinterpret_cast<uint4 *>(&sQ[n][c]) = v;
+      }
+    } else {
+      // consecutive threads take consecutive n (contiguous when qs_n == 1)
+      for (int i = tid; i < kProjTN * kProjTK; i += 128) {
+        const int n = i % kProjTN, c = i / kProjTN;
+        const int64_t gn = n0 + n, gk = k0 + c;
+        sQ[n][c] = (gn < N && gk < ke) ? Qm[gn * qs_n + gk * qs_k] : static_cast<uint16_t>(0);
+      }
     }
     __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < kProjTK; ++kk) {
-      const float a0 = sP[kk][tm], a1 = sP[kk][tm + 32];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float b = sQ[kk][tn + j];
-        acc[0][j] = fmaf(a0, b, acc[0][j]);
-        acc[1][j] = fmaf(a1, b, acc[1][j]);
+    for (int kk = 0; kk < kProjTK; kk += 16) {
+      const int r = warp * 16 + g;
+      const uint32_t a0 = *reinterpret_cast<const uint32_t *>(&sP[r][kk + 2 * t]);
+      const uint32_t a1 = *reinterpret_cast<const uint32_t *>(&sP[r + 8][kk + 2 * t]);
+      const uint32_t a2 = *reinterpret_cast<const uint32_t *>(&sP[r][kk + 2 * t + 8]);
+      const uint32_t a3 = *reinterpret_cast<const uint32_t *>(&sP[r + 8][kk + 2 * t + 8]);
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const uint32_t b0 = *reinterpret_cast<const uint32_t *>(&sQ[nt * 8 + g][kk + 2 * t]);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t *>(&sQ[nt * 8 + g][kk + 2 * t + 8]);
+        mma_bf16_16816_acc(acc[nt], a0, a1, a2, a3, b0, b1);
       }
     }
     __syncthreads();
   }
   float *C = part + static_cast<int64_t>(blockIdx.z) * M * N;
 #pragma unroll
-  for (int i = 0; i < 2; ++i)
+  for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int64_t gm = m0 + tm + 32 * i, gn = n0 + tn + j;
-      if (gm < M && gn < N) C[gm * N + gn] = s * acc[i][j];
+    for (int e = 0; e < 4; ++e) {
+      const int64_t gm = m0 + warp * 16 + g + 8 * (e >> 1), gn = n0 + nt * 8 + 2 * t + (e & 1);
+      if (gm < M && gn < N) C[gm * N + gn] = s * acc[nt][e];
     }
+  }
 }
 
 // C = sum over the S splits of part (in split order).  Writes the fp32 result
