@@ -366,22 +366,24 @@ qn_status check_layer(const qn_nf4 *Q, const void *in, int64_t M, const void *A,
   return QN_OK;
 }
 
-// Adapter projection C = s P Qop^T (M x N, K deep) split over K so that at
-// least two waves of CTAs run, then the splits summed in order into C32 (fp32)
+// Adapter projection C = s P Qop^T (M x N, K deep) split over K so that
+// about six CTAs per SM run, then the splits summed in order into C32 (fp32)
 // or, with C2 set, its bf16 hi/lo split (each half padded to R columns).
 qn_status launch_lora_proj(const uint16_t *P, int64_t M, int64_t K, const uint16_t *Qm, int64_t N, int64_t qs_n,
                            int64_t qs_k, float s, float *part, float *C32, int R, uint16_t *C2, cudaStream_t st) {
-  const int64_t tiles = qn_ceil_div(M, qn::kProjTM) * qn_ceil_div(N, qn::kProjTN);
-  int64_t S = qn_ceil_div(2 * static_cast<int64_t>(sm_count()), tiles);
+  const int TN = N <= 16 ? 16 : 64;
+  const int64_t tiles = qn_ceil_div(M, qn::kProjTM) * qn_ceil_div(N, TN);
+  int64_t S = qn_ceil_div(6 * static_cast<int64_t>(sm_count()), tiles);
   const int64_t smax = qn_ceil_div(K, 256);
   if (S > smax) S = smax;
   if (S > qn::kProjMaxSplit) S = qn::kProjMaxSplit;
   if (S < 1) S = 1;
   const int64_t kchunk = qn_ceil_div(qn_ceil_div(K, S), qn::kProjTK) * qn::kProjTK;
   S = qn_ceil_div(K, kchunk);
-  dim3 grid(static_cast<unsigned>(qn_ceil_div(M, qn::kProjTM)), static_cast<unsigned>(qn_ceil_div(N, qn::kProjTN)),
+  dim3 grid(static_cast<unsigned>(qn_ceil_div(M, qn::kProjTM)), static_cast<unsigned>(qn_ceil_div(N, TN)),
             static_cast<unsigned>(S));
-  qn::lora_proj_kernel<<<grid, 128, 0, st>>>(P, M, K, Qm, N, qs_n, qs_k, s, kchunk, part);
+  if (TN == 16) qn::lora_proj_kernel<16><<<grid, 128, 0, st>>>(P, M, K, Qm, N, qs_n, qs_k, s, kchunk, part);
+  else qn::lora_proj_kernel<64><<<grid, 128, 0, st>>>(P, M, K, Qm, N, qs_n, qs_k, s, kchunk, part);
   QN_LAUNCH_CHECK("lora_proj_kernel");
   const int64_t n = M * (C2 ? R : N);
   qn::lora_reduce_kernel<<<static_cast<unsigned>(qn_ceil_div(n, 256)), 256, 0, st>>>(part, static_cast<int>(S), M, N,

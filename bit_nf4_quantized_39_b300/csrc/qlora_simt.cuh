@@ -16,13 +16,14 @@ namespace qn {
 // Adapter projection  C[m, n] = s * sum_kk P[m, kk] * Qop(n, kk)   (fp32 out)
 // with Qop(n, kk) = Qm[n * qs_n + kk * qs_k] and P bf16 [M x K] row-major,
 // on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).
-// CTA tile 64 x 64 (4 warps of 16 rows x 8 n8-tiles), K staged 64 at a time
+// CTA tile 64 x TN (4 warps of 16 rows x TN / 8 n8-tiles; TN = 16 for ranks up
+// to 16, else 64), K staged 64 at a time
 // through padded shared-memory tiles (row stride 72 elements, so fragment
 // loads do not conflict).  K is split over gridDim.z CTAs of kchunk columns
 // each (a multiple of 64); split z writes its partial sums to
 // part + z * M * N, and lora_reduce_kernel adds the splits in order.
 // ---------------------------------------------------------------------------
-constexpr int kProjTM = 64, kProjTN = 64, kProjTK = 64, kProjStride = kProjTK + 8;
+constexpr int kProjTM = 64, kProjTK = 64, kProjStride = kProjTK + 8;
 constexpr int kProjMaxSplit = 16;
 
 __device__ __forceinline__ void mma_bf16_16816_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -34,21 +35,23 @@ __device__ __forceinline__ void mma_bf16_16816_acc(float (&d)[4], uint32_t a0, u
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+template <int TN>
 __global__ void __launch_bounds__(128)
 lora_proj_kernel(const uint16_t *__restrict__ P, int64_t M, int64_t K,
                  const uint16_t *__restrict__ Qm, int64_t N, int64_t qs_n, int64_t qs_k,
                  float s, int64_t kchunk, float *__restrict__ part) {
   __shared__ __align__(16) uint16_t sP[kProjTM][kProjStride];
-  __shared__ __align__(16) uint16_t sQ[kProjTN][kProjStride];
+  __shared__ __align__(16) uint16_t sQ[TN][kProjStride];
+  constexpr int NT = TN / 8;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t = lane & 3;
   const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kProjTM;
-  const int64_t n0 = static_cast<int64_t>(blockIdx.y) * kProjTN;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.y) * TN;
   const int64_t kb = static_cast<int64_t>(blockIdx.z) * kchunk;
   const int64_t ke = (kb + kchunk < K) ? kb + kchunk : K;
   const bool pvec = (K % 8) == 0;
   const bool qvec = qs_k == 1 && (qs_n % 8) == 0;
-  float acc[8][4] = {};
+  float acc[NT][4] = {};
   for (int64_t k0 = kb; k0 < ke; k0 += kProjTK) {
     // P tile: 64 rows x 64 columns
     if (pvec) {
@@ -71,7 +74,7 @@ lora_proj_kernel(const uint16_t *__restrict__ P, int64_t M, int64_t K,
     }
     // Q tile: sQ[n][kk] = Qop(n0 + n, k0 + kk)
     if (qvec) {
-      for (int i = tid; i < kProjTN * kProjTK / 8; i += 128) {
+      for (int i = tid; i < TN * kProjTK / 8; i += 128) {
         const int n = i >> 3, c = (i & 7) * 8;
         const int64_t gn = n0 + n, gk = k0 + c;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -83,8 +86,8 @@ lora_proj_kernel(const uint16_t *__restrict__ P, int64_t M, int64_t K,
       }
     } else {
       // consecutive threads take consecutive n (contiguous when qs_n == 1)
-      for (int i = tid; i < kProjTN * kProjTK; i += 128) {
-        const int n = i % kProjTN, c = i / kProjTN;
+      for (int i = tid; i < TN * kProjTK; i += 128) {
+        const int n = i % TN, c = i / TN;
         const int64_t gn = n0 + n, gk = k0 + c;
         sQ[n][c] = (gn < N && gk < ke) ? Qm[gn * qs_n + gk * qs_k] : static_cast<uint16_t>(0);
       }
@@ -98,7 +101,7 @@ lora_proj_kernel(const uint16_t *__restrict__ P, int64_t M, int64_t K,
       const uint32_t a2 = *reinterpret_cast<const uint32_t *>(&sP[r][kk + 2 * t + 8]);
       const uint32_t a3 = *reinterpret_cast<const uint32_t *>(&sP[r + 8][kk + 2 * t + 8]);
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
+      for (int nt = 0; nt < NT; ++nt) {
         const uint32_t b0 = *reinterpret_cast<const uint32_t *>(&sQ[nt * 8 + g][kk + 2 * t]);
         const uint32_t b1 = *reinterpret_cast<const uint32_t *>(&sQ[nt * 8 + g][kk + 2 * t + 8]);
         mma_bf16_16816_acc(acc[nt], a0, a1, a2, a3, b0, b1);
@@ -108,7 +111,7 @@ lora_proj_kernel(const uint16_t *__restrict__ P, int64_t M, int64_t K,
   }
   float *C = part + static_cast<int64_t>(blockIdx.z) * M * N;
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
+  for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int64_t gm = m0 + warp * 16 + g + 8 * (e >> 1), gn = n0 + nt * 8 + 2 * t + (e & 1);
