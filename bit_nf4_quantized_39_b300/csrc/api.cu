@@ -160,7 +160,7 @@ qn_status launch_quantize(const void *W, qn_dtype wdt, const qn_nf4 *Q, unsigned
     QN_LAUNCH_CHECK("nf4_quant_tail_kernel");
   }
   {
-    const int64_t bpc = (qn::kQuantThreads / 32) * (wdt == QN_F32 ? 4 : 8);  // blocks per CTA-iteration
+    const int64_t bpc = (qn::kQuantThreads / 32) * 4;  // blocks per CTA-iteration (8 lanes per block)
     int64_t grid = qn_ceil_div(nfull, bpc);
     const int64_t cap = static_cast<int64_t>(sms) * 4;  // resident CTAs (registers, 31 KB of shared tables)
     if (grid > cap) grid = cap;

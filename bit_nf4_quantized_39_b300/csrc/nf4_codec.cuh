@@ -148,28 +148,11 @@ __device__ float exact_mean_from_bins(const unsigned long long *__restrict__ bin
   return __uint_as_float(bits);
 }
 
-// Each lane owns 32 input bytes of one block per iteration: 16 bf16 or 8 fp32.
+// Each lane owns 8 elements of one block per iteration (32 bytes of fp32 or
+// 16 bytes of bf16); eight lanes share a block.
 template <typename T> struct QuantVec;
 template <> struct QuantVec<float> { static constexpr int kVec = 8; };
-template <> struct QuantVec<__nv_bfloat16> { static constexpr int kVec = 16; };
-
-// Loads kVec consecutive elements (32 bytes) as fp32.
-__device__ __forceinline__ void load_vec(const float *p, float (&v)[8]) {
-  const float4 a = __ldcs(reinterpret_cast<const float4 *>(p));
-  const float4 b = __ldcs(reinterpret_cast<const float4 *>(p) + 1);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-__device__ __forceinline__ void load_vec(const __nv_bfloat16 *p, float (&v)[16]) {
-  const uint4 a = __ldcs(reinterpret_cast<const uint4 *>(p));
-  const uint4 b = __ldcs(reinterpret_cast<const uint4 *>(p) + 1);
-  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    v[2 * i] = __uint_as_float(w[i] << 16);
-    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
+template <> struct QuantVec<__nv_bfloat16> { static constexpr int kVec = 8; };
 
 // ---------------------------------------------------------------------------
 // Nearest-level decision by bucket lookup.  A normalised value v in [-1, 1]
@@ -217,11 +200,20 @@ __device__ __forceinline__ void build_bucket_entry(int idx, BucketEntry *tab) {
 // a bank whatever buckets they hit.
 __device__ __forceinline__ uint32_t bucket_code(float v, const BucketEntry *tab) {
   const uint32_t bits = __float_as_uint(v);
+  uint32_t ek;  // exponent and top 3 significand bits: bits 20 .. 30
+  asm("bfe.u32 %0, %1, 20, 11;" : "=r"(ek) : "r"(bits));
   // |v| <= 1 gives key <= 48; the upper clamp only keeps non-finite inputs
   // (outside the method's domain) inside the table.
-  const uint32_t key = min(max((bits & 0x7FFFFFFFu) >> 20, kBucketKeyMin) - kBucketKeyMin, 55u);
-  const BucketEntry en = tab[(key + (bits >> 31) * 56u) * 32u];
+  const uint32_t key = min(max(ek, kBucketKeyMin) - kBucketKeyMin, 55u);
+  const BucketEntry en = tab[(key + ((bits >> 31) ? 56u : 0u)) * 32u];
   return en.base + ((v > en.thr) ? 1u : 0u);
+}
+
+// w with bits [4 i, 4 i + 4) replaced by the low 4 bits of c.
+__device__ __forceinline__ uint32_t put_nibble(uint32_t w, uint32_t c, int i) {
+  uint32_t r;
+  asm("bfi.b32 %0, %1, %2, %3, 4;" : "=r"(r) : "r"(c), "r"(w), "r"(4 * i));
+  return r;
 }
 
 // IEEE-correct x / m for |x| <= m with m in [2^-125, 2^125], from the
@@ -269,15 +261,42 @@ nf4_quant_kernel(const T *__restrict__ x, int64_t nfull, int64_t nblk, uint8_t *
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
 
-  for (int64_t b0 = warp * BPW; b0 < nfull; b0 += nwarps * BPW) {
+  // The loads of the next iteration are issued before the current block is
+  // processed (one iteration of register prefetch).
+  constexpr bool kF32 = sizeof(T) == 4;
+  uint4 na = make_uint4(0u, 0u, 0u, 0u), nb = na;  // the next block's 8 elements of this lane
+  int64_t b0 = warp * BPW;
+  if (b0 + sub < nfull) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(x + (b0 + sub) * 64 + li * V);
+    na = __ldcs(p);
+    if (kF32) nb = __ldcs(p + 1);
+  }
+  for (; b0 < nfull; b0 += nwarps * BPW) {
     const int64_t blk = b0 + sub;
     const bool valid = blk < nfull;
     float v[V];
-    if (valid) {
-      load_vec(x + blk * 64 + li * V, v);
-    } else {
+    if constexpr (kF32) {
+      const uint32_t w[8] = {na.x, na.y, na.z, na.w, nb.x, nb.y, nb.z, nb.w};
 #pragma unroll
-      for (int i = 0; i < V; ++i) v[i] = 0.f;
+      for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(w[i]);
+    } else {
+      const uint32_t w[4] = {na.x, na.y, na.z, na.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    }
+    {
+      const int64_t nblk2 = b0 + nwarps * BPW + sub;
+      if (nblk2 < nfull) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(x + nblk2 * 64 + li * V);
+        na = __ldcs(p);
+        if (kF32) nb = __ldcs(p + 1);
+      } else {
+        na = make_uint4(0u, 0u, 0u, 0u);
+        nb = na;
+      }
     }
     float m = 0.f;
 #pragma unroll
@@ -297,19 +316,10 @@ nf4_quant_kernel(const T *__restrict__ x, int64_t nfull, int64_t nblk, uint8_t *
       for (int i = 0; i < V; ++i) v[i] = (m > 0.f) ? __fdiv_rn(v[i], m) : 0.f;
     }
     if (valid) {
-      if constexpr (V == 8) {
-        uint32_t packed = 0;
+      uint32_t packed = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) packed |= bucket_code(v[i], my_tab) << (4 * i);
-        reinterpret_cast<uint32_t *>(codes + blk * 32)[li] = packed;
-      } else {
-        uint32_t p0 = 0, p1 = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) p0 |= bucket_code(v[i], my_tab) << (4 * i);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) p1 |= bucket_code(v[8 + i], my_tab) << (4 * i);
-        reinterpret_cast<uint2 *>(codes + blk * 32)[li] = make_uint2(p0, p1);
-      }
+      for (int i = 0; i < 8; ++i) packed = put_nibble(packed, bucket_code(v[i], my_tab), i);
+      reinterpret_cast<uint32_t *>(codes + blk * 32)[li] = packed;
       if (li == 0) {
         absmax[blk] = m;
         if (bins) bin_add_shared(s_bins, m);
