@@ -161,8 +161,12 @@ qn_status nf4_dequantize(const qn_nf4 *Q, void *Wout, qn_dtype odt, void *stream
  *   Q     quantised weight, d x k with k % 64 == 0.
  *   X     device bf16 [M x k];  A device bf16 [r x k];  B device bf16 [d x r].
  *   Y     device bf16 [M x d] (written).
- *   1 <= M, 1 <= r <= 256.  Accumulation is fp32; the weight enters the
- *   tensor-core path as bf16(deq(Q)).  ws: qn_workspace_bytes(QN_OP_LINEAR_FWD).
+ *   1 <= M, 1 <= r <= 256.  Accumulation is fp32.  M == 1 multiplies the fp32
+ *   levels by x; for M >= 2 the weight enters the tensor cores as
+ *   bf16(deq(Q)) and the adapter term uses u split into bf16 hi + lo.  The
+ *   few-token path (2 <= M <= 16) streams the int8 block constants with bulk
+ *   copies when Q->absmax_q is 16-byte aligned (else it reads them through
+ *   L1).  ws: qn_workspace_bytes(QN_OP_LINEAR_FWD).
  */
 qn_status qlora_linear_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M,
                            const uint16_t *A, const uint16_t *B, int32_t r,
@@ -178,9 +182,10 @@ qn_status qlora_linear_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M,
  *          (each as in qlora_linear_fwd); every Q[g] has the same k.
  *   X      device bf16 [M x k], shared.
  *   ws     qn_workspace_bytes(QN_OP_LINEAR_FWD, M, sum of d, k, sum of r).
- * With M == 1 (and sum of d <= 32768) the group runs as one kernel whose
+ * With M <= 16 (and k <= 16384) the group runs as one launch sequence whose
  * memory round trips overlap across projections; otherwise it is the n
- * single calls in order.  Results equal those of n qlora_linear_fwd calls.
+ * single calls in order.  Results equal those of n qlora_linear_fwd calls
+ * up to fp32 summation order.
  */
 qn_status qlora_linear_fwd_group(int32_t n, const qn_nf4 *const *Q, const uint16_t *X, int64_t M,
                                  const uint16_t *const *A, const uint16_t *const *B, const int32_t *r,
@@ -190,7 +195,9 @@ qn_status qlora_linear_fwd_group(int32_t n, const qn_nf4 *const *Q, const uint16
 /*
  * qlora_linear_bwd_dx -- dX = dY deq(Q) + (alpha/r) (dY B) A.
  *   dY device bf16 [M x d]; A, B as in the forward; dX device bf16 [M x k].
- *   Same size rules and workspace query (QN_OP_LINEAR_BWD_DX).
+ *   Same size rules and workspace query (QN_OP_LINEAR_BWD_DX); for M > 16,
+ *   r <= 64 and d % 8 == 0 the workspace also holds bf16 W^T (k x d) for the
+ *   tensor-core GEMM.
  */
 qn_status qlora_linear_bwd_dx(const qn_nf4 *Q, const uint16_t *dY, int64_t M,
                               const uint16_t *A, const uint16_t *B, int32_t r,
