@@ -317,16 +317,39 @@ qlora_decode_kernel(const __grid_constant__ DecGroup g, unsigned int *__restrict
   int c_p = 0;
   float mu = 0.f;
   bool c_dq = false;
+  // Adapter operands of the current unit, fetched when the unit starts so
+  // that finishing it needs no memory round trip: B[row, lane + 32 h] for the
+  // unit's rows (ranks up to 64 in registers, larger ones read at the end),
+  // and u[lane + 32 h] once the ready counter has been seen.
+  constexpr int kPreR = 64;
+  float bpre[kDecRows][2];
+  float upre[2] = {0.f, 0.f};
+  int upre_p = -1;  // projection whose u is in upre
+  bool have_u = false;
+  auto load_u = [&]() {
+    const DecProj &p = g.p[c_p];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) upre[h] = (lane + 32 * h < p.r) ? __ldcg(u + p.u_off + lane + 32 * h) : 0.f;
+    upre_p = c_p;
+  };
   auto enter_unit = [&]() {
     if (c_unit < nunits) {
       c_p = dec_find(g, c_unit, unit_of);
       c_row0 = (c_unit - g.p[c_p].unit_off) * kDecRows;
-      c_dq = g.p[c_p].q.dq != 0;
-      mu = c_dq ? __ldg(g.p[c_p].q.absmax_mean) : 0.f;
+      const DecProj &p = g.p[c_p];
+      c_dq = p.q.dq != 0;
+      mu = c_dq ? __ldg(p.q.absmax_mean) : 0.f;
+#pragma unroll
+      for (int rr = 0; rr < kDecRows; ++rr) {
+        const int64_t row = c_row0 + rr;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          bpre[rr][h] = (row < p.q.d && lane + 32 * h < p.r) ? bf16_bits_to_f32(__ldg(p.B + row * p.r + lane + 32 * h)) : 0.f;
+      }
+      if (have_u && upre_p != c_p) load_u();
     }
   };
   enter_unit();
-  bool have_u = false;
   float rsum[kDecRows];
 #pragma unroll
   for (int rr = 0; rr < kDecRows; ++rr) rsum[rr] = 0.f;
@@ -350,14 +373,17 @@ qlora_decode_kernel(const __grid_constant__ DecGroup g, unsigned int *__restrict
       }
       __syncwarp();
       have_u = true;
+      load_u();
+    } else if (upre_p != c_p) {
+      load_u();
     }
     float acc[kDecRows];
 #pragma unroll
     for (int rr = 0; rr < kDecRows; ++rr) {
       const int64_t row = c_row0 + rr;
-      float a = 0.f;
-      if (row < d)
-        for (int j = lane; j < p.r; j += 32)
+      float a = fmaf(upre[0], bpre[rr][0], upre[1] * bpre[rr][1]);
+      if (row < d && p.r > kPreR)
+        for (int j = lane + kPreR; j < p.r; j += 32)
           a = fmaf(__ldcg(u + p.u_off + j), bf16_bits_to_f32(p.B[row * p.r + j]), a);
       acc[rr] = a;
     }
