@@ -117,11 +117,18 @@ def barrier(ws):
 
 
 def max_over_ranks(x: float, ws: int) -> float:
+    """Largest x over the ranks (the timed region ends when the slowest rank does)."""
     if ws == 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_value(bytes_per_step_per_rank: float, steps: int, ws: int, total_ms: float) -> float:
+    """Whole-job GB/s: the bytes every rank processed over the slowest rank's time."""
+    return bytes_per_step_per_rank * steps * ws / (total_ms * 1e-3) / 1e9
 
 
 # ----------------------------------------------------------------- workloads
@@ -488,7 +495,7 @@ def main():
     clocks = clk.summary()
     total_ms = max_over_ranks(res["total_ms"], ws)
     w4, lora, act = decode_bytes(mats, 1, r)
-    value = w4 * args.steps * ws / (total_ms * 1e-3) / 1e9
+    value = job_value(w4, args.steps, ws, total_ms)
 
     # roofline of the dominant kernel (qlora_decode_kernel, one launch per
     # call): algorithmic bytes per launch / mean CUDA-event launch duration,
