@@ -48,56 +48,6 @@ __host__ __device__ constexpr size_t tc_smem_bytes(int R) {
   return 1024 + static_cast<size_t>(kTcXStages) * kTcXStageBytes + tc_u_bytes(R) + 256;
 }
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
-}
-
-// Byte tables of the 16 scaled levels: L[i] / H[i] hold the low / high bytes
-// of the bf16 values of levels 4i .. 4i+3.
-struct ScaledLevels {
-  uint32_t L[4], H[4];
-};
-
-__device__ __forceinline__ ScaledLevels scaled_levels(float m) {
-  uint32_t P[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-    P[j] = pack_bf16x2(__fmul_rn(c_nf4_levels[2 * j], m), __fmul_rn(c_nf4_levels[2 * j + 1], m));
-  ScaledLevels t;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    t.L[i] = prmt(P[2 * i], P[2 * i + 1], 0x6420u);
-    t.H[i] = prmt(P[2 * i], P[2 * i + 1], 0x7531u);
-  }
-  return t;
-}
-
-// Eight 4-bit codes (element 0 in the low nibble) -> four bf16x2 words.
-__device__ __forceinline__ void decode_word(uint32_t w, const ScaledLevels &t, uint32_t *out) {
-  const uint32_t sel = w & 0x77777777u;   // level index within its half of the table
-  const uint32_t w4 = w << 4;
-  // byte masks: 0xFF where the code's bit 3 is set (upper half of the table)
-  const uint32_t m_lo = prmt(w4, w, 0xD9C8u);
-  const uint32_t m_hi = prmt(w4, w, 0xFBEAu);
-  const uint32_t s_hi = sel >> 16;
-  {
-    const uint32_t la = prmt(t.L[0], t.L[1], sel), lb = prmt(t.L[2], t.L[3], sel);
-    const uint32_t ha = prmt(t.H[0], t.H[1], sel), hb = prmt(t.H[2], t.H[3], sel);
-    const uint32_t lo = (la & ~m_lo) | (lb & m_lo), hi = (ha & ~m_lo) | (hb & m_lo);
-    out[0] = prmt(lo, hi, 0x5140u);
-    out[1] = prmt(lo, hi, 0x7362u);
-  }
-  {
-    const uint32_t la = prmt(t.L[0], t.L[1], s_hi), lb = prmt(t.L[2], t.L[3], s_hi);
-    const uint32_t ha = prmt(t.H[0], t.H[1], s_hi), hb = prmt(t.H[2], t.H[3], s_hi);
-    const uint32_t lo = (la & ~m_hi) | (lb & m_hi), hi = (ha & ~m_hi) | (hb & m_hi);
-    out[2] = prmt(lo, hi, 0x5140u);
-    out[3] = prmt(lo, hi, 0x7362u);
-  }
-}
-
 struct TcBars {
   uint64_t x_full[kTcXStages], x_empty[kTcXStages];
   uint64_t a_full[kTcAStages], a_empty[kTcAStages];
