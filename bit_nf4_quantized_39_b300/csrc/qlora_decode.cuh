@@ -247,43 +247,40 @@ qlora_decode_kernel(const __grid_constant__ DecGroup g, unsigned int *__restrict
     }
   };
 
-  // ---- prologue: weight loads first, then x -----------------------------------
+  // ---- prologue: x loads first (one round covers k <= 16384), the weight
+  // loads behind them, the level-pair table while they are in flight, then x
+  // into shared memory and one barrier -------------------------------------------
+  constexpr int kPer = 8;  // 16-byte x loads per thread
+  static_assert(kPer * kDecThreads * 8 >= kDecMaxK, "one round of x loads must cover k");
+  const int64_t nvec = dec_xs_floats(k) / 8;
+  uint4 xt[kPer];
+#pragma unroll
+  for (int v = 0; v < kPer; ++v) {
+    const int64_t vi = v * kDecThreads + tid;
+    xt[v] = (vi * 8 < k) ? __ldg(reinterpret_cast<const uint4 *>(g.X) + vi) : make_uint4(0u, 0u, 0u, 0u);
+  }
   DecStep buf[kDecDepth];
 #pragma unroll
   for (int i = 0; i < kDecDepth; ++i) load_next(buf[i]);
-  __shared__ float s_lv[16];
-  if (tid < 16) s_lv[tid] = c_nf4_levels[tid];
-  {
-    constexpr int kPer = 8;  // 16-byte x loads in flight per thread per round
-    const int64_t nvec = dec_xs_floats(k) / 8;
-    for (int64_t base = 0; base < nvec; base += static_cast<int64_t>(kDecThreads) * kPer) {
-      uint4 t[kPer];
+#pragma unroll 4
+  for (int n = 0; n < 32; ++n) {
+    const int b = warp + 8 * n;  // entry b of this lane: (level[b & 15], level[b >> 4]); warp-uniform index
+    *reinterpret_cast<float2 *>(lut + 256 * b + 8 * lane) = make_float2(c_nf4_levels[b & 15], c_nf4_levels[b >> 4]);
+  }
 #pragma unroll
-      for (int v = 0; v < kPer; ++v) {
-        const int64_t vi = base + v * kDecThreads + tid;
-        t[v] = (vi * 8 < k) ? __ldg(reinterpret_cast<const uint4 *>(g.X) + vi) : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int v = 0; v < kPer; ++v) {
-        const int64_t vi = base + v * kDecThreads + tid;
-        if (vi < nvec) {
-          const int64_t e = vi * 8;  // 8 consecutive elements: two float4 groups of one lane
-          *reinterpret_cast<float4 *>(xs + dec_xs_index(e)) =
-              make_float4(__uint_as_float(t[v].x << 16), __uint_as_float(t[v].x & 0xFFFF0000u),
-                          __uint_as_float(t[v].y << 16), __uint_as_float(t[v].y & 0xFFFF0000u));
-          *reinterpret_cast<float4 *>(xs + dec_xs_index(e + 4)) =
-              make_float4(__uint_as_float(t[v].z << 16), __uint_as_float(t[v].z & 0xFFFF0000u),
-                          __uint_as_float(t[v].w << 16), __uint_as_float(t[v].w & 0xFFFF0000u));
-        }
-      }
+  for (int v = 0; v < kPer; ++v) {
+    const int64_t vi = v * kDecThreads + tid;
+    if (vi < nvec) {
+      const int64_t e = vi * 8;  // 8 consecutive elements: two float4 groups of one lane
+      *reinterpret_cast<float4 *>(xs + dec_xs_index(e)) =
+          make_float4(__uint_as_float(xt[v].x << 16), __uint_as_float(xt[v].x & 0xFFFF0000u),
+                      __uint_as_float(xt[v].y << 16), __uint_as_float(xt[v].y & 0xFFFF0000u));
+      *reinterpret_cast<float4 *>(xs + dec_xs_index(e + 4)) =
+          make_float4(__uint_as_float(xt[v].z << 16), __uint_as_float(xt[v].z & 0xFFFF0000u),
+                      __uint_as_float(xt[v].w << 16), __uint_as_float(xt[v].w & 0xFFFF0000u));
     }
   }
-  __syncthreads();  // s_lv and xs ready
-  for (int i = tid; i < 256 * 32; i += kDecThreads) {
-    const int b = i >> 5, l = i & 31;  // entry b of lane l: (level[b & 15], level[b >> 4])
-    *reinterpret_cast<float2 *>(lut + 256 * b + 8 * l) = make_float2(s_lv[b & 15], s_lv[b >> 4]);
-  }
-  __syncthreads();  // lut ready
+  __syncthreads();  // table and x ready
 
   // ---- adapter rows: u[j] = s * A[j] . x, one warp slot per row ---------------
   for (int64_t j = wslot; j < g.nadapter; j += W) {
