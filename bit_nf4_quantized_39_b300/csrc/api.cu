@@ -210,7 +210,7 @@ size_t proj_ws_bytes(int64_t M, int32_t r) {
 
 size_t fwd_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
   size_t b = kSemBytes + round256(static_cast<size_t>(M) * r * sizeof(float));  // u
-  if (!use_skinny(M, k)) b += proj_ws_bytes(M, r) + qn::tc_ws_bytes(M, d, k, r);
+  if (!use_skinny(M, k)) b += proj_ws_bytes(M, r) + qn::tc_fwd_ws_bytes(M, d, k, r);
   return b;
 }
 
@@ -368,9 +368,11 @@ qn_status check_layer(const qn_nf4 *Q, const void *in, int64_t M, const void *A,
 
 // Adapter projection C = s P Qop^T (M x N, K deep) split over K so that
 // about six CTAs per SM run, then the splits summed in order into C32 (fp32)
-// or, with C2 set, its bf16 hi/lo split (each half padded to R columns).
+// or, with C2 set, its bf16 hi/lo split (each half padded to R columns, rows
+// of pitch ld2 >= 2R, zero past 2R).
 qn_status launch_lora_proj(const uint16_t *P, int64_t M, int64_t K, const uint16_t *Qm, int64_t N, int64_t qs_n,
-                           int64_t qs_k, float s, float *part, float *C32, int R, uint16_t *C2, cudaStream_t st) {
+                           int64_t qs_k, float s, float *part, float *C32, int R, uint16_t *C2, int64_t ld2,
+                           cudaStream_t st) {
   const int TN = N <= 16 ? 16 : 64;
   const int64_t tiles = qn_ceil_div(M, qn::kProjTM) * qn_ceil_div(N, TN);
   int64_t S = qn_ceil_div(6 * static_cast<int64_t>(sm_count()), tiles);
@@ -387,7 +389,7 @@ qn_status launch_lora_proj(const uint16_t *P, int64_t M, int64_t K, const uint16
   QN_LAUNCH_CHECK("lora_proj_kernel");
   const int64_t n = M * (C2 ? R : N);
   qn::lora_reduce_kernel<<<static_cast<unsigned>(qn_ceil_div(n, 256)), 256, 0, st>>>(part, static_cast<int>(S), M, N,
-                                                                                      C32, R, C2);
+                                                                                      C32, R, C2, ld2);
   QN_LAUNCH_CHECK("lora_reduce_kernel");
   return QN_OK;
 }
@@ -423,20 +425,28 @@ qn_status launch_tc_bwd(const qn_nf4 *Q, const uint16_t *dY, int64_t M, const ui
   return QN_OK;
 }
 
-// Large-M forward on the tensor cores: one CTA per 128 weight rows x 256
-// tokens (qlora_fwd_tc_kernel); u2 is the bf16 hi/lo split of u = s X A^T.
+// Large-M forward on the tensor cores: the block constants of W into the
+// workspace (nf4_block_scale_kernel), then one CTA per 128 weight rows x 256
+// tokens (qlora_fwd_tc_kernel); u2 is the bf16 hi/lo split of u = s X A^T,
+// rows [hi | lo] of kTfUCols columns, each half zero-padded to 64.
 qn_status launch_tc_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M, const uint16_t *u2, const uint16_t *B,
-                        int32_t r, uint16_t *Y, cudaStream_t st) {
-  const int R = qn::tc_pad_r(r);
-  CUtensorMap xmap;
-  if (const char *e = qn::make_bf16_tile_map(&xmap, X, static_cast<uint64_t>(Q->k), static_cast<uint64_t>(M), qn::kTcBM))
+                        int32_t r, uint16_t *Y, Span &sp, cudaStream_t st) {
+  const int64_t d = Q->d, k = Q->k, kp = qn::tf_scale_pitch(k);
+  float *scales = sp.take<float>(static_cast<size_t>(d) * kp);
+  qn::nf4_block_scale_kernel<<<static_cast<unsigned>(qn_ceil_div(d * kp, 256)), 256, 0, st>>>(view_of(Q), kp, scales);
+  QN_LAUNCH_CHECK("nf4_block_scale_kernel");
+  CUtensorMap xmap, umap;
+  if (const char *e = qn::make_bf16_tile_map(&xmap, X, static_cast<uint64_t>(k), static_cast<uint64_t>(M), qn::kTcBM))
     return fail(QN_ECUDA, "tcgen05 forward: %s", e);
-  const size_t smem = qn::tc_smem_bytes(R);
+  if (const char *e = qn::make_bf16_tile_map(&umap, u2, static_cast<uint64_t>(qn::kTfUCols), static_cast<uint64_t>(M),
+                                             qn::kTcBM))
+    return fail(QN_ECUDA, "tcgen05 forward: %s", e);
   QN_TRY(cuda_check(cudaFuncSetAttribute(qn::qlora_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(qn::tc_smem_bytes(qn::kTcMaxR))),
+                                         static_cast<int>(qn::kTfSmemBytes)),
                     "tcgen05 forward shared-memory limit"));
-  dim3 grid(static_cast<unsigned>(qn_ceil_div(Q->d, qn::kTcBN)), static_cast<unsigned>(qn_ceil_div(M, qn::kTcBM)));
-  qn::qlora_fwd_tc_kernel<<<grid, qn::kTcThreads, smem, st>>>(xmap, view_of(Q), M, B, r, R, u2, Y);
+  dim3 grid(static_cast<unsigned>(qn_ceil_div(d, qn::kTcBN)), static_cast<unsigned>(qn_ceil_div(M, qn::kTcBM)));
+  qn::qlora_fwd_tc_kernel<<<grid, qn::kTfThreads, qn::kTfSmemBytes, st>>>(
+      xmap, umap, static_cast<const uint8_t *>(Q->codes), scales, d, k, M, B, r, Y);
   QN_LAUNCH_CHECK("qlora_fwd_tc_kernel");
   return QN_OK;
 }
@@ -559,12 +569,11 @@ qn_status qlora_linear_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M, const 
   float *u = sp.take<float>(static_cast<size_t>(M) * r);
   float *part = sp.take<float>(static_cast<size_t>(qn::kProjMaxSplit) * M * r);
   if (qn::tc_supported(M, d, k, r)) {
-    const int R = qn::tc_pad_r(r);
-    uint16_t *u2 = sp.take<uint16_t>(static_cast<size_t>(M) * 2 * R);
-    QN_TRY(launch_lora_proj(X, M, k, A, r, k, 1, s, part, nullptr, R, u2, st));
-    return launch_tc_fwd(Q, X, M, u2, B, r, Y, st);
+    uint16_t *u2 = sp.take<uint16_t>(static_cast<size_t>(M) * qn::kTfUCols);
+    QN_TRY(launch_lora_proj(X, M, k, A, r, k, 1, s, part, nullptr, qn::kTfUCols / 2, u2, qn::kTfUCols, st));
+    return launch_tc_fwd(Q, X, M, u2, B, r, Y, sp, st);
   }
-  QN_TRY(launch_lora_proj(X, M, k, A, r, k, 1, s, part, u, 0, nullptr, st));
+  QN_TRY(launch_lora_proj(X, M, k, A, r, k, 1, s, part, u, 0, nullptr, 0, st));
   dim3 grid(static_cast<unsigned>(qn_ceil_div(d, qn::kTileN)), static_cast<unsigned>(qn_ceil_div(M, qn::kTileM)));
   qn::qlora_gemm_simt_kernel<false><<<grid, 256, 0, st>>>(view_of(Q), X, M, u, B, r, Y);
   QN_LAUNCH_CHECK("qlora_gemm_simt_kernel<fwd>");
@@ -620,10 +629,10 @@ qn_status qlora_linear_bwd_dx(const qn_nf4 *Q, const uint16_t *dY, int64_t M, co
   if (qn::tc_bwd_supported(M, d, k, r)) {
     const int R = qn::tc_pad_r(r);
     uint16_t *v2 = sp.take<uint16_t>(static_cast<size_t>(M) * 2 * R);
-    QN_TRY(launch_lora_proj(dY, M, d, B, r, 1, r, s, part, nullptr, R, v2, st));
+    QN_TRY(launch_lora_proj(dY, M, d, B, r, 1, r, s, part, nullptr, R, v2, 2 * R, st));
     return launch_tc_bwd(Q, dY, M, v2, A, r, dX, sp, st);
   }
-  QN_TRY(launch_lora_proj(dY, M, d, B, r, 1, r, s, part, v, 0, nullptr, st));
+  QN_TRY(launch_lora_proj(dY, M, d, B, r, 1, r, s, part, v, 0, nullptr, 0, st));
   dim3 grid(static_cast<unsigned>(qn_ceil_div(k, qn::kTileN)), static_cast<unsigned>(qn_ceil_div(M, qn::kTileM)));
   qn::qlora_gemm_simt_kernel<true><<<grid, 256, 0, st>>>(view_of(Q), dY, M, v, A, r, dX);
   QN_LAUNCH_CHECK("qlora_gemm_simt_kernel<bwd>");

@@ -122,9 +122,10 @@ lora_proj_kernel(const uint16_t *__restrict__ P, int64_t M, int64_t K,
 
 // C = sum over the S splits of part (in split order).  Writes the fp32 result
 // to C32 (if not null) and, if C2 is not null, its bf16 hi/lo split
-// C2[m, :] = [bf16(c) | bf16(c - bf16(c))], each half zero-padded to R columns.
+// C2[m, :] = [bf16(c) | bf16(c - bf16(c)) | 0], each half zero-padded to R
+// columns and the row zero-padded to its pitch ld2 >= 2R.
 __global__ void lora_reduce_kernel(const float *__restrict__ part, int S, int64_t M, int64_t N,
-                                   float *__restrict__ C32, int R, uint16_t *__restrict__ C2) {
+                                   float *__restrict__ C32, int R, uint16_t *__restrict__ C2, int64_t ld2) {
   const int64_t cols = C2 ? R : N;
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= M * cols) return;
@@ -135,8 +136,9 @@ __global__ void lora_reduce_kernel(const float *__restrict__ part, int S, int64_
   if (C32 && j < N) C32[m * N + j] = v;
   if (C2) {
     const uint16_t hi = f32_to_bf16_bits(v);
-    C2[m * 2 * R + j] = hi;
-    C2[m * 2 * R + R + j] = f32_to_bf16_bits(v - bf16_bits_to_f32(hi));
+    C2[m * ld2 + j] = hi;
+    C2[m * ld2 + R + j] = f32_to_bf16_bits(v - bf16_bits_to_f32(hi));
+    for (int64_t p = 2 * R + j; p < ld2; p += R) C2[m * ld2 + p] = 0;
   }
 }
 

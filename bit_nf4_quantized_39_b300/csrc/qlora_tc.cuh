@@ -1,28 +1,35 @@
-// qlora_tc.cuh -- fused QLoRA forward on the 5th-generation tensor cores
-// (tcgen05, sm_100 family):
+// qlora_tc.cuh -- fused QLoRA forward and backward on the 5th-generation
+// tensor cores (tcgen05, sm_100 family).
 //
-//   Y^T tile [128 weight rows x 256 tokens] = deq(Q) tile . X tile^T + B . U2^T
+// Forward, per output tile of 128 weight rows x 256 tokens (one CTA):
 //
-// Per CTA: one output tile, 192 threads in three roles.
-//   warps 0-3  dequantisers, then epilogue.  Thread i owns weight row
-//              n0 + i, which is tensor-memory lane i: per 64-column stage it
-//              loads its 32 code bytes, builds the 16 levels scaled by the
-//              block constant as bf16 (exactly bf16(fp32(c * m')), the value
+//   Y^T tile = sum over K stages of deq(Q) stage . X stage^T  +  [B | B] . U2^T
+//
+// A stage is 128 columns of K; 320 threads in three roles.
+//   warps 0-7  dequantisers, then epilogue.  Warp w owns the 32 weight rows of
+//              tensor-memory lane quadrant w % 4 and half w / 4 (64 columns)
+//              of every stage: its code bytes and block constant arrive by
+//              cp.async two stages ahead (the constants precomputed in fp32 by
+//              nf4_block_scale_kernel), it builds the 16 levels scaled by the
+//              constant as bf16 (exactly bf16(fp32(c * m')), the value
 //              nf4_dequantize writes), selects them with byte permutes and
 //              writes the 64 bf16 weights straight into tensor memory with
 //              tcgen05.st -- the weight operand never touches shared memory.
-//   warp 4     TMA producer: X tiles (256 tokens x 64, 128-byte swizzle)
-//              into a 4-stage shared-memory ring.
-//   warp 5     allocates tensor memory and issues the MMAs (one elected
-//              thread): A = dequantised weights from tensor memory, B = X from
-//              shared memory, D = fp32 accumulator in tensor memory.
-// The adapter term s (X A^T) B^T enters as one more MMA with K = 2R: A holds
-// [B | B] (bf16, in tensor memory) and the shared-memory operand holds
-// U2 = [hi | lo] with hi = bf16(u), lo = bf16(u - hi), u = s X A^T (written by
-// lora_reduce_kernel), so the product keeps about 16 significant bits of u.
+//   warp 8     TMA producer: X stages (256 tokens x 128, two 128-byte-swizzled
+//              64-column halves) into a 3-stage shared-memory ring.
+//   warp 9     allocates tensor memory and issues the MMAs (one thread): A =
+//              weights from tensor memory, B = X from shared memory, fp32
+//              accumulator in tensor memory.  It waits on one barrier per
+//              stage (eight MMAs), which the producer's bytes and all eight
+//              dequantiser warps complete together.
+// The adapter term is one more stage at the end: the producer loads U2 =
+// [hi | lo] (hi = bf16(u), lo = bf16(u - hi), u = s X A^T from
+// lora_reduce_kernel, each half zero-padded to 64 columns) in place of X and
+// the dequantisers write the row [B | B] (each copy zero-padded to 64) in
+// place of weights, so the product keeps about 16 significant bits of u.
 //
-// Tensor-memory columns: [0, 256) accumulator, [256, 384) four 32-column
-// weight stages, [384, 384 + R) the adapter operand.
+// Tensor memory: accumulator columns [0, 256), three 64-column weight stages
+// at [256, 448).
 #pragma once
 
 #include "common.cuh"
@@ -33,255 +40,235 @@ namespace qn {
 constexpr int kTcBN = 128;   // weight rows per tile  (MMA M)
 constexpr int kTcBM = 256;   // tokens per tile       (MMA N)
 constexpr int kTcBK = 64;    // K per stage
-constexpr int kTcXStages = 4;
-constexpr int kTcAStages = 4;
 constexpr int kTcMaxR = 64;  // padded adapter rank R (multiple of 8)
-constexpr int kTcThreads = 192;
 constexpr uint32_t kTcXStageBytes = kTcBM * kTcBK * 2;  // 32 KiB
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCol = 0, kACol = 256, kLoraCol = 384;
+constexpr uint32_t kAccCol = 0;
 
 __host__ __device__ constexpr int tc_pad_r(int r) { return (r + 7) & ~7; }
-__host__ __device__ constexpr size_t tc_u_bytes(int R) { return static_cast<size_t>(kTcBM) * 2 * R * 2; }
-__host__ __device__ constexpr size_t tc_smem_bytes(int R) {
-  // 1024 alignment slack + X ring + U2 tile + barriers / bookkeeping
-  return 1024 + static_cast<size_t>(kTcXStages) * kTcXStageBytes + tc_u_bytes(R) + 256;
+
+// ---- forward ----------------------------------------------------------------
+// A stage covers 128 columns of K: two 64-column halves (one 128-byte swizzle
+// span each for X), so the MMA issuer waits on one barrier per eight MMAs.
+constexpr int kTfBK = 128;
+constexpr int kTfStages = 3;                                  // operand ring depth
+constexpr int kTfCodeStages = 3;                              // code + constant ring depth (cp.async)
+constexpr int kTfDeqWarps = 8;                                // two per weight-row quadrant: one per half stage
+constexpr int kTfThreads = (kTfDeqWarps + 2) * 32;            // + TMA producer + MMA issuer
+constexpr int kTfProducerWarp = kTfDeqWarps, kTfMmaWarp = kTfDeqWarps + 1;
+constexpr uint32_t kTfXHalfBytes = kTcBM * 64 * 2;            // 32 KiB
+constexpr uint32_t kTfXStageBytes = 2 * kTfXHalfBytes;        // 64 KiB
+// Code ring slot: four 2 KiB chunks (chunk j of row i at j * 2 KiB + i * 16:
+// code bytes 16 j .. 16 j + 15 of the row's 64 in this stage), then the two
+// block constants of every row (half h of row i at 8 KiB + h * 512 + i * 4).
+constexpr uint32_t kTfCodeStageBytes = 4 * 2048 + 2 * kTcBN * 4;  // 9 KiB
+constexpr uint32_t kTfACols = kTfBK / 2;                      // tensor-memory columns of a weight stage
+constexpr uint32_t kTfACol = 256;                             // weight stages at [256, 256 + 3 * 64)
+constexpr int kTfUCols = 128;                                 // U2 row: [hi | 0 .. | lo | 0 ..], 64 + 64
+constexpr size_t kTfSmemBytes = 1024 + static_cast<size_t>(kTfStages) * kTfXStageBytes +
+                                static_cast<size_t>(kTfCodeStages) * kTfCodeStageBytes + 256;
+
+// Block constants per weight stage: 2 per 128 columns, rows of tf_scale_pitch(k) floats.
+__host__ __device__ constexpr int64_t tf_scale_pitch(int64_t k) { return 2 * ((k + kTfBK - 1) / kTfBK); }
+
+// m[n, j] = the effective constant of block j of row n (exact absmax or its
+// DQ decode, the value nf4_dequantize uses), zero for the pad slot past k / 64.
+__global__ void nf4_block_scale_kernel(QnNF4View q, int64_t kp, float *__restrict__ out) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= q.d * kp) return;
+  const int64_t n = i / kp, j = i % kp, kb = q.k >> 6;
+  out[i] = (j < kb) ? block_scale(q, n * kb + j) : 0.f;
 }
 
-struct TcBars {
-  uint64_t x_full[kTcXStages], x_empty[kTcXStages];
-  uint64_t a_full[kTcAStages], a_empty[kTcAStages];
-  uint64_t lora_full, acc_full, done;
+struct TfBars {
+  uint64_t full[kTfStages], empty[kTfStages];
+  uint64_t acc_full, done;
   uint32_t tmem_base;
   int abort;
 };
 
-__global__ void __launch_bounds__(kTcThreads, 1)
-qlora_fwd_tc_kernel(const __grid_constant__ CUtensorMap xmap, QnNF4View q, int64_t M,
-                    const uint16_t *__restrict__ Bm, int r, int R, const uint16_t *__restrict__ u2,
-                    uint16_t *__restrict__ Y) {
+__global__ void __launch_bounds__(kTfThreads, 1)
+qlora_fwd_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap umap,
+                    const uint8_t *__restrict__ codes, const float *__restrict__ scales, int64_t d, int64_t k,
+                    int64_t M, const uint16_t *__restrict__ Bm, int r, uint16_t *__restrict__ Y) {
   extern __shared__ __align__(1024) unsigned char tc_smem_raw[];
   unsigned char *base = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   unsigned char *xring = base;
-  unsigned char *utile = base + kTcXStages * kTcXStageBytes;
-  TcBars *bars = reinterpret_cast<TcBars *>(utile + tc_u_bytes(R));
+  unsigned char *cring = xring + kTfStages * kTfXStageBytes;
+  TfBars *bars = reinterpret_cast<TfBars *>(cring + kTfCodeStages * kTfCodeStageBytes);
   volatile int *abort = &bars->abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int64_t d = q.d, k = q.k;
   const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kTcBN;
   const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kTcBM;
-  const int nk = static_cast<int>(k / kTcBK);
+  const int nk = static_cast<int>((k + kTfBK - 1) / kTfBK);  // weight stages; stage nk is the adapter's
 
   if (tid == 0) {
-    for (int i = 0; i < kTcXStages; ++i) {
-      mbar_init(smem_u32(&bars->x_full[i]), 1);
-      mbar_init(smem_u32(&bars->x_empty[i]), 1);
+    for (int i = 0; i < kTfStages; ++i) {
+      mbar_init(smem_u32(&bars->full[i]), 1 + kTfDeqWarps);  // the producer's arrival (+ bytes), one per dequantiser warp
+      mbar_init(smem_u32(&bars->empty[i]), 1);
     }
-    for (int i = 0; i < kTcAStages; ++i) {
-      mbar_init(smem_u32(&bars->a_full[i]), 4);  // one arrival per dequantiser warp
-      mbar_init(smem_u32(&bars->a_empty[i]), 1);
-    }
-    mbar_init(smem_u32(&bars->lora_full), 4);
     mbar_init(smem_u32(&bars->acc_full), 1);
     mbar_init(smem_u32(&bars->done), 1);
     bars->abort = 0;
     mbar_fence_init();
   }
-  if (warp == 5) {
+  if (warp == kTfMmaWarp) {
     tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) tma_prefetch_desc(&xmap);
+  if (warp == kTfProducerWarp && lane == 0) {
+    tma_prefetch_desc(&xmap);
+    tma_prefetch_desc(&umap);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp < 4) {
+  if (warp < kTfDeqWarps) {
     // ======================= dequantisers, then epilogue =======================
-    const int64_t n = n0 + tid;           // this thread's weight row = TMEM lane tid
+    // Warp w owns weight rows 32 (w % 4) .. (tensor-memory lanes of its
+    // quadrant) and half h = w / 4 of every stage (columns 64 h .. 64 h + 63).
+    const int quad = warp & 3, h = warp >> 2;
+    const int row = quad * 32 + lane;
+    const int64_t n = n0 + row;
     const bool row_ok = n < d;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const float mu = (q.dq && row_ok) ? __ldg(q.absmax_mean) : 0.f;
-    const int64_t kb = k >> 6;
-
-    // U2 tile into shared memory, canonical K-major layout without swizzle:
-    // 8-row x 16-byte core matrices, K-adjacent cores 128 B apart, row groups
-    // (2R/8) * 128 B apart.
-    {
-      const int kgroups = (2 * R) / 8;
-      for (int tt = tid; tt < kTcBM; tt += 128) {
-        const int64_t t = m0 + tt;
-        for (int g = 0; g < kgroups; ++g) {
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (t < M) v = __ldg(reinterpret_cast<const uint4 *>(u2 + t * 2 * R) + g);
-          const uint32_t off = ((tt >> 3) * kgroups + g) * 128 + (tt & 7) * 16;
-          *reinterpret_cast<uint4 *>(utile + off) = v;
-        }
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const int64_t kp = tf_scale_pitch(k);
+    const unsigned char *crow = codes + (row_ok ? n : 0) * (k >> 1);
+    const float *srow = scales + (row_ok ? n : 0) * kp;
+    const uint32_t cbase = smem_u32(cring);
+    auto prefetch = [&](int s) {
+      if (row_ok && s < nk && static_cast<int64_t>(s) * kTfBK + h * 64 < k) {
+        const uint32_t slot = cbase + static_cast<uint32_t>(s % kTfCodeStages) * kTfCodeStageBytes;
+        const unsigned char *src = crow + static_cast<int64_t>(s) * (kTfBK / 2) + h * 32;
+        cp_async16(slot + (2 * h) * 2048u + row * 16u, src);
+        cp_async16(slot + (2 * h + 1) * 2048u + row * 16u, src + 16);
+        cp_async4(slot + 8192u + h * 512u + row * 4u, srow + 2 * s + h);
       }
-      fence_proxy_async_smem();
-    }
-    // Adapter operand [B | B] of this row into tensor memory.
-    {
-      uint32_t v[32];
-      const int half = R / 2;  // words per copy
+      cp_async_commit();  // one group per stage, empty or not
+    };
+    for (int s = 0; s < kTfCodeStages - 1; ++s) prefetch(s);
+    // This row of B as bf16 pairs (word c = columns 2c, 2c + 1), zero past r.
+    uint32_t bw[kTcMaxR / 2];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int j = 2 * (c % half);
-        uint32_t w = 0;
-        if (row_ok && c < 2 * half) {
-          const uint32_t lo = (j < r) ? Bm[n * r + j] : 0u;
-          const uint32_t hi = (j + 1 < r) ? Bm[n * r + j + 1] : 0u;
-          w = lo | (hi << 16);
-        }
-        v[c] = w;
+    for (int c = 0; c < kTcMaxR / 2; ++c) {
+      uint32_t w = 0;
+      if (row_ok && 2 * c < r) {
+        w = Bm[n * r + 2 * c];
+        if (2 * c + 1 < r) w |= static_cast<uint32_t>(Bm[n * r + 2 * c + 1]) << 16;
       }
-      tmem_st_x32(lane_addr + kLoraCol, v);
-      if (R > 32) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int cc = 32 + c;
-          const int j = 2 * (cc % half);
-          uint32_t w = 0;
-          if (row_ok && cc < 2 * half) {
-            const uint32_t lo = (j < r) ? Bm[n * r + j] : 0u;
-            const uint32_t hi = (j + 1 < r) ? Bm[n * r + j + 1] : 0u;
-            w = lo | (hi << 16);
-          }
-          v[c] = w;
-        }
-        tmem_st_x32(lane_addr + kLoraCol + 32, v);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->lora_full));
+      bw[c] = w;
     }
 
-    // Main dequantisation loop; codes and block constants run two stages
-    // ahead in a register pipeline (f0: stage s, f1: stage s + 1).
-    const uint4 *crow = reinterpret_cast<const uint4 *>(q.codes + (row_ok ? n : 0) * (k >> 1));
-    struct Fetch {
-      uint4 c0, c1;
-      float sc;
-      int qv;
-    };
-    auto fetch = [&](int s) {
-      Fetch f{make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u), 0.f, 0};
-      if (row_ok && s < nk) {
-        f.c0 = __ldg(crow + 2 * s);
-        f.c1 = __ldg(crow + 2 * s + 1);
-        const int64_t blk = n * kb + s;
-        if (q.dq) {
-          f.qv = __ldg(q.absmax_q + blk);
-          f.sc = __ldg(q.absmax_scale + (blk >> 8));
-        } else {
-          f.sc = __ldg(q.absmax + blk);
-        }
-      }
-      return f;
-    };
-    Fetch f0 = fetch(0), f1 = fetch(1);
     bool ok = true;
-    for (int s = 0; s < nk && ok; ++s) {
-      const uint4 c0 = f0.c0, c1 = f0.c1;
-      const float m = q.dq ? dq_absmax(static_cast<int8_t>(f0.qv), f0.sc, mu) : f0.sc;
-      f0 = f1;
-      f1 = fetch(s + 2);
-      const int st = s % kTcAStages;
-      if (s >= kTcAStages) ok = mbar_wait(smem_u32(&bars->a_empty[st]), ((s / kTcAStages) - 1) & 1, abort);
+    for (int s = 0; s <= nk; ++s) {
+      const uint32_t slot = s % kTfStages;
+      if (s >= kTfStages) ok = mbar_wait(smem_u32(&bars->empty[slot]), ((s / kTfStages) - 1) & 1, abort);
       ok = __all_sync(0xffffffffu, ok);  // tcgen05.st is warp-collective: leave together
       if (!ok) break;
       tc_fence_after();
-      uint32_t v[32];
-      if (row_ok) {
-        const ScaledLevels t = scaled_levels(m);
-        decode_word(c0.x, t, v + 0);
-        decode_word(c0.y, t, v + 4);
-        decode_word(c0.z, t, v + 8);
-        decode_word(c0.w, t, v + 12);
-        decode_word(c1.x, t, v + 16);
-        decode_word(c1.y, t, v + 20);
-        decode_word(c1.z, t, v + 24);
-        decode_word(c1.w, t, v + 28);
-      } else {
+      const uint32_t aaddr = lane_addr + kTfACol + slot * kTfACols + h * 32;
+      if (s < nk) {
+        cp_async_wait_group<kTfCodeStages - 2>();  // this stage's copies have landed
+        const uint32_t cs = cbase + static_cast<uint32_t>(s % kTfCodeStages) * kTfCodeStageBytes;
+        uint4 c0, c1;
+        float m;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(c0.x), "=r"(c0.y), "=r"(c0.z), "=r"(c0.w) : "r"(cs + (2 * h) * 2048u + row * 16u));
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(c1.x), "=r"(c1.y), "=r"(c1.z), "=r"(c1.w) : "r"(cs + (2 * h + 1) * 2048u + row * 16u));
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(m) : "r"(cs + 8192u + h * 512u + row * 4u));
+        prefetch(s + kTfCodeStages - 1);  // refills the slot read one stage ago
+        uint32_t v[32];
+        if (row_ok && static_cast<int64_t>(s) * kTfBK + h * 64 < k) {
+          const ScaledLevels tl = scaled_levels(m);
+          decode_word(c0.x, tl, v + 0);
+          decode_word(c0.y, tl, v + 4);
+          decode_word(c0.z, tl, v + 8);
+          decode_word(c0.w, tl, v + 12);
+          decode_word(c1.x, tl, v + 16);
+          decode_word(c1.y, tl, v + 20);
+          decode_word(c1.z, tl, v + 24);
+          decode_word(c1.w, tl, v + 28);
+        } else {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) v[c] = 0u;
+          for (int c = 0; c < 32; ++c) v[c] = 0u;
+        }
+        tmem_st_x32(aaddr, v);
+      } else {
+        // Adapter stage: the row [B | B], each copy zero-padded to 64 columns,
+        // against U2 = [hi | lo] padded the same way.
+        tmem_st_x32(aaddr, bw);
       }
-      tmem_st_x32(lane_addr + kACol + st * 32, v);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->a_full[st]));
+      if (lane == 0) mbar_arrive(smem_u32(&bars->full[slot]));
     }
+    cp_async_wait_all();  // no copy may still target shared memory at exit
 
-    // Epilogue: accumulator lane = this row, columns = tokens.
+    // Epilogue: accumulator lane = this row, columns = tokens 128 h .. 128 h + 127.
     if (ok) ok = mbar_wait(smem_u32(&bars->acc_full), 0, abort);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < kTcBM / 32; ++c) {
+      for (int c = 0; c < kTcBM / 64; ++c) {
+        const int tc0 = h * (kTcBM / 2) + c * 32;
         uint32_t acc[32];
-        tmem_ld_x32(lane_addr + kAccCol + c * 32, acc);
+        tmem_ld_x32(lane_addr + kAccCol + tc0, acc);
         tmem_ld_wait();
         if (row_ok) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const int64_t t = m0 + c * 32 + j;
+            const int64_t t = m0 + tc0 + j;
             if (t < M) Y[t * d + n] = f32_to_bf16_bits(__uint_as_float(acc[j]));
           }
         }
       }
     }
-  } else if (warp == 4) {
-    // =============================== TMA producer ===============================
+  } else if (warp == kTfProducerWarp) {
+    // ================================ TMA producer ================================
     if (lane == 0) {
       int issued = 0;
-      for (int s = 0; s < nk; ++s) {
-        const int st = s % kTcXStages;
-        if (s >= kTcXStages && !mbar_wait(smem_u32(&bars->x_empty[st]), ((s / kTcXStages) - 1) & 1, abort)) break;
-        const uint32_t full = smem_u32(&bars->x_full[st]);
-        mbar_arrive_expect_tx(full, kTcXStageBytes);
-        tma_load_2d(smem_u32(xring + st * kTcXStageBytes), &xmap, s * kTcBK, static_cast<int32_t>(m0), full);
+      for (int s = 0; s <= nk; ++s) {
+        const uint32_t slot = s % kTfStages;
+        if (s >= kTfStages && !mbar_wait(smem_u32(&bars->empty[slot]), ((s / kTfStages) - 1) & 1, abort)) break;
+        const uint32_t full = smem_u32(&bars->full[slot]);
+        mbar_arrive_expect_tx(full, kTfXStageBytes);
+        const uint32_t dst = smem_u32(xring + slot * kTfXStageBytes);
+        const CUtensorMap *map = (s < nk) ? &xmap : &umap;
+        const int32_t x0 = (s < nk) ? s * kTfBK : 0;
+        tma_load_2d(dst, map, x0, static_cast<int32_t>(m0), full);
+        tma_load_2d(dst + kTfXHalfBytes, map, x0 + 64, static_cast<int32_t>(m0), full);
         ++issued;
       }
       // Before the CTA can retire, every copy it started must have landed.
-      for (int s = (issued > kTcXStages ? issued - kTcXStages : 0); s < issued; ++s)
-        mbar_wait(smem_u32(&bars->x_full[s % kTcXStages]), (s / kTcXStages) & 1, abort);
+      for (int s = (issued > kTfStages ? issued - kTfStages : 0); s < issued; ++s)
+        mbar_wait(smem_u32(&bars->full[s % kTfStages]), (s / kTfStages) & 1, abort);
     }
   } else {
-    // ================================ MMA issuer ================================
+    // ================================= MMA issuer =================================
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kTcBN, kTcBM);
       const uint32_t d_tmem = tmem + kAccCol;
-      bool ok = mbar_wait(smem_u32(&bars->lora_full), 0, abort);
-      if (ok) {
-        // The U2 tile was written by the dequantiser warps (generic proxy,
-        // fenced); it is complete once all four arrived on lora_full.
+      bool ok = true;
+      for (int s = 0; s <= nk && ok; ++s) {
+        const uint32_t slot = s % kTfStages;
+        if (!(ok = mbar_wait(smem_u32(&bars->full[slot]), (s / kTfStages) & 1, abort))) break;
         tc_fence_after();
-        const uint32_t ubase = smem_u32(utile);
-        const uint32_t sbo = static_cast<uint32_t>((2 * R) / 8) * 128u;
-        for (int kc = 0; kc < (2 * R) / 16; ++kc) {
-          const uint64_t bdesc = smem_desc(ubase + kc * 256, 128, sbo, 0);
-          tc_mma_tmem_a(d_tmem, tmem + kLoraCol + kc * 8, bdesc, idesc, kc > 0 ? 1u : 0u);
-        }
-      }
-      for (int s = 0; s < nk && ok; ++s) {
-        const int sx = s % kTcXStages, sa = s % kTcAStages;
-        ok = mbar_wait(smem_u32(&bars->x_full[sx]), (s / kTcXStages) & 1, abort) &&
-             mbar_wait(smem_u32(&bars->a_full[sa]), (s / kTcAStages) & 1, abort);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t xbase = smem_u32(xring + sx * kTcXStageBytes);
+        const uint32_t xbase = smem_u32(xring + slot * kTfXStageBytes);
+        const uint32_t abase = tmem + kTfACol + slot * kTfACols;
 #pragma unroll
-        for (int kk = 0; kk < kTcBK / 16; ++kk) {
-          const uint64_t bdesc = smem_desc(xbase + kk * 32, 16, 1024, 2);
-          tc_mma_tmem_a(d_tmem, tmem + kACol + sa * 32 + kk * 8, bdesc, idesc, 1u);
-        }
-        tc_commit(smem_u32(&bars->x_empty[sx]));
-        tc_commit(smem_u32(&bars->a_empty[sa]));
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_tmem_a(d_tmem, abase + hh * 32 + kk * 8,
+                          smem_desc(xbase + hh * kTfXHalfBytes + kk * 32, 16, 1024, 2), idesc,
+                          (s > 0 || hh > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(smem_u32(&bars->empty[slot]));
       }
       if (ok) tc_commit(smem_u32(&bars->acc_full));
       // Every MMA issued must be complete before tensor memory is released.
@@ -292,11 +279,26 @@ qlora_fwd_tc_kernel(const __grid_constant__ CUtensorMap xmap, QnNF4View q, int64
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kTfMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
+
+// ---------------------------------------------------------------------------
+// Backward shared definitions (the forward uses none of these).
+// ---------------------------------------------------------------------------
+constexpr int kTcXStages = 4;
+constexpr int kTcThreads = 192;
+constexpr uint32_t kLoraCol = 384;
+__host__ __device__ constexpr size_t tc_u_bytes(int R) { return static_cast<size_t>(kTcBM) * 2 * R * 2; }
+
+struct TcBars {
+  uint64_t x_full[kTcXStages], x_empty[kTcXStages];
+  uint64_t lora_full, acc_full, done;
+  uint32_t tmem_base;
+  int abort;
+};
 
 // ---------------------------------------------------------------------------
 // Backward dX = dY deq(Q) + s (dY B) A on the tensor cores, as
@@ -542,9 +544,14 @@ inline bool tc_supported(int64_t M, int64_t d, int64_t k, int32_t r) {
 inline bool tc_bwd_supported(int64_t M, int64_t d, int64_t k, int32_t r) {
   return M > 16 && r <= kTcMaxR && (d % 8) == 0 && k >= kTcBK;
 }
-inline size_t tc_ws_bytes(int64_t M, int64_t, int64_t, int32_t r) {
-  const int R = tc_pad_r(r);
-  return ((static_cast<size_t>(M) * 2 * R * sizeof(uint16_t)) + 255) & ~static_cast<size_t>(255);
+// u2 (forward, row pitch kTfUCols) or v2 (backward, row pitch 2R <= kTfUCols).
+inline size_t tc_ws_bytes(int64_t M, int64_t, int64_t, int32_t) {
+  return ((static_cast<size_t>(M) * kTfUCols * sizeof(uint16_t)) + 255) & ~static_cast<size_t>(255);
+}
+// Forward: u2 plus the block constants of every row (tf_scale_pitch(k) floats per row).
+inline size_t tc_fwd_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
+  return tc_ws_bytes(M, d, k, r) +
+         ((static_cast<size_t>(d) * tf_scale_pitch(k) * sizeof(float) + 255) & ~static_cast<size_t>(255));
 }
 inline int64_t tb_ldw(int64_t d) { return (d + 7) & ~int64_t{7}; }
 inline size_t tc_bwd_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
