@@ -395,32 +395,40 @@ qn_status launch_lora_proj(const uint16_t *P, int64_t M, int64_t K, const uint16
 }
 
 // Large-M backward dX on the tensor cores: W^T dequantised into the
-// workspace, then one CTA per 128 columns of W x 256 tokens
-// (qlora_bwd_tc_kernel); v2 is the bf16 hi/lo split of v = s dY B.
+// workspace and the adapter row operand AT2 packed, then one CTA per 128
+// columns of W x 256 tokens (qlora_bwd_tc_kernel); v2 is the bf16 hi/lo split
+// of v = s dY B in the U2 layout of the forward.
 qn_status launch_tc_bwd(const qn_nf4 *Q, const uint16_t *dY, int64_t M, const uint16_t *v2, const uint16_t *A,
                         int32_t r, uint16_t *dX, Span &sp, cudaStream_t st) {
   const int64_t d = Q->d, k = Q->k;
-  const int R = qn::tc_pad_r(r);
   const int64_t ldw = qn::tb_ldw(d);
   uint16_t *wt = sp.take<uint16_t>(static_cast<size_t>(ldw) * k);
+  uint16_t *at2 = sp.take<uint16_t>(static_cast<size_t>(k) * qn::kTfUCols);
   {
     dim3 grid(static_cast<unsigned>(k / 64), static_cast<unsigned>(qn_ceil_div(d, 64)));
     qn::nf4_dequant_t_kernel<<<grid, 256, 0, st>>>(view_of(Q), ldw, wt);
     QN_LAUNCH_CHECK("nf4_dequant_t_kernel");
+    qn::lora_pack_at2_kernel<<<static_cast<unsigned>(qn_ceil_div(k * qn::kTfUCols, 256)), 256, 0, st>>>(A, r, k, at2);
+    QN_LAUNCH_CHECK("lora_pack_at2_kernel");
   }
-  CUtensorMap amap, bmap;
+  CUtensorMap amap, bmap, atmap, vmap;
   if (const char *e = qn::make_tile_map(&amap, wt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(d),
                                         static_cast<uint64_t>(k), 64, qn::kTcBN, CU_TENSOR_MAP_SWIZZLE_128B,
                                         static_cast<uint64_t>(ldw) * 2))
     return fail(QN_ECUDA, "tcgen05 backward: %s", e);
   if (const char *e = qn::make_bf16_tile_map(&bmap, dY, static_cast<uint64_t>(d), static_cast<uint64_t>(M), qn::kTcBM))
     return fail(QN_ECUDA, "tcgen05 backward: %s", e);
-  const size_t smem = qn::tb_smem_bytes(R);
+  if (const char *e = qn::make_bf16_tile_map(&atmap, at2, static_cast<uint64_t>(qn::kTfUCols), static_cast<uint64_t>(k),
+                                             qn::kTcBN))
+    return fail(QN_ECUDA, "tcgen05 backward: %s", e);
+  if (const char *e = qn::make_bf16_tile_map(&vmap, v2, static_cast<uint64_t>(qn::kTfUCols), static_cast<uint64_t>(M),
+                                             qn::kTcBM))
+    return fail(QN_ECUDA, "tcgen05 backward: %s", e);
   QN_TRY(cuda_check(cudaFuncSetAttribute(qn::qlora_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(qn::tb_smem_bytes(qn::kTcMaxR))),
+                                         static_cast<int>(qn::kTbSmemBytes)),
                     "tcgen05 backward shared-memory limit"));
   dim3 grid(static_cast<unsigned>(qn_ceil_div(k, qn::kTcBN)), static_cast<unsigned>(qn_ceil_div(M, qn::kTcBM)));
-  qn::qlora_bwd_tc_kernel<<<grid, qn::kTcThreads, smem, st>>>(amap, bmap, M, d, k, A, r, R, v2, dX);
+  qn::qlora_bwd_tc_kernel<<<grid, qn::kTbThreads, qn::kTbSmemBytes, st>>>(amap, bmap, atmap, vmap, M, d, k, dX);
   QN_LAUNCH_CHECK("qlora_bwd_tc_kernel");
   return QN_OK;
 }
@@ -627,9 +635,8 @@ qn_status qlora_linear_bwd_dx(const qn_nf4 *Q, const uint16_t *dY, int64_t M, co
   float *part = sp.take<float>(static_cast<size_t>(qn::kProjMaxSplit) * M * r);
   // v[m, q] = s * sum_i dY[m, i] B[i, q]: Qop(n = q, kk = i) = B[i * r + q].
   if (qn::tc_bwd_supported(M, d, k, r)) {
-    const int R = qn::tc_pad_r(r);
-    uint16_t *v2 = sp.take<uint16_t>(static_cast<size_t>(M) * 2 * R);
-    QN_TRY(launch_lora_proj(dY, M, d, B, r, 1, r, s, part, nullptr, R, v2, 2 * R, st));
+    uint16_t *v2 = sp.take<uint16_t>(static_cast<size_t>(M) * qn::kTfUCols);
+    QN_TRY(launch_lora_proj(dY, M, d, B, r, 1, r, s, part, nullptr, qn::kTfUCols / 2, v2, qn::kTfUCols, st));
     return launch_tc_bwd(Q, dY, M, v2, A, r, dX, sp, st);
   }
   QN_TRY(launch_lora_proj(dY, M, d, B, r, 1, r, s, part, v, 0, nullptr, 0, st));

@@ -40,12 +40,9 @@ namespace qn {
 constexpr int kTcBN = 128;   // weight rows per tile  (MMA M)
 constexpr int kTcBM = 256;   // tokens per tile       (MMA N)
 constexpr int kTcBK = 64;    // K per stage
-constexpr int kTcMaxR = 64;  // padded adapter rank R (multiple of 8)
-constexpr uint32_t kTcXStageBytes = kTcBM * kTcBK * 2;  // 32 KiB
+constexpr int kTcMaxR = 64;  // largest adapter rank r
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;
-
-__host__ __device__ constexpr int tc_pad_r(int r) { return (r + 7) & ~7; }
 
 // ---- forward ----------------------------------------------------------------
 // A stage covers 128 columns of K: two 64-column halves (one 128-byte swizzle
@@ -286,36 +283,29 @@ qlora_fwd_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
 }
 
 // ---------------------------------------------------------------------------
-// Backward shared definitions (the forward uses none of these).
+// Backward dX = dY deq(Q) + s (dY B) A on the tensor cores, as
+//   dX^T tile [128 columns of W x 256 tokens] = W^T tile . dY tile^T + AT2 . V2^T
+// with W^T the dequantised weight transposed (bf16, written once per call by
+// nf4_dequant_t_kernel) so that both operands stream K-major (K = d) through
+// TMA in stages of 128 columns (one barrier per eight MMAs).  The adapter
+// term is one more stage at the end: AT2 = [A^T | A^T] and V2 = [bf16(v) |
+// bf16(v - bf16(v))], v = s dY B, each half zero-padded to 64 columns.
+// Warps: 0-3 epilogue, 4 TMA producer, 5 MMA issuer.
 // ---------------------------------------------------------------------------
-constexpr int kTcXStages = 4;
-constexpr int kTcThreads = 192;
-constexpr uint32_t kLoraCol = 384;
-__host__ __device__ constexpr size_t tc_u_bytes(int R) { return static_cast<size_t>(kTcBM) * 2 * R * 2; }
+constexpr int kTbBK = 128;
+constexpr int kTbStages = 2;
+constexpr int kTbThreads = 192;
+constexpr uint32_t kTbAHalfBytes = kTcBN * 64 * 2;                 // 16 KiB
+constexpr uint32_t kTbBHalfBytes = kTcBM * 64 * 2;                 // 32 KiB
+constexpr uint32_t kTbStageBytes = 2 * (kTbAHalfBytes + kTbBHalfBytes);  // 96 KiB
+constexpr size_t kTbSmemBytes = 1024 + static_cast<size_t>(kTbStages) * kTbStageBytes + 256;
 
-struct TcBars {
-  uint64_t x_full[kTcXStages], x_empty[kTcXStages];
-  uint64_t lora_full, acc_full, done;
+struct TbBars {
+  uint64_t full[kTbStages], empty[kTbStages];
+  uint64_t acc_full, done;
   uint32_t tmem_base;
   int abort;
 };
-
-// ---------------------------------------------------------------------------
-// Backward dX = dY deq(Q) + s (dY B) A on the tensor cores, as
-//   dX^T tile [128 columns of W x 256 tokens] = W^T tile . dY tile^T + A^T . V2^T
-// with W^T the dequantised weight transposed (bf16, written once per call by
-// nf4_dequant_t_kernel) so that both operands stream K-major (K = d) through
-// TMA, and the adapter term as one more MMA with K = 2R: A = [A^T | A^T] in
-// tensor memory, the column operand V2 = [bf16(v) | bf16(v - bf16(v))] with
-// v = s dY B.
-// Warps: 0-3 adapter operands then epilogue, 4 TMA producer, 5 MMA issuer.
-// ---------------------------------------------------------------------------
-constexpr int kTbStages = 3;
-constexpr uint32_t kTbAStageBytes = kTcBN * kTcBK * 2;  // 16 KiB
-constexpr uint32_t kTbStageBytes = kTbAStageBytes + kTcXStageBytes;  // 48 KiB
-__host__ __device__ constexpr size_t tb_smem_bytes(int R) {
-  return 1024 + static_cast<size_t>(kTbStages) * kTbStageBytes + tc_u_bytes(R) + 256;
-}
 
 // W^T[c, r] = bf16(level[code(r, c)] * m(r, c / 64)) for a 64 x 64 tile; W^T
 // has row stride ldw (d rounded up to a multiple of 8).
@@ -362,29 +352,37 @@ __global__ void __launch_bounds__(256) nf4_dequant_t_kernel(QnNF4View q, int64_t
   }
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1)
-qlora_bwd_tc_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap, int64_t M,
-                    int64_t d, int64_t k, const uint16_t *__restrict__ Am, int r, int R,
-                    const uint16_t *__restrict__ v2, uint16_t *__restrict__ dX) {
+// AT2[c, :] = [A[0 .. 63, c] | A[0 .. 63, c]] (rows of A past r read as zero):
+// the adapter stage's row operand, k rows of kTfUCols bf16.
+__global__ void lora_pack_at2_kernel(const uint16_t *__restrict__ Am, int r, int64_t k, uint16_t *__restrict__ at2) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= k * kTfUCols) return;
+  const int64_t c = i / kTfUCols;
+  const int j = static_cast<int>(i % kTfUCols) & 63;
+  at2[i] = (j < r) ? Am[static_cast<int64_t>(j) * k + c] : 0;
+}
+
+__global__ void __launch_bounds__(kTbThreads, 1)
+qlora_bwd_tc_kernel(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap bmap,
+                    const __grid_constant__ CUtensorMap atmap, const __grid_constant__ CUtensorMap vmap, int64_t M,
+                    int64_t d, int64_t k, uint16_t *__restrict__ dX) {
   extern __shared__ __align__(1024) unsigned char tb_smem_raw[];
   unsigned char *base = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(tb_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  unsigned char *ring = base;  // stage s: A tile (16 KiB) then B tile (32 KiB)
-  unsigned char *utile = base + kTbStages * kTbStageBytes;
-  TcBars *bars = reinterpret_cast<TcBars *>(utile + tc_u_bytes(R));
+  unsigned char *ring = base;  // stage s: A halves (2 x 16 KiB) then B halves (2 x 32 KiB)
+  TbBars *bars = reinterpret_cast<TbBars *>(ring + kTbStages * kTbStageBytes);
   volatile int *abort = &bars->abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t c0 = static_cast<int64_t>(blockIdx.x) * kTcBN;  // columns of W (rows of the MMA)
   const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kTcBM;  // tokens
-  const int nk = static_cast<int>((d + kTcBK - 1) / kTcBK);
+  const int nk = static_cast<int>((d + kTbBK - 1) / kTbBK);     // stages over d; stage nk is the adapter's
 
   if (tid == 0) {
     for (int i = 0; i < kTbStages; ++i) {
-      mbar_init(smem_u32(&bars->x_full[i]), 1);
-      mbar_init(smem_u32(&bars->x_empty[i]), 1);
+      mbar_init(smem_u32(&bars->full[i]), 1);
+      mbar_init(smem_u32(&bars->empty[i]), 1);
     }
-    mbar_init(smem_u32(&bars->lora_full), 4);
     mbar_init(smem_u32(&bars->acc_full), 1);
     mbar_init(smem_u32(&bars->done), 1);
     bars->abort = 0;
@@ -397,6 +395,8 @@ qlora_bwd_tc_kernel(const __grid_constant__ CUtensorMap amap, const __grid_const
   if (warp == 4 && lane == 0) {
     tma_prefetch_desc(&amap);
     tma_prefetch_desc(&bmap);
+    tma_prefetch_desc(&atmap);
+    tma_prefetch_desc(&vmap);
   }
   tc_fence_before();
   __syncthreads();
@@ -404,61 +404,9 @@ qlora_bwd_tc_kernel(const __grid_constant__ CUtensorMap amap, const __grid_const
   const uint32_t tmem = bars->tmem_base;
 
   if (warp < 4) {
-    // ===================== adapter operands, then epilogue =====================
-    const int64_t c = c0 + tid;  // this thread's column of W = TMEM lane tid
-    const bool col_ok = c < k;
+    // ================================== epilogue ==================================
+    const int64_t c = c0 + tid;  // this thread's column of W = tensor-memory lane tid
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    // V2 tile into shared memory, canonical K-major layout without swizzle.
-    {
-      const int kgroups = (2 * R) / 8;
-      for (int tt = tid; tt < kTcBM; tt += 128) {
-        const int64_t t = m0 + tt;
-        for (int gi = 0; gi < kgroups; ++gi) {
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (t < M) v = __ldg(reinterpret_cast<const uint4 *>(v2 + t * 2 * R) + gi);
-          const uint32_t off = ((tt >> 3) * kgroups + gi) * 128 + (tt & 7) * 16;
-          *reinterpret_cast<uint4 *>(utile + off) = v;
-        }
-      }
-      fence_proxy_async_smem();
-    }
-    // [A^T | A^T] of this column into tensor memory: element q is A[q, c].
-    {
-      uint32_t v[32];
-      const int half = R / 2;
-#pragma unroll
-      for (int cc = 0; cc < 32; ++cc) {
-        const int j = 2 * (cc % half);
-        uint32_t w = 0;
-        if (col_ok && cc < 2 * half) {
-          const uint32_t lo = (j < r) ? Am[static_cast<int64_t>(j) * k + c] : 0u;
-          const uint32_t hi = (j + 1 < r) ? Am[static_cast<int64_t>(j + 1) * k + c] : 0u;
-          w = lo | (hi << 16);
-        }
-        v[cc] = w;
-      }
-      tmem_st_x32(lane_addr + kLoraCol, v);
-      if (R > 32) {
-#pragma unroll
-        for (int cc0 = 0; cc0 < 32; ++cc0) {
-          const int cc = 32 + cc0;
-          const int j = 2 * (cc % half);
-          uint32_t w = 0;
-          if (col_ok && cc < 2 * half) {
-            const uint32_t lo = (j < r) ? Am[static_cast<int64_t>(j) * k + c] : 0u;
-            const uint32_t hi = (j + 1 < r) ? Am[static_cast<int64_t>(j + 1) * k + c] : 0u;
-            w = lo | (hi << 16);
-          }
-          v[cc0] = w;
-        }
-        tmem_st_x32(lane_addr + kLoraCol + 32, v);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->lora_full));
-    }
-    // Epilogue: accumulator lane = this column, columns = tokens.
     bool ok = mbar_wait(smem_u32(&bars->acc_full), 0, abort);
     if (__all_sync(0xffffffffu, ok)) {
       tc_fence_after();
@@ -467,7 +415,7 @@ qlora_bwd_tc_kernel(const __grid_constant__ CUtensorMap amap, const __grid_const
         uint32_t acc[32];
         tmem_ld_x32(lane_addr + kAccCol + cb * 32, acc);
         tmem_ld_wait();
-        if (col_ok) {
+        if (c < k) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int64_t t = m0 + cb * 32 + j;
@@ -480,45 +428,44 @@ qlora_bwd_tc_kernel(const __grid_constant__ CUtensorMap amap, const __grid_const
     // =============================== TMA producer ===============================
     if (lane == 0) {
       int issued = 0;
-      for (int s = 0; s < nk; ++s) {
-        const int st = s % kTbStages;
-        if (s >= kTbStages && !mbar_wait(smem_u32(&bars->x_empty[st]), ((s / kTbStages) - 1) & 1, abort)) break;
-        const uint32_t full = smem_u32(&bars->x_full[st]);
+      for (int s = 0; s <= nk; ++s) {
+        const uint32_t slot = s % kTbStages;
+        if (s >= kTbStages && !mbar_wait(smem_u32(&bars->empty[slot]), ((s / kTbStages) - 1) & 1, abort)) break;
+        const uint32_t full = smem_u32(&bars->full[slot]);
         mbar_arrive_expect_tx(full, kTbStageBytes);
-        unsigned char *stage = ring + st * kTbStageBytes;
-        tma_load_2d(smem_u32(stage), &amap, s * kTcBK, static_cast<int32_t>(c0), full);
-        tma_load_2d(smem_u32(stage + kTbAStageBytes), &bmap, s * kTcBK, static_cast<int32_t>(m0), full);
+        const uint32_t stage = smem_u32(ring + slot * kTbStageBytes);
+        const CUtensorMap *am = (s < nk) ? &amap : &atmap;
+        const CUtensorMap *bm = (s < nk) ? &bmap : &vmap;
+        const int32_t x0 = (s < nk) ? s * kTbBK : 0;
+        tma_load_2d(stage, am, x0, static_cast<int32_t>(c0), full);
+        tma_load_2d(stage + kTbAHalfBytes, am, x0 + 64, static_cast<int32_t>(c0), full);
+        tma_load_2d(stage + 2 * kTbAHalfBytes, bm, x0, static_cast<int32_t>(m0), full);
+        tma_load_2d(stage + 2 * kTbAHalfBytes + kTbBHalfBytes, bm, x0 + 64, static_cast<int32_t>(m0), full);
         ++issued;
       }
       for (int s = (issued > kTbStages ? issued - kTbStages : 0); s < issued; ++s)
-        mbar_wait(smem_u32(&bars->x_full[s % kTbStages]), (s / kTbStages) & 1, abort);
+        mbar_wait(smem_u32(&bars->full[s % kTbStages]), (s / kTbStages) & 1, abort);
     }
   } else {
     // ================================ MMA issuer ================================
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kTcBN, kTcBM);
       const uint32_t d_tmem = tmem + kAccCol;
-      bool ok = mbar_wait(smem_u32(&bars->lora_full), 0, abort);
-      if (ok) {
+      bool ok = true;
+      for (int s = 0; s <= nk && ok; ++s) {
+        const uint32_t slot = s % kTbStages;
+        if (!(ok = mbar_wait(smem_u32(&bars->full[slot]), (s / kTbStages) & 1, abort))) break;
         tc_fence_after();
-        const uint32_t ubase = smem_u32(utile);
-        const uint32_t sbo = static_cast<uint32_t>((2 * R) / 8) * 128u;
-        for (int kc = 0; kc < (2 * R) / 16; ++kc) {
-          const uint64_t bdesc = smem_desc(ubase + kc * 256, 128, sbo, 0);
-          tc_mma_tmem_a(d_tmem, tmem + kLoraCol + kc * 8, bdesc, idesc, kc > 0 ? 1u : 0u);
-        }
-      }
-      for (int s = 0; s < nk && ok; ++s) {
-        const int st = s % kTbStages;
-        ok = mbar_wait(smem_u32(&bars->x_full[st]), (s / kTbStages) & 1, abort);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t abase = smem_u32(ring + st * kTbStageBytes);
-        const uint32_t bbase = abase + kTbAStageBytes;
+        const uint32_t abase = smem_u32(ring + slot * kTbStageBytes);
+        const uint32_t bbase = abase + 2 * kTbAHalfBytes;
 #pragma unroll
-        for (int kk = 0; kk < kTcBK / 16; ++kk)
-          tc_mma_ss(d_tmem, smem_desc(abase + kk * 32, 16, 1024, 2), smem_desc(bbase + kk * 32, 16, 1024, 2), idesc, 1u);
-        tc_commit(smem_u32(&bars->x_empty[st]));
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_ss(d_tmem, smem_desc(abase + hh * kTbAHalfBytes + kk * 32, 16, 1024, 2),
+                      smem_desc(bbase + hh * kTbBHalfBytes + kk * 32, 16, 1024, 2), idesc,
+                      (s > 0 || hh > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(smem_u32(&bars->empty[slot]));
       }
       if (ok) tc_commit(smem_u32(&bars->acc_full));
       tc_commit(smem_u32(&bars->done));
@@ -554,8 +501,10 @@ inline size_t tc_fwd_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
          ((static_cast<size_t>(d) * tf_scale_pitch(k) * sizeof(float) + 255) & ~static_cast<size_t>(255));
 }
 inline int64_t tb_ldw(int64_t d) { return (d + 7) & ~int64_t{7}; }
+// Backward: v2, W^T (k rows of tb_ldw(d) bf16) and AT2 (k rows of kTfUCols bf16).
 inline size_t tc_bwd_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
-  return tc_ws_bytes(M, d, k, r) + ((static_cast<size_t>(tb_ldw(d)) * k * 2 + 255) & ~static_cast<size_t>(255));
+  return tc_ws_bytes(M, d, k, r) + ((static_cast<size_t>(tb_ldw(d)) * k * 2 + 255) & ~static_cast<size_t>(255)) +
+         ((static_cast<size_t>(k) * kTfUCols * 2 + 255) & ~static_cast<size_t>(255));
 }
 
 // Tensor map of a row-major bf16 matrix [rows x cols] read in boxes of
