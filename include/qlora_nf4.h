@@ -166,7 +166,9 @@ qn_status nf4_dequantize(const qn_nf4 *Q, void *Wout, qn_dtype odt, void *stream
  *   bf16(deq(Q)) and the adapter term uses u split into bf16 hi + lo.  The
  *   few-token path (2 <= M <= 16) streams the int8 block constants with bulk
  *   copies when Q->absmax_q is 16-byte aligned (else it reads them through
- *   L1).  ws: qn_workspace_bytes(QN_OP_LINEAR_FWD).
+ *   L1).  For M > 16 and r <= 64 the workspace also holds the bf16 hi/lo
+ *   split of u (M x 128) and the fp32 block constants of W (d x 2*ceil(k/128))
+ *   for the tensor-core kernel.  ws: qn_workspace_bytes(QN_OP_LINEAR_FWD).
  */
 qn_status qlora_linear_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M,
                            const uint16_t *A, const uint16_t *B, int32_t r,
@@ -196,8 +198,9 @@ qn_status qlora_linear_fwd_group(int32_t n, const qn_nf4 *const *Q, const uint16
  * qlora_linear_bwd_dx -- dX = dY deq(Q) + (alpha/r) (dY B) A.
  *   dY device bf16 [M x d]; A, B as in the forward; dX device bf16 [M x k].
  *   Same size rules and workspace query (QN_OP_LINEAR_BWD_DX); for M > 16,
- *   r <= 64 and d % 8 == 0 the workspace also holds bf16 W^T (k x d) for the
- *   tensor-core GEMM.
+ *   r <= 64 and d % 8 == 0 the workspace also holds bf16 W^T (k x d), the
+ *   bf16 hi/lo split of v = (alpha/r) dY B (M x 128) and [A^T | A^T]
+ *   (k x 128 bf16) for the tensor-core GEMM.
  */
 qn_status qlora_linear_bwd_dx(const qn_nf4 *Q, const uint16_t *dY, int64_t M,
                               const uint16_t *A, const uint16_t *B, int32_t r,
