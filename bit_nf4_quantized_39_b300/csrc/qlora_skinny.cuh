@@ -103,8 +103,6 @@ __host__ __device__ constexpr size_t sk_smem_bytes(int MT, int M, int64_t k, boo
          kSkScratchBytes + kSkBarBytes + kSkUBytes + (xs ? static_cast<size_t>(M) * k * 2 : 0);
 }
 
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // D += A * B, m16n8k16, bf16 inputs, fp32 accumulator.
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
