@@ -288,13 +288,9 @@ qn_status launch_decode_group(int n, const qn_nf4 *const *Q, const uint16_t *X, 
   if (grid < sms) grid = sms;
   if (grid > sms * per_sm) grid = sms * per_sm;
   float *u = sp.take<float>(static_cast<size_t>(us));
-  // Programmatic dependent launch: the kernel prefetches weights and builds
-  // its table before griddepcontrol.wait.  Its CTAs spin on counters that
-  // only co-resident CTAs can satisfy; a later grid can start launching only
-  // once every CTA of this one has issued launch_dependents, i.e. is
-  // resident, so that later grid never holds a slot this one still needs.
-  return launch_pdl(qn::qlora_decode_kernel, dim3(static_cast<unsigned>(grid)), dim3(qn::kDecThreads), smem, st,
-                    "qlora_decode_kernel", g, zero_area, u);
+  qn::qlora_decode_kernel<<<static_cast<unsigned>(grid), qn::kDecThreads, smem, st>>>(g, zero_area, u);
+  QN_LAUNCH_CHECK("qlora_decode_kernel");
+  return QN_OK;
 }
 
 template <int MT, bool XS>

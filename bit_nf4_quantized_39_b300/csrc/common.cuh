@@ -89,14 +89,6 @@ __device__ __forceinline__ float block_scale(const QnNF4View &q, int64_t j) {
 
 __host__ __device__ constexpr int64_t qn_ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Programmatic dependent launch: pdl_wait blocks until the grid launched
-// before this one on the stream has completed and its writes are visible
-// (it returns at once for a kernel launched without the attribute);
-// pdl_trigger lets the next grid start launching once every CTA of this one
-// has issued it.
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
 // ---------------------------------------------------------------------------
 // Register decode of 4-bit codes into exactly bf16(fp32(level * m)): the 16
 // levels scaled by a block constant m are built once as bf16 and split into

@@ -247,22 +247,9 @@ qlora_decode_kernel(const __grid_constant__ DecGroup g, unsigned int *__restrict
     }
   };
 
-  // ---- prologue: the first weight loads and the level-pair table depend on
-  // nothing the kernel before this one writes, so they run before
-  // griddepcontrol.wait (under programmatic dependent launch they overlap
-  // that kernel's tail); then x (one round covers k <= 16384) into shared
-  // memory and one barrier.  x, u, y and the workspace counters are touched
-  // only after the wait. ----------------------------------------------------------
-  pdl_trigger();  // the next launch may start as this grid's CTAs retire
-  DecStep buf[kDecDepth];
-#pragma unroll
-  for (int i = 0; i < kDecDepth; ++i) load_next(buf[i]);
-#pragma unroll 4
-  for (int n = 0; n < 32; ++n) {
-    const int b = warp + 8 * n;  // entry b of this lane: (level[b & 15], level[b >> 4]); warp-uniform index
-    *reinterpret_cast<float2 *>(lut + 256 * b + 8 * lane) = make_float2(c_nf4_levels[b & 15], c_nf4_levels[b >> 4]);
-  }
-  pdl_wait();
+  // ---- prologue: x loads first (one round covers k <= 16384), the weight
+  // loads behind them, the level-pair table while they are in flight, then x
+  // into shared memory and one barrier -------------------------------------------
   constexpr int kPer = 8;  // 16-byte x loads per thread
   static_assert(kPer * kDecThreads * 8 >= kDecMaxK, "one round of x loads must cover k");
   const int64_t nvec = dec_xs_floats(k) / 8;
@@ -271,6 +258,14 @@ qlora_decode_kernel(const __grid_constant__ DecGroup g, unsigned int *__restrict
   for (int v = 0; v < kPer; ++v) {
     const int64_t vi = v * kDecThreads + tid;
     xt[v] = (vi * 8 < k) ? __ldg(reinterpret_cast<const uint4 *>(g.X) + vi) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  DecStep buf[kDecDepth];
+#pragma unroll
+  for (int i = 0; i < kDecDepth; ++i) load_next(buf[i]);
+#pragma unroll 4
+  for (int n = 0; n < 32; ++n) {
+    const int b = warp + 8 * n;  // entry b of this lane: (level[b & 15], level[b >> 4]); warp-uniform index
+    *reinterpret_cast<float2 *>(lut + 256 * b + 8 * lane) = make_float2(c_nf4_levels[b & 15], c_nf4_levels[b >> 4]);
   }
 #pragma unroll
   for (int v = 0; v < kPer; ++v) {

@@ -36,8 +36,11 @@
 //    8 partials in a fixed order, adds u[t] . B[row] on the MMA (B rows
 //    prefetched with cp.async when the group starts) and writes bf16 Y.
 //    The producer streams and the consumers build the table before
-//    griddepcontrol.wait, so both overlap the kernel before; X, u and Y are
-//    touched only after it.
+//    griddepcontrol.wait; X, u and Y are touched only after it.  Neither
+//    kernel issues launch_dependents: a dependent's wait is only guaranteed
+//    to see writes made before the trigger (inside a CUDA graph a chained
+//    call was observed to read its input early when the trigger came first),
+//    and a CTA that never issues it counts as triggering when it exits.
 //
 // Every mbarrier wait is bounded (QN_DEV_TIMEOUT, then the warp winds down);
 // there is no wait on another CTA.
@@ -103,6 +106,7 @@ __host__ __device__ constexpr size_t sk_smem_bytes(int MT, int M, int64_t k, boo
          kSkScratchBytes + kSkBarBytes + kSkUBytes + (xs ? static_cast<size_t>(M) * k * 2 : 0);
 }
 
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // D += A * B, m16n8k16, bf16 inputs, fp32 accumulator.
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -119,7 +123,6 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kSkUThreads)
 skinny_u_kernel(const __grid_constant__ SkGroup g) {
-  pdl_trigger();
   const int64_t j = blockIdx.x;
   const int t = blockIdx.y;
   const int64_t k = g.k;
@@ -241,7 +244,6 @@ skinny_kernel(const __grid_constant__ SkGroup g) {
     *abort = 0;
     mbar_fence_init();
   }
-  pdl_trigger();
   __syncthreads();
 
   auto proj_of = [&](int rg) {

@@ -140,6 +140,62 @@ def test_decode_repeated_and_graph_replay(qn):
     assert torch.equal(Y1, Y2)
 
 
+@pytest.mark.parametrize("M", [1, 4])
+def test_chain_reads_previous_output(qn, M):
+    """Each call's input is the previous call's output.  The few-token kernels
+    are launched as programmatic dependents (start early, read x only after
+    griddepcontrol.wait) and the single-token kernel in plain stream order;
+    either way x must be read only once the call before has written it.  The
+    outputs start as NaN, so a read that comes too early shows; every link
+    must equal that link recomputed alone after a synchronise, eagerly and
+    replayed in one CUDA graph."""
+    d = k = 4096
+    n = 6
+    m = synth.decode_matrix(seed=5, d=d, k=k, r=16, M=M)
+    q = qn.nf4_quantize(torch.from_numpy(m["W"]).cuda())
+    A, B, X0 = m["A"].cuda(), m["B"].cuda(), m["X"].cuda()
+    ys = [torch.empty((M, d), dtype=torch.bfloat16, device="cuda") for _ in range(n)]
+
+    def chain():
+        x = X0
+        for y in ys:
+            qn.qlora_linear_fwd(q, x, A, B, m["alpha"], out=y)
+            x = y
+
+    def check():
+        prev = X0
+        for i, y in enumerate(ys):
+            ref = qn.qlora_linear_fwd(q, prev, A, B, m["alpha"])
+            torch.cuda.synchronize()
+            assert torch.isfinite(y.float()).all(), i
+            assert torch.equal(y, ref), i
+            prev = y
+
+    for y in ys:
+        y.fill_(float("nan"))
+    chain()
+    torch.cuda.synchronize()
+    check()
+    eager = [y.clone() for y in ys]
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        chain()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        chain()
+    for rep in range(2):
+        for y in ys:
+            y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for i, (y, e) in enumerate(zip(ys, eager)):
+            assert torch.equal(y, e), (rep, i)
+    qn.device_status()
+
+
 @pytest.mark.parametrize("M", [1, 3])
 def test_group_of_projections(qn, M):
     """Projections of one input in one call (query/key/value style), with
