@@ -15,8 +15,12 @@ Modules
             double quantisation of the absmax constants, dequantisation.
 ``exact``   exact rational helpers (exact mean of fp32 values, correct
             rounding of a rational to fp32 / bf16).
-``layer``   the QLoRA linear layer forward ``Y`` and backward ``dX`` in float64.
-``loftq``   the LoftQ alternation with an exact LAPACK SVD.
+``layer``   the QLoRA linear layer forward ``Y``, backward ``dX`` and the
+            adapter gradients ``dA``, ``dB`` in float64.
+``loftq``   the LoftQ alternation with an exact LAPACK SVD, and its one-step
+            variant that keeps a given quantised weight.
+``merge``   merge / unmerge of an adapter into an NF4 weight (dequantise,
+            add or subtract s B A, requantise).
 
 Sources (pages of the method, cited by title and section)
 --------------------------------------------------------
@@ -29,7 +33,8 @@ Sources (pages of the method, cited by title and section)
   B in R^{d x r}, A in R^{r x k}, h = Wx + BAx, (d+k) r trainable parameters;
   §4.2: NF4 + double quantisation.
 * "PEFT quantization guide" (huggingface docs, 量化): bf16 compute dtype,
-  nested (double) quantisation, dequantise-add-requantise merge semantics.
+  nested (double) quantisation, dequantise-add-requantise merge semantics,
+  one-step LoftQ (replace_lora_weights_loftq) that only refits the adapter.
 * "LoftQ explainer" (mhpn.cn/news/832204) §2.2 objective
   min ||W - (Q + Delta)||_F^2 with rank(Delta) <= r, §2.3 alternation
   (round-to-nearest Q-step, truncated-SVD Delta-step).
@@ -39,4 +44,4 @@ Pins (tests that tie each function to something other than itself) live in
 "parity unpinned".
 """
 
-from . import exact, nf4, layer, loftq  # noqa: F401
+from . import exact, nf4, layer, loftq, merge  # noqa: F401

@@ -10,6 +10,13 @@ X in R^{M x k}:
 
     Y  = X W'^T + s (X A^T) B^T                       (M x d)
     dX = dY W'  + s (dY B) A                          (M x k)
+    dB = s dY^T (X A^T)                               (d x r)
+    dA = s (dY B)^T X                                 (r x k)
+
+dA and dB are the gradients of a loss L with dL/dY = dY with respect to the
+adapter factors, the part of the backward pass that reaches the trainable
+weights ("QLoRA paper summary", abstract: gradients are back-propagated
+through the frozen 4-bit weight into the low-rank adapters).
 
 where W' is the fp32 dequantised weight.  Every operand is widened exactly
 to float64 and each product is one numpy matmul (a library primitive).
@@ -43,6 +50,25 @@ def linear_bwd_dx(dY, Wdeq, A, B, alpha: float, r: int) -> np.ndarray:
     B64 = np.asarray(B, dtype=np.float64)
     s = float(alpha) / float(r)
     return dY64 @ W64 + s * ((dY64 @ B64) @ A64)
+
+
+def lora_grads(X, dY, A, B, alpha: float, r: int):
+    """(dA, dB) in float64: dA = s (dY B)^T X  (r x k),  dB = s dY^T (X A^T)  (d x r).
+
+    Y depends on A only through s (X A^T) B^T and on B only through the same
+    term, so for L = <dY, Y>: dL/dB[i, q] = s sum_m dY[m, i] (X A^T)[m, q] and
+    dL/dA[q, j] = s sum_m (dY B)[m, q] X[m, j].
+    """
+    X64 = np.asarray(X, dtype=np.float64)
+    dY64 = np.asarray(dY, dtype=np.float64)
+    A64 = np.asarray(A, dtype=np.float64)
+    B64 = np.asarray(B, dtype=np.float64)
+    s = float(alpha) / float(r)
+    u = X64 @ A64.T          # M x r
+    v = dY64 @ B64           # M x r
+    dB = s * (dY64.T @ u)
+    dA = s * (v.T @ X64)
+    return dA, dB
 
 
 def rel_fro(a, b) -> float:

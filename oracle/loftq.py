@@ -14,6 +14,11 @@ layer's scale s = alpha / r, so the factors are split as
 B = U_r sqrt(Sigma_r) / sqrt(s), A = sqrt(Sigma_r) V_r^T / sqrt(s), giving
 s B A = Delta.  Residuals e_t = ||W - deq(Q_t) - s B_t A_t||_F for
 t = 0..T, where e_0 is plain QLoRA (Q_0 = NF4(W), no adapter).
+
+One-step variant ("PEFT quantization guide", section on
+replace_lora_weights_loftq): the base weight stays the quantised tensor the
+caller already has, and only the adapter is replaced by one Delta-step
+against it, B A from the top-r SVD of W - deq(Q).  Nothing is requantised.
 """
 
 from __future__ import annotations
@@ -65,3 +70,29 @@ def loftq(W, r: int, alpha: float, T: int, block: int = nf4.BLOCK,
         res.sing.append(S_all)
     res.Q, res.A, res.B = Q, A, B
     return res
+
+
+@dataclass
+class OneStepResult:
+    A: np.ndarray            # r x k, float64
+    B: np.ndarray            # d x r, float64
+    resid: list              # [||W - deq(Q)||_F, ||W - deq(Q) - s B A||_F]
+    sing: np.ndarray         # singular values of W - deq(Q)
+
+
+def loftq_one_step(W, Q: nf4.NF4Tensor, r: int, alpha: float) -> OneStepResult:
+    """One Delta-step against a given quantised weight Q (no Q-step).
+
+    R = W - deq(Q); B = U_r sqrt(Sigma_r) / sqrt(s), A = sqrt(Sigma_r) V_r^T / sqrt(s),
+    so s B A is the best rank-r approximation of R.
+    """
+    W64 = np.asarray(W, dtype=np.float32).astype(np.float64)
+    d, k = W64.shape
+    s = float(alpha) / float(r)
+    R = W64 - nf4.dequantize(Q).reshape(d, k).astype(np.float64)
+    U, S, Vt, S_all = rank_r(R, r)
+    sq = np.sqrt(S)
+    B = (U * sq[None, :]) / np.sqrt(s)
+    A = (sq[:, None] * Vt) / np.sqrt(s)
+    return OneStepResult(A=A, B=B, resid=[float(np.linalg.norm(R)), float(np.linalg.norm(R - s * (B @ A)))],
+                         sing=S_all)
