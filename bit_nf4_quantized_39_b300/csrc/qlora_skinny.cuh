@@ -11,8 +11,12 @@
 // Two kernels, chained with programmatic dependent launch (PDL):
 //
 // 1. skinny_u_kernel: u[t, j] = s_g A_g[j] . X[t] for every adapter row j of
-//    the group and token t; one CTA per (j, t).  It loads its A row before
-//    waiting on the previous kernel (A is a weight) and X after.
+//    the group and token t; one CTA per (j, t).  It reads nothing before
+//    waiting on the previous kernel: X and A (an adapter that an optimiser
+//    step may just have written) both come after griddepcontrol.wait.  The
+//    weight kernel's own early reads (codes and block constants) are safe
+//    because this kernel always runs between it and any earlier writer and
+//    waits for that writer to complete before it exits.
 // 2. skinny_kernel: the weights, one CTA per SM.  Work items are row groups
 //    of 16 rows of one projection (the M side of an m16n8k16 MMA).  A
 //    producer warp streams each row group's codes with TMA in stages of 16
@@ -136,21 +140,13 @@ skinny_u_kernel(const __grid_constant__ SkGroup g) {
   const int64_t nvec = k >> 3;
   constexpr int kPer = 8;
   float acc = 0.f;
-  bool waited = false;
+  pdl_wait();  // X and A may be written by the kernel before this one
   for (int64_t base = 0; base < nvec; base += static_cast<int64_t>(kSkUThreads) * kPer) {
     uint4 a[kPer], x[kPer];
 #pragma unroll
     for (int v = 0; v < kPer; ++v) {
       const int64_t c = base + v * kSkUThreads + threadIdx.x;
-      a[v] = (c < nvec) ? __ldg(arow + c) : make_uint4(0u, 0u, 0u, 0u);
-    }
-    if (!waited) {
-      pdl_wait();  // X may be written by the kernel before this one
-      waited = true;
-    }
-#pragma unroll
-    for (int v = 0; v < kPer; ++v) {
-      const int64_t c = base + v * kSkUThreads + threadIdx.x;
+      a[v] = (c < nvec) ? arow[c] : make_uint4(0u, 0u, 0u, 0u);
       x[v] = (c < nvec) ? xrow[c] : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
@@ -164,7 +160,6 @@ skinny_u_kernel(const __grid_constant__ SkGroup g) {
       }
     }
   }
-  if (!waited) pdl_wait();
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   __shared__ float red[kSkUThreads / 32];
@@ -301,9 +296,10 @@ skinny_kernel(const __grid_constant__ SkGroup g) {
                         (s * kSkStageBlocks + 4 * j) * 8, row0, full);
         }
       }
-      // Every copy this CTA started lands before it may retire.
+      // Every copy this CTA started lands before it may retire (a drain wait:
+      // not cut short when another warp has given up).
       for (uint32_t r = (qi > kSkStages ? qi - kSkStages : 0); r < qi; ++r)
-        mbar_wait(smem_u32(&st_full[r % kSkStages]), (r / kSkStages) & 1, abort);
+        mbar_wait_drain(smem_u32(&st_full[r % kSkStages]), (r / kSkStages) & 1);
     }
     return;
   }
@@ -557,6 +553,7 @@ skinny_kernel(const __grid_constant__ SkGroup g) {
       }
     }
   }
+  cp_async_wait_all();  // a warp that left early may still have a B-row prefetch in flight
 }
 
 }  // namespace qn

@@ -243,8 +243,11 @@ qlora_fwd_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
         ++issued;
       }
       // Before the CTA can retire, every copy it started must have landed.
+      // (After an abort a stage's barrier may also lack the dequantisers'
+      // arrivals; the drain then gives up after its bound, by which time the
+      // bytes have long landed.)
       for (int s = (issued > kTfStages ? issued - kTfStages : 0); s < issued; ++s)
-        mbar_wait(smem_u32(&bars->full[s % kTfStages]), (s / kTfStages) & 1, abort);
+        mbar_wait_drain(smem_u32(&bars->full[s % kTfStages]), (s / kTfStages) & 1);
     }
   } else {
     // ================================= MMA issuer =================================
@@ -270,7 +273,7 @@ qlora_fwd_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_const
       if (ok) tc_commit(smem_u32(&bars->acc_full));
       // Every MMA issued must be complete before tensor memory is released.
       tc_commit(smem_u32(&bars->done));
-      mbar_wait(smem_u32(&bars->done), 0, abort);
+      mbar_wait_drain(smem_u32(&bars->done), 0);
     }
   }
 
@@ -444,7 +447,7 @@ qlora_bwd_tc_kernel(const __grid_constant__ CUtensorMap amap, const __grid_const
         ++issued;
       }
       for (int s = (issued > kTbStages ? issued - kTbStages : 0); s < issued; ++s)
-        mbar_wait(smem_u32(&bars->full[s % kTbStages]), (s / kTbStages) & 1, abort);
+        mbar_wait_drain(smem_u32(&bars->full[s % kTbStages]), (s / kTbStages) & 1);
     }
   } else {
     // ================================ MMA issuer ================================
@@ -469,7 +472,7 @@ qlora_bwd_tc_kernel(const __grid_constant__ CUtensorMap amap, const __grid_const
       }
       if (ok) tc_commit(smem_u32(&bars->acc_full));
       tc_commit(smem_u32(&bars->done));
-      mbar_wait(smem_u32(&bars->done), 0, abort);
+      mbar_wait_drain(smem_u32(&bars->done), 0);
     }
   }
 

@@ -64,6 +64,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   return false;
 }
 
+// Wind-down wait for work this thread itself started (TMA copies landing in
+// shared memory, MMAs before tensor memory is released): bounded only by the
+// try count, never cut short by *abort, because leaving early would free
+// memory that the copies or MMAs still target.  False (and QN_DEV_TIMEOUT)
+// if the phase never completes.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  qn_flag_timeout();
+  return false;
+}
+
 // ---- cp.async (16-byte global -> shared copies, L1 bypassed) --------------------
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");

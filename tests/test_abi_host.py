@@ -117,5 +117,8 @@ def test_noalloc_quantize_argument_errors(qn):
     st = _struct(qn)
     assert L.nf4_quantize_noalloc(P, 9, ctypes.byref(st), None) == qn.QN_EINVAL
     assert L.nf4_quantize_noalloc(P + 8, 0, ctypes.byref(st), None) == qn.QN_EALIGN
-    huge = _struct(qn, d=1 << 21, k=1 << 20)          # 2^41 elements
+    # 2^41 elements: QN_ESHAPE comes from the shape check every entry point
+    # shares (d*k <= 2^40), which also bounds what the static scratch covers
+    huge = _struct(qn, d=1 << 21, k=1 << 20)
     assert L.nf4_quantize_noalloc(P, 0, ctypes.byref(huge), None) == qn.QN_ESHAPE
+    assert "too large" in qn.lib.qn_last_error().decode()
