@@ -11,7 +11,11 @@ The functions carry the names of the C ABI (``include/qlora_nf4.h``):
 * :func:`nf4_dequantize`      NF4Tensor -> fp32 / bf16 weights
 * :func:`qlora_linear_fwd`    Y  = X deq(Q)^T + (alpha/r) (X A^T) B^T
 * :func:`qlora_linear_bwd_dx` dX = dY deq(Q) + (alpha/r) (dY B) A
+* :func:`qlora_linear_bwd_lora`  dA = s (dY B)^T X, dB = s dY^T (X A^T)
+* :func:`qlora_linear_fwd_f32` / :func:`qlora_linear_bwd_dx_f32`  fp32 compute dtype
 * :func:`loftq_init`          LoftQ alternation -> (Q, A, B, residuals)
+* :func:`loftq_replace_lora`  one LoftQ step against a given Q -> (A, B, residuals)
+* :func:`nf4_merge_lora`      NF4(deq(Q) +- s B A) (merge / unmerge)
 
 If the shared library is missing, importing this package raises ImportError:
 there is no CPU fallback.
@@ -30,7 +34,8 @@ LIB_PATH = os.path.join(_HERE, "libqlora_nf4.so")
 
 QN_OK, QN_EINVAL, QN_ESHAPE, QN_EALIGN, QN_ENOMEM, QN_ECUDA, QN_ETIMEOUT, QN_EUNSUPPORTED = range(8)
 QN_F32, QN_BF16 = 0, 1
-QN_OP_QUANTIZE, QN_OP_DEQUANTIZE, QN_OP_LINEAR_FWD, QN_OP_LINEAR_BWD_DX, QN_OP_LOFTQ = range(5)
+(QN_OP_QUANTIZE, QN_OP_DEQUANTIZE, QN_OP_LINEAR_FWD, QN_OP_LINEAR_BWD_DX, QN_OP_LOFTQ, QN_OP_LINEAR_BWD_LORA,
+ QN_OP_LINEAR_F32, QN_OP_MERGE) = range(8)
 
 _STATUS_NAMES = {0: "QN_OK", 1: "QN_EINVAL", 2: "QN_ESHAPE", 3: "QN_EALIGN", 4: "QN_ENOMEM",
                  5: "QN_ECUDA", 6: "QN_ETIMEOUT", 7: "QN_EUNSUPPORTED"}
@@ -71,6 +76,12 @@ def _load():
         "nf4_quantize_noalloc": (ctypes.c_int, [vp, ctypes.c_int, P(qn_nf4), vp]),
         "qlora_linear_fwd_group": (ctypes.c_int, [i32, P(P(qn_nf4)), vp, i64, P(vp), P(vp), P(i32), P(f32), P(vp),
                                                   vp, sz, vp]),
+        "qlora_linear_bwd_lora": (ctypes.c_int, [vp, vp, i64, i64, i64, vp, vp, i32, f32, vp, vp, vp, sz, vp]),
+        "qlora_linear_fwd_f32": (ctypes.c_int, [P(qn_nf4), vp, i64, vp, vp, i32, f32, vp, vp, sz, vp]),
+        "qlora_linear_bwd_dx_f32": (ctypes.c_int, [P(qn_nf4), vp, i64, vp, vp, i32, f32, vp, vp, sz, vp]),
+        "loftq_replace_lora": (ctypes.c_int, [vp, P(qn_nf4), i32, f32, ctypes.c_uint64, i32, i32, vp, vp, vp,
+                                              vp, sz, vp]),
+        "nf4_merge_lora": (ctypes.c_int, [P(qn_nf4), vp, vp, i32, f32, i32, P(qn_nf4), vp, sz, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -82,7 +93,8 @@ def _load():
 lib = _load()
 EXPORTS = ("qn_abi_version", "qn_last_error", "qn_nf4_tables", "qn_workspace_bytes", "nf4_quantize",
            "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd_dx", "loftq_init", "qn_device_status",
-           "nf4_quantize_noalloc", "qlora_linear_fwd_group")
+           "nf4_quantize_noalloc", "qlora_linear_fwd_group", "qlora_linear_bwd_lora", "qlora_linear_fwd_f32",
+           "qlora_linear_bwd_dx_f32", "loftq_replace_lora", "nf4_merge_lora")
 
 
 def _check(status: int):
@@ -298,6 +310,101 @@ def loftq_init(W: torch.Tensor, r: int, alpha: float, T: int = 5, seed: int = 0,
                           ctypes.byref(st), A.data_ptr(), B.data_ptr(), ctypes.addressof(resid), wp, wn,
                           _stream_ptr(stream)))
     return q, A, B, list(resid)
+
+
+def qlora_linear_bwd_lora(X: torch.Tensor, dY: torch.Tensor, A: torch.Tensor, B: torch.Tensor, alpha: float,
+                          stream=None):
+    """(dA fp32 r x k, dB fp32 d x r): gradients of the adapter factors for dL/dY = dY."""
+    A = _dev_bf16(A, "A")
+    B = _dev_bf16(B, "B")
+    r, k = A.shape
+    d = B.shape[0]
+    X = _dev_bf16(X, "X").reshape(-1, k)
+    dY = _dev_bf16(dY, "dY").reshape(-1, d)
+    M = X.shape[0]
+    if dY.shape[0] != M:
+        raise ValueError("X and dY must have the same number of rows")
+    dA = torch.empty((r, k), dtype=torch.float32, device=X.device)
+    dB = torch.empty((d, r), dtype=torch.float32, device=X.device)
+    ws = _workspace(workspace_bytes(QN_OP_LINEAR_BWD_LORA, M, d, k, r), X.device)
+    wp, wn = _ws_ptr(ws)
+    _check(lib.qlora_linear_bwd_lora(X.data_ptr(), dY.data_ptr(), M, d, k, A.data_ptr(), B.data_ptr(), r,
+                                     float(alpha), dA.data_ptr(), dB.data_ptr(), wp, wn, _stream_ptr(stream)))
+    return dA, dB
+
+
+def _dev_f32(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.float32:
+        raise ValueError(f"{name} must be fp32 (got {t.dtype})")
+    return t.contiguous()
+
+
+def qlora_linear_fwd_f32(q: NF4Tensor, X: torch.Tensor, A: torch.Tensor, B: torch.Tensor, alpha: float,
+                         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Y = X deq(Q)^T + (alpha/r) (X A^T) B^T with fp32 X, A, B, Y (fp32 compute dtype)."""
+    X = _dev_f32(X, "X").reshape(-1, q.k)
+    A = _dev_f32(A, "A")
+    B = _dev_f32(B, "B")
+    r, M = A.shape[0], X.shape[0]
+    Y = out if out is not None else torch.empty((M, q.d), dtype=torch.float32, device=q.device)
+    ws = _workspace(workspace_bytes(QN_OP_LINEAR_F32, M, q.d, q.k, r), q.device)
+    wp, wn = _ws_ptr(ws)
+    st = q.c_struct()
+    _check(lib.qlora_linear_fwd_f32(ctypes.byref(st), X.data_ptr(), M, A.data_ptr(), B.data_ptr(), r, float(alpha),
+                                    Y.data_ptr(), wp, wn, _stream_ptr(stream)))
+    return Y
+
+
+def qlora_linear_bwd_dx_f32(q: NF4Tensor, dY: torch.Tensor, A: torch.Tensor, B: torch.Tensor, alpha: float,
+                            out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """dX = dY deq(Q) + (alpha/r) (dY B) A with fp32 operands (fp32 compute dtype)."""
+    dY = _dev_f32(dY, "dY").reshape(-1, q.d)
+    A = _dev_f32(A, "A")
+    B = _dev_f32(B, "B")
+    r, M = A.shape[0], dY.shape[0]
+    dX = out if out is not None else torch.empty((M, q.k), dtype=torch.float32, device=q.device)
+    ws = _workspace(workspace_bytes(QN_OP_LINEAR_F32, M, q.d, q.k, r), q.device)
+    wp, wn = _ws_ptr(ws)
+    st = q.c_struct()
+    _check(lib.qlora_linear_bwd_dx_f32(ctypes.byref(st), dY.data_ptr(), M, A.data_ptr(), B.data_ptr(), r,
+                                       float(alpha), dX.data_ptr(), wp, wn, _stream_ptr(stream)))
+    return dX
+
+
+def loftq_replace_lora(W: torch.Tensor, q: NF4Tensor, r: int, alpha: float, seed: int = 0, oversample: int = 8,
+                       power_iters: int = 4, stream=None):
+    """One LoftQ step against the given quantised weight q (kept as it is):
+    returns (A fp32 r x k, B fp32 d x r, [||W - deq(q)||_F, ||W - deq(q) - s B A||_F])."""
+    W = _dev_f32(W, "W")
+    if W.dim() != 2 or W.shape != (q.d, q.k):
+        raise ValueError("W must be a d x k fp32 CUDA tensor matching q")
+    A = torch.empty((r, q.k), dtype=torch.float32, device=W.device)
+    B = torch.empty((q.d, r), dtype=torch.float32, device=W.device)
+    resid = (ctypes.c_double * 2)()
+    ws = _workspace(workspace_bytes(QN_OP_LOFTQ, 0, q.d, q.k, r), W.device)
+    wp, wn = _ws_ptr(ws)
+    st = q.c_struct()
+    _check(lib.loftq_replace_lora(W.data_ptr(), ctypes.byref(st), r, float(alpha), seed, oversample, power_iters,
+                                  A.data_ptr(), B.data_ptr(), ctypes.addressof(resid), wp, wn, _stream_ptr(stream)))
+    return A, B, list(resid)
+
+
+def nf4_merge_lora(q: NF4Tensor, A: torch.Tensor, B: torch.Tensor, alpha: float, sign: int = 1,
+                   out: NF4Tensor | None = None, stream=None) -> NF4Tensor:
+    """NF4(deq(q) + sign (alpha/r) B A): sign +1 merges the adapter, -1 unmerges it.
+    ``out=q`` merges in place."""
+    A = _dev_bf16(A, "A")
+    B = _dev_bf16(B, "B")
+    r = A.shape[0]
+    o = out if out is not None else NF4Tensor.empty(q.d, q.k, q.dq, q.device)
+    ws = _workspace(workspace_bytes(QN_OP_MERGE, 0, q.d, q.k, r), q.device)
+    wp, wn = _ws_ptr(ws)
+    si, so = q.c_struct(), o.c_struct()
+    _check(lib.nf4_merge_lora(ctypes.byref(si), A.data_ptr(), B.data_ptr(), r, float(alpha), int(sign),
+                              ctypes.byref(so), wp, wn, _stream_ptr(stream)))
+    return o
 
 
 def device_status(stream=None) -> None:

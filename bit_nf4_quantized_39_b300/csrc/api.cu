@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 #include <string>
 
@@ -16,7 +17,11 @@
 #include "qlora_simt.cuh"
 #include "qlora_decode.cuh"
 #include "qlora_skinny.cuh"
+#include "qlora_gemv.cuh"
 #include "qlora_tc.cuh"
+#include "lora_grad.cuh"
+#include "qlora_f32.cuh"
+#include "nf4_merge.cuh"
 #include "loftq.cuh"
 
 namespace {
@@ -192,7 +197,7 @@ qn_status launch_dequantize(const qn_nf4 *Q, void *out, qn_dtype odt, cudaStream
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
   if (grid > cap) grid = cap;
   if (odt == QN_BF16)
-    qn::nf4_dequant_kernel<true><<<static_cast<unsigned>(grid), 256, 0, st>>>(view_of(Q), n, out);
+    qn::nf4_dequant_bf16_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(view_of(Q), n, static_cast<uint16_t *>(out));
   else
     qn::nf4_dequant_kernel<false><<<static_cast<unsigned>(grid), 256, 0, st>>>(view_of(Q), n, out);
   QN_LAUNCH_CHECK("nf4_dequant_kernel");
@@ -213,6 +218,23 @@ size_t fwd_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
   if (!use_skinny(M, k)) b += proj_ws_bytes(M, r) + qn::tc_fwd_ws_bytes(M, d, k, r);
   return b;
 }
+
+// Adapter gradients: u, v (M x r fp32), the projection's split-K partials,
+// the bf16 hi/lo transposes of u and v, and the token-split partials of the
+// larger of the two contractions.
+size_t lg_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
+  const int64_t Rp = qn::lg_rp(r), Mp = qn::lg_round(M, qn::kLgTK);
+  const int64_t Nmax = d > k ? d : k;
+  const int Smax = qn::lg_splits(M, d, r) > qn::lg_splits(M, k, r) ? qn::lg_splits(M, d, r) : qn::lg_splits(M, k, r);
+  return kSemBytes + 2 * round256(static_cast<size_t>(M) * r * sizeof(float)) + proj_ws_bytes(M, r) +
+         2 * round256(static_cast<size_t>(2) * Rp * Mp * sizeof(uint16_t)) +
+         round256(static_cast<size_t>(Smax) * Rp * Nmax * sizeof(float));
+}
+
+size_t loftq_ws_bytes(int64_t d, int64_t k);  // LoftQ workspace (defined with the LoftQ loop)
+
+// fp32-compute layer: the adapter projection (M x r fp32).
+size_t f32_ws_bytes(int64_t M, int32_t r) { return kSemBytes + round256(static_cast<size_t>(M) * r * sizeof(float)); }
 
 size_t bwd_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
   return kSemBytes + round256(static_cast<size_t>(M) * r * sizeof(float)) + proj_ws_bytes(M, r) +
@@ -291,6 +313,62 @@ qn_status launch_decode_group(int n, const qn_nf4 *const *Q, const uint16_t *X, 
   qn::qlora_decode_kernel<<<static_cast<unsigned>(grid), qn::kDecThreads, smem, st>>>(g, zero_area, u);
   QN_LAUNCH_CHECK("qlora_decode_kernel");
   return QN_OK;
+}
+
+// Forward of a group of projections of one input with M <= 8 tokens and
+// M * k <= 16384 on the persistent single-kernel path (qlora_gemv_kernel),
+// launched as a programmatic dependent of the kernel before it.  Sets *taken
+// to false, launching nothing, when the group exceeds that kernel's limits.
+qn_status launch_gemv_group(int n, const qn_nf4 *const *Q, const uint16_t *X, int64_t M, const uint16_t *const *A,
+                            const uint16_t *const *B, const int32_t *r, const float *alpha, uint16_t *const *Y,
+                            unsigned int *zero_area, Span &sp, cudaStream_t st, bool *taken) {
+  *taken = false;
+  const int64_t k = Q[0]->k;
+  qn::GvGroup g = {};
+  g.n = n;
+  g.M = static_cast<int>(M);
+  g.k = k;
+  g.X = X;
+  g.zero_area = zero_area;
+  int64_t tiles = 0, us = 0;
+  for (int i = 0; i < n; ++i) {
+    qn::GvProj &p = g.p[i];
+    p.q = view_of(Q[i]);
+    p.A = A[i];
+    p.B = B[i];
+    p.Y = Y[i];
+    p.r = r[i];
+    p.s = alpha[i] / static_cast<float>(r[i]);
+    p.tile_off = tiles;
+    p.u_off = us;
+    tiles += qn_ceil_div(Q[i]->d, qn::kGvRows);
+    us += r[i];
+  }
+  const int64_t grid = tiles < sm_count() ? tiles : sm_count();
+  if (M > qn::kGvMaxM || !qn::gv_fits(static_cast<int>(M), k, tiles, us, static_cast<int>(grid))) return QN_OK;
+  for (int i = 0; i < n; ++i) {
+    // codes as uint32 [d][k / 8]: one box = 16 rows x 128 bytes (4 blocks)
+    if (const char *e = qn::make_tile_map(&g.p[i].tmap, Q[i]->codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4,
+                                          static_cast<uint64_t>(k / 8), static_cast<uint64_t>(Q[i]->d),
+                                          qn::kGvBoxBytes / 4, qn::kGvRows, CU_TENSOR_MAP_SWIZZLE_128B))
+      return fail(QN_ECUDA, "single-kernel forward: %s", e);
+  }
+  g.ntiles = tiles;
+  g.rtot = us;
+  g.u = sp.take<float>(static_cast<size_t>(M) * us);
+  static int attr_set[64] = {0};
+  int dev = 0;
+  QN_TRY(cuda_check(cudaGetDevice(&dev), "cudaGetDevice"));
+  if (dev < 0 || dev >= 64) return fail(QN_EUNSUPPORTED, "device ordinal out of range");
+  if (!attr_set[dev]) {
+    QN_TRY(cuda_check(cudaFuncSetAttribute(qn::qlora_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(qn::kGvSmemBytes)),
+                      "cudaFuncSetAttribute(single-kernel forward smem)"));
+    attr_set[dev] = 1;
+  }
+  *taken = true;
+  return launch_pdl(qn::qlora_gemv_kernel, dim3(static_cast<unsigned>(grid)), dim3(qn::kGvThreads), qn::kGvSmemBytes,
+                    st, "qlora_gemv_kernel", g);
 }
 
 template <int MT, bool XS>
@@ -459,6 +537,57 @@ qn_status launch_tc_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M, const uin
   return QN_OK;
 }
 
+// C = scale * P1 Op1 (+ P2 Op2) on the fp32 CUDA-core GEMM (qlora_f32.cuh).
+qn_status launch_f32_gemm(const qn::F32Gemm &gp, cudaStream_t st) {
+  const unsigned gx = static_cast<unsigned>(qn_ceil_div(gp.N, qn::kF32BN));
+  if (gp.M <= 16) {
+    qn::f32_gemm_kernel<16><<<dim3(gx, static_cast<unsigned>(qn_ceil_div(gp.M, 16))), qn::kF32Threads, 0, st>>>(gp);
+  } else {
+    qn::f32_gemm_kernel<64><<<dim3(gx, static_cast<unsigned>(qn_ceil_div(gp.M, 64))), qn::kF32Threads, 0, st>>>(gp);
+  }
+  QN_LAUNCH_CHECK("f32_gemm_kernel");
+  return QN_OK;
+}
+
+qn::F32Operand f32_mat(const float *F, int64_t sn, int64_t sk) {
+  qn::F32Operand o = {};
+  o.kind = qn::F32_OP_MAT;
+  o.F = F;
+  o.sn = sn;
+  o.sk = sk;
+  return o;
+}
+qn::F32Operand f32_nf4(const qn_nf4 *Q, bool cols) {
+  qn::F32Operand o = {};
+  o.kind = cols ? qn::F32_OP_NF4_COLS : qn::F32_OP_NF4_ROWS;
+  o.q = view_of(Q);
+  return o;
+}
+
+// Token contraction C[q, n] = sum_m V[m, q] P[m, n] of the adapter gradients
+// (lora_grad.cuh), written as C (transpose_out = 0) or C^T.
+qn_status launch_lora_grad(const uint16_t *P, int64_t M, int64_t N, const uint16_t *vt2, int32_t r, float *part,
+                           int transpose_out, float *out, cudaStream_t st) {
+  const int64_t Rp = qn::lg_rp(r), Mp = qn::lg_round(M, qn::kLgTK);
+  const int rch = qn::lg_rch(r);
+  const int S = qn::lg_splits(M, N, r);
+  const int64_t tps = qn::lg_round(qn_ceil_div(M, S), qn::kLgTK);
+  const int Sused = static_cast<int>(qn_ceil_div(M, tps));
+  dim3 grid(static_cast<unsigned>(qn_ceil_div(N, qn::kLgTN)), static_cast<unsigned>(Sused),
+            static_cast<unsigned>(Rp / rch));
+  switch (rch / 16) {
+    case 1: qn::lora_grad_kernel<1><<<grid, qn::kLgThreads, 0, st>>>(P, M, N, vt2, Rp, Mp, tps, part); break;
+    case 2: qn::lora_grad_kernel<2><<<grid, qn::kLgThreads, 0, st>>>(P, M, N, vt2, Rp, Mp, tps, part); break;
+    case 3: qn::lora_grad_kernel<3><<<grid, qn::kLgThreads, 0, st>>>(P, M, N, vt2, Rp, Mp, tps, part); break;
+    default: qn::lora_grad_kernel<4><<<grid, qn::kLgThreads, 0, st>>>(P, M, N, vt2, Rp, Mp, tps, part); break;
+  }
+  QN_LAUNCH_CHECK("lora_grad_kernel");
+  qn::lora_grad_reduce_kernel<<<static_cast<unsigned>(qn_ceil_div(static_cast<int64_t>(r) * N, 256)), 256, 0, st>>>(
+      part, Sused, Rp, N, r, transpose_out, out);
+  QN_LAUNCH_CHECK("lora_grad_reduce_kernel");
+  return QN_OK;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -518,18 +647,10 @@ size_t qn_workspace_bytes(qn_op op, int64_t M, int64_t d, int64_t k, int32_t r) 
     case QN_OP_DEQUANTIZE: return 0;
     case QN_OP_LINEAR_FWD: return (M < 1 || d < 1 || k < 1 || r < 1) ? 0 : fwd_ws_bytes(M, d, k, r);
     case QN_OP_LINEAR_BWD_DX: return (M < 1 || d < 1 || k < 1 || r < 1) ? 0 : bwd_ws_bytes(M, d, k, r);
-    case QN_OP_LOFTQ: {
-      if (d < 1 || k < 1) return 0;
-      const size_t P = qn::kLqMaxP;
-      size_t b = kSemBytes + round256(static_cast<size_t>(d) * k * sizeof(float));  // target / residual
-      b += round256(static_cast<size_t>(d) * P * sizeof(float));            // Y
-      b += 2 * round256(static_cast<size_t>(k) * P * sizeof(float));        // Zt, Omega
-      b += round256(P * P * sizeof(double)) + round256(P * P * sizeof(float)) + round256(P * sizeof(float));  // G, V, lam
-      b += round256(P * P * sizeof(float));                                  // Linv
-      b += round256(1024 * sizeof(double)) + round256(sizeof(double));       // partials, norm
-      b += round256(kQuantWs);
-      return b;
-    }
+    case QN_OP_LINEAR_BWD_LORA: return (M < 1 || d < 1 || k < 1 || r < 1) ? 0 : lg_ws_bytes(M, d, k, r);
+    case QN_OP_LINEAR_F32: return (M < 1 || r < 1) ? 0 : f32_ws_bytes(M, r);
+    case QN_OP_MERGE: return kQuantWs;
+    case QN_OP_LOFTQ: return (d < 1 || k < 1) ? 0 : loftq_ws_bytes(d, k);
   }
   return 0;
 }
@@ -572,6 +693,11 @@ qn_status qlora_linear_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M, const 
   Span sp{static_cast<char *>(ws), ws_bytes, 0};
   unsigned int *sem = sp.take<unsigned int>(kSemBytes / sizeof(unsigned int));
   const float s = alpha / static_cast<float>(r);
+  if (use_skinny(M, k)) {
+    bool taken = false;
+    QN_TRY(launch_gemv_group(1, &Q, X, M, &A, &B, &r, &alpha, &Y, sem, sp, st, &taken));
+    if (taken) return QN_OK;
+  }
   if (use_decode(M, k)) return launch_decode_group(1, &Q, X, &A, &B, &r, &alpha, &Y, sem, sp, st);
   if (use_skinny(M, k)) return launch_skinny_group(1, &Q, X, M, &A, &B, &r, &alpha, &Y, sp, st);
   float *u = sp.take<float>(static_cast<size_t>(M) * r);
@@ -610,6 +736,9 @@ qn_status qlora_linear_fwd_group(int32_t n, const qn_nf4 *const *Q, const uint16
   if (use_decode(M, k) || use_skinny(M, k)) {
     Span sp{static_cast<char *>(ws), ws_bytes, 0};
     unsigned int *sem = sp.take<unsigned int>(kSemBytes / sizeof(unsigned int));
+    bool taken = false;
+    QN_TRY(launch_gemv_group(n, Q, X, M, A, B, r, alpha, Y, sem, sp, st, &taken));
+    if (taken) return QN_OK;
     if (use_decode(M, k)) return launch_decode_group(n, Q, X, A, B, r, alpha, Y, sem, sp, st);
     return launch_skinny_group(n, Q, X, M, A, B, r, alpha, Y, sp, st);
   }
@@ -646,6 +775,97 @@ qn_status qlora_linear_bwd_dx(const qn_nf4 *Q, const uint16_t *dY, int64_t M, co
   return QN_OK;
 }
 
+qn_status qlora_linear_bwd_lora(const uint16_t *X, const uint16_t *dY, int64_t M, int64_t d, int64_t k,
+                                const uint16_t *A, const uint16_t *B, int32_t r, float alpha, float *dA, float *dB,
+                                void *ws, size_t ws_bytes, void *stream) {
+  g_last_error.clear();
+  if (!X || !dY || !A || !B || !dA || !dB) return fail(QN_EINVAL, "NULL tensor pointer");
+  if (M < 1 || d < 1 || k < 1) return fail(QN_ESHAPE, "M, d and k must be positive");
+  if (d > (int64_t(1) << 40) / k || M > (int64_t(1) << 40) / (d > k ? d : k)) return fail(QN_ESHAPE, "sizes too large");
+  if (r < 1 || r > 256) return fail(QN_ESHAPE, "r must be in [1, 256] (got %d)", r);
+  if (!std::isfinite(alpha)) return fail(QN_EINVAL, "alpha must be finite");
+  if (!aligned(X, 16) || !aligned(dY, 16) || !aligned(A, 16) || !aligned(B, 16) || !aligned(dA, 16) ||
+      !aligned(dB, 16))
+    return fail(QN_EALIGN, "tensor pointers must be 16-byte aligned");
+  const size_t need = lg_ws_bytes(M, d, k, r);
+  if (!ws) return fail(QN_EINVAL, "workspace NULL");
+  if (ws_bytes < need) return fail(QN_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (!aligned(ws, 256)) return fail(QN_EALIGN, "workspace not 256-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Span sp{static_cast<char *>(ws), ws_bytes, 0};
+  (void)sp.take<unsigned int>(kSemBytes / sizeof(unsigned int));
+  const float s = alpha / static_cast<float>(r);
+  float *u = sp.take<float>(static_cast<size_t>(M) * r);
+  float *v = sp.take<float>(static_cast<size_t>(M) * r);
+  float *part = sp.take<float>(static_cast<size_t>(qn::kProjMaxSplit) * M * r);
+  const int64_t Rp = qn::lg_rp(r), Mp = qn::lg_round(M, qn::kLgTK);
+  uint16_t *ut2 = sp.take<uint16_t>(static_cast<size_t>(2) * Rp * Mp);
+  uint16_t *vt2 = sp.take<uint16_t>(static_cast<size_t>(2) * Rp * Mp);
+  const int Sd = qn::lg_splits(M, d, r), Sk = qn::lg_splits(M, k, r);
+  const size_t gpart_n = std::max(static_cast<size_t>(Sd) * Rp * d, static_cast<size_t>(Sk) * Rp * k);
+  float *gpart = sp.take<float>(gpart_n);
+  // u = s X A^T (Qop(n = q, kk = j) = A[q * k + j]);  v = s dY B (Qop(n = q, kk = i) = B[i * r + q])
+  QN_TRY(launch_lora_proj(X, M, k, A, r, k, 1, s, part, u, 0, nullptr, 0, st));
+  QN_TRY(launch_lora_proj(dY, M, d, B, r, 1, r, s, part, v, 0, nullptr, 0, st));
+  const unsigned pg = static_cast<unsigned>(qn_ceil_div(Rp * Mp, 256));
+  qn::lora_vt_pack_kernel<<<pg, 256, 0, st>>>(u, M, r, Rp, Mp, ut2);
+  QN_LAUNCH_CHECK("lora_vt_pack_kernel(u)");
+  qn::lora_vt_pack_kernel<<<pg, 256, 0, st>>>(v, M, r, Rp, Mp, vt2);
+  QN_LAUNCH_CHECK("lora_vt_pack_kernel(v)");
+  // dB^T[q, i] = sum_m u[m, q] dY[m, i]  (written as dB, d x r);  dA[q, j] = sum_m v[m, q] X[m, j]
+  QN_TRY(launch_lora_grad(dY, M, d, ut2, r, gpart, 1, dB, st));
+  QN_TRY(launch_lora_grad(X, M, k, vt2, r, gpart, 0, dA, st));
+  return QN_OK;
+}
+
+qn_status qlora_linear_fwd_f32(const qn_nf4 *Q, const float *X, int64_t M, const float *A, const float *B, int32_t r,
+                               float alpha, float *Y, void *ws, size_t ws_bytes, void *stream) {
+  g_last_error.clear();
+  QN_TRY(check_layer(Q, X, M, A, B, r, alpha, Y));
+  const int64_t d = Q->d, k = Q->k;
+  const size_t need = f32_ws_bytes(M, r);
+  if (!ws) return fail(QN_EINVAL, "workspace NULL");
+  if (ws_bytes < need) return fail(QN_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (!aligned(ws, 256)) return fail(QN_EALIGN, "workspace not 256-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Span sp{static_cast<char *>(ws), ws_bytes, 0};
+  (void)sp.take<unsigned int>(kSemBytes / sizeof(unsigned int));
+  float *u = sp.take<float>(static_cast<size_t>(M) * r);
+  const float s = alpha / static_cast<float>(r);
+  qn::F32Gemm g1 = {};  // u = s X A^T: Op(kk = j, n = q) = A[q * k + j]
+  g1.P1 = X; g1.K1 = k; g1.op1 = f32_mat(A, k, 1); g1.M = M; g1.N = r; g1.scale = s; g1.C = u;
+  QN_TRY(launch_f32_gemm(g1, st));
+  qn::F32Gemm g2 = {};  // Y = X W'^T + u B^T: Op1(kk = j, n) = W'[n, j], Op2(kk = q, n) = B[n * r + q]
+  g2.P1 = X; g2.K1 = k; g2.op1 = f32_nf4(Q, false);
+  g2.P2 = u; g2.K2 = r; g2.op2 = f32_mat(B, r, 1);
+  g2.M = M; g2.N = d; g2.scale = 1.f; g2.C = Y;
+  return launch_f32_gemm(g2, st);
+}
+
+qn_status qlora_linear_bwd_dx_f32(const qn_nf4 *Q, const float *dY, int64_t M, const float *A, const float *B,
+                                  int32_t r, float alpha, float *dX, void *ws, size_t ws_bytes, void *stream) {
+  g_last_error.clear();
+  QN_TRY(check_layer(Q, dY, M, A, B, r, alpha, dX));
+  const int64_t d = Q->d, k = Q->k;
+  const size_t need = f32_ws_bytes(M, r);
+  if (!ws) return fail(QN_EINVAL, "workspace NULL");
+  if (ws_bytes < need) return fail(QN_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (!aligned(ws, 256)) return fail(QN_EALIGN, "workspace not 256-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Span sp{static_cast<char *>(ws), ws_bytes, 0};
+  (void)sp.take<unsigned int>(kSemBytes / sizeof(unsigned int));
+  float *v = sp.take<float>(static_cast<size_t>(M) * r);
+  const float s = alpha / static_cast<float>(r);
+  qn::F32Gemm g1 = {};  // v = s dY B: Op(kk = i, n = q) = B[i * r + q]
+  g1.P1 = dY; g1.K1 = d; g1.op1 = f32_mat(B, 1, r); g1.M = M; g1.N = r; g1.scale = s; g1.C = v;
+  QN_TRY(launch_f32_gemm(g1, st));
+  qn::F32Gemm g2 = {};  // dX = dY W' + v A: Op1(kk = i, n = c) = W'[i, c], Op2(kk = q, n = c) = A[q * k + c]
+  g2.P1 = dY; g2.K1 = d; g2.op1 = f32_nf4(Q, true);
+  g2.P2 = v; g2.K2 = r; g2.op2 = f32_mat(A, 1, k);
+  g2.M = M; g2.N = k; g2.scale = 1.f; g2.C = dX;
+  return launch_f32_gemm(g2, st);
+}
+
 qn_status nf4_quantize_noalloc(const void *W, qn_dtype wdt, const qn_nf4 *Q, void *stream) {
   g_last_error.clear();
   if (!tables_consistent()) return fail(QN_EUNSUPPORTED, "internal NF4 tables inconsistent");
@@ -674,38 +894,45 @@ qn_status qn_device_status(void *stream) {
   return QN_OK;
 }
 
-qn_status loftq_init(const float *W, int64_t d, int64_t k, int32_t r, float alpha, int32_t T, uint64_t seed,
-                     int32_t oversample, int32_t power_iters, const qn_nf4 *Q, float *A, float *B, double *resid,
-                     void *ws, size_t ws_bytes, void *stream) {
-  g_last_error.clear();
-  if (!W || !A || !B || !resid || !Q) return fail(QN_EINVAL, "NULL pointer");
-  QN_TRY(check_nf4(Q, true));
-  if (Q->d != d || Q->k != k) return fail(QN_ESHAPE, "Q shape %lldx%lld != W shape", (long long)Q->d, (long long)Q->k);
-  if (d % 64 || k % 64) return fail(QN_ESHAPE, "d and k must be multiples of 64");
-  const int p = r + oversample;
-  if (r < 1 || oversample < 0 || p > qn::kLqMaxP) return fail(QN_ESHAPE, "need 1 <= r and r + oversample <= 32");
-  if (p > d || p > k) return fail(QN_ESHAPE, "r + oversample exceeds a matrix dimension");
-  if (T < 0 || T > 64) return fail(QN_ESHAPE, "T must be in [0, 64]");
-  if (power_iters < 0 || power_iters > 32) return fail(QN_ESHAPE, "power_iters must be in [0, 32]");
-  if (!std::isfinite(alpha) || alpha == 0.f) return fail(QN_EINVAL, "alpha must be finite and non-zero");
-  if (!aligned(W, 16) || !aligned(A, 16) || !aligned(B, 16)) return fail(QN_EALIGN, "W/A/B not 16-byte aligned");
-  const size_t need = qn_workspace_bytes(QN_OP_LOFTQ, 0, d, k, r);
-  if (!ws) return fail(QN_EINVAL, "workspace NULL");
-  if (ws_bytes < need) return fail(QN_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, need);
-  if (!aligned(ws, 256)) return fail(QN_EALIGN, "workspace not 256-byte aligned");
+}  // extern "C"
 
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  constexpr int P = qn::kLqMaxP;
+namespace {
+
+// LoftQ workspace: the d x k residual, the panels Y (d x P), Zt and Omega
+// (k x P), the Gram partials and the small P x P factors.
+size_t loftq_ws_bytes(int64_t d, int64_t k) {
+  const size_t P = qn::kLqMaxP;
+  const size_t nb = static_cast<size_t>(qn_ceil_div(d > k ? d : k, qn::kLqGramRows));
+  size_t b = kSemBytes + round256(static_cast<size_t>(d) * k * sizeof(float));  // target / residual
+  b += round256(static_cast<size_t>(d) * P * sizeof(float));                  // Y
+  b += 2 * round256(static_cast<size_t>(k) * P * sizeof(float));              // Zt, Omega
+  b += round256(nb * P * P * sizeof(float));                                  // Gram partials
+  b += round256(P * P * sizeof(double)) + 2 * round256(P * P * sizeof(float)) + round256(P * sizeof(float));
+  b += round256(1024 * sizeof(double)) + round256(sizeof(double));            // norm partials, norm
+  b += round256(kQuantWs);
+  return b;
+}
+
+// The LoftQ loop on panels of P columns (r + oversample <= P).  requantise:
+// Q_0 = NF4(W) and T alternations (loftq_init); otherwise Q is the caller's
+// quantised weight, kept as it is, and one Delta-step is taken against it
+// (loftq_replace_lora, T == 1).
+template <int P>
+qn_status loftq_run_p(const float *W, int64_t d, int64_t k, int32_t r, float alpha, int32_t T, uint64_t seed, int p,
+                      int32_t power_iters, const qn_nf4 *Q, float *A, float *B, double *resid, void *ws,
+                      size_t ws_bytes, cudaStream_t st, bool requantise) {
   Span sp{static_cast<char *>(ws), ws_bytes, 0};
   unsigned int *sem = sp.take<unsigned int>(kSemBytes / sizeof(unsigned int));  // zero on entry and exit
   float *Tbuf = sp.take<float>(static_cast<size_t>(d) * k);
-  float *Y = sp.take<float>(static_cast<size_t>(d) * P);
-  float *Zt = sp.take<float>(static_cast<size_t>(k) * P);
-  float *Om = sp.take<float>(static_cast<size_t>(k) * P);
-  double *G = sp.take<double>(P * P);
-  float *V = sp.take<float>(P * P);
-  float *lam = sp.take<float>(P);
-  float *Linv = sp.take<float>(P * P);
+  float *Y = sp.take<float>(static_cast<size_t>(d) * qn::kLqMaxP);
+  float *Zt = sp.take<float>(static_cast<size_t>(k) * qn::kLqMaxP);
+  float *Om = sp.take<float>(static_cast<size_t>(k) * qn::kLqMaxP);
+  const int64_t nbmax = qn_ceil_div(d > k ? d : k, qn::kLqGramRows);
+  float *gpart = sp.take<float>(static_cast<size_t>(nbmax) * qn::kLqMaxP * qn::kLqMaxP);
+  double *G = sp.take<double>(qn::kLqMaxP * qn::kLqMaxP);
+  float *V = sp.take<float>(qn::kLqMaxP * qn::kLqMaxP);
+  float *Linv = sp.take<float>(qn::kLqMaxP * qn::kLqMaxP);
+  float *lam = sp.take<float>(qn::kLqMaxP);
   double *partial = sp.take<double>(1024);
   double *norm2 = sp.take<double>(1);
   unsigned long long *bins = sp.take<unsigned long long>(qn::kNumBins);
@@ -715,6 +942,16 @@ qn_status loftq_init(const float *W, int64_t d, int64_t k, int32_t r, float alph
   const int64_t n = d * k;
   const QnNF4View qv = view_of(Q);
   const int red_blocks = sms * 4 < 1024 ? sms * 4 : 1024;
+  static int attr_set[64] = {0};
+  int dev = 0;
+  QN_TRY(cuda_check(cudaGetDevice(&dev), "cudaGetDevice"));
+  if (dev < 0 || dev >= 64) return fail(QN_EUNSUPPORTED, "device ordinal out of range");
+  if (!attr_set[dev]) {
+    QN_TRY(cuda_check(cudaFuncSetAttribute(qn::lq_jacobi_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(qn::lq_jacobi_smem<P>())),
+                      "cudaFuncSetAttribute(jacobi smem)"));
+    attr_set[dev] = 1;
+  }
 
   QN_TRY(cuda_check(cudaMemsetAsync(A, 0, sizeof(float) * r * k, st), "memset A"));
   QN_TRY(cuda_check(cudaMemsetAsync(B, 0, sizeof(float) * d * r, st), "memset B"));
@@ -729,35 +966,37 @@ qn_status loftq_init(const float *W, int64_t d, int64_t k, int32_t r, float alph
     *outp = std::sqrt(*outp);
     return QN_OK;
   };
-  auto orth = [&](float *Ym, int64_t rows) -> qn_status {
+  auto gram = [&](const float *Ym, int64_t rows) -> qn_status {  // G = Ym^T Ym (fp64)
+    const int nb = static_cast<int>(qn_ceil_div(rows, qn::kLqGramRows));
+    qn::lq_gram_part_kernel<P><<<nb, 256, 0, st>>>(Ym, rows, gpart);
+    QN_LAUNCH_CHECK("lq_gram_part_kernel");
+    qn::lq_gram_reduce_kernel<P><<<static_cast<unsigned>(qn_ceil_div(P * P, 256)), 256, 0, st>>>(gpart, nb, G);
+    QN_LAUNCH_CHECK("lq_gram_reduce_kernel");
+    return QN_OK;
+  };
+  auto orth = [&](float *Ym, int64_t rows) -> qn_status {  // CholeskyQR2
     for (int rep = 0; rep < 2; ++rep) {
-      QN_TRY(cuda_check(cudaMemsetAsync(G, 0, sizeof(double) * P * P, st), "memset G"));
-      const int64_t rpb = 256;
-      qn::gram_kernel<P><<<static_cast<unsigned>(qn_ceil_div(rows, rpb)), P * P, 0, st>>>(Ym, rows, rpb, G);
-      QN_LAUNCH_CHECK("gram_kernel");
-      qn::chol_inv_kernel<P><<<1, P, 0, st>>>(G, p, Linv);
-      QN_LAUNCH_CHECK("chol_inv_kernel");
-      qn::apply_linv_kernel<P><<<static_cast<unsigned>(qn_ceil_div(rows, 8)), 256, 0, st>>>(Ym, rows, Linv, p);
-      QN_LAUNCH_CHECK("apply_linv_kernel");
+      QN_TRY(gram(Ym, rows));
+      qn::lq_chol_inv_kernel<P><<<1, 256, 0, st>>>(G, p, Linv);
+      QN_LAUNCH_CHECK("lq_chol_inv_kernel");
+      qn::lq_apply_linv_kernel<P><<<static_cast<unsigned>(qn_ceil_div(rows, 16)), 256, 0, st>>>(Ym, rows, Linv);
+      QN_LAUNCH_CHECK("lq_apply_linv_kernel");
     }
     return QN_OK;
   };
   auto r_times = [&](const float *Z, float *Yo) -> qn_status {  // Yo = R Z   (d x P)
-    qn::rz_kernel<P><<<static_cast<unsigned>(qn_ceil_div(d, 8)), 256, 0, st>>>(Tbuf, d, k, Z, p, Yo);
-    QN_LAUNCH_CHECK("rz_kernel");
+    qn::lq_rz_kernel<P><<<static_cast<unsigned>(qn_ceil_div(d, 16)), 256, 0, st>>>(Tbuf, d, k, Z, Yo);
+    QN_LAUNCH_CHECK("lq_rz_kernel");
     return QN_OK;
   };
   auto rt_times = [&](const float *Ym, float *Zo) -> qn_status {  // Zo = R^T Y  (k x P)
-    QN_TRY(cuda_check(cudaMemsetAsync(Zo, 0, sizeof(float) * k * P, st), "memset Zt"));
-    const int64_t slices = 8;
-    dim3 grid(static_cast<unsigned>(qn_ceil_div(k, 128)), static_cast<unsigned>(slices));
-    qn::rty_kernel<P><<<grid, 128, 0, st>>>(Tbuf, d, k, Ym, qn_ceil_div(d, slices), Zo);
-    QN_LAUNCH_CHECK("rty_kernel");
+    qn::lq_rty_kernel<P><<<static_cast<unsigned>(qn_ceil_div(k, 32)), 256, 0, st>>>(Tbuf, d, k, Ym, Zo);
+    QN_LAUNCH_CHECK("lq_rty_kernel");
     return QN_OK;
   };
 
-  // t = 0: Q_0 = NF4(W), residual without adapter.
-  QN_TRY(launch_quantize(W, QN_F32, Q, bins, sem, st));
+  // t = 0: Q_0 = NF4(W) (or the caller's Q), residual without adapter.
+  if (requantise) QN_TRY(launch_quantize(W, QN_F32, Q, bins, sem, st));
   qn::residual_kernel<<<sms * 8, 256, 0, st>>>(qv, W, Tbuf, n);
   QN_LAUNCH_CHECK("residual_kernel");
   QN_TRY(residual_norm(0, &resid[0]));
@@ -783,16 +1022,111 @@ qn_status loftq_init(const float *W, int64_t d, int64_t k, int32_t r, float alph
       QN_TRY(orth(Y, d));
     }
     QN_TRY(rt_times(Y, Zt));  // Zt = R^T Y, i.e. (Y^T R)^T
-    QN_TRY(cuda_check(cudaMemsetAsync(G, 0, sizeof(double) * P * P, st), "memset G"));
-    qn::gram_kernel<P><<<static_cast<unsigned>(qn_ceil_div(k, 256)), P * P, 0, st>>>(Zt, k, 256, G);
-    QN_LAUNCH_CHECK("gram_kernel");
-    qn::jacobi_eig_kernel<P><<<1, P, 0, st>>>(G, p, lam, V);
-    QN_LAUNCH_CHECK("jacobi_eig_kernel");
-    qn::project_kernel<P><<<static_cast<unsigned>(qn_ceil_div(d, 256)), 256, 0, st>>>(Y, d, V, lam, r, s, 0, B, 0);
-    QN_LAUNCH_CHECK("project_kernel(B)");
-    qn::project_kernel<P><<<static_cast<unsigned>(qn_ceil_div(k, 256)), 256, 0, st>>>(Zt, k, V, lam, r, s, 1, A, 1);
-    QN_LAUNCH_CHECK("project_kernel(A)");
+    QN_TRY(gram(Zt, k));
+    qn::lq_jacobi_kernel<P><<<1, 256, qn::lq_jacobi_smem<P>(), st>>>(G, p, lam, V);
+    QN_LAUNCH_CHECK("lq_jacobi_kernel");
+    qn::lq_project_kernel<P><<<static_cast<unsigned>(qn_ceil_div(d, 256)), 256, 0, st>>>(Y, d, V, lam, r, s, 0, B, 0);
+    QN_LAUNCH_CHECK("lq_project_kernel(B)");
+    qn::lq_project_kernel<P><<<static_cast<unsigned>(qn_ceil_div(k, 256)), 256, 0, st>>>(Zt, k, V, lam, r, s, 1, A,
+                                                                                         1);
+    QN_LAUNCH_CHECK("lq_project_kernel(A)");
     QN_TRY(residual_norm(r, &resid[t]));
+  }
+  return QN_OK;
+}
+
+qn_status loftq_run(const float *W, int64_t d, int64_t k, int32_t r, float alpha, int32_t T, uint64_t seed,
+                    int32_t oversample, int32_t power_iters, const qn_nf4 *Q, float *A, float *B, double *resid,
+                    void *ws, size_t ws_bytes, void *stream, bool requantise) {
+  if (!W || !A || !B || !resid || !Q) return fail(QN_EINVAL, "NULL pointer");
+  QN_TRY(check_nf4(Q, true));
+  if (Q->d != d || Q->k != k) return fail(QN_ESHAPE, "Q shape %lldx%lld != W shape", (long long)Q->d, (long long)Q->k);
+  if (d % 64 || k % 64) return fail(QN_ESHAPE, "d and k must be multiples of 64");
+  const int p = r + oversample;
+  if (r < 1 || oversample < 0 || p > qn::kLqMaxP)
+    return fail(QN_ESHAPE, "need 1 <= r and r + oversample <= %d", qn::kLqMaxP);
+  if (p > d || p > k) return fail(QN_ESHAPE, "r + oversample exceeds a matrix dimension");
+  if (T < 0 || T > 64) return fail(QN_ESHAPE, "T must be in [0, 64]");
+  if (power_iters < 0 || power_iters > 32) return fail(QN_ESHAPE, "power_iters must be in [0, 32]");
+  if (!std::isfinite(alpha) || alpha == 0.f) return fail(QN_EINVAL, "alpha must be finite and non-zero");
+  if (!aligned(W, 16) || !aligned(A, 16) || !aligned(B, 16)) return fail(QN_EALIGN, "W/A/B not 16-byte aligned");
+  const size_t need = loftq_ws_bytes(d, k);
+  if (!ws) return fail(QN_EINVAL, "workspace NULL");
+  if (ws_bytes < need) return fail(QN_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, need);
+  if (!aligned(ws, 256)) return fail(QN_EALIGN, "workspace not 256-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p <= 32) return loftq_run_p<32>(W, d, k, r, alpha, T, seed, p, power_iters, Q, A, B, resid, ws, ws_bytes, st, requantise);
+  if (p <= 64) return loftq_run_p<64>(W, d, k, r, alpha, T, seed, p, power_iters, Q, A, B, resid, ws, ws_bytes, st, requantise);
+  return loftq_run_p<96>(W, d, k, r, alpha, T, seed, p, power_iters, Q, A, B, resid, ws, ws_bytes, st, requantise);
+}
+
+}  // namespace
+
+extern "C" {
+
+qn_status loftq_init(const float *W, int64_t d, int64_t k, int32_t r, float alpha, int32_t T, uint64_t seed,
+                     int32_t oversample, int32_t power_iters, const qn_nf4 *Q, float *A, float *B, double *resid,
+                     void *ws, size_t ws_bytes, void *stream) {
+  g_last_error.clear();
+  return loftq_run(W, d, k, r, alpha, T, seed, oversample, power_iters, Q, A, B, resid, ws, ws_bytes, stream, true);
+}
+
+qn_status loftq_replace_lora(const float *W, const qn_nf4 *Q, int32_t r, float alpha, uint64_t seed,
+                             int32_t oversample, int32_t power_iters, float *A, float *B, double *resid,
+                             void *ws, size_t ws_bytes, void *stream) {
+  g_last_error.clear();
+  if (!Q) return fail(QN_EINVAL, "Q is NULL");
+  return loftq_run(W, Q->d, Q->k, r, alpha, 1, seed, oversample, power_iters, Q, A, B, resid, ws, ws_bytes, stream,
+                   false);
+}
+
+qn_status nf4_merge_lora(const qn_nf4 *Q, const uint16_t *A, const uint16_t *B, int32_t r, float alpha, int32_t sign,
+                         const qn_nf4 *Qout, void *ws, size_t ws_bytes, void *stream) {
+  g_last_error.clear();
+  if (!tables_consistent()) return fail(QN_EUNSUPPORTED, "internal NF4 tables inconsistent");
+  QN_TRY(check_nf4(Q, true));
+  QN_TRY(check_nf4(Qout, true));
+  if (Qout->d != Q->d || Qout->k != Q->k) return fail(QN_ESHAPE, "Qout shape differs from Q");
+  if (Q->k % 64) return fail(QN_ESHAPE, "k must be a multiple of 64 (got %lld)", (long long)Q->k);
+  if (r < 1 || r > 256) return fail(QN_ESHAPE, "r must be in [1, 256] (got %d)", r);
+  if (sign != 1 && sign != -1) return fail(QN_EINVAL, "sign must be +1 (merge) or -1 (unmerge)");
+  if (!std::isfinite(alpha)) return fail(QN_EINVAL, "alpha must be finite");
+  if (!A || !B) return fail(QN_EINVAL, "NULL adapter pointer");
+  if (!aligned(A, 16) || !aligned(B, 16)) return fail(QN_EALIGN, "A/B not 16-byte aligned");
+  if (Qout->dq) {
+    if (!ws) return fail(QN_EINVAL, "workspace NULL");
+    if (ws_bytes < kQuantWs) return fail(QN_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, kQuantWs);
+    if (!aligned(ws, 16)) return fail(QN_EALIGN, "workspace not 16-byte aligned");
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t d = Q->d, k = Q->k, nblk = d * (k >> 6);
+  unsigned long long *bins = Qout->dq ? reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kSemBytes)
+                                      : nullptr;
+  unsigned int *ticket = static_cast<unsigned int *>(ws);
+  if (bins) QN_TRY(cuda_check(cudaMemsetAsync(bins, 0, qn::kNumBins * sizeof(unsigned long long), st), "memset bins"));
+  static int attr_set[64] = {0};
+  int dev = 0;
+  QN_TRY(cuda_check(cudaGetDevice(&dev), "cudaGetDevice"));
+  if (dev < 0 || dev >= 64) return fail(QN_EUNSUPPORTED, "device ordinal out of range");
+  if (!attr_set[dev]) {
+    QN_TRY(cuda_check(cudaFuncSetAttribute(qn::nf4_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(qn::kMgSmemBytes)),
+                      "cudaFuncSetAttribute(merge smem)"));
+    attr_set[dev] = 1;
+  }
+  const float s = alpha / static_cast<float>(r);
+  dim3 grid(static_cast<unsigned>(qn_ceil_div(k, qn::kMgCols)), static_cast<unsigned>(qn_ceil_div(d, qn::kMgRows)));
+  qn::nf4_merge_kernel<<<grid, qn::kMgThreads, qn::kMgSmemBytes, st>>>(
+      view_of(Q), A, B, r, s, sign, Qout->codes, Qout->absmax, bins, ticket, Qout->absmax_mean);
+  QN_LAUNCH_CHECK("nf4_merge_kernel");
+  if (Qout->dq) {
+    const int64_t ngrp = qn_ceil_div(nblk, 256);
+    int64_t g2 = qn_ceil_div(ngrp, qn::kDqWarps);
+    const int64_t cap = static_cast<int64_t>(sm_count()) * 4;
+    if (g2 > cap) g2 = cap;
+    qn::nf4_dq_kernel<<<static_cast<unsigned>(g2), qn::kDqWarps * 32, 0, st>>>(Qout->absmax, nblk, Qout->absmax_mean,
+                                                                              Qout->absmax_q, Qout->absmax_scale);
+    QN_LAUNCH_CHECK("nf4_dq_kernel");
   }
   return QN_OK;
 }

@@ -16,7 +16,7 @@
 
 namespace qn {
 
-constexpr int kLqMaxP = 32;  // r + oversample
+constexpr int kLqMaxP = 96;  // largest r + oversample (panels of 32, 64 or 96 columns)
 
 // ---------------------------------------------------------------- Philox4x32-10
 struct U4 { uint32_t x, y, z, w; };
@@ -109,268 +109,369 @@ residual_kernel(QnNF4View q, const float *__restrict__ W, float *__restrict__ R,
 }
 
 // ------------------------------------------------------------- skinny products
-// Y[i, c] = sum_j R[i, j] Z[j, c]   (R: n_rows x n_cols, Z: n_cols x p).
-// One warp per row; lanes stride the row; per-lane partial sums reduced by
-// shuffles.  Z rows are read through the read-only cache.
+// The rank-r step works on panels of P columns (P = 32, 64 or 96, the padded
+// r + oversample; columns past p are kept zero).
+
+// Y[i, c] = sum_j R[i, j] Z[j, c]   (R: n_rows x n_cols, Z: n_cols x P).
+// CTA: 16 rows of R; column chunks of 64 staged in shared memory with the
+// matching 64 x P block of Z; thread (row tid / 16, columns (tid % 16) P/16 ..)
+// keeps P/16 sums.  Every element of R is read once.
 template <int P>
 __global__ void __launch_bounds__(256)
-rz_kernel(const float *__restrict__ R, int64_t n_rows, int64_t n_cols,
-          const float *__restrict__ Z, int p, float *__restrict__ Y) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * 8 + warp; i < n_rows;
-       i += static_cast<int64_t>(gridDim.x) * 8) {
-    float acc[P];
+lq_rz_kernel(const float *__restrict__ R, int64_t n_rows, int64_t n_cols, const float *__restrict__ Z,
+             float *__restrict__ Y) {
+  constexpr int CW = P / 16;
+  __shared__ float sR[16][64 + 1];
+  __shared__ __align__(16) float sZ[64][P];
+  const int tid = threadIdx.x, tr = tid / 16, tc = tid % 16;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * 16;
+  float acc[CW];
 #pragma unroll
-    for (int c = 0; c < P; ++c) acc[c] = 0.f;
-    const float *row = R + i * n_cols;
-    for (int64_t j = lane; j < n_cols; j += 32) {
-      const float rv = __ldcs(row + j);
-      const float4 *zr = reinterpret_cast<const float4 *>(Z + j * P);
-#pragma unroll
-      for (int c4 = 0; c4 < P / 4; ++c4) {
-        const float4 z = __ldg(zr + c4);
-        acc[4 * c4] = fmaf(rv, z.x, acc[4 * c4]);
-        acc[4 * c4 + 1] = fmaf(rv, z.y, acc[4 * c4 + 1]);
-        acc[4 * c4 + 2] = fmaf(rv, z.z, acc[4 * c4 + 2]);
-        acc[4 * c4 + 3] = fmaf(rv, z.w, acc[4 * c4 + 3]);
-      }
+  for (int c = 0; c < CW; ++c) acc[c] = 0.f;
+  for (int64_t j0 = 0; j0 < n_cols; j0 += 64) {
+    for (int t = tid; t < 16 * 64; t += 256) {
+      const int rr = t / 64, cc = t % 64;
+      const int64_t i = i0 + rr, j = j0 + cc;
+      sR[rr][cc] = (i < n_rows && j < n_cols) ? __ldcs(R + i * n_cols + j) : 0.f;
     }
-#pragma unroll
-    for (int c = 0; c < P; ++c) {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], off);
+    for (int t = tid; t < 64 * P; t += 256) {
+      const int rr = t / P, cc = t % P;
+      const int64_t j = j0 + rr;
+      sZ[rr][cc] = (j < n_cols) ? Z[j * P + cc] : 0.f;
     }
-    {
-      float v = 0.f;
+    __syncthreads();
+#pragma unroll 8
+    for (int jj = 0; jj < 64; ++jj) {
+      const float rv = sR[tr][jj];
 #pragma unroll
-      for (int c = 0; c < P; ++c) if (c == lane) v = acc[c];
-      if (lane < P) Y[i * P + lane] = (lane < p) ? v : 0.f;
+      for (int c = 0; c < CW; ++c) acc[c] = fmaf(rv, sZ[jj][tc * CW + c], acc[c]);
     }
+    __syncthreads();
+  }
+  const int64_t i = i0 + tr;
+  if (i < n_rows) {
+#pragma unroll
+    for (int c = 0; c < CW; ++c) Y[i * P + tc * CW + c] = acc[c];
   }
 }
 
-// Zt[j, c] += sum_{i in slice} R[i, j] Y[i, c]  (Zt zeroed by the caller).
-// Threads own columns j; the row slice is split across blockIdx.y.
+// Zt[j, c] = sum_i R[i, j] Y[i, c]  (R: n_rows x n_cols, Y: n_rows x P).
+// CTA: 32 columns of R, all rows in chunks of 64 staged with the matching
+// 64 x P block of Y; thread (column tid / 8, panel columns (tid % 8) P/8 ..).
+// No atomics: every output has one writer and a fixed summation order.
 template <int P>
-__global__ void __launch_bounds__(128)
-rty_kernel(const float *__restrict__ R, int64_t n_rows, int64_t n_cols,
-           const float *__restrict__ Y, int64_t rows_per_slice, float *__restrict__ Zt) {
-  __shared__ float sY[64][P];
-  const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t i_begin = static_cast<int64_t>(blockIdx.y) * rows_per_slice;
-  const int64_t i_end = (i_begin + rows_per_slice < n_rows) ? i_begin + rows_per_slice : n_rows;
-  float acc[P];
+__global__ void __launch_bounds__(256)
+lq_rty_kernel(const float *__restrict__ R, int64_t n_rows, int64_t n_cols, const float *__restrict__ Y,
+              float *__restrict__ Zt) {
+  constexpr int CW = P / 8;
+  __shared__ float sR[64][32 + 1];
+  __shared__ __align__(16) float sY[64][P];
+  const int tid = threadIdx.x, tj = tid / 8, tc = tid % 8;
+  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * 32;
+  float acc[CW];
 #pragma unroll
-  for (int c = 0; c < P; ++c) acc[c] = 0.f;
-  for (int64_t i0 = i_begin; i0 < i_end; i0 += 64) {
-    __syncthreads();
-    for (int t = threadIdx.x; t < 64 * P; t += blockDim.x) {
-      const int64_t ii = i0 + t / P;
-      sY[t / P][t % P] = (ii < i_end) ? Y[ii * P + t % P] : 0.f;
+  for (int c = 0; c < CW; ++c) acc[c] = 0.f;
+  for (int64_t i0 = 0; i0 < n_rows; i0 += 64) {
+    for (int t = tid; t < 64 * 32; t += 256) {
+      const int rr = t / 32, cc = t % 32;
+      const int64_t i = i0 + rr, j = j0 + cc;
+      sR[rr][cc] = (i < n_rows && j < n_cols) ? __ldcs(R + i * n_cols + j) : 0.f;
+    }
+    for (int t = tid; t < 64 * P; t += 256) {
+      const int rr = t / P, cc = t % P;
+      const int64_t i = i0 + rr;
+      sY[rr][cc] = (i < n_rows) ? Y[i * P + cc] : 0.f;
     }
     __syncthreads();
-    const int lim = static_cast<int>((i_end - i0) < 64 ? (i_end - i0) : 64);
-    if (j < n_cols) {
-      for (int ii = 0; ii < lim; ++ii) {
-        const float rv = __ldcs(R + (i0 + ii) * n_cols + j);
+#pragma unroll 8
+    for (int ii = 0; ii < 64; ++ii) {
+      const float rv = sR[ii][tj];
 #pragma unroll
-        for (int c = 0; c < P; ++c) acc[c] = fmaf(rv, sY[ii][c], acc[c]);
-      }
+      for (int c = 0; c < CW; ++c) acc[c] = fmaf(rv, sY[ii][tc * CW + c], acc[c]);
     }
+    __syncthreads();
   }
+  const int64_t j = j0 + tj;
   if (j < n_cols) {
 #pragma unroll
-    for (int c = 0; c < P; ++c) atomicAdd(&Zt[j * P + c], acc[c]);
+    for (int c = 0; c < CW; ++c) Zt[j * P + tc * CW + c] = acc[c];
   }
 }
 
-// G[a, b] += sum_i Y[i, a] Y[i, b]   (fp64, G zeroed by the caller, p x p).
+// Gram matrix G = Y^T Y (P x P) of a panel Y (n x P): kLqGramRows rows per
+// CTA summed in fp32 into part[block][P][P], then lq_gram_reduce_kernel adds
+// the blocks in order in fp64.  Thread (a-tile, b-tile) holds an
+// (P/16) x (P/16) tile of the P x P result.
+constexpr int kLqGramRows = 256;
+
 template <int P>
-__global__ void __launch_bounds__(P * P)
-gram_kernel(const float *__restrict__ Y, int64_t n, int64_t rows_per_block, double *__restrict__ G) {
-  __shared__ float sY[32][P];
-  const int a = threadIdx.x / P, b = threadIdx.x % P;
-  const int64_t i_begin = static_cast<int64_t>(blockIdx.x) * rows_per_block;
-  const int64_t i_end = (i_begin + rows_per_block < n) ? i_begin + rows_per_block : n;
-  double acc = 0.0;
-  for (int64_t i0 = i_begin; i0 < i_end; i0 += 32) {
-    __syncthreads();
-    for (int t = threadIdx.x; t < 32 * P; t += blockDim.x) {
-      const int64_t ii = i0 + t / P;
-      sY[t / P][t % P] = (ii < i_end) ? Y[ii * P + t % P] : 0.f;
+__global__ void __launch_bounds__(256)
+lq_gram_part_kernel(const float *__restrict__ Y, int64_t n, float *__restrict__ part) {
+  constexpr int TW = P / 16;
+  __shared__ __align__(16) float sY[32][P];
+  const int tid = threadIdx.x, ta = tid / 16, tb = tid % 16;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kLqGramRows;
+  float acc[TW][TW];
+#pragma unroll
+  for (int a = 0; a < TW; ++a)
+#pragma unroll
+    for (int b = 0; b < TW; ++b) acc[a][b] = 0.f;
+  for (int64_t i0 = r0; i0 < r0 + kLqGramRows && i0 < n; i0 += 32) {
+    for (int t = tid; t < 32 * P; t += 256) {
+      const int rr = t / P, cc = t % P;
+      const int64_t i = i0 + rr;
+      sY[rr][cc] = (i < n && i < r0 + kLqGramRows) ? Y[i * P + cc] : 0.f;
     }
     __syncthreads();
 #pragma unroll 4
-    for (int ii = 0; ii < 32; ++ii) acc += static_cast<double>(sY[ii][a]) * static_cast<double>(sY[ii][b]);
+    for (int ii = 0; ii < 32; ++ii) {
+      float ya[TW], yb[TW];
+#pragma unroll
+      for (int a = 0; a < TW; ++a) ya[a] = sY[ii][ta * TW + a];
+#pragma unroll
+      for (int b = 0; b < TW; ++b) yb[b] = sY[ii][tb * TW + b];
+#pragma unroll
+      for (int a = 0; a < TW; ++a)
+#pragma unroll
+        for (int b = 0; b < TW; ++b) acc[a][b] = fmaf(ya[a], yb[b], acc[a][b]);
+    }
+    __syncthreads();
   }
-  atomicAdd(&G[a * P + b], acc);
+  float *pp = part + static_cast<int64_t>(blockIdx.x) * P * P;
+#pragma unroll
+  for (int a = 0; a < TW; ++a)
+#pragma unroll
+    for (int b = 0; b < TW; ++b) pp[(ta * TW + a) * P + tb * TW + b] = acc[a][b];
 }
 
-// One CTA of P threads: Cholesky G = L L^T of the leading p x p block of the
-// Gram matrix (accumulated in fp64, factored in fp32) and Linv = L^{-1}
-// (lower triangular, fp32 [P x P], zero outside the p x p block).  A pivot
+template <int P>
+__global__ void lq_gram_reduce_kernel(const float *__restrict__ part, int nblocks, double *__restrict__ G) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= P * P) return;
+  double s = 0.0;
+  for (int b = 0; b < nblocks; ++b) s += static_cast<double>(part[static_cast<int64_t>(b) * P * P + e]);
+  G[e] = s;
+}
+
+// One CTA of 256 threads: Cholesky G = L L^T of the leading p x p block (G
+// accumulated in fp64, factored in fp32) and Linv = L^{-1} (lower
+// triangular, fp32 [P x P], zero outside the p x p block).  One P x P array
+// holds both: L's strict lower triangle in place, its diagonal in dL, and
+// Linv^T in the upper triangle (Linv[i][t] at M[t][i], i >= t).  A pivot
 // that is not positive (rank deficiency) is clamped to a tiny positive value.
 template <int P>
-__global__ void __launch_bounds__(P)
-chol_inv_kernel(const double *__restrict__ G, int p, float *__restrict__ Linv) {
-  __shared__ float L[P][P + 1];
-  __shared__ float Li[P][P + 1];
-  __shared__ float s_diag_floor;
-  const int t = threadIdx.x;
-  for (int j = 0; j < P; ++j) {
-    L[t][j] = (t < p && j < p) ? static_cast<float>(G[t * P + j]) : 0.f;
-    Li[t][j] = 0.f;
+__global__ void __launch_bounds__(256)
+lq_chol_inv_kernel(const double *__restrict__ G, int p, float *__restrict__ Linv) {
+  __shared__ float Mx[P][P + 1];
+  __shared__ float dL[P];
+  __shared__ float s_floor;
+  const int tid = threadIdx.x;
+  for (int t = tid; t < P * P; t += 256) {
+    const int i = t / P, j = t % P;
+    Mx[i][j] = (i < p && j < p) ? static_cast<float>(G[i * P + j]) : 0.f;
   }
   __syncthreads();
-  if (t == 0) {
+  if (tid < 32) {
     float mx = 0.f;
-    for (int i = 0; i < p; ++i) mx = fmaxf(mx, L[i][i]);
-    s_diag_floor = fmaxf(mx, 1e-30f) * 1e-12f;
+    for (int i = tid; i < p; i += 32) mx = fmaxf(mx, Mx[i][i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (tid == 0) s_floor = fmaxf(mx, 1e-30f) * 1e-12f;
   }
   __syncthreads();
-  // Right-looking Cholesky on the lower triangle held in L.
   for (int j = 0; j < p; ++j) {
-    if (t == 0) L[j][j] = sqrtf(fmaxf(L[j][j], s_diag_floor));
+    if (tid == 0) Mx[j][j] = sqrtf(fmaxf(Mx[j][j], s_floor));
     __syncthreads();
-    const float inv = 1.0f / L[j][j];
-    if (t > j && t < p) L[t][j] *= inv;
+    const float inv = 1.0f / Mx[j][j];
+    for (int i = j + 1 + tid; i < p; i += 256) Mx[i][j] *= inv;
     __syncthreads();
-    if (t > j && t < p) {
-      const float ltj = L[t][j];
-      for (int c = j + 1; c <= t; ++c) L[t][c] -= ltj * L[c][j];
+    // trailing update of the lower triangle: M[i][c] -= L[i][j] L[c][j], j < c <= i < p
+    const int m = p - j - 1;
+    for (int t = tid; t < m * m; t += 256) {
+      const int i = j + 1 + t / m, c = j + 1 + t % m;
+      if (c <= i) Mx[i][c] -= Mx[i][j] * Mx[c][j];
     }
     __syncthreads();
   }
-  // Column t of L^{-1} by forward substitution.
-  if (t < p) {
+  for (int i = tid; i < P; i += 256) dL[i] = (i < p) ? Mx[i][i] : 1.f;
+  __syncthreads();
+  // column t of L^{-1} by forward substitution (one thread per column), stored transposed above the diagonal
+  for (int t = tid; t < p; t += 256) {
     for (int i = t; i < p; ++i) {
       float acc = (i == t) ? 1.f : 0.f;
-      for (int q = t; q < i; ++q) acc -= L[i][q] * Li[q][t];
-      Li[i][t] = acc / L[i][i];
+      for (int q = t; q < i; ++q) acc -= Mx[i][q] * Mx[t][q];   // L[i][q] * Linv[q][t]
+      Mx[t][i] = acc / dL[i];                                     // Linv[i][t]
     }
   }
   __syncthreads();
-  for (int j = 0; j < P; ++j) Linv[t * P + j] = Li[t][j];
+  for (int e = tid; e < P * P; e += 256) {
+    const int i = e / P, t = e % P;  // Linv[i][t]
+    Linv[e] = (i < p && t <= i) ? Mx[t][i] : 0.f;
+  }
 }
 
-// Y[i, :] <- Y[i, :] Linv^T   (in place).  One warp per row: lane c holds
-// Y[i, c] and computes sum_b Y[i, b] Linv[c, b] with the row broadcast by
-// shuffles (P == 32).
+// Y[i, :] <- Y[i, :] Linv^T in place: 16 rows per CTA; thread (row tid / 16,
+// columns (tid % 16) P/16 ..).
 template <int P>
 __global__ void __launch_bounds__(256)
-apply_linv_kernel(float *__restrict__ Y, int64_t n, const float *__restrict__ Linv, int p) {
-  static_assert(P == 32, "one lane per column");
+lq_apply_linv_kernel(float *__restrict__ Y, int64_t n, const float *__restrict__ Linv) {
+  constexpr int CW = P / 16;
   __shared__ float sL[P][P + 1];
-  for (int t = threadIdx.x; t < P * P; t += blockDim.x) sL[t / P][t % P] = Linv[t];
+  __shared__ float sY[16][P + 1];
+  const int tid = threadIdx.x, tr = tid / 16, tc = tid % 16;
+  for (int t = tid; t < P * P; t += 256) sL[t / P][t % P] = Linv[t];
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * 16;
+  for (int t = tid; t < 16 * P; t += 256) {
+    const int64_t i = i0 + t / P;
+    sY[t / P][t % P] = (i < n) ? Y[i * P + t % P] : 0.f;
+  }
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * 8 + warp; i < n; i += static_cast<int64_t>(gridDim.x) * 8) {
-    const float y = Y[i * P + lane];
-    float acc = 0.f;
+  float acc[CW];
 #pragma unroll
-    for (int b = 0; b < P; ++b) acc = fmaf(__shfl_sync(0xffffffffu, y, b), sL[lane][b], acc);
-    Y[i * P + lane] = (lane < p) ? acc : 0.f;
+  for (int c = 0; c < CW; ++c) acc[c] = 0.f;
+  for (int b = 0; b < P; ++b) {
+    const float y = sY[tr][b];
+#pragma unroll
+    for (int c = 0; c < CW; ++c) acc[c] = fmaf(y, sL[tc * CW + c][b], acc[c]);
+  }
+  const int64_t i = i0 + tr;
+  if (i < n) {
+#pragma unroll
+    for (int c = 0; c < CW; ++c) Y[i * P + tc * CW + c] = acc[c];
   }
 }
 
-// One CTA of P threads: cyclic Jacobi eigen-decomposition (fp32) of the
-// symmetric leading p x p block of G (accumulated in fp64).  Outputs the
-// eigenvalues sorted descending (lam[P], zero past p) and the matching
+// One CTA of 256 threads: parallel cyclic Jacobi eigen-decomposition (fp32)
+// of the symmetric leading p x p block of G (accumulated in fp64), with the
+// round-robin pair ordering, so that n / 2 disjoint rotations run at once
+// (n = p rounded up to even; a padding row and column stay zero).  Outputs
+// the eigenvalues sorted descending (lam[P], zero past p) and the matching
 // eigenvectors as the columns of V (fp32 [P x P], V[row * P + col]).
 template <int P>
-__global__ void __launch_bounds__(P)
-jacobi_eig_kernel(const double *__restrict__ G, int p, float *__restrict__ lam, float *__restrict__ V) {
-  __shared__ float A[P][P + 1];
-  __shared__ float E[P][P + 1];
-  __shared__ float s_c, s_s;
-  __shared__ int s_done;
-  const int t = threadIdx.x;
-  for (int j = 0; j < P; ++j) {
-    A[t][j] = (t < p && j < p) ? static_cast<float>(G[t * P + j]) : 0.f;
-    E[t][j] = (t == j) ? 1.f : 0.f;
+constexpr size_t lq_jacobi_smem() { return 2 * static_cast<size_t>(P) * (P + 1) * sizeof(float); }
+
+template <int P>
+__global__ void __launch_bounds__(256)
+lq_jacobi_kernel(const double *__restrict__ G, int p, float *__restrict__ lam, float *__restrict__ V) {
+  extern __shared__ float lq_jac_smem[];  // A then E, P x (P + 1) each
+  float (*A)[P + 1] = reinterpret_cast<float (*)[P + 1]>(lq_jac_smem);
+  float (*E)[P + 1] = reinterpret_cast<float (*)[P + 1]>(lq_jac_smem + P * (P + 1));
+  __shared__ float cs[P / 2][2];
+  __shared__ int pos[P];
+  __shared__ int pr[P / 2][2];
+  __shared__ float s_off, s_dg;
+  __shared__ int order[P];
+  const int tid = threadIdx.x;
+  const int n = p + (p & 1);
+  const int np = n / 2;
+  for (int t = tid; t < P * P; t += 256) {
+    const int i = t / P, j = t % P;
+    A[i][j] = (i < p && j < p) ? static_cast<float>(G[i * P + j]) : 0.f;
+    E[i][j] = (i == j) ? 1.f : 0.f;
   }
+  for (int t = tid; t < P; t += 256) pos[t] = t;
   __syncthreads();
-  for (int sweep = 0; sweep < 20; ++sweep) {
-    if (t == 0) {
+  for (int sweep = 0; sweep < 30; ++sweep) {
+    if (tid < 32) {  // convergence: off-diagonal mass against the diagonal
       float off = 0.f, dg = 0.f;
-      for (int i = 0; i < p; ++i) {
-        dg += A[i][i] * A[i][i];
-        for (int j = 0; j < p; ++j) if (i != j) off += A[i][j] * A[i][j];
+      for (int t = tid; t < n * n; t += 32) {
+        const int i = t / n, j = t % n;
+        const float v = A[i][j] * A[i][j];
+        if (i == j) dg += v; else off += v;
       }
-      s_done = (off <= 1e-13f * dg) ? 1 : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        off += __shfl_xor_sync(0xffffffffu, off, o);
+        dg += __shfl_xor_sync(0xffffffffu, dg, o);
+      }
+      if (tid == 0) { s_off = off; s_dg = dg; }
     }
     __syncthreads();
-    if (s_done) break;
-    for (int i = 0; i < p - 1; ++i) {
-      for (int j = i + 1; j < p; ++j) {
-        if (t == 0) {
-          const float aij = A[i][j];
-          float c = 1.f, sn = 0.f;
-          if (fabsf(aij) > 1e-30f * (fabsf(A[i][i]) + fabsf(A[j][j]))) {
-            const float theta = (A[j][j] - A[i][i]) / (2.f * aij);
-            const float tt = copysignf(1.f, theta) / (fabsf(theta) + sqrtf(theta * theta + 1.f));
-            c = 1.f / sqrtf(tt * tt + 1.f);
-            sn = tt * c;
-          }
-          s_c = c;
-          s_s = sn;
+    if (s_off <= 1e-13f * s_dg) break;
+    for (int step = 0; step < n - 1; ++step) {
+      // pairs of this step and their rotations
+      for (int k = tid; k < np; k += 256) {
+        int a = pos[k], b = pos[n - 1 - k];
+        if (a > b) { const int tmp = a; a = b; b = tmp; }
+        pr[k][0] = a;
+        pr[k][1] = b;
+        const float aij = A[a][b];
+        float c = 1.f, sn = 0.f;
+        if (fabsf(aij) > 1e-30f * (fabsf(A[a][a]) + fabsf(A[b][b]))) {
+          const float theta = (A[b][b] - A[a][a]) / (2.f * aij);
+          const float tt = copysignf(1.f, theta) / (fabsf(theta) + sqrtf(theta * theta + 1.f));
+          c = 1.f / sqrtf(tt * tt + 1.f);
+          sn = tt * c;
         }
-        __syncthreads();
-        const float c = s_c, sn = s_s;
-        if (sn != 0.f) {
-          // A <- J^T A J and E <- E J for the rotation in the (i, j) plane.
-          const float ati = A[t][i], atj = A[t][j];
-          __syncthreads();
-          A[t][i] = c * ati - sn * atj;
-          A[t][j] = sn * ati + c * atj;
-          __syncthreads();
-          const float ait = A[i][t], ajt = A[j][t];
-          __syncthreads();
-          A[i][t] = c * ait - sn * ajt;
-          A[j][t] = sn * ait + c * ajt;
-          const float eti = E[t][i], etj = E[t][j];
-          E[t][i] = c * eti - sn * etj;
-          E[t][j] = sn * eti + c * etj;
-        }
-        __syncthreads();
+        cs[k][0] = c;
+        cs[k][1] = sn;
       }
+      __syncthreads();
+      // rows: A <- J^T A
+      for (int t = tid; t < np * n; t += 256) {
+        const int k = t / n, col = t % n;
+        const int a = pr[k][0], b = pr[k][1];
+        const float c = cs[k][0], sn = cs[k][1];
+        const float ra = A[a][col], rb = A[b][col];
+        A[a][col] = c * ra - sn * rb;
+        A[b][col] = sn * ra + c * rb;
+      }
+      __syncthreads();
+      // columns: A <- A J and E <- E J
+      for (int t = tid; t < np * n; t += 256) {
+        const int k = t / n, row = t % n;
+        const int a = pr[k][0], b = pr[k][1];
+        const float c = cs[k][0], sn = cs[k][1];
+        const float ca = A[row][a], cb = A[row][b];
+        A[row][a] = c * ca - sn * cb;
+        A[row][b] = sn * ca + c * cb;
+        const float ea = E[row][a], eb = E[row][b];
+        E[row][a] = c * ea - sn * eb;
+        E[row][b] = sn * ea + c * eb;
+      }
+      __syncthreads();
+      // round-robin: position 0 fixed, the others rotate by one
+      if (tid == 0) {
+        const int last = pos[n - 1];
+        for (int q = n - 1; q > 1; --q) pos[q] = pos[q - 1];
+        pos[1] = last;
+      }
+      __syncthreads();
     }
   }
-  __syncthreads();
-  if (t == 0) {
-    int order[P];
+  if (tid == 0) {
     for (int i = 0; i < P; ++i) order[i] = i;
     for (int i = 0; i < p; ++i) {
       int best = i;
       for (int j = i + 1; j < p; ++j) if (A[order[j]][order[j]] > A[order[best]][order[best]]) best = j;
       const int tmp = order[i]; order[i] = order[best]; order[best] = tmp;
     }
-    for (int i = 0; i < P; ++i) lam[i] = (i < p) ? A[order[i]][order[i]] : 0.f;
-    for (int row = 0; row < P; ++row)
-      for (int col = 0; col < P; ++col) V[row * P + col] = (col < p) ? E[row][order[col]] : 0.f;
+  }
+  __syncthreads();
+  for (int i = tid; i < P; i += 256) lam[i] = (i < p) ? A[order[i]][order[i]] : 0.f;
+  for (int t = tid; t < P * P; t += 256) {
+    const int row = t / P, col = t % P;
+    V[t] = (col < p) ? E[row][order[col]] : 0.f;
   }
 }
 
 // out[i, q] = sum_b in[i, b] * V[b, q] * scale[q]  for q < r;  in: n x P fp32.
-// transpose_out: write out[q * n + i] (r x n) instead of out[i * r + q].
+// for_A == 0 (B): coefficient V[b, q] sqrt(sigma_q) / sqrt(s); for_A == 1 (A):
+// V[b, q] / (sqrt(sigma_q) sqrt(s)), sigma_q = sqrt(lam_q) (lam: eigenvalues of
+// the Gram matrix).  transpose_out: out[q * n + i] (r x n) instead of out[i * r + q].
 template <int P>
 __global__ void __launch_bounds__(256)
-project_kernel(const float *__restrict__ in, int64_t n, const float *__restrict__ V,
-               const float *__restrict__ lam, int r, float s, int for_A,
-               float *__restrict__ out, int transpose_out) {
-  __shared__ float sC[P][P];
-  // for_A == 0 (B):  coefficient V[b, q] * sqrt(sigma_q) / sqrt(s)
-  // for_A == 1 (A):  coefficient V[b, q] / (sqrt(sigma_q) * sqrt(s)),
-  // sigma_q = sqrt(lam_q) (lam are eigenvalues of the Gram matrix).
+lq_project_kernel(const float *__restrict__ in, int64_t n, const float *__restrict__ V,
+                  const float *__restrict__ lam, int r, float s, int for_A,
+                  float *__restrict__ out, int transpose_out) {
+  __shared__ float sC[P][P + 1];
   for (int t = threadIdx.x; t < P * P; t += blockDim.x) {
     const int b = t / P, q = t % P;
     float cval = 0.f;
     if (q < r) {
       const float sigma = sqrtf(fmaxf(lam[q], 0.f));
       const float rs = sqrtf(sigma);
-      float sc;
-      if (for_A) sc = (rs > 0.f) ? 1.f / (rs * sqrtf(s)) : 0.f;
-      else sc = rs / sqrtf(s);
+      const float sc = for_A ? ((rs > 0.f) ? 1.f / (rs * sqrtf(s)) : 0.f) : rs / sqrtf(s);
       cval = V[b * P + q] * sc;
     }
     sC[b][q] = cval;
@@ -378,15 +479,21 @@ project_kernel(const float *__restrict__ in, int64_t n, const float *__restrict_
   __syncthreads();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    float x[P];
+    for (int q0 = 0; q0 < r; q0 += 16) {
+      float acc[16];
 #pragma unroll
-    for (int b = 0; b < P; ++b) x[b] = in[i * P + b];
-    for (int q = 0; q < r; ++q) {
-      float acc = 0.f;
+      for (int q = 0; q < 16; ++q) acc[q] = 0.f;
+      for (int b = 0; b < P; ++b) {
+        const float x = in[i * P + b];
 #pragma unroll
-      for (int b = 0; b < P; ++b) acc = fmaf(x[b], sC[b][q], acc);
-      if (transpose_out) out[static_cast<int64_t>(q) * n + i] = acc;
-      else out[i * r + q] = acc;
+        for (int q = 0; q < 16; ++q) acc[q] = fmaf(x, sC[b][(q0 + q) < P ? q0 + q : P - 1], acc[q]);
+      }
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        if (q0 + q >= r) break;
+        if (transpose_out) out[static_cast<int64_t>(q0 + q) * n + i] = acc[q];
+        else out[i * r + q0 + q] = acc[q];
+      }
     }
   }
 }

@@ -234,6 +234,68 @@ __device__ __forceinline__ void div_pair_by_scale(float &x0, float &x1, unsigned
   (void)m2;
 }
 
+// Quantises the 8 elements a lane holds of a 64-block that 8 consecutive
+// lanes own together (every lane of the warp must call it): m = the block
+// absmax (max |x| over the 64 elements, same on the 8 lanes), and the 8
+// nearest-level codes of fp32(x / m), packed element 0 in the low nibble.
+__device__ __forceinline__ uint32_t nf4_quant_lane8(float (&v)[8], const BucketEntry *tab, float &m_out) {
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+#pragma unroll
+  for (int off = 4; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if (m >= 0x1.0p-125f && m <= 0x1.0p+125f) {
+    const float rcp = __frcp_rn(m);
+    unsigned long long rcp2, nm2;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(rcp2) : "f"(rcp));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(nm2) : "f"(-m));
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) div_pair_by_scale(v[i], v[i + 1], 0ull, rcp2, nm2);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = (m > 0.f) ? __fdiv_rn(v[i], m) : 0.f;
+  }
+  uint32_t packed = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) packed = put_nibble(packed, bucket_code(v[i], tab), i);
+  m_out = m;
+  return packed;
+}
+
+// The bucket table, per-lane replicated in shared memory (s_one: kBuckets
+// entries of scratch, s_tab: kBuckets * 32); every thread of the CTA calls it.
+__device__ __forceinline__ void build_bucket_tables(BucketEntry *s_one, BucketEntry *s_tab) {
+  if (threadIdx.x < kBuckets) build_bucket_entry(threadIdx.x, s_one);
+  __syncthreads();
+  for (int i = threadIdx.x; i < kBuckets * 32; i += blockDim.x) s_tab[i] = s_one[i >> 5];
+  __syncthreads();
+}
+
+// End of a quantising kernel with double quantisation (every thread of the
+// CTA calls it): the CTA's exponent bins go to the global bins; the last CTA
+// to finish forms the exact mean of all nblk block constants, stores it and
+// returns the ticket to zero.
+__device__ __forceinline__ void quant_mean_epilogue(unsigned long long *s_bins, unsigned long long *bins,
+                                                    unsigned int *ticket, int64_t nblk, float *absmax_mean) {
+  __shared__ bool s_last;
+  __syncthreads();
+  for (int i = threadIdx.x; i < kNumBins; i += blockDim.x)
+    if (s_bins[i]) atomicAdd(&bins[i], s_bins[i]);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(ticket, 1u) == gridDim.x - 1u);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (threadIdx.x < 32) {
+    const float mu = exact_mean_from_bins(bins, static_cast<uint64_t>(nblk));
+    if (threadIdx.x == 0) {
+      *absmax_mean = mu;
+      *ticket = 0u;
+    }
+  }
+}
+
 // Lanes in groups of G = 64 / kVec own one 64-element block each per
 // iteration; the last CTA to finish derives the double-quantisation mean
 // from the exact exponent-binned sum and resets the ticket counter.
@@ -245,15 +307,12 @@ nf4_quant_kernel(const T *__restrict__ x, int64_t nfull, int64_t nblk, uint8_t *
   constexpr int V = QuantVec<T>::kVec;
   constexpr int G = 64 / V;        // lanes per block
   constexpr int BPW = 32 / G;      // blocks per warp-iteration
+  static_assert(V == 8 && G == 8, "eight lanes of eight elements per block");
   __shared__ unsigned long long s_bins[kNumBins];
   __shared__ BucketEntry s_one[kBuckets];
   __shared__ BucketEntry s_tab[kBuckets * 32];
-  __shared__ bool s_last;
   for (int i = threadIdx.x; i < kNumBins; i += blockDim.x) s_bins[i] = 0ull;
-  if (threadIdx.x < kBuckets) build_bucket_entry(threadIdx.x, s_one);
-  __syncthreads();
-  for (int i = threadIdx.x; i < kBuckets * 32; i += blockDim.x) s_tab[i] = s_one[i >> 5];
-  __syncthreads();
+  build_bucket_tables(s_one, s_tab);
   const int lane = threadIdx.x & 31;
   const BucketEntry *my_tab = s_tab + lane;
   const int sub = lane / G;
@@ -298,27 +357,9 @@ nf4_quant_kernel(const T *__restrict__ x, int64_t nfull, int64_t nblk, uint8_t *
         nb = na;
       }
     }
-    float m = 0.f;
-#pragma unroll
-    for (int i = 0; i < V; ++i) m = fmaxf(m, fabsf(v[i]));
-#pragma unroll
-    for (int off = G / 2; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-
-    if (m >= 0x1.0p-125f && m <= 0x1.0p+125f) {
-      const float rcp = __frcp_rn(m);
-      unsigned long long rcp2, nm2;
-      asm("mov.b64 %0, {%1, %1};" : "=l"(rcp2) : "f"(rcp));
-      asm("mov.b64 %0, {%1, %1};" : "=l"(nm2) : "f"(-m));
-#pragma unroll
-      for (int i = 0; i < V; i += 2) div_pair_by_scale(v[i], v[i + 1], 0ull, rcp2, nm2);
-    } else {
-#pragma unroll
-      for (int i = 0; i < V; ++i) v[i] = (m > 0.f) ? __fdiv_rn(v[i], m) : 0.f;
-    }
+    float m;
+    const uint32_t packed = nf4_quant_lane8(v, my_tab, m);
     if (valid) {
-      uint32_t packed = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) packed = put_nibble(packed, bucket_code(v[i], my_tab), i);
       reinterpret_cast<uint32_t *>(codes + blk * 32)[li] = packed;
       if (li == 0) {
         absmax[blk] = m;
@@ -327,22 +368,7 @@ nf4_quant_kernel(const T *__restrict__ x, int64_t nfull, int64_t nblk, uint8_t *
     }
   }
   if (!bins) return;
-  __syncthreads();
-  for (int i = threadIdx.x; i < kNumBins; i += blockDim.x)
-    if (s_bins[i]) atomicAdd(&bins[i], s_bins[i]);
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(ticket, 1u) == gridDim.x - 1u);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (threadIdx.x < 32) {
-    const float mu = exact_mean_from_bins(bins, static_cast<uint64_t>(nblk));
-    if (threadIdx.x == 0) {
-      *absmax_mean = mu;
-      *ticket = 0u;
-    }
-  }
+  quant_mean_epilogue(s_bins, bins, ticket, nblk, absmax_mean);
 }
 
 // The final partial block: one warp, scalar loads.
@@ -462,6 +488,54 @@ nf4_dequant_kernel(QnNF4View q, int64_t n, void *__restrict__ out) {
       const float wv = __fmul_rn(s_lut[code], block_scale(q, e >> 6));
       if constexpr (kBf16Out) static_cast<uint16_t *>(out)[e] = f32_to_bf16_bits(wv);
       else static_cast<float *>(out)[e] = wv;
+    }
+  }
+}
+
+// bf16 output with the register decoder: each lane decodes 32 elements (one
+// 16-byte code load) at a time, two chunks per iteration with both loads in
+// flight; the 16 levels scaled by the block constant are built in registers
+// as exactly bf16(fp32(c * m)) (scaled_levels) and selected with byte
+// permutes (decode_word), so no shared memory is touched.
+__global__ void __launch_bounds__(256)
+nf4_dequant_bf16_kernel(QnNF4View q, int64_t n, uint16_t *__restrict__ out) {
+  const int64_t nchunk = n / 32;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t c0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c0 < nchunk; c0 += 2 * stride) {
+    const int64_t c1 = c0 + stride;
+    const uint4 w0 = __ldcs(reinterpret_cast<const uint4 *>(q.codes) + c0);
+    const uint4 w1 = (c1 < nchunk) ? __ldcs(reinterpret_cast<const uint4 *>(q.codes) + c1) : make_uint4(0u, 0u, 0u, 0u);
+    const float m0 = block_scale(q, c0 >> 1);
+    const float m1 = (c1 < nchunk) ? block_scale(q, c1 >> 1) : 0.f;
+    {
+      const ScaledLevels t = scaled_levels(m0);
+      uint32_t o[16];
+      decode_word(w0.x, t, o);
+      decode_word(w0.y, t, o + 4);
+      decode_word(w0.z, t, o + 8);
+      decode_word(w0.w, t, o + 12);
+      uint4 *dst = reinterpret_cast<uint4 *>(out + c0 * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) __stcs(dst + i, make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]));
+    }
+    if (c1 < nchunk) {
+      const ScaledLevels t = scaled_levels(m1);
+      uint32_t o[16];
+      decode_word(w1.x, t, o);
+      decode_word(w1.y, t, o + 4);
+      decode_word(w1.z, t, o + 8);
+      decode_word(w1.w, t, o + 12);
+      uint4 *dst = reinterpret_cast<uint4 *>(out + c1 * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) __stcs(dst + i, make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]));
+    }
+  }
+  // Tail: elements [nchunk*32, n), one thread each.
+  if (blockIdx.x == 0) {
+    for (int64_t e = nchunk * 32 + threadIdx.x; e < n; e += blockDim.x) {
+      const uint32_t byte = q.codes[e >> 1];
+      const uint32_t code = (e & 1) ? (byte >> 4) : (byte & 15u);
+      out[e] = f32_to_bf16_bits(__fmul_rn(c_nf4_levels[code], block_scale(q, e >> 6)));
     }
   }
 }

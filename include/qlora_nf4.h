@@ -22,9 +22,27 @@
  *       dX = dY deq(Q) + (alpha/r) (dY B) A: the gradient flowing through the
  *       frozen 4-bit weight into the inputs ("QLoRA paper summary", abstract).
  *
+ *   qlora_linear_bwd_lora
+ *       dA = (alpha/r) (dY B)^T X and dB = (alpha/r) dY^T (X A^T): the
+ *       gradients that reach the trainable adapter ("QLoRA paper summary",
+ *       abstract: back-propagation through the frozen 4-bit weight into LoRA).
+ *
+ *   qlora_linear_fwd_f32 / qlora_linear_bwd_dx_f32
+ *       the layer with fp32 compute dtype (bnb_4bit_compute_dtype = float32:
+ *       "LoftQ explainer" §3.2 and its troubleshooting table).
+ *
  *   loftq_init
  *       T alternations of Q_t = NF4(W - s B A) and a rank-r approximation of
  *       W - deq(Q_t) ("LoftQ explainer" (mhpn.cn) §2.2 objective, §2.3 algorithm).
+ *
+ *   loftq_replace_lora
+ *       one LoftQ step that keeps the caller's quantised weight and only
+ *       replaces the adapter ("PEFT quantization guide", replace_lora_weights_loftq).
+ *
+ *   nf4_merge_lora
+ *       merge (or unmerge) an adapter into the quantised weight: dequantise,
+ *       add (subtract) s B A, quantise again ("PEFT quantization guide",
+ *       merging adapters into quantised weights).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -59,7 +77,7 @@
 extern "C" {
 #endif
 
-#define QN_ABI_VERSION 1
+#define QN_ABI_VERSION 2
 
 typedef enum {
   QN_OK = 0,
@@ -79,7 +97,10 @@ typedef enum {
   QN_OP_DEQUANTIZE = 1,
   QN_OP_LINEAR_FWD = 2,
   QN_OP_LINEAR_BWD_DX = 3,
-  QN_OP_LOFTQ = 4
+  QN_OP_LOFTQ = 4,            /* loftq_init and loftq_replace_lora */
+  QN_OP_LINEAR_BWD_LORA = 5,
+  QN_OP_LINEAR_F32 = 6,       /* qlora_linear_fwd_f32 and qlora_linear_bwd_dx_f32 */
+  QN_OP_MERGE = 7
 } qn_op;
 
 /*
@@ -127,8 +148,8 @@ void qn_nf4_tables(float codebook[16], float thresholds[15]);
 
 /*
  * Workspace bytes the call `op` needs for the given sizes (0 if none).
- * M: rows of X / dY; d, k: W is d x k; r: LoRA rank (LoftQ: rank r and
- * oversampling are taken at their maximum supported value, 256 + 32).
+ * M: rows of X / dY; d, k: W is d x k; r: LoRA rank (LoftQ: sized for the
+ * largest r + oversample it accepts).
  */
 size_t qn_workspace_bytes(qn_op op, int64_t M, int64_t d, int64_t k, int32_t r);
 
@@ -161,14 +182,23 @@ qn_status nf4_dequantize(const qn_nf4 *Q, void *Wout, qn_dtype odt, void *stream
  *   Q     quantised weight, d x k with k % 64 == 0.
  *   X     device bf16 [M x k];  A device bf16 [r x k];  B device bf16 [d x r].
  *   Y     device bf16 [M x d] (written).
- *   1 <= M, 1 <= r <= 256.  Accumulation is fp32.  M == 1 multiplies the fp32
- *   levels by x; for M >= 2 the weight enters the tensor cores as
- *   bf16(deq(Q)) and the adapter term uses u split into bf16 hi + lo.  The
- *   few-token path (2 <= M <= 16) streams the int8 block constants with bulk
- *   copies when Q->absmax_q is 16-byte aligned (else it reads them through
- *   L1).  For M > 16 and r <= 64 the workspace also holds the bf16 hi/lo
- *   split of u (M x 128) and the fp32 block constants of W (d x 2*ceil(k/128))
- *   for the tensor-core kernel.  ws: qn_workspace_bytes(QN_OP_LINEAR_FWD).
+ *   1 <= M, 1 <= r <= 256.  Accumulation is fp32.  The tensor-core paths
+ *   multiply the NF4 levels (or bf16(deq(Q)) for M > 16) by bf16 X; the
+ *   adapter term keeps about 16 significant bits of u = s X A^T.
+ *   Paths: M <= 8 with M * k <= 16384 (and the per-CTA limits of that
+ *   kernel) -- one persistent kernel; other M <= 16 -- the few-token
+ *   kernels; M > 16 and r <= 64 -- the tcgen05 GEMM, whose workspace also
+ *   holds the bf16 hi/lo split of u (M x 128) and the fp32 block constants
+ *   of W (d x 2*ceil(k/128)).  ws: qn_workspace_bytes(QN_OP_LINEAR_FWD).
+ *   Stream order: the M <= 16 kernels are launched as programmatic
+ *   dependents of the kernel before them (they start early and wait for it
+ *   with griddepcontrol.wait before reading any operand), so the call may
+ *   directly follow the kernel that writes X, Q, A or B.
+ *   The persistent kernel hands u between its CTAs through the workspace
+ *   counters; if that hand-off times out (all CTAs could not be resident,
+ *   e.g. other work filled the GPU for seconds) Y is wrong and the next
+ *   qn_device_status() returns QN_ETIMEOUT: results are valid once
+ *   qn_device_status() has returned QN_OK.
  */
 qn_status qlora_linear_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M,
                            const uint16_t *A, const uint16_t *B, int32_t r,
@@ -218,11 +248,72 @@ qn_status qlora_linear_bwd_dx(const qn_nf4 *Q, const uint16_t *dY, int64_t M,
  *   resid host fp64[T+1]: resid[t] = ||W - deq(Q_t) - s B_t A_t||_F, with
  *   resid[0] the plain QLoRA residual ||W - deq(NF4(W))||_F.
  *   1 <= r, r + oversample <= 32, 0 <= T <= 64, d, k multiples of 64 and >= r + oversample.
+ *   Block size 64 and the DQ setting are taken from Q (Q->dq); the rank-r
+ *   step is always the randomised one.
  */
 qn_status loftq_init(const float *W, int64_t d, int64_t k, int32_t r, float alpha,
                      int32_t T, uint64_t seed, int32_t oversample, int32_t power_iters,
                      const qn_nf4 *Q, float *A, float *B, double *resid,
                      void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * loftq_replace_lora -- one LoftQ step against the caller's quantised weight.
+ *   W     device fp32 [Q->d x Q->k], the unquantised reference weight.
+ *   Q     the quantised weight (input only: it is not requantised).
+ *   A, B  device fp32 [r x k], [d x r] (written): B A s is the rank-r
+ *         approximation of R = W - deq(Q) (randomised subspace iteration as
+ *         in loftq_init, with `seed`, `oversample`, `power_iters`);
+ *         B = U_r sqrt(S_r)/sqrt(s), A = sqrt(S_r) V_r^T/sqrt(s), s = alpha/r.
+ *   resid host fp64[2]: ||R||_F and ||R - s B A||_F.
+ *   Sizes, limits and workspace as loftq_init (qn_workspace_bytes(QN_OP_LOFTQ)).
+ */
+qn_status loftq_replace_lora(const float *W, const qn_nf4 *Q, int32_t r, float alpha, uint64_t seed,
+                             int32_t oversample, int32_t power_iters, float *A, float *B, double *resid,
+                             void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * qlora_linear_bwd_lora -- gradients of the adapter factors for dL/dY = dY:
+ *   dA = s (dY B)^T X   (r x k),   dB = s dY^T (X A^T)   (d x r),   s = alpha/r.
+ *   X  device bf16 [M x k];  dY device bf16 [M x d];  A bf16 [r x k];  B bf16 [d x r].
+ *   dA, dB device fp32 (written).  1 <= M, d, k;  1 <= r <= 256.
+ *   The token contractions run on the tensor cores with X A^T and dY B kept
+ *   as bf16 hi + lo (about 16 significant bits), fp32 accumulation, and a
+ *   fixed summation order (results do not depend on the launch).
+ *   ws: qn_workspace_bytes(QN_OP_LINEAR_BWD_LORA, M, d, k, r).
+ */
+qn_status qlora_linear_bwd_lora(const uint16_t *X, const uint16_t *dY, int64_t M, int64_t d, int64_t k,
+                                const uint16_t *A, const uint16_t *B, int32_t r, float alpha,
+                                float *dA, float *dB, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * qlora_linear_fwd_f32 / qlora_linear_bwd_dx_f32 -- the layer with fp32
+ * compute dtype: X, A, B, Y (dY, dX) are device fp32 with the shapes of
+ * qlora_linear_fwd / qlora_linear_bwd_dx, and the weight enters as its exact
+ * fp32 dequantisation (the value nf4_dequantize writes).  fp32 FMA on the
+ * CUDA cores, fp32 accumulation.  Size rules as the bf16 calls; ws:
+ * qn_workspace_bytes(QN_OP_LINEAR_F32, M, d, k, r) (the M x r projection).
+ */
+qn_status qlora_linear_fwd_f32(const qn_nf4 *Q, const float *X, int64_t M, const float *A, const float *B,
+                               int32_t r, float alpha, float *Y, void *ws, size_t ws_bytes, void *stream);
+qn_status qlora_linear_bwd_dx_f32(const qn_nf4 *Q, const float *dY, int64_t M, const float *A, const float *B,
+                                  int32_t r, float alpha, float *dX, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * nf4_merge_lora -- Qout = NF4(deq(Q) + sign * s * B A), s = alpha / r;
+ * sign = +1 merges the adapter, -1 unmerges it.  Because the result is
+ * quantised again, unmerge(merge(Q)) is not Q in general.
+ *   Q     input quantised weight, d x k with k % 64 == 0.
+ *   A, B  device bf16 [r x k], [d x r], 1 <= r <= 256.
+ *   Qout  output state with Q's shape (its own dq setting); Qout == Q
+ *         (the same buffers) merges in place.
+ *   The adapter product is summed in fp32 in ascending rank order (each
+ *   bf16 x bf16 term is exact), t = fp32(s * sum), w = fp32(deq +- t), then
+ *   quantised exactly as nf4_quantize does (bit-identical to quantising
+ *   that fp32 tensor).  ws: qn_workspace_bytes(QN_OP_MERGE) (needed when
+ *   Qout->dq).
+ */
+qn_status nf4_merge_lora(const qn_nf4 *Q, const uint16_t *A, const uint16_t *B, int32_t r, float alpha,
+                         int32_t sign, const qn_nf4 *Qout, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * nf4_quantize_noalloc -- nf4_quantize without a caller workspace.  The

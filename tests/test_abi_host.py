@@ -31,7 +31,9 @@ def header_functions():
 
 def test_header_declares_the_entry_points():
     names = header_functions()
-    for n in ("nf4_quantize", "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd_dx", "loftq_init"):
+    for n in ("nf4_quantize", "nf4_dequantize", "qlora_linear_fwd", "qlora_linear_bwd_dx", "loftq_init",
+              "qlora_linear_bwd_lora", "qlora_linear_fwd_f32", "qlora_linear_bwd_dx_f32", "loftq_replace_lora",
+              "nf4_merge_lora"):
         assert n in names
 
 
@@ -40,7 +42,7 @@ def test_library_exports_every_declared_symbol(qn):
     for n in header_functions():
         assert hasattr(raw, n), n
     assert set(header_functions()) <= set(qn.EXPORTS)
-    assert qn.lib.qn_abi_version() == 1
+    assert qn.lib.qn_abi_version() == 2
 
 
 def test_tables_match_oracle_codebook_and_thresholds(qn):
@@ -102,8 +104,8 @@ def test_argument_errors_return_before_launch(qn):
     assert "workspace" in msg
     # LoftQ: rank + oversample bound, T bound, shape agreement
     res = (ctypes.c_double * 8)()
-    assert L.loftq_init(P, 128, 128, 30, 16.0, 5, 0, 8, 4, ctypes.byref(st), P, P, ctypes.addressof(res), P,
-                        1 << 30, None) == qn.QN_ESHAPE
+    assert L.loftq_init(P, 128, 128, 90, 16.0, 5, 0, 8, 4, ctypes.byref(st), P, P, ctypes.addressof(res), P,
+                        1 << 30, None) == qn.QN_ESHAPE      # r + oversample = 98 > 96
     assert L.loftq_init(P, 128, 128, 8, 16.0, 99, 0, 8, 4, ctypes.byref(st), P, P, ctypes.addressof(res), P,
                         1 << 30, None) == qn.QN_ESHAPE
     assert L.loftq_init(P, 64, 128, 8, 16.0, 5, 0, 8, 4, ctypes.byref(st), P, P, ctypes.addressof(res), P,
@@ -122,3 +124,32 @@ def test_noalloc_quantize_argument_errors(qn):
     huge = _struct(qn, d=1 << 21, k=1 << 20)
     assert L.nf4_quantize_noalloc(P, 0, ctypes.byref(huge), None) == qn.QN_ESHAPE
     assert "too large" in qn.lib.qn_last_error().decode()
+
+
+def test_new_entry_points_reject_bad_arguments(qn):
+    L = qn.lib
+    P = 0x10000
+    st = _struct(qn)
+    res = (ctypes.c_double * 2)()
+    # adapter gradients: rank bound, NULL, alignment, workspace
+    assert L.qlora_linear_bwd_lora(P, P, 4, 64, 64, P, P, 0, 16.0, P, P, P, 1 << 30, None) == qn.QN_ESHAPE
+    assert L.qlora_linear_bwd_lora(P, None, 4, 64, 64, P, P, 8, 16.0, P, P, P, 1 << 30, None) == qn.QN_EINVAL
+    assert L.qlora_linear_bwd_lora(P + 4, P, 4, 64, 64, P, P, 8, 16.0, P, P, P, 1 << 30, None) == qn.QN_EALIGN
+    assert L.qlora_linear_bwd_lora(P, P, 4, 64, 64, P, P, 8, 16.0, P, P, P, 16, None) == qn.QN_ENOMEM
+    # fp32 layer: k % 64, r range, workspace
+    odd_k = _struct(qn, k=100)
+    assert L.qlora_linear_fwd_f32(ctypes.byref(odd_k), P, 1, P, P, 8, 16.0, P, P, 1 << 20, None) == qn.QN_ESHAPE
+    assert L.qlora_linear_bwd_dx_f32(ctypes.byref(st), P, 1, P, P, 300, 16.0, P, P, 1 << 20, None) == qn.QN_ESHAPE
+    assert L.qlora_linear_fwd_f32(ctypes.byref(st), P, 1, P, P, 8, 16.0, P, P, 4, None) == qn.QN_ENOMEM
+    # merge: sign, rank, shape agreement
+    assert L.nf4_merge_lora(ctypes.byref(st), P, P, 8, 16.0, 0, ctypes.byref(st), P, 1 << 20, None) == qn.QN_EINVAL
+    assert L.nf4_merge_lora(ctypes.byref(st), P, P, 0, 16.0, 1, ctypes.byref(st), P, 1 << 20, None) == qn.QN_ESHAPE
+    other = _struct(qn, d=st.d * 2)
+    assert L.nf4_merge_lora(ctypes.byref(st), P, P, 8, 16.0, 1, ctypes.byref(other), P, 1 << 20, None) == qn.QN_ESHAPE
+    # one-step LoftQ: rank + oversample bound
+    assert L.loftq_replace_lora(P, ctypes.byref(st), 90, 16.0, 0, 8, 4, P, P, ctypes.addressof(res), P, 1 << 30,
+                                None) == qn.QN_ESHAPE      # r + oversample = 98 > 96
+    # workspace queries of the new operations
+    assert qn.workspace_bytes(qn.QN_OP_LINEAR_BWD_LORA, 4096, 11008, 4096, 16) > 256 * 1024
+    assert qn.workspace_bytes(qn.QN_OP_LINEAR_F32, 16, 1024, 1024, 8) >= 256 * 1024 + 16 * 8 * 4
+    assert qn.workspace_bytes(qn.QN_OP_MERGE, 0, 1024, 1024, 8) == qn.workspace_bytes(qn.QN_OP_QUANTIZE, 0, 1024, 1024, 0)

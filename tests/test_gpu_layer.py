@@ -27,6 +27,19 @@ def _f64(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
+def tile_max_rel(Y, Yref, rows=256, cols=128):
+    """Largest relative Frobenius error over rows x cols tiles of the output
+    (token tiles x weight-row tiles), so that one wrong tile cannot hide in
+    the global norm."""
+    Y = np.asarray(Y, np.float64)
+    Yref = np.asarray(Yref, np.float64)
+    worst = 0.0
+    for i in range(0, Y.shape[0], rows):
+        for j in range(0, Y.shape[1], cols):
+            worst = max(worst, layer.rel_fro(Y[i:i + rows, j:j + cols], Yref[i:i + rows, j:j + cols]))
+    return worst
+
+
 def _run(qn, W, X, A, B, alpha, dY=None):
     q = qn.nf4_quantize(torch.from_numpy(W).cuda(), dq=True)
     ref = nf4.quantize(W, 64, dq=True)
@@ -46,6 +59,8 @@ def test_layer_case(qn):
     o = _run(qn, c["W"], c["X"], c["A"], c["B"], c["alpha"], c["dY"])
     assert layer.rel_fro(_f64(o["Y"]), o["Yref"]) < TOL
     assert layer.rel_fro(_f64(o["dX"]), o["dXref"]) < TOL
+    assert tile_max_rel(_f64(o["Y"]), o["Yref"], 16, 16) < TOL
+    assert tile_max_rel(_f64(o["dX"]), o["dXref"], 16, 16) < TOL
 
 
 @pytest.mark.parametrize("M,d,k,r", [
@@ -57,6 +72,8 @@ def test_shapes_with_ragged_tails(qn, M, d, k, r):
     o = _run(qn, c["W"], c["X"], c["A"], c["B"], c["alpha"], c["dY"])
     assert layer.rel_fro(_f64(o["Y"]), o["Yref"]) < TOL, (M, d, k, r)
     assert layer.rel_fro(_f64(o["dX"]), o["dXref"]) < TOL, (M, d, k, r)
+    assert tile_max_rel(_f64(o["Y"]), o["Yref"], 64, 16) < TOL, (M, d, k, r)
+    assert tile_max_rel(_f64(o["dX"]), o["dXref"], 64, 64) < TOL, (M, d, k, r)
 
 
 def test_degenerate_adapter_and_weight(qn):
@@ -77,11 +94,14 @@ def test_decode_shapes(qn, shape, M):
     m = synth.decode_matrix(seed=1, d=d, k=k, r=64, M=M)
     o = _run(qn, m["W"], m["X"], m["A"], m["B"], m["alpha"])
     assert layer.rel_fro(_f64(o["Y"]), o["Yref"]) < TOL
+    assert tile_max_rel(_f64(o["Y"]), o["Yref"], 16, 16) < TOL   # every 16-row tile of W
 
 
 def test_prefill_full_size_sampled_rows(qn):
     """M=4096, d=11008, k=4096, r=16: full Y and dX on the GPU; the oracle
-    checks 48 sampled rows of each (the full float64 product is 0.7 TFLOP)."""
+    checks 48 sampled token rows of each (the full float64 product is 0.7
+    TFLOP), three from every 256-token tile, and every 128-column tile of
+    those rows on its own."""
     c = synth.prefill_case(seed=2)
     W = c["W"]
     q = qn.nf4_quantize(torch.from_numpy(W).cuda(), dq=True)
@@ -91,12 +111,14 @@ def test_prefill_full_size_sampled_rows(qn):
     ref = nf4.quantize(W, 64, dq=True)
     Wd = nf4.dequantize(ref).reshape(W.shape)
     g = np.random.default_rng(2)
-    rows = np.sort(g.choice(c["M"], 48, replace=False))
+    rows = np.sort(np.concatenate([t0 + g.choice(256, 3, replace=False) for t0 in range(0, c["M"], 256)]))
     A, B = _f64(c["A"]), _f64(c["B"])
     Yref = layer.linear_fwd(_f64(c["X"])[rows], Wd, A, B, c["alpha"], c["r"])
     dXref = layer.linear_bwd_dx(_f64(c["dY"])[rows], Wd, A, B, c["alpha"], c["r"])
     assert layer.rel_fro(_f64(Y)[rows], Yref) < TOL
     assert layer.rel_fro(_f64(dX)[rows], dXref) < TOL
+    assert tile_max_rel(_f64(Y)[rows], Yref, 3, 128) < TOL      # 3 rows of one token tile x 128 weight rows
+    assert tile_max_rel(_f64(dX)[rows], dXref, 3, 128) < TOL
     # every output finite and of the right scale
     assert torch.isfinite(Y.float()).all() and torch.isfinite(dX.float()).all()
 
@@ -218,3 +240,61 @@ def test_group_of_projections(qn, M):
     # same bits as the single-projection calls
     for q, A, B, a, Y in zip(qs, As, Bs, alphas, Ys):
         assert torch.equal(qn.qlora_linear_fwd(q, X.cuda(), A, B, a), Y)
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_forward_right_after_its_inputs_are_written(qn, M):
+    """The forward starts as a programmatic dependent of the kernel before it.
+    Here that kernel writes the forward's own operands: nf4_quantize writes Q
+    (its last kernel writes the DQ codes and scales) and a torch copy writes
+    A and B, each immediately before the call.  Q starts as garbage (codes
+    0xFF, scales NaN) and A, B as NaN, so a read that comes too early shows.
+    Checked eagerly and in a CUDA graph replay against the same call made
+    after a synchronise."""
+    d = k = 4096
+    m = synth.decode_matrix(seed=6, d=d, k=k, r=16, M=M)
+    W = torch.from_numpy(m["W"]).cuda()
+    A0, B0, X = m["A"].cuda(), m["B"].cuda(), m["X"].cuda()
+    q = qn.NF4Tensor.empty(d, k, True, "cuda")
+    A = torch.empty_like(A0)
+    B = torch.empty_like(B0)
+    Y = torch.empty((M, d), dtype=torch.bfloat16, device="cuda")
+    qref = qn.nf4_quantize(W)
+    ref = qn.qlora_linear_fwd(qref, X, A0, B0, m["alpha"])
+    torch.cuda.synchronize()
+
+    def poison():
+        q.codes.fill_(0xFF)
+        q.absmax_q.fill_(127)
+        q.absmax_scale.fill_(float("nan"))
+        A.fill_(float("nan"))
+        B.fill_(float("nan"))
+        Y.fill_(float("nan"))
+
+    def step():
+        qn.nf4_quantize(W, out=q)
+        A.copy_(A0)
+        B.copy_(B0)
+        qn.qlora_linear_fwd(q, X, A, B, m["alpha"], out=Y)
+
+    for _ in range(2):
+        poison()
+        torch.cuda.synchronize()
+        step()
+        torch.cuda.synchronize()
+        assert torch.equal(Y, ref)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(3):
+        poison()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(Y, ref)
+    qn.device_status()

@@ -25,7 +25,9 @@ def qn():
     return mod
 
 
-@pytest.mark.parametrize("d,k,r,T", [(256, 256, 8, 3), (512, 384, 16, 5), (192, 640, 4, 2)])
+# Panels of 32, 64 and 96 columns: r + oversample = 12, 16, 24 (32); 40 (64); 72 and 96 (96).
+@pytest.mark.parametrize("d,k,r,T", [(256, 256, 8, 3), (512, 384, 16, 5), (192, 640, 4, 2), (1024, 1024, 64, 3),
+                                     (384, 512, 32, 2), (320, 448, 88, 2)])
 def test_small_against_oracle(qn, d, k, r, T):
     W = synth.loftq_case(seed=4, d=d, k=k)
     q, A, B, resid = qn.loftq_init(torch.from_numpy(W).cuda(), r=r, alpha=float(r), T=T, seed=1,
@@ -41,6 +43,12 @@ def test_small_against_oracle(qn, d, k, r, T):
     Wd = qn.nf4_dequantize(q, torch.float32).double()
     R = torch.from_numpy(W).cuda().double() - Wd - (B.double() @ A.double())
     assert abs(torch.linalg.norm(R).item() - resid[T]) <= 1e-4 * resid[T]
+
+
+def test_rank_above_the_panel_limit_is_rejected(qn):
+    W = torch.from_numpy(synth.loftq_case(seed=4, d=256, k=256)).cuda()
+    with pytest.raises(qn.QnError):
+        qn.loftq_init(W, r=90, alpha=90.0, T=1, oversample=8)      # 98 > 96
 
 
 def test_T0_equals_plain_quantizer(qn):

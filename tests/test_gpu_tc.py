@@ -4,9 +4,9 @@ against the float64 oracle, relative Frobenius error <= 5e-3.
 The shapes put ragged edges on every tile boundary of that kernel: weight
 rows not a multiple of 128, token counts below, at and above one 256-token
 tile, a single 64-column stage, padded adapter ranks (r = 1, 33, 40) and the
-largest rank it takes (64), and forward grids with more tiles than SMs (the
-persistent kernel's accumulator reuse); r = 65 checks the CUDA-core kernel
-that takes over above that rank."""
+largest rank it takes (64), and forward grids of several waves of tiles
+(more tiles than SMs); r = 65 checks the CUDA-core kernel that takes over
+above that rank."""
 
 import numpy as np
 import pytest
@@ -42,8 +42,7 @@ def _fwd(qn, W, X, A, B, alpha, dq=True):
 @pytest.mark.parametrize("M,d,k,r", [
     (17, 128, 64, 8), (256, 256, 128, 16), (257, 384, 192, 1), (300, 200, 576, 33),
     (600, 1000, 256, 64), (1024, 512, 1024, 40), (40, 130, 64, 65),
-    # more tiles than SMs: every CTA of the persistent kernel takes two or
-    # three tiles, so both accumulators are reused; ragged rows and tokens
+    # more tiles than SMs: the grid runs in several waves; ragged rows and tokens
     (1300, 6500, 128, 24), (2100, 2600, 320, 64),
 ])
 def test_tc_forward_shapes(qn, M, d, k, r):
