@@ -197,7 +197,7 @@ qn_status launch_dequantize(const qn_nf4 *Q, void *out, qn_dtype odt, cudaStream
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
   if (grid > cap) grid = cap;
   if (odt == QN_BF16)
-    qn::nf4_dequant_bf16_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(view_of(Q), n, static_cast<uint16_t *>(out));
+    qn::nf4_dequant_kernel<true><<<static_cast<unsigned>(grid), 256, 0, st>>>(view_of(Q), n, out);
   else
     qn::nf4_dequant_kernel<false><<<static_cast<unsigned>(grid), 256, 0, st>>>(view_of(Q), n, out);
   QN_LAUNCH_CHECK("nf4_dequant_kernel");
@@ -346,6 +346,18 @@ qn_status launch_gemv_group(int n, const qn_nf4 *const *Q, const uint16_t *X, in
   }
   const int64_t grid = tiles < sm_count() ? tiles : sm_count();
   if (M > qn::kGvMaxM || !qn::gv_fits(static_cast<int>(M), k, tiles, us, static_cast<int>(grid))) return QN_OK;
+  static int fits_block[64] = {0};  // 1: a 320-thread CTA of the kernel can launch on this device; -1: cannot
+  {
+    int dv = 0;
+    QN_TRY(cuda_check(cudaGetDevice(&dv), "cudaGetDevice"));
+    if (dv < 0 || dv >= 64) return fail(QN_EUNSUPPORTED, "device ordinal out of range");
+    if (!fits_block[dv]) {
+      cudaFuncAttributes fa;
+      QN_TRY(cuda_check(cudaFuncGetAttributes(&fa, qn::qlora_gemv_kernel), "cudaFuncGetAttributes"));
+      fits_block[dv] = fa.maxThreadsPerBlock >= qn::kGvThreads ? 1 : -1;
+    }
+    if (fits_block[dv] < 0) return QN_OK;
+  }
   for (int i = 0; i < n; ++i) {
     // codes as uint32 [d][k / 8]: one box = 16 rows x 128 bytes (4 blocks)
     if (const char *e = qn::make_tile_map(&g.p[i].tmap, Q[i]->codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4,
@@ -898,14 +910,28 @@ qn_status qn_device_status(void *stream) {
 
 namespace {
 
+// K splits of the two panel products: about four CTAs per SM, at least four
+// 32-wide chunks of K per split.
+int lq_splits(int64_t out_rows, int64_t kdim) {
+  const int64_t tiles = qn_ceil_div(out_rows, qn::kLqTile);
+  int64_t S = qn_ceil_div(4 * static_cast<int64_t>(sm_count()), tiles);
+  const int64_t smax = kdim / (4 * qn::kLqTile);
+  if (S > smax) S = smax;
+  if (S > 16) S = 16;
+  return S < 1 ? 1 : static_cast<int>(S);
+}
+
 // LoftQ workspace: the d x k residual, the panels Y (d x P), Zt and Omega
-// (k x P), the Gram partials and the small P x P factors.
+// (k x P), the split partials of the products, the Gram partials and the
+// small P x P factors.
 size_t loftq_ws_bytes(int64_t d, int64_t k) {
   const size_t P = qn::kLqMaxP;
   const size_t nb = static_cast<size_t>(qn_ceil_div(d > k ? d : k, qn::kLqGramRows));
+  const size_t prt = std::max(static_cast<size_t>(lq_splits(d, k)) * d, static_cast<size_t>(lq_splits(k, d)) * k);
   size_t b = kSemBytes + round256(static_cast<size_t>(d) * k * sizeof(float));  // target / residual
   b += round256(static_cast<size_t>(d) * P * sizeof(float));                  // Y
   b += 2 * round256(static_cast<size_t>(k) * P * sizeof(float));              // Zt, Omega
+  b += round256(prt * P * sizeof(float));                                     // product split partials
   b += round256(nb * P * P * sizeof(float));                                  // Gram partials
   b += round256(P * P * sizeof(double)) + 2 * round256(P * P * sizeof(float)) + round256(P * sizeof(float));
   b += round256(1024 * sizeof(double)) + round256(sizeof(double));            // norm partials, norm
@@ -927,11 +953,13 @@ qn_status loftq_run_p(const float *W, int64_t d, int64_t k, int32_t r, float alp
   float *Y = sp.take<float>(static_cast<size_t>(d) * qn::kLqMaxP);
   float *Zt = sp.take<float>(static_cast<size_t>(k) * qn::kLqMaxP);
   float *Om = sp.take<float>(static_cast<size_t>(k) * qn::kLqMaxP);
+  const int Srz = lq_splits(d, k), Srty = lq_splits(k, d);
+  float *ppart = sp.take<float>(std::max(static_cast<size_t>(Srz) * d, static_cast<size_t>(Srty) * k) * qn::kLqMaxP);
   const int64_t nbmax = qn_ceil_div(d > k ? d : k, qn::kLqGramRows);
   float *gpart = sp.take<float>(static_cast<size_t>(nbmax) * qn::kLqMaxP * qn::kLqMaxP);
   double *G = sp.take<double>(qn::kLqMaxP * qn::kLqMaxP);
   float *V = sp.take<float>(qn::kLqMaxP * qn::kLqMaxP);
-  float *Linv = sp.take<float>(qn::kLqMaxP * qn::kLqMaxP);
+  float *Lf = sp.take<float>(qn::kLqMaxP * qn::kLqMaxP);
   float *lam = sp.take<float>(qn::kLqMaxP);
   double *partial = sp.take<double>(1024);
   double *norm2 = sp.take<double>(1);
@@ -974,25 +1002,36 @@ qn_status loftq_run_p(const float *W, int64_t d, int64_t k, int32_t r, float alp
     QN_LAUNCH_CHECK("lq_gram_reduce_kernel");
     return QN_OK;
   };
-  auto orth = [&](float *Ym, int64_t rows) -> qn_status {  // CholeskyQR2
+  auto orth = [&](float *Ym, int64_t rows) -> qn_status {  // CholeskyQR2: Ym <- Ym L^{-T}, twice
     for (int rep = 0; rep < 2; ++rep) {
       QN_TRY(gram(Ym, rows));
-      qn::lq_chol_inv_kernel<P><<<1, 256, 0, st>>>(G, p, Linv);
-      QN_LAUNCH_CHECK("lq_chol_inv_kernel");
-      qn::lq_apply_linv_kernel<P><<<static_cast<unsigned>(qn_ceil_div(rows, 16)), 256, 0, st>>>(Ym, rows, Linv);
-      QN_LAUNCH_CHECK("lq_apply_linv_kernel");
+      qn::lq_chol_kernel<P><<<1, 256, 0, st>>>(G, p, Lf);
+      QN_LAUNCH_CHECK("lq_chol_kernel");
+      qn::lq_trsm_rows_kernel<P><<<static_cast<unsigned>(qn_ceil_div(rows, 128)), 128, 0, st>>>(Ym, rows, Lf, p);
+      QN_LAUNCH_CHECK("lq_trsm_rows_kernel");
     }
     return QN_OK;
   };
-  auto r_times = [&](const float *Z, float *Yo) -> qn_status {  // Yo = R Z   (d x P)
-    qn::lq_rz_kernel<P><<<static_cast<unsigned>(qn_ceil_div(d, 16)), 256, 0, st>>>(Tbuf, d, k, Z, Yo);
-    QN_LAUNCH_CHECK("lq_rz_kernel");
+  auto reduce = [&](int S, int64_t n_out, float *out) -> qn_status {
+    qn::lq_split_reduce_kernel<<<static_cast<unsigned>(qn_ceil_div(n_out, 256)), 256, 0, st>>>(ppart, S, n_out, out);
+    QN_LAUNCH_CHECK("lq_split_reduce_kernel");
     return QN_OK;
   };
+  auto r_times = [&](const float *Z, float *Yo) -> qn_status {  // Yo = R Z   (d x P)
+    const int64_t cps = qn_ceil_div(qn_ceil_div(k, Srz), qn::kLqTile) * qn::kLqTile;
+    const int S = static_cast<int>(qn_ceil_div(k, cps));
+    qn::lq_rz_kernel<P><<<dim3(static_cast<unsigned>(qn_ceil_div(d, qn::kLqTile)), static_cast<unsigned>(S)), 256, 0,
+                         st>>>(Tbuf, d, k, Z, cps, ppart);
+    QN_LAUNCH_CHECK("lq_rz_kernel");
+    return reduce(S, d * P, Yo);
+  };
   auto rt_times = [&](const float *Ym, float *Zo) -> qn_status {  // Zo = R^T Y  (k x P)
-    qn::lq_rty_kernel<P><<<static_cast<unsigned>(qn_ceil_div(k, 32)), 256, 0, st>>>(Tbuf, d, k, Ym, Zo);
+    const int64_t rps = qn_ceil_div(qn_ceil_div(d, Srty), qn::kLqTile) * qn::kLqTile;
+    const int S = static_cast<int>(qn_ceil_div(d, rps));
+    qn::lq_rty_kernel<P><<<dim3(static_cast<unsigned>(k / qn::kLqTile), static_cast<unsigned>(S)), 256, 0, st>>>(
+        Tbuf, d, k, Ym, rps, ppart);
     QN_LAUNCH_CHECK("lq_rty_kernel");
-    return QN_OK;
+    return reduce(S, k * P, Zo);
   };
 
   // t = 0: Q_0 = NF4(W) (or the caller's Q), residual without adapter.

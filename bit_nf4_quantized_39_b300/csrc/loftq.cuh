@@ -110,99 +110,144 @@ residual_kernel(QnNF4View q, const float *__restrict__ W, float *__restrict__ R,
 
 // ------------------------------------------------------------- skinny products
 // The rank-r step works on panels of P columns (P = 32, 64 or 96, the padded
-// r + oversample; columns past p are kept zero).
+// r + oversample; columns past p are kept zero).  Both products read R once;
+// K is split over gridDim.y so that enough CTAs stream it, each split's
+// partial panel goes to `part`, and lq_split_reduce_kernel adds the splits
+// in order (no atomics: the result does not depend on the launch).  Tiles
+// are double-buffered through shared memory with cp.async.
 
-// Y[i, c] = sum_j R[i, j] Z[j, c]   (R: n_rows x n_cols, Z: n_cols x P).
-// CTA: 16 rows of R; column chunks of 64 staged in shared memory with the
-// matching 64 x P block of Z; thread (row tid / 16, columns (tid % 16) P/16 ..)
-// keeps P/16 sums.  Every element of R is read once.
+constexpr int kLqTile = 32;  // rows of the output panel per CTA, and the K chunk
+
+// part[split][i][c] = sum over the split's j of R[i, j] Z[j, c]  (R: n_rows x n_cols, Z: n_cols x P).
+// Thread (row tid / 8, panel columns (tid % 8) P/8 ..).  n_cols % 32 == 0.
 template <int P>
 __global__ void __launch_bounds__(256)
 lq_rz_kernel(const float *__restrict__ R, int64_t n_rows, int64_t n_cols, const float *__restrict__ Z,
-             float *__restrict__ Y) {
-  constexpr int CW = P / 16;
-  __shared__ float sR[16][64 + 1];
-  __shared__ __align__(16) float sZ[64][P];
-  const int tid = threadIdx.x, tr = tid / 16, tc = tid % 16;
-  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * 16;
+             int64_t cols_per_split, float *__restrict__ part) {
+  constexpr int CW = P / 8;
+  __shared__ __align__(16) float sR[2][kLqTile][kLqTile + 4];
+  __shared__ __align__(16) float sZ[2][kLqTile][P];
+  const int tid = threadIdx.x, tr = tid / 8, tc = tid % 8;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kLqTile;
+  const int64_t jb = static_cast<int64_t>(blockIdx.y) * cols_per_split;
+  int64_t je = jb + cols_per_split;
+  if (je > n_cols) je = n_cols;
+  auto stage = [&](int b, int64_t j0) {
+    for (int t = tid; t < kLqTile * kLqTile / 4; t += 256) {  // R tile: 32 rows x 32 columns
+      const int rr = t / (kLqTile / 4), c4 = (t % (kLqTile / 4)) * 4;
+      const int64_t i = i0 + rr;
+      if (i < n_rows) cp_async16(smem_u32(&sR[b][rr][c4]), R + i * n_cols + j0 + c4);
+      else *reinterpret_cast<float4 *>(&sR[b][rr][c4]) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int t = tid; t < kLqTile * P / 4; t += 256) {  // Z tile: 32 rows x P
+      const int rr = t / (P / 4), c4 = (t % (P / 4)) * 4;
+      cp_async16(smem_u32(&sZ[b][rr][c4]), Z + (j0 + rr) * P + c4);
+    }
+    cp_async_commit();
+  };
   float acc[CW];
 #pragma unroll
   for (int c = 0; c < CW; ++c) acc[c] = 0.f;
-  for (int64_t j0 = 0; j0 < n_cols; j0 += 64) {
-    for (int t = tid; t < 16 * 64; t += 256) {
-      const int rr = t / 64, cc = t % 64;
-      const int64_t i = i0 + rr, j = j0 + cc;
-      sR[rr][cc] = (i < n_rows && j < n_cols) ? __ldcs(R + i * n_cols + j) : 0.f;
-    }
-    for (int t = tid; t < 64 * P; t += 256) {
-      const int rr = t / P, cc = t % P;
-      const int64_t j = j0 + rr;
-      sZ[rr][cc] = (j < n_cols) ? Z[j * P + cc] : 0.f;
+  const int nch = static_cast<int>((je - jb) / kLqTile);
+  if (nch > 0) stage(0, jb);
+  for (int ch = 0; ch < nch; ++ch) {
+    const int b = ch & 1;
+    if (ch + 1 < nch) {
+      stage(b ^ 1, jb + static_cast<int64_t>(ch + 1) * kLqTile);
+      cp_async_wait_group<1>();
+    } else {
+      cp_async_wait_group<0>();
     }
     __syncthreads();
 #pragma unroll 8
-    for (int jj = 0; jj < 64; ++jj) {
-      const float rv = sR[tr][jj];
+    for (int jj = 0; jj < kLqTile; ++jj) {
+      const float rv = sR[b][tr][jj];
 #pragma unroll
-      for (int c = 0; c < CW; ++c) acc[c] = fmaf(rv, sZ[jj][tc * CW + c], acc[c]);
+      for (int c = 0; c < CW; ++c) acc[c] = fmaf(rv, sZ[b][jj][tc * CW + c], acc[c]);
     }
     __syncthreads();
   }
   const int64_t i = i0 + tr;
   if (i < n_rows) {
+    float *dst = part + (static_cast<int64_t>(blockIdx.y) * n_rows + i) * P + tc * CW;
 #pragma unroll
-    for (int c = 0; c < CW; ++c) Y[i * P + tc * CW + c] = acc[c];
+    for (int c = 0; c < CW; ++c) dst[c] = acc[c];
   }
 }
 
-// Zt[j, c] = sum_i R[i, j] Y[i, c]  (R: n_rows x n_cols, Y: n_rows x P).
-// CTA: 32 columns of R, all rows in chunks of 64 staged with the matching
-// 64 x P block of Y; thread (column tid / 8, panel columns (tid % 8) P/8 ..).
-// No atomics: every output has one writer and a fixed summation order.
+// part[split][j][c] = sum over the split's i of R[i, j] Y[i, c]  (R: n_rows x n_cols, Y: n_rows x P).
+// Thread (column tid / 8, panel columns (tid % 8) P/8 ..).  n_cols % 32 == 0.
 template <int P>
 __global__ void __launch_bounds__(256)
 lq_rty_kernel(const float *__restrict__ R, int64_t n_rows, int64_t n_cols, const float *__restrict__ Y,
-              float *__restrict__ Zt) {
+              int64_t rows_per_split, float *__restrict__ part) {
   constexpr int CW = P / 8;
-  __shared__ float sR[64][32 + 1];
-  __shared__ __align__(16) float sY[64][P];
+  __shared__ __align__(16) float sR[2][kLqTile][kLqTile + 4];
+  __shared__ __align__(16) float sY[2][kLqTile][P];
   const int tid = threadIdx.x, tj = tid / 8, tc = tid % 8;
-  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * 32;
+  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * kLqTile;
+  const int64_t ib = static_cast<int64_t>(blockIdx.y) * rows_per_split;
+  int64_t ie = ib + rows_per_split;
+  if (ie > n_rows) ie = n_rows;
+  auto stage = [&](int b, int64_t i0) {
+    for (int t = tid; t < kLqTile * kLqTile / 4; t += 256) {  // R tile: 32 rows x 32 columns
+      const int rr = t / (kLqTile / 4), c4 = (t % (kLqTile / 4)) * 4;
+      const int64_t i = i0 + rr;
+      if (i < ie) cp_async16(smem_u32(&sR[b][rr][c4]), R + i * n_cols + j0 + c4);
+      else *reinterpret_cast<float4 *>(&sR[b][rr][c4]) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int t = tid; t < kLqTile * P / 4; t += 256) {  // Y tile: 32 rows x P
+      const int rr = t / (P / 4), c4 = (t % (P / 4)) * 4;
+      const int64_t i = i0 + rr;
+      if (i < ie) cp_async16(smem_u32(&sY[b][rr][c4]), Y + i * P + c4);
+      else *reinterpret_cast<float4 *>(&sY[b][rr][c4]) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    cp_async_commit();
+  };
   float acc[CW];
 #pragma unroll
   for (int c = 0; c < CW; ++c) acc[c] = 0.f;
-  for (int64_t i0 = 0; i0 < n_rows; i0 += 64) {
-    for (int t = tid; t < 64 * 32; t += 256) {
-      const int rr = t / 32, cc = t % 32;
-      const int64_t i = i0 + rr, j = j0 + cc;
-      sR[rr][cc] = (i < n_rows && j < n_cols) ? __ldcs(R + i * n_cols + j) : 0.f;
-    }
-    for (int t = tid; t < 64 * P; t += 256) {
-      const int rr = t / P, cc = t % P;
-      const int64_t i = i0 + rr;
-      sY[rr][cc] = (i < n_rows) ? Y[i * P + cc] : 0.f;
+  const int nch = static_cast<int>((ie - ib + kLqTile - 1) / kLqTile);
+  if (nch > 0) stage(0, ib);
+  for (int ch = 0; ch < nch; ++ch) {
+    const int b = ch & 1;
+    if (ch + 1 < nch) {
+      stage(b ^ 1, ib + static_cast<int64_t>(ch + 1) * kLqTile);
+      cp_async_wait_group<1>();
+    } else {
+      cp_async_wait_group<0>();
     }
     __syncthreads();
 #pragma unroll 8
-    for (int ii = 0; ii < 64; ++ii) {
-      const float rv = sR[ii][tj];
+    for (int ii = 0; ii < kLqTile; ++ii) {
+      const float rv = sR[b][ii][tj];
 #pragma unroll
-      for (int c = 0; c < CW; ++c) acc[c] = fmaf(rv, sY[ii][tc * CW + c], acc[c]);
+      for (int c = 0; c < CW; ++c) acc[c] = fmaf(rv, sY[b][ii][tc * CW + c], acc[c]);
     }
     __syncthreads();
   }
   const int64_t j = j0 + tj;
   if (j < n_cols) {
+    float *dst = part + (static_cast<int64_t>(blockIdx.y) * n_cols + j) * P + tc * CW;
 #pragma unroll
-    for (int c = 0; c < CW; ++c) Zt[j * P + tc * CW + c] = acc[c];
+    for (int c = 0; c < CW; ++c) dst[c] = acc[c];
   }
+}
+
+// out[e] = sum over the S splits, in order, of part[split][e]   (e < n).
+__global__ void lq_split_reduce_kernel(const float *__restrict__ part, int S, int64_t n, float *__restrict__ out) {
+  const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (e >= n) return;
+  float v = 0.f;
+  for (int z = 0; z < S; ++z) v += part[static_cast<int64_t>(z) * n + e];
+  out[e] = v;
 }
 
 // Gram matrix G = Y^T Y (P x P) of a panel Y (n x P): kLqGramRows rows per
 // CTA summed in fp32 into part[block][P][P], then lq_gram_reduce_kernel adds
 // the blocks in order in fp64.  Thread (a-tile, b-tile) holds an
 // (P/16) x (P/16) tile of the P x P result.
-constexpr int kLqGramRows = 256;
+constexpr int kLqGramRows = 32;
 
 template <int P>
 __global__ void __launch_bounds__(256)
@@ -254,16 +299,13 @@ __global__ void lq_gram_reduce_kernel(const float *__restrict__ part, int nblock
 }
 
 // One CTA of 256 threads: Cholesky G = L L^T of the leading p x p block (G
-// accumulated in fp64, factored in fp32) and Linv = L^{-1} (lower
-// triangular, fp32 [P x P], zero outside the p x p block).  One P x P array
-// holds both: L's strict lower triangle in place, its diagonal in dL, and
-// Linv^T in the upper triangle (Linv[i][t] at M[t][i], i >= t).  A pivot
-// that is not positive (rank deficiency) is clamped to a tiny positive value.
+// accumulated in fp64, factored in fp32).  L (lower triangular, fp32 [P x P])
+// is the identity outside the p x p block.  A pivot that is not positive
+// (rank deficiency) is clamped to a tiny positive value.
 template <int P>
 __global__ void __launch_bounds__(256)
-lq_chol_inv_kernel(const double *__restrict__ G, int p, float *__restrict__ Linv) {
+lq_chol_kernel(const double *__restrict__ G, int p, float *__restrict__ Lout) {
   __shared__ float Mx[P][P + 1];
-  __shared__ float dL[P];
   __shared__ float s_floor;
   const int tid = threadIdx.x;
   for (int t = tid; t < P * P; t += 256) {
@@ -293,52 +335,39 @@ lq_chol_inv_kernel(const double *__restrict__ G, int p, float *__restrict__ Linv
     }
     __syncthreads();
   }
-  for (int i = tid; i < P; i += 256) dL[i] = (i < p) ? Mx[i][i] : 1.f;
-  __syncthreads();
-  // column t of L^{-1} by forward substitution (one thread per column), stored transposed above the diagonal
-  for (int t = tid; t < p; t += 256) {
-    for (int i = t; i < p; ++i) {
-      float acc = (i == t) ? 1.f : 0.f;
-      for (int q = t; q < i; ++q) acc -= Mx[i][q] * Mx[t][q];   // L[i][q] * Linv[q][t]
-      Mx[t][i] = acc / dL[i];                                     // Linv[i][t]
-    }
-  }
-  __syncthreads();
   for (int e = tid; e < P * P; e += 256) {
-    const int i = e / P, t = e % P;  // Linv[i][t]
-    Linv[e] = (i < p && t <= i) ? Mx[t][i] : 0.f;
+    const int i = e / P, c = e % P;
+    Lout[e] = (i < p && c < p) ? ((c <= i) ? Mx[i][c] : 0.f) : ((i == c) ? 1.f : 0.f);
   }
 }
 
-// Y[i, :] <- Y[i, :] Linv^T in place: 16 rows per CTA; thread (row tid / 16,
-// columns (tid % 16) P/16 ..).
+// Y[i, :] <- Y[i, :] L^{-T} in place (the Q factor of CholeskyQR): each row
+// solves L q = y by forward substitution, one thread per row; columns past
+// p come out zero.
 template <int P>
-__global__ void __launch_bounds__(256)
-lq_apply_linv_kernel(float *__restrict__ Y, int64_t n, const float *__restrict__ Linv) {
-  constexpr int CW = P / 16;
+__global__ void __launch_bounds__(128)
+lq_trsm_rows_kernel(float *__restrict__ Y, int64_t n, const float *__restrict__ L, int p) {
   __shared__ float sL[P][P + 1];
-  __shared__ float sY[16][P + 1];
-  const int tid = threadIdx.x, tr = tid / 16, tc = tid % 16;
-  for (int t = tid; t < P * P; t += 256) sL[t / P][t % P] = Linv[t];
-  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * 16;
-  for (int t = tid; t < 16 * P; t += 256) {
-    const int64_t i = i0 + t / P;
-    sY[t / P][t % P] = (i < n) ? Y[i * P + t % P] : 0.f;
-  }
+  for (int t = threadIdx.x; t < P * P; t += blockDim.x) sL[t / P][t % P] = L[t];
   __syncthreads();
-  float acc[CW];
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float y[P];
 #pragma unroll
-  for (int c = 0; c < CW; ++c) acc[c] = 0.f;
-  for (int b = 0; b < P; ++b) {
-    const float y = sY[tr][b];
-#pragma unroll
-    for (int c = 0; c < CW; ++c) acc[c] = fmaf(y, sL[tc * CW + c][b], acc[c]);
+  for (int c = 0; c < P; c += 4) {
+    const float4 v = *reinterpret_cast<const float4 *>(Y + i * P + c);
+    y[c] = v.x; y[c + 1] = v.y; y[c + 2] = v.z; y[c + 3] = v.w;
   }
-  const int64_t i = i0 + tr;
-  if (i < n) {
 #pragma unroll
-    for (int c = 0; c < CW; ++c) Y[i * P + tc * CW + c] = acc[c];
+  for (int c = 0; c < P; ++c) {
+    float acc = y[c];
+#pragma unroll
+    for (int b = 0; b < c; ++b) acc = fmaf(-sL[c][b], y[b], acc);
+    y[c] = (c < p) ? acc / sL[c][c] : 0.f;
   }
+#pragma unroll
+  for (int c = 0; c < P; c += 4)
+    *reinterpret_cast<float4 *>(Y + i * P + c) = make_float4(y[c], y[c + 1], y[c + 2], y[c + 3]);
 }
 
 // One CTA of 256 threads: parallel cyclic Jacobi eigen-decomposition (fp32)
@@ -371,7 +400,7 @@ lq_jacobi_kernel(const double *__restrict__ G, int p, float *__restrict__ lam, f
   }
   for (int t = tid; t < P; t += 256) pos[t] = t;
   __syncthreads();
-  for (int sweep = 0; sweep < 30; ++sweep) {
+  for (int sweep = 0; sweep < 15; ++sweep) {
     if (tid < 32) {  // convergence: off-diagonal mass against the diagonal
       float off = 0.f, dg = 0.f;
       for (int t = tid; t < n * n; t += 32) {
@@ -387,7 +416,7 @@ lq_jacobi_kernel(const double *__restrict__ G, int p, float *__restrict__ lam, f
       if (tid == 0) { s_off = off; s_dg = dg; }
     }
     __syncthreads();
-    if (s_off <= 1e-13f * s_dg) break;
+    if (s_off <= 1e-10f * s_dg) break;  // off-diagonal mass at the fp32 noise level
     for (int step = 0; step < n - 1; ++step) {
       // pairs of this step and their rotations
       for (int k = tid; k < np; k += 256) {

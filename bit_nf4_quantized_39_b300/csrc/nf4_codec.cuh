@@ -273,8 +273,8 @@ __device__ __forceinline__ void build_bucket_tables(BucketEntry *s_one, BucketEn
 
 // End of a quantising kernel with double quantisation (every thread of the
 // CTA calls it): the CTA's exponent bins go to the global bins; the last CTA
-// to finish forms the exact mean of all nblk block constants, stores it and
-// returns the ticket to zero.
+// of the whole grid (1-D or not) to finish forms the exact mean of all nblk
+// block constants, stores it and returns the ticket to zero.
 __device__ __forceinline__ void quant_mean_epilogue(unsigned long long *s_bins, unsigned long long *bins,
                                                     unsigned int *ticket, int64_t nblk, float *absmax_mean) {
   __shared__ bool s_last;
@@ -283,7 +283,8 @@ __device__ __forceinline__ void quant_mean_epilogue(unsigned long long *s_bins, 
     if (s_bins[i]) atomicAdd(&bins[i], s_bins[i]);
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(ticket, 1u) == gridDim.x - 1u);
+  const unsigned int nctas = gridDim.x * gridDim.y * gridDim.z;  // every CTA of the grid, whatever its shape
+  if (threadIdx.x == 0) s_last = (atomicAdd(ticket, 1u) == nctas - 1u);
   __syncthreads();
   if (!s_last) return;
   __threadfence();
@@ -441,7 +442,8 @@ nf4_dq_kernel(const float *__restrict__ absmax, int64_t nblk, const float *__res
 }
 
 // ---------------------------------------------------------------------------
-// Dequantisation: one thread per 32 elements (16 code bytes, one 128-bit load).
+// Dequantisation: one thread per 32 elements (16 code bytes, one 128-bit
+// load), two such chunks per iteration.
 // ---------------------------------------------------------------------------
 template <bool kBf16Out>
 __global__ void __launch_bounds__(256)
@@ -450,10 +452,21 @@ nf4_dequant_kernel(QnNF4View q, int64_t n, void *__restrict__ out) {
   if (threadIdx.x < 16) s_lut[threadIdx.x] = c_nf4_levels[threadIdx.x];
   __syncthreads();
   const int64_t nchunk = n / 32;
-  for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < nchunk;
-       c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const uint4 w4 = __ldcs(reinterpret_cast<const uint4 *>(q.codes) + c);
-    const float m = block_scale(q, c >> 1);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  // Two chunks per iteration: both code loads (and both constants) are in
+  // flight before either chunk is decoded.
+  for (int64_t c0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c0 < nchunk; c0 += 2 * stride) {
+    const int64_t c1 = c0 + stride;
+    const uint4 wa = __ldcs(reinterpret_cast<const uint4 *>(q.codes) + c0);
+    const uint4 wb = (c1 < nchunk) ? __ldcs(reinterpret_cast<const uint4 *>(q.codes) + c1) : make_uint4(0u, 0u, 0u, 0u);
+    const float ma = block_scale(q, c0 >> 1);
+    const float mb = (c1 < nchunk) ? block_scale(q, c1 >> 1) : 0.f;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+    const int64_t c = half ? c1 : c0;
+    if (c >= nchunk) break;
+    const uint4 w4 = half ? wb : wa;
+    const float m = half ? mb : ma;
     const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
     if constexpr (kBf16Out) {
       uint32_t o[16];
@@ -478,6 +491,7 @@ nf4_dequant_kernel(QnNF4View q, int64_t n, void *__restrict__ out) {
         __stcs(dst + 2 * i + 1, make_float4(f[4], f[5], f[6], f[7]));
       }
     }
+    }
   }
   // Tail: elements [nchunk*32, n), one thread each.
   const int64_t t0 = nchunk * 32;
@@ -488,54 +502,6 @@ nf4_dequant_kernel(QnNF4View q, int64_t n, void *__restrict__ out) {
       const float wv = __fmul_rn(s_lut[code], block_scale(q, e >> 6));
       if constexpr (kBf16Out) static_cast<uint16_t *>(out)[e] = f32_to_bf16_bits(wv);
       else static_cast<float *>(out)[e] = wv;
-    }
-  }
-}
-
-// bf16 output with the register decoder: each lane decodes 32 elements (one
-// 16-byte code load) at a time, two chunks per iteration with both loads in
-// flight; the 16 levels scaled by the block constant are built in registers
-// as exactly bf16(fp32(c * m)) (scaled_levels) and selected with byte
-// permutes (decode_word), so no shared memory is touched.
-__global__ void __launch_bounds__(256)
-nf4_dequant_bf16_kernel(QnNF4View q, int64_t n, uint16_t *__restrict__ out) {
-  const int64_t nchunk = n / 32;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t c0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c0 < nchunk; c0 += 2 * stride) {
-    const int64_t c1 = c0 + stride;
-    const uint4 w0 = __ldcs(reinterpret_cast<const uint4 *>(q.codes) + c0);
-    const uint4 w1 = (c1 < nchunk) ? __ldcs(reinterpret_cast<const uint4 *>(q.codes) + c1) : make_uint4(0u, 0u, 0u, 0u);
-    const float m0 = block_scale(q, c0 >> 1);
-    const float m1 = (c1 < nchunk) ? block_scale(q, c1 >> 1) : 0.f;
-    {
-      const ScaledLevels t = scaled_levels(m0);
-      uint32_t o[16];
-      decode_word(w0.x, t, o);
-      decode_word(w0.y, t, o + 4);
-      decode_word(w0.z, t, o + 8);
-      decode_word(w0.w, t, o + 12);
-      uint4 *dst = reinterpret_cast<uint4 *>(out + c0 * 32);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) __stcs(dst + i, make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]));
-    }
-    if (c1 < nchunk) {
-      const ScaledLevels t = scaled_levels(m1);
-      uint32_t o[16];
-      decode_word(w1.x, t, o);
-      decode_word(w1.y, t, o + 4);
-      decode_word(w1.z, t, o + 8);
-      decode_word(w1.w, t, o + 12);
-      uint4 *dst = reinterpret_cast<uint4 *>(out + c1 * 32);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) __stcs(dst + i, make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]));
-    }
-  }
-  // Tail: elements [nchunk*32, n), one thread each.
-  if (blockIdx.x == 0) {
-    for (int64_t e = nchunk * 32 + threadIdx.x; e < n; e += blockDim.x) {
-      const uint32_t byte = q.codes[e >> 1];
-      const uint32_t code = (e & 1) ? (byte >> 4) : (byte & 15u);
-      out[e] = f32_to_bf16_bits(__fmul_rn(c_nf4_levels[code], block_scale(q, e >> 6)));
     }
   }
 }

@@ -19,11 +19,11 @@
 //   barriers; everything that another kernel may write -- codes, block
 //   constants, X, A, B, u, Y, the workspace counters -- is read or written
 //   after the wait, through L2 (TMA, bulk copies, ld.global.cg);
-// * warp 8 streams each tile's codes with TMA (16 rows x 16 blocks = 8 KiB
-//   per stage, four 128-byte-swizzled boxes) through an 11-stage ring, plus
+// * warp 16 streams each tile's codes with TMA (16 rows x 16 blocks = 8 KiB
+//   per stage, four 128-byte-swizzled boxes) through an 8-stage ring, plus
 //   the tile's block constants (int8 DQ codes or fp32 absmax) as one bulk
 //   copy with its first stage;
-// * warps 0-7 take two 64-blocks of every stage each: a lane (group g,
+// * warps 0-15 take one 64-block of every stage each: a lane (group g,
 //   thread t) turns 8 code bytes of rows g and g+8 into bf16x2 A-fragment
 //   registers through a per-lane replicated byte-pair table (one byte
 //   permute and one shared load per byte), multiplies them on mma.sync
@@ -31,12 +31,14 @@
 //   in the unused half of every table row, and scales each block's dot
 //   products by its block constant in fp32.  The MMA's k order is a
 //   permutation of the block's elements, the same for both operands.  At the
-//   end of a tile the eight warps' partial sums are added in a fixed order
-//   into the tile's row sums (shared memory);
-// * warp 9 computes this CTA's share of u = s X A^T (adapter rows j with
-//   j mod gridDim == blockIdx), publishes them through a workspace counter,
-//   waits (bounded) until every CTA has published, and then forms
-//   u . B[row] for every row of the CTA's range while the weights stream;
+//   end of a tile the sixteen warps' partial sums are added in a fixed order
+//   into the tile's row sums (shared memory).  The consumer warps also
+//   compute the adapter rows u = s X A^T (row j by warp j / gridDim of CTA
+//   j mod gridDim) right after staging X, and publish them through a
+//   workspace counter;
+// * warp 17 copies the B rows of its CTA's range into shared memory, waits
+//   (bounded) until every CTA has published its rows of u, and forms
+//   u . B[row] for every row of the range while the weights stream;
 // * the epilogue writes bf16 Y = row sum + adapter term.
 //
 // Every CTA is resident at once (one per SM, at most one per SM), so the
@@ -48,15 +50,15 @@
 
 namespace qn {
 
-constexpr int kGvConsumers = 8;
-constexpr int kGvProducerWarp = 8;
-constexpr int kGvAdapterWarp = 9;
-constexpr int kGvThreads = 320;
+constexpr int kGvConsumers = 16;                     // one 64-block of every stage each
+constexpr int kGvProducerWarp = kGvConsumers;
+constexpr int kGvAdapterWarp = kGvConsumers + 1;
+constexpr int kGvThreads = (kGvConsumers + 2) * 32;
 constexpr int kGvRows = 16;                          // rows per tile (MMA M)
 constexpr int kGvStageBlocks = 16;                   // 64-blocks per stage
 constexpr int kGvStageBytes = kGvRows * kGvStageBlocks * 32;  // 8 KiB of codes
 constexpr int kGvBoxBytes = 128;                     // TMA box width: one swizzle span, 4 blocks
-constexpr int kGvStages = 9;                         // ring depth (72 KiB in flight per SM)
+constexpr int kGvStages = 8;                         // ring depth (64 KiB in flight per SM)
 constexpr int kGvMaxNb = 256;                        // 64-blocks per row (k <= 16384)
 constexpr int kGvCSlots = 2;                         // block-constant tiles in flight
 constexpr int kGvCSlotBytes = kGvRows * kGvMaxNb * 4;  // one tile's fp32 constants (or int8 codes)
@@ -204,7 +206,8 @@ __device__ __forceinline__ uint32_t gv_cbytes(const QnNF4View &q, int64_t row0, 
   return static_cast<uint32_t>(nrows * nb * (q.dq ? 1 : 4)) & ~15u;
 }
 
-__global__ void __maxnreg__(200)
+// 320 threads are allocated as 12 warps' worth of registers: at most 168 per thread.
+__global__ void __launch_bounds__(kGvThreads, 1)
 qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
   extern __shared__ unsigned char gv_raw[];
   unsigned char *base = reinterpret_cast<unsigned char *>(
@@ -321,12 +324,18 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
     pdl_wait_grid();
     const int64_t rtot = g.rtot;
     const int64_t nrows_cta = static_cast<int64_t>(ntl) * kGvRows;
-    int64_t bro[kGvMaxGroup];  // element offset of projection i's first row in `brows` (-1: not staged)
+    // brows + bro[i] + row * r is row `row` of projection i's B when staged;
+    // the offset itself may be negative (rows before the range are not staged).
+    int64_t bro[kGvMaxGroup];
+    bool staged[kGvMaxGroup];
     {
       int64_t off = 0;
       bool fits = true;
 #pragma unroll
-      for (int i = 0; i < kGvMaxGroup; ++i) bro[i] = -1;
+      for (int i = 0; i < kGvMaxGroup; ++i) {
+        bro[i] = 0;
+        staged[i] = false;
+      }
       for (int i = 0; i < g.n; ++i) {
         const GvProj &p = g.p[i];
         const int64_t tend = (i + 1 < g.n) ? g.p[i + 1].tile_off : g.ntiles;
@@ -344,6 +353,7 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
         const uint16_t *src = p.B + ra * p.r;
         for (int64_t e = static_cast<int64_t>(lane) * 8; e < elems; e += 32 * 8) cp_async16(smem_u32(brows + off + e), src + e);
         bro[i] = off - ra * p.r;
+        staged[i] = true;
         off += padded;
       }
       cp_async_commit();
@@ -385,7 +395,7 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
       for (int tt = 0; tt < kGvMaxM; ++tt) a[tt] = 0.f;
       if (row < p.q.d) {
         const float *ur = us + p.u_off;
-        if (bro[pi] >= 0) {
+        if (staged[pi]) {
           const uint16_t *br = brows + bro[pi] + row * p.r;
           for (int q = 0; q < p.r; q += 2) {
             const uint32_t bw = *reinterpret_cast<const uint32_t *>(br + q);
@@ -393,6 +403,27 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
 #pragma unroll
             for (int tt = 0; tt < kGvMaxM; ++tt)
               if (tt < M) a[tt] = fmaf(ur[tt * rtot + q + 1], b1, fmaf(ur[tt * rtot + q], b0, a[tt]));
+          }
+        } else if ((p.r & 7) == 0 && (reinterpret_cast<uintptr_t>(p.B) & 15u) == 0) {
+          // not staged: 8 values per 16-byte load, four loads in flight
+          const uint16_t *brow = p.B + row * p.r;
+          for (int q0 = 0; q0 < p.r; q0 += 32) {
+            uint4 bv[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              bv[c] = (q0 + 8 * c < p.r) ? ld_cg_v4(brow + q0 + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              if (q0 + 8 * c >= p.r) break;
+              const uint32_t bw[4] = {bv[c].x, bv[c].y, bv[c].z, bv[c].w};
+#pragma unroll
+              for (int h = 0; h < 8; ++h) {
+                const float b = (h & 1) ? __uint_as_float(bw[h >> 1] & 0xFFFF0000u) : __uint_as_float(bw[h >> 1] << 16);
+#pragma unroll
+                for (int tt = 0; tt < kGvMaxM; ++tt)
+                  if (tt < M) a[tt] = fmaf(ur[tt * rtot + q0 + 8 * c + h], b, a[tt]);
+              }
+            }
           }
         } else {
           const uint16_t *brow = p.B + row * p.r;
@@ -423,7 +454,7 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
 
   // ================================= consumers ==================================
   const int gq = lane >> 2, tq = lane & 3;
-  const int cw = warp;  // takes blocks cw and cw + 8 of every stage
+  const int cw = warp;  // takes block cw of every stage
   const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
   {
     // table entry b of lane l: bf16(level[b & 15]) | bf16(level[b >> 4]) << 16
@@ -433,29 +464,19 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
     for (int i = 0; i < 16; ++i) lv[i] = f32_to_bf16_bits(c_nf4_levels[i]);
     uint32_t *lw = reinterpret_cast<uint32_t *>(lut);
 #pragma unroll
-    for (int n = 0; n < 32; ++n) {
-      const int b = b0 + 8 * n;
-      lw[b * 64 + l] = lv[b0 + 8 * (n & 1)] | (lv[n >> 1] << 16);
+    for (int n = 0; n < 256 / kGvConsumers; ++n) {
+      const int b = b0 + kGvConsumers * n;  // b & 15 = b0, b >> 4 = n
+      lw[b * 64 + l] = lv[b0] | (lv[n] << 16);
     }
   }
   pdl_wait_grid();
-  // Adapter rows of u done by this warp: j = blockIdx + G (warp + 8 i); their
-  // first 4096 columns of A are loaded now, ahead of the X staging.
+  // Adapter rows of u done by this warp: j = blockIdx + G (warp + 8 i).  The
+  // X loads and the first 2048 columns of the first row of A are issued
+  // together, then X goes to shared memory.
   const int64_t rtot = g.rtot;
   const int64_t j_first = blockIdx.x + static_cast<int64_t>(G) * warp;
-  constexpr int kAV = 16;  // 16-byte A loads per lane in flight (4096 columns)
+  constexpr int kAV = 4;  // 16-byte A loads per lane in flight (1024 columns)
   uint4 apre[kAV];
-  if (j_first < rtot) {
-    const GvProj &p = g.p[gv_proj_of_urow(g, j_first)];
-    const uint16_t *arow = p.A + (j_first - p.u_off) * k;
-#pragma unroll
-    for (int v = 0; v < kAV; ++v) {
-      const int64_t e = (v * 32 + lane) * 8;
-      apre[v] = (e < k) ? ld_cg_v4(arow + e) : make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
-  // X (M x k bf16, token-major) into the upper halves of the table rows: all
-  // loads first, then the stores.
   {
     const int64_t nvec = static_cast<int64_t>(M) * k / 8;
     uint4 xv[kGvXPer];
@@ -463,6 +484,15 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
     for (int v = 0; v < kGvXPer; ++v) {
       const int64_t i = v * (kGvConsumers * 32) + tid;
       xv[v] = (i < nvec) ? ld_cg_v4(g.X + i * 8) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (j_first < rtot) {
+      const GvProj &p = g.p[gv_proj_of_urow(g, j_first)];
+      const uint16_t *arow = p.A + (j_first - p.u_off) * k;
+#pragma unroll
+      for (int v = 0; v < kAV; ++v) {
+        const int64_t e = (v * 32 + lane) * 8;
+        apre[v] = (e < k) ? ld_cg_v4(arow + e) : make_uint4(0u, 0u, 0u, 0u);
+      }
     }
 #pragma unroll
     for (int v = 0; v < kGvXPer; ++v) {
@@ -564,14 +594,11 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       const unsigned char *stage = ring + slot * kGvStageBytes;
-      uint32_t a[2][2][8];  // [item][row half][byte]
-      float m[2][2];
-      int bi[2];
-#pragma unroll
-      for (int it = 0; it < 2; ++it) {
-        const int cb = cw + 8 * it;
-        const int b = s * kGvStageBlocks + cb;
-        bi[it] = b;
+      uint32_t av[2][8];  // [row half][byte]: bf16 pairs of the block's codes
+      float m[2];
+      const int cb = cw;
+      const int b = s * kGvStageBlocks + cb;
+      {
         const int chunk = 2 * (cb & 3) + (tq >> 1);
         const uint32_t off =
             (cb >> 2) * (kGvRows * kGvBoxBytes) + gq * kGvBoxBytes + ((chunk ^ gq) << 4) + ((tq & 1) << 3);
@@ -579,10 +606,10 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
         const uint2 c1 = *reinterpret_cast<const uint2 *>(stage + off + 8 * kGvBoxBytes);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          a[it][0][i] = *reinterpret_cast<const uint32_t *>(lut + gv_lut_off(c0.x, lane4, 0x5504u | (i << 4)));
-          a[it][0][4 + i] = *reinterpret_cast<const uint32_t *>(lut + gv_lut_off(c0.y, lane4, 0x5504u | (i << 4)));
-          a[it][1][i] = *reinterpret_cast<const uint32_t *>(lut + gv_lut_off(c1.x, lane4, 0x5504u | (i << 4)));
-          a[it][1][4 + i] = *reinterpret_cast<const uint32_t *>(lut + gv_lut_off(c1.y, lane4, 0x5504u | (i << 4)));
+          av[0][i] = *reinterpret_cast<const uint32_t *>(lut + gv_lut_off(c0.x, lane4, 0x5504u | (i << 4)));
+          av[0][4 + i] = *reinterpret_cast<const uint32_t *>(lut + gv_lut_off(c0.y, lane4, 0x5504u | (i << 4)));
+          av[1][i] = *reinterpret_cast<const uint32_t *>(lut + gv_lut_off(c1.x, lane4, 0x5504u | (i << 4)));
+          av[1][4 + i] = *reinterpret_cast<const uint32_t *>(lut + gv_lut_off(c1.y, lane4, 0x5504u | (i << 4)));
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -599,15 +626,12 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
               mm = (o * 4 < cbytes) ? reinterpret_cast<const float *>(ct)[o] : ld_cg_f32(qv.absmax + blk);
             }
           }
-          m[it][h] = mm;
+          m[h] = mm;
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&bars->empty[slot]));  // codes are in registers now
-#pragma unroll
-      for (int it = 0; it < 2; ++it) {
-        const int b = bi[it];
-        if (b >= nb) continue;
+      if (b < nb) {
         uint4 x0 = make_uint4(0u, 0u, 0u, 0u), x1 = x0;
         if (gq < M) {
           const uint32_t o = static_cast<uint32_t>((gq * k + static_cast<int64_t>(b) * 64 + tq * 16) * 2);
@@ -615,18 +639,19 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
           x1 = *reinterpret_cast<const uint4 *>(lut + gv_x_off(o + 16));
         }
         const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        float dsum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int st = 0; st < 4; ++st)
-          gv_mma(dsum, a[it][0][2 * st], a[it][1][2 * st], a[it][0][2 * st + 1], a[it][1][2 * st + 1], xw[2 * st],
-                 xw[2 * st + 1]);
-        acc[0] = fmaf(dsum[0], m[it][0], acc[0]);
-        acc[1] = fmaf(dsum[1], m[it][0], acc[1]);
-        acc[2] = fmaf(dsum[2], m[it][1], acc[2]);
-        acc[3] = fmaf(dsum[3], m[it][1], acc[3]);
+        // two independent accumulation chains (steps 0, 2 and 1, 3)
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+        gv_mma(d0, av[0][0], av[1][0], av[0][1], av[1][1], xw[0], xw[1]);
+        gv_mma(d1, av[0][2], av[1][2], av[0][3], av[1][3], xw[2], xw[3]);
+        gv_mma(d0, av[0][4], av[1][4], av[0][5], av[1][5], xw[4], xw[5]);
+        gv_mma(d1, av[0][6], av[1][6], av[0][7], av[1][7], xw[6], xw[7]);
+        acc[0] = fmaf(d0[0] + d1[0], m[0], acc[0]);
+        acc[1] = fmaf(d0[1] + d1[1], m[0], acc[1]);
+        acc[2] = fmaf(d0[2] + d1[2], m[1], acc[2]);
+        acc[3] = fmaf(d0[3] + d1[3], m[1], acc[3]);
       }
     }
-    // ---- end of the tile: the eight warps' partial sums, added in warp order
+    // ---- end of the tile: the warps' partial sums, added in warp order
     float *ps = part + (tl & 1) * (kGvConsumers * kGvRows * kGvMaxM);
     {
       float *pw = ps + cw * (kGvRows * kGvMaxM);
@@ -637,7 +662,7 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kGvConsumers * 32) : "memory");
     if (tid == 0) mbar_arrive(smem_u32(&bars->cfree[tl % kGvCSlots]));  // every warp is done with the constants
-    if (cw == (tl & 7)) {
+    if (cw == (tl % kGvConsumers)) {
       for (int e = lane; e < kGvRows * M; e += 32) {
         const int row = e / M, tok = e % M;
         float v = 0.f;
