@@ -10,8 +10,11 @@ flush is needed between steps).
 
 Secondary numbers measured in the same run: the same set at M = 16, the
 prefill-shaped layer (M = 4096, 11008 x 4096, r = 16) forward and backward
-dX in TFLOP/s, bulk NF4 quantise / dequantise of the 6.48 B-parameter bf16
-set in GB/s, and LoftQ (4096 x 4096, r = 16, T = 5) seconds per alternation.
+dX in TFLOP/s, the adapter gradients dA, dB of that layer in GB/s, the
+fp32-compute forward, merge of the adapter into the NF4 weight, bulk NF4
+quantise / dequantise of the 6.48 B-parameter bf16 set in GB/s, and LoftQ
+(4096 x 4096, r = 16, T = 5) seconds per alternation plus its one-step
+variant.
 
 --impl reference times the CPU oracle on the same metric (bounded sample).
 Under torchrun every rank runs its own replica of the decode set (weak
@@ -259,6 +262,24 @@ def decode_bytes(mats, M, r):
     return w4, lora, act
 
 
+# fp32 FMA peak of the CUDA cores: 148 SMs x 128 lanes x 2 flops x 2.032 GHz
+FP32_FMA_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+
+
+def _time_call(fn, reps):
+    """Mean CUDA-event time of `reps` back-to-back calls after two warm-up calls."""
+    for _ in range(2):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return {"ms": e0.elapsed_time(e1) / reps}
+
+
 def secondary(qn, device, pk, quick: bool):
     """Prefill TFLOP/s, bulk quantise/dequantise GB/s, LoftQ s/alternation."""
     out = {}
@@ -290,7 +311,33 @@ def secondary(qn, device, pk, quick: bool):
         tf = flops / (ms * 1e-3) / 1e12
         out[name] = {"ms": ms, "tflops": tf, "frac_of_bf16_peak": tf / pk["bf16_tflops"],
                      "workload": "M=4096, d=11008, k=4096, r=16, alpha=32"}
-    del X, dY, q
+    # adapter gradients at the prefill shape: HBM bound (X and dY read once)
+    reps = 3 if quick else 10
+    grad_bytes = 2 * M * (c_k + c_d) + 2 * r * (c_k + c_d) + 4 * r * (c_k + c_d)
+    out["lora_grads"] = _time_call(lambda: qn.qlora_linear_bwd_lora(X, dY, A, B, alpha), reps)
+    out["lora_grads"].update(gbs=grad_bytes / (out["lora_grads"]["ms"] * 1e-3) / 1e9, bytes=grad_bytes,
+                             workload="dA, dB at M=4096, d=11008, k=4096, r=16 (algorithmic bytes: X, dY, A, B "
+                                      "read, dA, dB written)")
+    out["lora_grads"]["frac_of_hbm"] = out["lora_grads"]["gbs"] / pk["hbm_gbs"]
+    # fp32 compute dtype: prefill-shaped forward (CUDA-core fp32 FMA) and one decode matrix
+    Xf, Af, Bf = X.float(), A.float(), B.float()
+    out["fp32_fwd"] = _time_call(lambda: qn.qlora_linear_fwd_f32(q, Xf, Af, Bf, alpha), max(2, reps // 2))
+    tf = flops / (out["fp32_fwd"]["ms"] * 1e-3) / 1e12
+    out["fp32_fwd"].update(tflops=tf, frac_of_fp32_peak=tf / FP32_FMA_TFLOPS,
+                           workload="fp32 compute dtype, M=4096, d=11008, k=4096, r=16; CUDA-core FMA")
+    del Xf
+    x1 = torch.randn((1, c_k), device=device, generator=gen)
+    out["fp32_fwd_m1"] = _time_call(lambda: qn.qlora_linear_fwd_f32(q, x1, Af, Bf, alpha), reps)
+    out["fp32_fwd_m1"]["gbs"] = q.nbytes() / (out["fp32_fwd_m1"]["ms"] * 1e-3) / 1e9
+    out["fp32_fwd_m1"]["workload"] = "fp32 compute dtype, M=1, 11008 x 4096 (GB/s of 4-bit weight bytes)"
+    # merge / unmerge of the adapter into the quantised weight
+    qo = qn.NF4Tensor.empty(c_d, c_k, True, device)
+    merge_bytes = 2 * q.nbytes() + 2 * r * (c_k + c_d)
+    out["merge"] = _time_call(lambda: qn.nf4_merge_lora(q, A, B, alpha, 1, out=qo), reps)
+    out["merge"].update(gbs=merge_bytes / (out["merge"]["ms"] * 1e-3) / 1e9, bytes=merge_bytes,
+                        workload="NF4+DQ 11008 x 4096, r=16: deq + s B A + requantise (state read and written)")
+    out["merge"]["frac_of_hbm"] = out["merge"]["gbs"] / pk["hbm_gbs"]
+    del X, dY, qo
 
     # bulk quantise / dequantise of the 32-layer bf16 set (one tensor per call)
     layers = 4 if quick else 32
@@ -348,6 +395,12 @@ def secondary(qn, device, pk, quick: bool):
     dt = time.perf_counter() - t0
     out["loftq"] = {"s_per_alternation": dt / T, "T": T, "resid": resid,
                     "workload": "4096x4096 Student-t, r=16, oversample 8, 4 power iterations"}
+    q0 = qn.nf4_quantize(Wl)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    _, _, res1 = qn.loftq_replace_lora(Wl, q0, 16, 16.0, seed=0)
+    out["loftq_one_step"] = {"s": time.perf_counter() - t0, "resid": res1,
+                             "workload": "4096x4096 Student-t, r=16, one Delta-step against NF4(W)"}
     return out
 
 

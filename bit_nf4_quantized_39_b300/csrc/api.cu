@@ -315,72 +315,116 @@ qn_status launch_decode_group(int n, const qn_nf4 *const *Q, const uint16_t *X, 
   return QN_OK;
 }
 
+// Where dynamic shared memory starts for a kernel without static shared
+// memory (the few-token kernel addresses its level table with an immediate
+// offset from there).  One launch per device, cached.
+__global__ void qn_smem_base_probe(unsigned int *out) {
+  extern __shared__ __align__(1024) unsigned char probe_smem[];
+  if (threadIdx.x == 0) out[0] = static_cast<unsigned int>(__cvta_generic_to_shared(probe_smem));
+}
+
+qn_status smem_base_matches(unsigned int *scratch, cudaStream_t st, bool *ok) {
+  static int known[64] = {0};  // 1: matches, -1: does not
+  int dev = 0;
+  QN_TRY(cuda_check(cudaGetDevice(&dev), "cudaGetDevice"));
+  if (dev < 0 || dev >= 64) return fail(QN_EUNSUPPORTED, "device ordinal out of range");
+  if (!known[dev]) {
+    // Inside a stream capture nothing may synchronize: take the path and let
+    // the kernel's own check (QN_DEV_LAYOUT) report a mismatch.
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    QN_TRY(cuda_check(cudaStreamIsCapturing(st, &cs), "cudaStreamIsCapturing"));
+    if (cs != cudaStreamCaptureStatusNone) {
+      *ok = true;
+      return QN_OK;
+    }
+    const int bytes = 64 * 1024;
+    QN_TRY(cuda_check(cudaFuncSetAttribute(qn_smem_base_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
+                      "cudaFuncSetAttribute(probe)"));
+    unsigned int h = 0;
+    qn_smem_base_probe<<<1, 32, bytes, st>>>(scratch);
+    QN_LAUNCH_CHECK("qn_smem_base_probe");
+    QN_TRY(cuda_check(cudaMemcpyAsync(&h, scratch, sizeof(h), cudaMemcpyDeviceToHost, st), "probe readback"));
+    QN_TRY(cuda_check(cudaStreamSynchronize(st), "probe synchronize"));
+    known[dev] = (h == qn::kGvSmemBase) ? 1 : -1;
+  }
+  *ok = known[dev] > 0;
+  return QN_OK;
+}
+
 // Forward of a group of projections of one input with M <= 8 tokens and
-// M * k <= 16384 on the persistent single-kernel path (qlora_gemv_kernel),
-// launched as a programmatic dependent of the kernel before it.  Sets *taken
-// to false, launching nothing, when the group exceeds that kernel's limits.
+// M * k <= 16384 (qlora_gemv_kernel), launched as a programmatic dependent of
+// the kernel before it.  Sets *taken to false, launching nothing, when the
+// group exceeds that kernel's limits or its pointers are not 16-byte aligned.
 qn_status launch_gemv_group(int n, const qn_nf4 *const *Q, const uint16_t *X, int64_t M, const uint16_t *const *A,
                             const uint16_t *const *B, const int32_t *r, const float *alpha, uint16_t *const *Y,
                             unsigned int *zero_area, Span &sp, cudaStream_t st, bool *taken) {
   *taken = false;
   const int64_t k = Q[0]->k;
+  if (M < 1 || M > qn::kGvMaxM || n > qn::kGvMaxGroup || !aligned(X, 16)) return QN_OK;
   qn::GvGroup g = {};
   g.n = n;
   g.M = static_cast<int>(M);
   g.k = k;
   g.X = X;
   g.zero_area = zero_area;
-  int64_t tiles = 0, us = 0;
+  int64_t rows = 0, us = 0;
+  int esz = 1;
+  bool any_dq = false;
   for (int i = 0; i < n; ++i) {
     qn::GvProj &p = g.p[i];
-    p.q = view_of(Q[i]);
+    p.codes = Q[i]->codes;
+    p.dq = Q[i]->dq ? 1 : 0;
+    p.consts = p.dq ? static_cast<const void *>(Q[i]->absmax_q) : static_cast<const void *>(Q[i]->absmax);
+    p.absmax_scale = Q[i]->absmax_scale;
+    p.absmax_mean = Q[i]->absmax_mean;
     p.A = A[i];
     p.B = B[i];
     p.Y = Y[i];
+    p.d = Q[i]->d;
     p.r = r[i];
     p.s = alpha[i] / static_cast<float>(r[i]);
-    p.tile_off = tiles;
+    p.row_off = rows;
     p.u_off = us;
-    tiles += qn_ceil_div(Q[i]->d, qn::kGvRows);
+    if (!aligned(p.consts, 16) || !aligned(p.A, 16) || !aligned(p.B, 16) ||
+        (p.dq && !aligned(p.absmax_scale, 16)))
+      return QN_OK;
+    rows += Q[i]->d;
     us += r[i];
+    if (!p.dq) esz = 4;
+    any_dq = any_dq || p.dq;
   }
-  const int64_t grid = tiles < sm_count() ? tiles : sm_count();
-  if (M > qn::kGvMaxM || !qn::gv_fits(static_cast<int>(M), k, tiles, us, static_cast<int>(grid))) return QN_OK;
-  static int fits_block[64] = {0};  // 1: a 320-thread CTA of the kernel can launch on this device; -1: cannot
-  {
-    int dv = 0;
-    QN_TRY(cuda_check(cudaGetDevice(&dv), "cudaGetDevice"));
-    if (dv < 0 || dv >= 64) return fail(QN_EUNSUPPORTED, "device ordinal out of range");
-    if (!fits_block[dv]) {
-      cudaFuncAttributes fa;
-      QN_TRY(cuda_check(cudaFuncGetAttributes(&fa, qn::qlora_gemv_kernel), "cudaFuncGetAttributes"));
-      fits_block[dv] = fa.maxThreadsPerBlock >= qn::kGvThreads ? 1 : -1;
-    }
-    if (fits_block[dv] < 0) return QN_OK;
-  }
-  for (int i = 0; i < n; ++i) {
-    // codes as uint32 [d][k / 8]: one box = 16 rows x 128 bytes (4 blocks)
-    if (const char *e = qn::make_tile_map(&g.p[i].tmap, Q[i]->codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4,
-                                          static_cast<uint64_t>(k / 8), static_cast<uint64_t>(Q[i]->d),
-                                          qn::kGvBoxBytes / 4, qn::kGvRows, CU_TENSOR_MAP_SWIZZLE_128B))
-      return fail(QN_ECUDA, "single-kernel forward: %s", e);
-  }
-  g.ntiles = tiles;
+  g.rows = rows;
   g.rtot = us;
+  const int grid = static_cast<int>(sm_count());
+  if (!qn::gv_plan(g, grid, esz, any_dq)) return QN_OK;
   g.u = sp.take<float>(static_cast<size_t>(M) * us);
-  static int attr_set[64] = {0};
+  bool base_ok = false;  // the u buffer is scratch for the one-time probe
+  QN_TRY(smem_base_matches(reinterpret_cast<unsigned int *>(g.u), st, &base_ok));
+  if (!base_ok) return QN_OK;
+  const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8;
+  void (*kern)(qn::GvGroup) = mt == 1 ? qn::qlora_gemv_kernel<1>
+                              : mt == 2 ? qn::qlora_gemv_kernel<2>
+                              : mt == 4 ? qn::qlora_gemv_kernel<4>
+                                        : qn::qlora_gemv_kernel<8>;
+  static int attr_set[64][4] = {};
   int dev = 0;
   QN_TRY(cuda_check(cudaGetDevice(&dev), "cudaGetDevice"));
   if (dev < 0 || dev >= 64) return fail(QN_EUNSUPPORTED, "device ordinal out of range");
-  if (!attr_set[dev]) {
-    QN_TRY(cuda_check(cudaFuncSetAttribute(qn::qlora_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(qn::kGvSmemBytes)),
-                      "cudaFuncSetAttribute(single-kernel forward smem)"));
-    attr_set[dev] = 1;
+  const int vi = mt == 1 ? 0 : mt == 2 ? 1 : mt == 4 ? 2 : 3;
+  if (!attr_set[dev][vi]) {
+    QN_TRY(cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(qn::kGvSmemCap)),
+                      "cudaFuncSetAttribute(few-token forward smem)"));
+    QN_TRY(cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100),
+                      "cudaFuncSetAttribute(few-token forward carveout)"));
+    cudaFuncAttributes fa;
+    QN_TRY(cuda_check(cudaFuncGetAttributes(&fa, kern), "cudaFuncGetAttributes"));
+    attr_set[dev][vi] = fa.maxThreadsPerBlock >= qn::kGvThreads ? 1 : -1;
   }
+  if (attr_set[dev][vi] < 0) return QN_OK;
   *taken = true;
-  return launch_pdl(qn::qlora_gemv_kernel, dim3(static_cast<unsigned>(grid)), dim3(qn::kGvThreads), qn::kGvSmemBytes,
-                    st, "qlora_gemv_kernel", g);
+  return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(qn::kGvThreads), g.smem, st,
+                    "qlora_gemv_kernel", g);
 }
 
 template <int MT, bool XS>
@@ -903,6 +947,7 @@ qn_status qn_device_status(void *stream) {
   QN_TRY(cuda_check(cudaMemcpyFromSymbol(&h, g_qn_status, sizeof(h)), "read status word"));
   QN_TRY(cuda_check(cudaMemcpyToSymbol(g_qn_status, &zero, sizeof(zero)), "clear status word"));
   if (h & QN_DEV_TIMEOUT) return fail(QN_ETIMEOUT, "a bounded device wait expired");
+  if (h & QN_DEV_LAYOUT) return fail(QN_EUNSUPPORTED, "a kernel found its shared memory at an unexpected address");
   return QN_OK;
 }
 

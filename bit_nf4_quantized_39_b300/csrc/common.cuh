@@ -38,7 +38,7 @@ __constant__ float c_nf4_thresholds[15] = QN_NF4_THRESHOLDS;
 // Device status word written by bounded waits that expire (never a trap).
 __device__ unsigned int g_qn_status;
 
-enum : unsigned int { QN_DEV_OK = 0u, QN_DEV_TIMEOUT = 1u };
+enum : unsigned int { QN_DEV_OK = 0u, QN_DEV_TIMEOUT = 1u, QN_DEV_LAYOUT = 2u };
 
 __device__ __forceinline__ void qn_flag_timeout() { atomicOr(&g_qn_status, QN_DEV_TIMEOUT); }
 

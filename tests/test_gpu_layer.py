@@ -298,3 +298,33 @@ def test_forward_right_after_its_inputs_are_written(qn, M):
         torch.cuda.synchronize()
         assert torch.equal(Y, ref)
     qn.device_status()
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_small_m_adapter_term_on_its_own(qn, M):
+    """The single-kernel path for M <= 8 forms the adapter term u . B[row] in a
+    separate warp and hands it to the epilogue.  With W = 0 (every code is the
+    exact zero) Y is that term alone, so a missing or stale hand-off shows in
+    every tile; a large adapter on a grouped call checks it next to X W^T."""
+    k = 4096
+    g = np.random.default_rng(70 + M)
+    X = synth.to_bf16(g.standard_normal((M, k), dtype=np.float32))
+    qs, As, Bs, refs = [], [], [], []
+    for i, d in enumerate((4096, 4096, 1024)):
+        W = np.zeros((d, k), np.float32) if i == 0 else (g.standard_normal((d, k)) * 0.02).astype(np.float32)
+        A = synth.to_bf16((g.standard_normal((64, k)) / np.sqrt(k)).astype(np.float32))
+        B = synth.to_bf16((g.standard_normal((d, 64)) * (1.0 if i else 0.05)).astype(np.float32))
+        qs.append(qn.nf4_quantize(torch.from_numpy(W).cuda()))
+        As.append(A.cuda()); Bs.append(B.cuda())
+        Wd = nf4.dequantize(nf4.quantize(W, 64, dq=True)).reshape(d, k)
+        refs.append(layer.linear_fwd(_f64(X), Wd, _f64(A), _f64(B), 16.0, 64))
+    Ys = qn.qlora_linear_fwd_group(qs, X.cuda(), As, Bs, [16.0] * 3)
+    qn.device_status()
+    for Y, ref in zip(Ys, refs):
+        assert layer.rel_fro(_f64(Y), ref) < TOL
+        assert tile_max_rel(_f64(Y), ref, 16, 16) < TOL
+    # the same projections one at a time
+    for q, A, B, ref in zip(qs, As, Bs, refs):
+        Y = qn.qlora_linear_fwd(q, X.cuda(), A, B, 16.0)
+        qn.device_status()
+        assert tile_max_rel(_f64(Y), ref, 16, 16) < TOL
