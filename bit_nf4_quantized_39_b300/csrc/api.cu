@@ -315,6 +315,14 @@ qn_status launch_decode_group(int n, const qn_nf4 *const *Q, const uint16_t *X, 
   return QN_OK;
 }
 
+// bf16 bits of a finite float, rounded to nearest even (host side).
+uint16_t bf16_bits_rne(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, sizeof(u));
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
 // Where dynamic shared memory starts for a kernel without static shared
 // memory (the few-token kernel addresses its level table with an immediate
 // offset from there).  One launch per device, cached.
@@ -395,6 +403,7 @@ qn_status launch_gemv_group(int n, const qn_nf4 *const *Q, const uint16_t *X, in
   }
   g.rows = rows;
   g.rtot = us;
+  for (int i = 0; i < 16; ++i) g.lev16[i] = bf16_bits_rne(kNF4Levels[i]);
   const int grid = static_cast<int>(sm_count());
   if (!qn::gv_plan(g, grid, esz, any_dq)) return QN_OK;
   g.u = sp.take<float>(static_cast<size_t>(M) * us);

@@ -50,11 +50,13 @@
 
 namespace qn {
 
-constexpr int kGvWarps = 16;
-constexpr int kGvThreads = kGvWarps * 32;
-constexpr int kGvRing = 6;                          // stage slots (kGvRing - 1 in flight)
-constexpr int kGvStageBlocks = 32;                  // 64-blocks per stage (2048 columns)
-constexpr uint32_t kGvStageBytes = 16 * kGvStageBlocks * 32;  // 16 KiB of codes
+constexpr int kGvWarps = 16;                        // consumer warps (MMA)
+constexpr int kGvProducers = 64;                    // producer threads (two warps: stage copies)
+constexpr int kGvThreads = kGvWarps * 32 + kGvProducers;
+constexpr int kGvMaxRing = 8;                       // stage slots at most (the plan picks what fits)
+constexpr int kGvStageBlocks = 64;                  // 64-blocks per stage (4096 columns)
+constexpr uint32_t kGvStageRow = kGvStageBlocks * 32;  // bytes of one row in a stage
+constexpr uint32_t kGvStageBytes = 16 * kGvStageRow;  // 32 KiB of codes
 constexpr int kGvMaxM = 8;
 constexpr int kGvMaxGroup = 8;
 constexpr int kGvMaxXElems = 16384;                 // M * k staged in the table rows
@@ -63,7 +65,6 @@ constexpr int kGvMaxURows = 4;                      // adapter rows per CTA
 constexpr int kGvUVec = 2;                          // 16-byte A loads per lane in flight
 constexpr int kGvMaxU = 2048;                       // M * (adapter rows of the group)
 constexpr uint32_t kGvSmemCap = 227 * 1024;
-constexpr int64_t kGvPrefetchBytes = (kGvRing - 1) * static_cast<int64_t>(kGvStageBytes);  // before the wait
 constexpr unsigned kGvSpinLimit = 1u << 20;         // polls of the ready counter (128 ns apart)
 constexpr int kGvFlagReady = 0, kGvFlagExit = 1;    // zero-area words
 
@@ -82,7 +83,7 @@ struct GvProj {
   float s;
 };
 
-struct GvGroup {
+struct GvGroup {  // the kernel's parameter block (copied to shared memory at entry)
   GvProj p[kGvMaxGroup];
   int n, M;
   int64_t k, rows, rtot;       // shared k, total rows, total adapter rows
@@ -90,10 +91,15 @@ struct GvGroup {
   float *u;                    // M x rtot fp32 (workspace)
   unsigned int *zero_area;     // ready and exit counters, zero between calls
   // shared-memory layout: byte offsets from the start of dynamic shared memory (gv_plan)
-  uint32_t off_ring, off_raw, off_sig, off_rows, off_mw, off_part, off_rsum, off_us, off_ured, off_meta, smem;
+  uint32_t off_ring, off_raw, off_sig, off_rows, off_m, off_part, off_us, off_ured, off_meta, off_bar, smem;
   int rows_cta;                // largest row range of a CTA
+  int ring;                    // stage slots
+  int ms;                      // row stride (floats, odd) of the decoded block constants
+  uint16_t lev16[16];          // bf16 bits of the 16 levels (round to nearest even)
   int bvec;                    // every r is a multiple of 8: B rows read in 16-byte pieces
 };
+
+static_assert(sizeof(GvGroup) % 8 == 0, "parameter block copied in 8-byte pieces");
 
 // A CTA's rows of one projection, with where its block constants and DQ
 // scales sit in shared memory.  Each copy covers the 16-byte-aligned superset
@@ -170,14 +176,19 @@ __device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
 }
+// Arrives on the mbarrier once this thread's earlier cp.async copies have
+// landed (the barrier's count includes this arrival).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 __device__ __forceinline__ uint2 lds_v2(uint32_t a) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
   return v;
 }
-__device__ __forceinline__ uint2 lds_v2_off8k(uint32_t a) {  // 8 rows of a stage further
+__device__ __forceinline__ uint2 lds_v2_off8r(uint32_t a) {  // 8 rows of a stage further
   uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2+8192];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2+16384];" : "=r"(v.x), "=r"(v.y) : "r"(a));
   return v;
 }
 __device__ __forceinline__ uint4 lds_v4(uint32_t a) {
@@ -219,7 +230,9 @@ __device__ __forceinline__ uint32_t gv_x_chunk(uint32_t c, uint32_t t) {
 }
 
 
-// Layout of one launch (host side).  False if the group does not fit.
+// Layout of one launch (host side): the stage ring gets what the rest
+// leaves of the shared memory, 2..kGvMaxRing slots.  False if the group does
+// not fit.
 inline bool gv_plan(GvGroup &g, int grid, int esz_max, bool any_dq) {
   const int64_t k = g.k, nb = k >> 6;
   const int64_t rows_cta = qn_ceil_div(g.rows, grid);
@@ -231,39 +244,42 @@ inline bool gv_plan(GvGroup &g, int grid, int esz_max, bool any_dq) {
   for (int i = 0; i < n; ++i)
     if (g.p[i].r % 8) g.bvec = 0;
   auto a16 = [](int64_t v) { return (v + 15) & ~int64_t{15}; };
-  int64_t off = kGvLutBytes;
-  g.off_ring = static_cast<uint32_t>(off);
-  off += static_cast<int64_t>(kGvRing) * kGvStageBytes;
+  g.ms = static_cast<int>(nb | 1);
+  int64_t off = kGvLutBytes + a16(sizeof(GvGroup));  // the table, then a copy of this block
   g.off_raw = static_cast<uint32_t>(off);
   off += a16(rows_cta * nb * esz_max + 32 * n);
   g.off_sig = static_cast<uint32_t>(off);
   off += any_dq ? a16((rows_cta * nb / 256 + 2 + 8) * 4 * n) : 0;
   g.off_rows = static_cast<uint32_t>(off);
   off += a16(ntl * 16 * static_cast<int64_t>(sizeof(GvRow)));
-  g.off_mw = static_cast<uint32_t>(off);
-  off += static_cast<int64_t>(kGvWarps) * 32 * 4;
+  g.off_m = static_cast<uint32_t>(off);
+  off += a16(ntl * 16 * g.ms * 4);
   g.off_part = static_cast<uint32_t>(off);
-  off += a16(2LL * kGvWarps * 16 * M * 4);
-  g.off_rsum = static_cast<uint32_t>(off);
-  off += a16(ntl * 16 * M * 4);
+  off += a16(ntl * kGvWarps * 16 * M * 4);
   g.off_us = static_cast<uint32_t>(off);
   off += a16(g.rtot * M * 4);
   g.off_ured = static_cast<uint32_t>(off);
   off += a16(static_cast<int64_t>(kGvMaxURows) * kGvWarps * M * 4);
   g.off_meta = static_cast<uint32_t>(off);
   off += a16(sizeof(GvMeta));
-  if (off > kGvSmemCap) return false;
-  g.smem = static_cast<uint32_t>(off);
+  g.off_bar = static_cast<uint32_t>(off);
+  off += a16(2 * kGvMaxRing * 8 + 16);
+  off = (off + 1023) & ~int64_t{1023};
+  const int64_t room = (static_cast<int64_t>(kGvSmemCap) - off) / kGvStageBytes;
+  if (room < 2) return false;
+  g.ring = static_cast<int>(room < kGvMaxRing ? room : kGvMaxRing);
+  g.off_ring = static_cast<uint32_t>(off);
+  g.smem = static_cast<uint32_t>(off + static_cast<int64_t>(g.ring) * kGvStageBytes);
   g.rows_cta = static_cast<int>(rows_cta);
   return true;
 }
 
-// Shared-memory offset of byte x (0..1023) of row r (0..15) of a stage: the
+// Shared-memory offset of byte x (0..2047) of row r (0..15) of a stage: the
 // 16-byte pieces of each 128-byte span are xor-swizzled by r mod 8, so the
 // 8-byte reads of rows g (and g + 8) of one column by eight lane groups hit
 // different banks.
 __device__ __forceinline__ uint32_t gv_stage_off(uint32_t r, uint32_t x) {
-  return r * 1024u + (x & ~127u) + ((((x >> 4) & 7u) ^ (r & 7u)) << 4) + (x & 15u);
+  return r * kGvStageRow + (x & ~127u) + ((((x >> 4) & 7u) ^ (r & 7u)) << 4) + (x & 15u);
 }
 
 // Copies [g0, g0 + len) of an array of `size` bytes to shared memory (16-byte
@@ -271,7 +287,7 @@ __device__ __forceinline__ uint32_t gv_stage_off(uint32_t r, uint32_t x) {
 __device__ __forceinline__ void gv_copy(uint32_t dst, const void *base, int64_t g0, uint32_t len, int64_t size) {
   const char *src = static_cast<const char *>(base) + g0;
   const int64_t avail = size - g0;
-  for (uint32_t c = threadIdx.x * 16u; c < len; c += kGvThreads * 16u) {
+  for (uint32_t c = threadIdx.x * 16u; c < len; c += kGvWarps * 32 * 16u) {  // consumer threads
     const int64_t left = avail - c;
     cp_async16_zfill(dst + c, src + c, static_cast<uint32_t>(left < 16 ? left : 16));
   }
@@ -289,7 +305,7 @@ __device__ __forceinline__ void gv_prefetch(const void *base, int64_t g0, int64_
 
 template <int MT>
 __global__ void __launch_bounds__(kGvThreads, 1)
-qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
+qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
   extern __shared__ __align__(1024) unsigned char gv_raw[];
   pdl_trigger();  // the next call may launch as soon as SMs free up
   // The level table is addressed with an immediate offset: the window must
@@ -300,10 +316,23 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
   }
   unsigned char *base = gv_raw;
   const uint32_t sb = kGvSmemBase;
+  {
+    // The parameter block into shared memory: one parallel read instead of a
+    // chain of constant-cache misses over its ~900 bytes.
+    const uint2 *src = reinterpret_cast<const uint2 *>(&gp);
+    uint2 *dst = reinterpret_cast<uint2 *>(base + kGvLutBytes);
+    for (int i = threadIdx.x; i < static_cast<int>(sizeof(GvGroup) / 8); i += kGvThreads) dst[i] = src[i];
+  }
+  __syncthreads();
+  const GvGroup &g = *reinterpret_cast<const GvGroup *>(base + kGvLutBytes);
   GvMeta &mt = *reinterpret_cast<GvMeta *>(base + g.off_meta);
   GvRow *rows = reinterpret_cast<GvRow *>(base + g.off_rows);
   float *part = reinterpret_cast<float *>(base + g.off_part);
-  float *rsum = reinterpret_cast<float *>(base + g.off_rsum);
+  float *mconst = reinterpret_cast<float *>(base + g.off_m);
+  uint64_t *full = reinterpret_cast<uint64_t *>(base + g.off_bar);  // [kGvMaxRing]: a stage has landed
+  uint64_t *empty = full + kGvMaxRing;                               // [kGvMaxRing]: every warp is done with it
+  uint64_t *upart = empty + kGvMaxRing;                              // the consumers' parts of u are written
+  volatile int *abort = reinterpret_cast<volatile int *>(upart + 1);
   float *us = reinterpret_cast<float *>(base + g.off_us);
   float *ured = reinterpret_cast<float *>(base + g.off_ured);
 
@@ -313,7 +342,15 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
   const int nb = static_cast<int>(k >> 6);
   const int M = g.M;
   const int G = gridDim.x;
-  const int64_t R0 = g.rows * blockIdx.x / G, R1 = g.rows * (blockIdx.x + 1) / G;
+  int64_t R0, R1;  // this CTA's rows [R0, R1) of the group's list
+  if (g.rows < (int64_t{1} << 24)) {
+    const uint32_t rr = static_cast<uint32_t>(g.rows);
+    R0 = rr * blockIdx.x / static_cast<uint32_t>(G);
+    R1 = rr * (blockIdx.x + 1) / static_cast<uint32_t>(G);
+  } else {
+    R0 = g.rows * blockIdx.x / G;
+    R1 = g.rows * (blockIdx.x + 1) / G;
+  }
   const int nrows = static_cast<int>(R1 - R0);
   const int ntl = (nrows + 15) >> 4;
   const int nch = (nb + kGvStageBlocks - 1) / kGvStageBlocks;  // stages per tile
@@ -321,27 +358,24 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
   const int64_t rtot = g.rtot;
   const int nu = static_cast<int>((rtot - blockIdx.x + G - 1) / G);  // adapter rows of this CTA (j = blockIdx + G i)
 
-  // ---- before the wait: segments, L2 prefetch, level table, row table ------------
-  if (tid == 0) {
-    int ns = 0;
-    uint32_t raw = sb + g.off_raw, sig = sb + g.off_sig;
-    for (int i = 0; i < g.n; ++i) mt.p[i] = g.p[i];
-    for (int iu = 0; iu < nu; ++iu) {  // A rows of this CTA's adapter rows
-      const int64_t j = blockIdx.x + static_cast<int64_t>(G) * iu;
-      int pi = 0;
-      for (int i = 1; i < g.n; ++i)
-        if (j >= g.p[i].u_off) pi = i;
-      gv_prefetch(g.p[pi].A, (j - g.p[pi].u_off) * k * 2, k * 2, static_cast<int64_t>(g.p[pi].r) * k * 2);
+  // ---- before the wait: projections and segments (thread i: projection i),
+  // L2 prefetch, level table, row table --------------------------------------------
+  if (warp == 8 && lane < kGvMaxGroup) {
+    const int pj = lane;  // projection
+    const GvProj p = g.p[pj];
+    GvSeg s;
+    s.p = pj;
+    s.lr0 = s.lr1 = 0x7fffffff;  // no rows in this CTA
+    s.ra = s.raw_g0 = s.sig_g0 = 0;
+    s.raw_len = s.sig_len = 0;
+    int64_t a = 0, e = 0;
+    if (pj < g.n) {
+      mt.p[pj] = p;
+      a = R0 > p.row_off ? R0 : p.row_off;
+      e = R1 < p.row_off + p.d ? R1 : p.row_off + p.d;
     }
-    // the first stages' rows
-    const int pre_rows = 16 * ((kGvRing - 1 + nch - 1) / nch);
-    for (int i = 0; i < g.n; ++i) {
-      const GvProj &p = g.p[i];
-      const int64_t a = R0 > p.row_off ? R0 : p.row_off;
-      const int64_t e = R1 < p.row_off + p.d ? R1 : p.row_off + p.d;
-      if (a >= e) continue;
-      GvSeg &s = mt.seg[ns++];
-      s.p = i;
+    const bool has = a < e;
+    if (has) {
       s.lr0 = static_cast<int>(a - R0);
       s.lr1 = static_cast<int>(e - R0);
       s.ra = a - p.row_off;
@@ -350,48 +384,69 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
       const int64_t b0 = s.ra * nb * esz, b1 = (s.ra + nr) * nb * esz;
       s.raw_g0 = b0 & ~int64_t{15};
       s.raw_len = static_cast<uint32_t>(((b1 + 15) & ~int64_t{15}) - s.raw_g0);
-      s.raw_off = raw;
-      raw += s.raw_len;
       if (p.dq) {  // DQ group scales: floats [f0, f1]
         const int64_t f0 = (s.ra * nb) >> 8, f1 = ((s.ra + nr) * nb - 1) >> 8;
         s.sig_g0 = (f0 * 4) & ~int64_t{15};
         s.sig_len = static_cast<uint32_t>((((f1 + 1) * 4 + 15) & ~int64_t{15}) - s.sig_g0);
-      } else {
-        s.sig_g0 = 0;
-        s.sig_len = 0;
       }
-      s.sig_off = sig;
-      sig += s.sig_len;
-      gv_prefetch(p.consts, s.raw_g0, s.raw_len, p.d * nb * esz);
-      if (p.dq) gv_prefetch(p.absmax_scale, s.sig_g0, s.sig_len, ((p.d * nb + 255) >> 8) * 4);
-      gv_prefetch(p.B, (s.ra * p.r * 2) & ~int64_t{15}, nr * p.r * 2 + 16, p.d * p.r * 2);
-      const int64_t pr = pre_rows - s.lr0;
-      if (pr > 0) gv_prefetch(p.codes, s.ra * kh, (pr < nr ? pr : nr) * kh, p.d * kh);
     }
-    mt.nseg = ns;
+    // shared-memory places of the copies: exclusive prefix sums over projections
+    uint32_t rx = 0, sx = 0;
+#pragma unroll
+    for (int j = 0; j < kGvMaxGroup; ++j) {
+      const uint32_t rl = __shfl_sync(0xffu, s.raw_len, j), sl = __shfl_sync(0xffu, s.sig_len, j);
+      if (j < pj) {
+        rx += rl;
+        sx += sl;
+      }
+    }
+    s.raw_off = sb + g.off_raw + rx;
+    s.sig_off = sb + g.off_sig + sx;
+    mt.seg[pj] = s;
+    if (pj == 0) mt.nseg = g.n;
   }
-  // table entry b of lane l: bf16(level[b & 15]) | bf16(level[b >> 4]) << 16
-  for (int e = tid; e < 256 * 32; e += kGvThreads) {
-    const int b = e >> 5;
-    *reinterpret_cast<uint32_t *>(base + b * 256 + (e & 31) * 4) =
-        pack_bf16x2(c_nf4_levels[b & 15], c_nf4_levels[b >> 4]);
+  if (warp == 9 && lane == 0) {
+    for (int i = 0; i < kGvMaxRing; ++i) {
+      mbar_init(smem_u32(&full[i]), kGvProducers);
+      mbar_init(smem_u32(&empty[i]), kGvWarps);
+    }
+    mbar_init(smem_u32(upart), 1);
+    *abort = 0;
+    mbar_fence_init();
+  }
+  if (tid < 256) {
+    // table entry b: bf16(level[b & 15]) | bf16(level[b >> 4]) << 16, written by
+    // thread b into all 32 lane slots of row b (16-byte stores in a rotated
+    // order, so that eight neighbouring threads hit different banks)
+    const uint32_t lv = g.lev16[lane & 15];
+    const uint32_t v = __shfl_sync(0xffffffffu, lv, tid & 15) | (__shfl_sync(0xffffffffu, lv, tid >> 4) << 16);
+    const uint4 v4 = make_uint4(v, v, v, v);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4 *>(base + tid * 256 + 16 * ((q + tid) & 7)) = v4;
   }
   __syncthreads();
+  if (tid >= 32 && tid < 32 + nu) {  // A rows of this CTA's adapter rows into L2
+    const int64_t j = blockIdx.x + static_cast<int64_t>(G) * (tid - 32);
+    int pi = 0;
+    for (int i = 1; i < mt.nseg; ++i)
+      if (j >= mt.p[i].u_off) pi = i;
+    gv_prefetch(mt.p[pi].A, (j - mt.p[pi].u_off) * k * 2, k * 2, static_cast<int64_t>(mt.p[pi].r) * k * 2);
+  }
   for (int lr = tid; lr < ntl * 16; lr += kGvThreads) {
     // padding rows of the last tile read the first row's codes (their block
     // constants are 0)
     const bool pad = lr >= nrows;
     const int lq = pad ? 0 : lr;
     int si = 0;
-    for (int i = 1; i < mt.nseg; ++i)
-      if (lq >= mt.seg[i].lr0) si = i;
+    for (int i = 0; i < mt.nseg; ++i)
+      if (lq >= mt.seg[i].lr0 && lq < mt.seg[i].lr1) si = i;
     const GvSeg &s = mt.seg[si];
     const GvProj &p = mt.p[s.p];
-    const int64_t prow = s.ra + (lq - s.lr0);
-    const int64_t e0 = prow * nb;  // first block of the row
+    const int prow = static_cast<int>(s.ra) + (lq - s.lr0);
+    const int64_t e0 = static_cast<int64_t>(prow) * nb;  // first block of the row
     GvRow rw;
     rw.code = p.codes + prow * kh;
-    rw.prow = static_cast<int>(prow);
+    rw.prow = prow;
     rw.p = static_cast<signed char>(s.p);
     rw.dq = pad ? static_cast<signed char>(-1) : static_cast<signed char>(p.dq);
     rw.e0 = static_cast<short>(e0 & 255);
@@ -402,42 +457,99 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
   __syncthreads();
   pdl_wait_grid();
 
-  // ---- after the wait: small copies (one group), then the first stages ----------
+  // ---- after the wait -----------------------------------------------------------
   const uint32_t kc = static_cast<uint32_t>(k >> 3);  // 16-byte chunks per token
+  const uint32_t ring = sb + g.off_ring;
+  const int R = g.ring;
+  if (warp >= kGvWarps) {
+    // ================================ producers =================================
+    // Stages in order (tile, chunk) into slots 0, 1, ... R - 1, 0, ...: thread
+    // p copies the 16-byte columns 16 p and 16 p + 1024 of the chunk's 2048
+    // bytes of all 16 rows, then arrives on the slot's full barrier once its
+    // copies land.
+    const uint32_t x = static_cast<uint32_t>(tid - kGvWarps * 32) << 4;
+    // The second producer warp adds the consumers' parts of this CTA's
+    // adapter rows (in warp order) and publishes them once the ring is full;
+    // its fence then stalls no consumer.
+    bool published = warp != kGvWarps + 1 || nu == 0;
+    auto publish = [&]() {
+      published = true;
+      if (!mbar_wait(smem_u32(upart), 0, abort)) return;
+      if (lane < nu * M) {
+        const int iu = lane / M, t = lane - iu * M;
+        const int64_t j = blockIdx.x + static_cast<int64_t>(G) * iu;
+        int pi = 0;
+        for (int i = 1; i < g.n; ++i)
+          if (j >= mt.p[i].u_off) pi = i;
+        float v = 0.f;
+        for (int w = 0; w < kGvWarps; ++w) v += ured[(iu * kGvWarps + w) * M + t];
+        g.u[t * rtot + j] = mt.p[pi].s * v;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        atomicAdd(&g.zero_area[kGvFlagReady], static_cast<unsigned>(nu));
+      }
+    };
+    int tl = 0, ch = 0;
+    for (int s = 0; s < nst; ++s) {
+      if (s == R && !published) publish();
+      const int slot = s % R;
+      if (s >= R && !mbar_wait(smem_u32(&empty[slot]), ((s / R) - 1) & 1, abort)) break;
+      const int cbl = (nb - ch * kGvStageBlocks) < kGvStageBlocks ? nb - ch * kGvStageBlocks : kGvStageBlocks;
+      const uint32_t dst = ring + static_cast<uint32_t>(slot) * kGvStageBytes;
+      const int64_t co = static_cast<int64_t>(ch) * kGvStageRow;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t xh = x + 1024u * h;
+        if (xh < static_cast<uint32_t>(cbl) * 32u) {
+#pragma unroll 4
+          for (int r = 0; r < 16; ++r) cp_async16(dst + gv_stage_off(r, xh), rows[tl * 16 + r].code + co + xh);
+        }
+      }
+      cp_async_mbar_arrive(smem_u32(&full[slot]));
+      if (++ch == nch) {
+        ch = 0;
+        ++tl;
+      }
+    }
+    if (!published) publish();
+    cp_async_wait_all();
+    if (warp == kGvWarps) {
+      // While the consumers finish: wait (bounded) until every CTA has
+      // published its rows of u, then stage u; the final barrier hands it over.
+      if (lane == 0) {
+        unsigned int spins = 0;
+        while (gv_ld_acquire(&g.zero_area[kGvFlagReady]) < static_cast<unsigned>(rtot)) {
+          if (++spins > kGvSpinLimit) {
+            qn_flag_timeout();
+            break;
+          }
+          __nanosleep(128);
+        }
+      }
+      __syncwarp();
+#pragma unroll 4
+      for (int e = lane; e < rtot * M; e += 32) us[e] = ld_cg_f32(g.u + e);
+    }
+  } else {
+  // ================================ consumers ===================================
+  // small copies: X (swizzled into the table rows), block constants, DQ scales
   for (int t = 0; t < M; ++t)
-    for (uint32_t v = tid; v < kc; v += kGvThreads)
+    for (uint32_t v = tid; v < kc; v += kGvWarps * 32)
       cp_async16(sb + gv_x_chunk(t * kc + v, t), g.X + static_cast<int64_t>(t) * k + v * 8);
   for (int i = 0; i < mt.nseg; ++i) {
     const GvSeg &s = mt.seg[i];
+    if (s.lr0 >= s.lr1) continue;
     const GvProj &p = mt.p[s.p];
     gv_copy(s.raw_off, p.consts, s.raw_g0, s.raw_len, p.d * nb * (p.dq ? 1 : 4));
     if (p.dq) gv_copy(s.sig_off, p.absmax_scale, s.sig_g0, s.sig_len, ((p.d * nb + 255) >> 8) * 4);
   }
   cp_async_commit();
-  // Stage s (tile s / nch, chunk s % nch) into slot s % kGvRing: thread i
-  // copies 16-byte pieces i and i + 512 of the stage (row = piece / 64).
-  const uint32_t ring = sb + g.off_ring;
-  auto issue_stage = [&](int s) {
-    if (s < nst) {
-      const int tl = s / nch, ch = s - tl * nch;
-      const int cbl = (nb - ch * kGvStageBlocks) < kGvStageBlocks ? nb - ch * kGvStageBlocks : kGvStageBlocks;
-      const uint32_t slot = ring + static_cast<uint32_t>(s % kGvRing) * kGvStageBytes;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int pc = tid + h * kGvThreads;  // piece 0..1023
-        const int r = pc >> 6, x = (pc & 63) << 4;
-        if (x < cbl * 32)
-          cp_async16(slot + gv_stage_off(r, x), rows[tl * 16 + r].code + ch * (kGvStageBlocks * 32) + x);
-      }
-    }
-    cp_async_commit();
-  };
-#pragma unroll 1
-  for (int s = 0; s < kGvRing - 1; ++s) issue_stage(s);
   // adapter rows of this CTA: warp slice [v0, v1) of the k / 8 vectors
   const int v0 = static_cast<int>(kc * warp / kGvWarps), v1 = static_cast<int>(kc * (warp + 1) / kGvWarps);
-  uint4 av[kGvUVec];
-  auto load_a = [&](int iu, int bt) {
+  uint4 av0[kGvUVec], av1[kGvUVec];  // A pieces of two adapter rows
+  auto load_a = [&](uint4 (&av)[kGvUVec], int iu, int bt) {
     const int64_t j = blockIdx.x + static_cast<int64_t>(G) * iu;
     int pi = 0;
     for (int i = 1; i < g.n; ++i)
@@ -449,20 +561,65 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
       av[i] = (v < v1) ? ld_cg_v4(arow + static_cast<int64_t>(v) * 8) : make_uint4(0u, 0u, 0u, 0u);
     }
   };
-  if (nu > 0) load_a(0, 0);
+  if (nu > 0) load_a(av0, 0, 0);
+  if (nu > 1) load_a(av1, 1, 0);
   if (tid < g.n) mt.mu[tid] = mt.p[tid].dq ? ld_cg_f32(mt.p[tid].absmax_mean) : 0.f;
-  cp_async_wait_group<kGvRing - 1>();  // the small copies
-  __syncthreads();
+  cp_async_wait_all();  // the small copies
+  asm volatile("bar.sync 1, %0;" ::"n"(kGvWarps * 32) : "memory");
+  // block constants of the range, decoded once into mconst[lr * ms + b]: warp
+  // w takes rows w, w + 16, ...; when nb is a multiple of 4, lane c takes
+  // blocks 4c .. 4c + 3 of the row (one 32-bit read of DQ codes: a row starts
+  // at a multiple of 4 blocks, so the four share one 256-block DQ group; or
+  // one 16-byte read of fp32 constants), else one block at a time.
+  const bool by4 = (nb & 3) == 0;
+#pragma unroll 4
+  for (int lr = warp; lr < ntl * 16; lr += kGvWarps) {
+    const GvRow &rw = rows[lr];
+    float *mr = mconst + lr * g.ms;
+    if (!by4) {
+      for (int b = lane; b < nb; b += 32) {
+        float m = 0.f;
+        if (rw.dq > 0) {
+          const int8_t q = *reinterpret_cast<const int8_t *>(base + (rw.raw - kGvSmemBase) + b);
+          const float sg = *reinterpret_cast<const float *>(base + (rw.sig - kGvSmemBase) + ((rw.e0 + b) >> 8) * 4);
+          m = dq_absmax(q, sg, mt.mu[rw.p]);
+        } else if (rw.dq == 0) {
+          m = *reinterpret_cast<const float *>(base + (rw.raw - kGvSmemBase) + b * 4);
+        }
+        mr[b] = m;
+      }
+      continue;
+    }
+    for (int c = lane; 4 * c < nb; c += 32) {
+      float m[4] = {0.f, 0.f, 0.f, 0.f};
+      if (rw.dq > 0) {
+        const uint32_t wq = *reinterpret_cast<const uint32_t *>(base + (rw.raw - kGvSmemBase) + 4 * c);
+        const float sg = *reinterpret_cast<const float *>(base + (rw.sig - kGvSmemBase) + ((rw.e0 + 4 * c) >> 8) * 4);
+        const float mu = mt.mu[rw.p];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) m[j] = dq_absmax(static_cast<int8_t>((wq >> (8 * j)) & 0xFFu), sg, mu);
+      } else if (rw.dq == 0) {
+        const uint4 wf = *reinterpret_cast<const uint4 *>(base + (rw.raw - kGvSmemBase) + 16 * c);
+        m[0] = __uint_as_float(wf.x);
+        m[1] = __uint_as_float(wf.y);
+        m[2] = __uint_as_float(wf.z);
+        m[3] = __uint_as_float(wf.w);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mr[4 * c + j] = m[j];
+    }
+  }
 
   {
     const int span = v1 - v0;
     const int nbt = span > 0 ? (span + 32 * kGvUVec - 1) / (32 * kGvUVec) : 1;
-    for (int iu = 0; iu < nu; ++iu) {
+    // this warp's part of u[t, j] for adapter row j = blockIdx + G iu, into ured
+    auto u_row = [&](uint4 (&av)[kGvUVec], int iu) {
       float ua[MT];
 #pragma unroll
       for (int t = 0; t < MT; ++t) ua[t] = 0.f;
       for (int bt = 0; bt < nbt; ++bt) {
-        if (iu > 0 || bt > 0) load_a(iu, bt);
+        if (bt > 0) load_a(av, iu, bt);
 #pragma unroll
         for (int i = 0; i < kGvUVec; ++i) {
           const int v = v0 + lane + 32 * (bt * kGvUVec + i);
@@ -491,109 +648,97 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
         for (int t = 0; t < MT; ++t)
           if (t < M) ured[(iu * kGvWarps + warp) * M + t] = ua[t];
       }
+    };
+    for (int iu = 0; iu < nu; iu += 2) {
+      if (iu >= 2) {
+        load_a(av0, iu, 0);
+        if (iu + 1 < nu) load_a(av1, iu + 1, 0);
+      }
+      u_row(av0, iu);
+      if (iu + 1 < nu) u_row(av1, iu + 1);
     }
   }
-  __syncthreads();
-  if (warp == 0 && nu > 0) {
-    // warp 0 finishes this CTA's adapter rows; the other warps go on
-    if (lane < nu * M) {
-      const int iu = lane / M, t = lane - iu * M;
-      const int64_t j = blockIdx.x + static_cast<int64_t>(G) * iu;
-      int pi = 0;
-      for (int i = 1; i < g.n; ++i)
-        if (j >= mt.p[i].u_off) pi = i;
-      float v = 0.f;
-      for (int w = 0; w < kGvWarps; ++w) v += ured[(iu * kGvWarps + w) * M + t];
-      g.u[t * rtot + j] = mt.p[pi].s * v;
-    }
-    __syncwarp();
-    if (lane == 0) {
-      __threadfence();
-      atomicAdd(&g.zero_area[kGvFlagReady], static_cast<unsigned>(nu));
-    }
-  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kGvWarps * 32) : "memory");
+  if (tid == 0) mbar_arrive(smem_u32(upart));  // the second producer warp finishes and publishes them
 
-  // ---- weight loop: one barrier per stage ---------------------------------------
-  float *mw = reinterpret_cast<float *>(base + g.off_mw) + warp * 32;  // [block 0/1][16 rows]
-  const uint32_t mw_s = smem_u32(mw) + static_cast<uint32_t>(gq) * 4u;
+  // ---- weight loop: wait for a stage, consume blocks warp + 16 j, j = 0..3 ---------
   const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
-  const uint32_t xb0 = sb + gv_x_chunk(gq * kc + 2u * tq, gq);
-  const uint32_t xb1 = sb + gv_x_chunk(gq * kc + 2u * tq + 1u, gq);
-  // tile sums: warp tl mod 16 adds the 16 warps' partials of tile tl in warp order
-  auto reduce_tile = [&](int tl) {
-    const float *pb = part + (tl & 1) * (kGvWarps * 16 * M);
-    for (int e = lane; e < 16 * M; e += 32) {
-      float v = 0.f;
+  // this lane's code bytes of block `warp`, row gq (block warp + 16 j: +512 j; row gq + 8: +16384)
+  const uint32_t cofs = gv_stage_off(static_cast<uint32_t>(gq), static_cast<uint32_t>(warp * 32 + tq * 8));
+  // x of token gq, elements 64 warp + 16 tq .. + 15 (block warp + 16 j: +4096 j bytes)
+  const uint32_t xw0 = sb + gv_x_chunk(gq * kc + 2u * tq, gq) + (static_cast<uint32_t>(warp) << 8);
+  const uint32_t xw1 = sb + gv_x_chunk(gq * kc + 2u * tq + 1u, gq) + (static_cast<uint32_t>(warp) << 8);
+  const bool xtok = gq < M;
+  auto lut8 = [&](uint2 c, uint32_t (&a)[8]) {
 #pragma unroll
-      for (int w = 0; w < kGvWarps; ++w) v += pb[w * 16 * M + e];
-      rsum[tl * 16 * M + e] = v;
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t sel = 0x5504u | (static_cast<uint32_t>(i) << 4);
+      a[i] = lds_lut(gv_lut_off(c.x, lane4, sel));
+      a[4 + i] = lds_lut(gv_lut_off(c.y, lane4, sel));
     }
   };
+  const uint32_t mrow = static_cast<uint32_t>(16 * g.ms * 4);  // bytes per tile of decoded constants
+  uint32_t mb0 = smem_u32(mconst) + static_cast<uint32_t>(gq * g.ms * 4) + static_cast<uint32_t>(warp * 4);
+  uint32_t mb1 = mb0 + static_cast<uint32_t>(8 * g.ms * 4);
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  bool ok = true;
+  int tl = 0, ch = 0;
 #pragma unroll 1
   for (int s = 0; s < nst; ++s) {
-    cp_async_wait_group<kGvRing - 2>();  // this thread's pieces of stage s
-    __syncthreads();                     // every piece of stage s; the slot of stage s - 1 is free
-    issue_stage(s + kGvRing - 1);
-    const int tl = s / nch, ch = s - tl * nch;
-    const int cbl = (nb - ch * kGvStageBlocks) < kGvStageBlocks ? nb - ch * kGvStageBlocks : kGvStageBlocks;
-    if (ch == 0 && tl > 0 && warp == ((tl - 1) & (kGvWarps - 1))) reduce_tile(tl - 1);
-    {
-      // block constant of row lane mod 16, block warp + 16 (lane / 16) of this stage
-      const int rr = lane & 15, blk = warp + 16 * (lane >> 4);
-      const GvRow &rw = rows[tl * 16 + rr];
-      float m = 0.f;
-      if (blk < cbl && rw.dq >= 0) {
-        const int b = ch * kGvStageBlocks + blk;
-        if (rw.dq) {
-          const int8_t q = *reinterpret_cast<const int8_t *>(base + (rw.raw - kGvSmemBase) + b);
-          const float sg = *reinterpret_cast<const float *>(base + (rw.sig - kGvSmemBase) + ((rw.e0 + b) >> 8) * 4);
-          m = dq_absmax(q, sg, mt.mu[rw.p]);
-        } else {
-          m = *reinterpret_cast<const float *>(base + (rw.raw - kGvSmemBase) + b * 4);
+    const int slot = s % R;
+    if (ok) ok = mbar_wait(smem_u32(&full[slot]), (s / R) & 1, abort);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      const int cbl = (nb - ch * kGvStageBlocks) < kGvStageBlocks ? nb - ch * kGvStageBlocks : kGvStageBlocks;
+      const uint32_t ca = ring + static_cast<uint32_t>(slot) * kGvStageBytes + cofs;
+      const uint32_t xo = static_cast<uint32_t>(ch) << 14;  // 64 blocks of 256 bytes per chunk
+      const uint32_t mo = static_cast<uint32_t>(ch * kGvStageBlocks) * 4u;
+#pragma unroll
+      for (int jp = 0; jp < 4; jp += 2) {
+        // blocks warp + 16 jp and warp + 16 (jp + 1) side by side; a block past
+        // the chunk's end reads in-bounds leftovers of the slot with x = 0, m = 0
+        const bool v0 = warp + 16 * jp < cbl, v1 = warp + 16 * (jp + 1) < cbl;
+        if (!v0) break;  // the same in the whole warp
+        const uint32_t cj = ca + 512u * jp;
+        const uint2 c00 = lds_v2(cj), c01 = lds_v2_off8r(cj), c10 = lds_v2(cj + 512u), c11 = lds_v2_off8r(cj + 512u);
+        uint4 x00 = make_uint4(0u, 0u, 0u, 0u), x01 = x00, x10 = x00, x11 = x00;
+        const uint32_t xj = xo + 4096u * jp;
+        if (xtok) {
+          x00 = lds_v4(xw0 + xj);
+          x01 = lds_v4(xw1 + xj);
+          if (v1) {
+            x10 = lds_v4(xw0 + xj + 4096u);
+            x11 = lds_v4(xw1 + xj + 4096u);
+          }
         }
+        const uint32_t mj = mo + 64u * jp;
+        const float m00 = lds_f32(mb0 + mj), m01 = lds_f32(mb1 + mj);
+        const float m10 = v1 ? lds_f32(mb0 + mj + 64u) : 0.f, m11 = v1 ? lds_f32(mb1 + mj + 64u) : 0.f;
+        uint32_t a0[8], a1[8], b0[8], b1[8];  // bf16 pairs: block 0 rows g, g + 8; block 1 rows g, g + 8
+        lut8(c00, a0);
+        lut8(c01, a1);
+        lut8(c10, b0);
+        lut8(c11, b1);
+        float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+        gv_mma(d, a0[0], a1[0], a0[1], a1[1], x00.x, x00.y);
+        gv_mma(e, b0[0], b1[0], b0[1], b1[1], x10.x, x10.y);
+        gv_mma(d, a0[2], a1[2], a0[3], a1[3], x00.z, x00.w);
+        gv_mma(e, b0[2], b1[2], b0[3], b1[3], x10.z, x10.w);
+        gv_mma(d, a0[4], a1[4], a0[5], a1[5], x01.x, x01.y);
+        gv_mma(e, b0[4], b1[4], b0[5], b1[5], x11.x, x11.y);
+        gv_mma(d, a0[6], a1[6], a0[7], a1[7], x01.z, x01.w);
+        gv_mma(e, b0[6], b1[6], b0[7], b1[7], x11.z, x11.w);
+        acc[0] = fmaf(e[0], m10, fmaf(d[0], m00, acc[0]));
+        acc[1] = fmaf(e[1], m10, fmaf(d[1], m00, acc[1]));
+        acc[2] = fmaf(e[2], m11, fmaf(d[2], m01, acc[2]));
+        acc[3] = fmaf(e[3], m11, fmaf(d[3], m01, acc[3]));
       }
-      __syncwarp();
-      mw[(lane >> 4) * 16 + rr] = m;
-      __syncwarp();
     }
-    const uint32_t slot = ring + static_cast<uint32_t>(s % kGvRing) * kGvStageBytes;
-#pragma unroll
-    for (int bi = 0; bi < 2; ++bi) {
-      const int blk = warp + 16 * bi;
-      if (blk >= cbl) break;
-      const uint32_t ca = slot + gv_stage_off(static_cast<uint32_t>(gq), static_cast<uint32_t>(blk * 32 + tq * 8));
-      const uint2 c0 = lds_v2(ca), c1 = lds_v2_off8k(ca);
-      uint32_t a0[8], a1[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t sel = 0x5504u | (static_cast<uint32_t>(i) << 4);
-        a0[i] = lds_lut(gv_lut_off(c0.x, lane4, sel));
-        a0[4 + i] = lds_lut(gv_lut_off(c0.y, lane4, sel));
-        a1[i] = lds_lut(gv_lut_off(c1.x, lane4, sel));
-        a1[4 + i] = lds_lut(gv_lut_off(c1.y, lane4, sel));
-      }
-      uint4 x0 = make_uint4(0u, 0u, 0u, 0u), x1 = x0;
-      if (gq < M) {
-        const uint32_t xo = static_cast<uint32_t>(ch * kGvStageBlocks + blk) << 8;
-        x0 = lds_v4(xb0 + xo);
-        x1 = lds_v4(xb1 + xo);
-      }
-      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-      gv_mma(d0, a0[0], a1[0], a0[1], a1[1], x0.x, x0.y);
-      gv_mma(d1, a0[2], a1[2], a0[3], a1[3], x0.z, x0.w);
-      gv_mma(d0, a0[4], a1[4], a0[5], a1[5], x1.x, x1.y);
-      gv_mma(d1, a0[6], a1[6], a0[7], a1[7], x1.z, x1.w);
-      const uint32_t mo = mw_s + static_cast<uint32_t>(bi) * 64u;
-      const float m0 = lds_f32(mo), m1 = lds_f32_off32(mo);
-      acc[0] = fmaf(d0[0] + d1[0], m0, acc[0]);
-      acc[1] = fmaf(d0[1] + d1[1], m0, acc[1]);
-      acc[2] = fmaf(d0[2] + d1[2], m1, acc[2]);
-      acc[3] = fmaf(d0[3] + d1[3], m1, acc[3]);
-    }
-    if (ch == nch - 1) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));  // this warp is done with the slot
+    if (++ch == nch) {
       // end of tile tl: this warp's partial sums
-      float *pw = part + (tl & 1) * (kGvWarps * 16 * M) + warp * 16 * M;
+      float *pw = part + (tl * kGvWarps + warp) * 16 * M;
       if (2 * tq < M) {
         pw[gq * M + 2 * tq] = acc[0];
         pw[(gq + 8) * M + 2 * tq] = acc[2];
@@ -603,9 +748,13 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
         pw[(gq + 8) * M + 2 * tq + 1] = acc[3];
       }
       acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+      ch = 0;
+      ++tl;
+      mb0 += mrow;
+      mb1 += mrow;
     }
   }
-  cp_async_wait_all();
+  }  // consumers
 
   // ---- adapter terms and output -------------------------------------------------
   // Thread lr takes row lr of the range: the first 64 values of its B row are
@@ -619,23 +768,8 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
 #pragma unroll
     for (int c = 0; c < 8; ++c) bq[c] = (8 * c < p.r) ? ld_cg_v4(br + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
   }
-  __syncthreads();  // every partial sum written
-  if (ntl > 0 && warp == ((ntl - 1) & (kGvWarps - 1))) reduce_tile(ntl - 1);
-  if (tid == 0) {
-    unsigned int spins = 0;
-    while (gv_ld_acquire(&g.zero_area[kGvFlagReady]) < static_cast<unsigned>(rtot)) {
-      if (++spins > kGvSpinLimit) {
-        qn_flag_timeout();
-        break;
-      }
-      __nanosleep(128);
-    }
-    __threadfence();
-  }
-  __syncthreads();
-  for (int e = tid; e < rtot * M; e += kGvThreads) us[e] = ld_cg_f32(g.u + e);
-  __syncthreads();
-  // Y = row sum + u . B[row]
+  __syncthreads();  // every partial sum written; u staged
+  // Y = (partial sums of the warps, in warp order) + u . B[row]
   for (int lr = tid; lr < nrows; lr += kGvThreads) {
     const GvRow &rw = rows[lr];
     const GvProj &p = mt.p[rw.p];
@@ -674,10 +808,14 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup g) {
         }
       }
     }
+    const int tl = lr >> 4, r16 = lr & 15;
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
       if (t >= M) break;
-      p.Y[t * p.d + rw.prow] = f32_to_bf16_bits(rsum[lr * M + t] + (a[t][0] + a[t][1]));
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kGvWarps; ++w) v += part[((tl * kGvWarps + w) * 16 + r16) * M + t];
+      p.Y[t * p.d + rw.prow] = f32_to_bf16_bits(v + (a[t][0] + a[t][1]));
     }
   }
   // the last CTA to get here returns the counters to zero
