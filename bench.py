@@ -49,6 +49,26 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
 
+# DRAM bytes (read + write) per launch of qlora_gemv_kernel for each kind of
+# decode call, from one ncu capture (`ncu --set full --clock-control none -k
+# regex:qlora_gemv -s 4 -c 4 python bench.py --profile decode`).  They hold
+# for the kernel source they were taken on (its sha256); for any other source
+# the bench reports traffic as null.
+GEMV_TRAFFIC_SHA256 = "e51a7232ed24ad3ad4b973a75c64aa6a9b4552cb2d8467858abfcfac7eecac2b"
+GEMV_TRAFFIC = {"qkv": 29217792, "o": 9809664, "gate_up": 50492160 + 124672, "down": 25313024}
+
+
+def gemv_traffic(per_kind):
+    """Launch-weighted DRAM bytes per launch, or None if the kernel changed."""
+    import hashlib
+    src = os.path.join(ROOT, "bit_nf4_quantized_39_b300", "csrc", "qlora_gemv.cuh")
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != GEMV_TRAFFIC_SHA256:
+            return None
+    n = sum(v["launches"] for v in per_kind.values())
+    return sum(GEMV_TRAFFIC[k] * v["launches"] for k, v in per_kind.items()) / n
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -555,15 +575,16 @@ def main():
     w4, lora, act = decode_bytes(mats, 1, r)
     value = job_value(w4, args.steps, ws, total_ms)
 
-    # roofline of the dominant kernel (qlora_decode_kernel, one launch per
+    # roofline of the dominant kernel (qlora_gemv_kernel, one launch per
     # call): algorithmic bytes per launch / mean CUDA-event launch duration,
     # weighted over the four kinds of call of a decode step.
     tot_bytes = sum(v["bytes"] * v["launches"] for v in res["per_kind"].values())
     tot_s = sum(v["us"] * 1e-6 * v["launches"] for v in res["per_kind"].values())
     achieved = tot_bytes / tot_s / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "traffic": None,
-                "kernel": "qlora_decode_kernel (M=1; 4-bit weight + LoRA A, B + x + y bytes per launch)",
+                "frac": achieved / pk["hbm_gbs"], "traffic": gemv_traffic(res["per_kind"]),
+                "kernel": "qlora_gemv_kernel (M=1; 4-bit weight + block constants + LoRA A, B + x + y bytes "
+                          "per launch)",
                 "peak_source": pk["source"], "per_call": res["per_kind"]}
     e2e = {"value": w4 * res["e2e_steps"] / (res["e2e_ms"] * 1e-3) / 1e9, "unit": "GB/s",
            "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
@@ -590,12 +611,13 @@ def main():
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                 "data": "synthetic (seeded device draws: N(0,0.02^2) weights with 0.1% N(0,0.2^2) outliers)",
                 "config": {"workload": WORKLOAD, "M": 1, "layers": args.layers, "matrices": 7 * args.layers,
                            "weight_bytes_per_step": w4, "lora_bytes_per_step": lora,
                            "l2": "no flush: 3.34 GB weight set per step >> 126 MB L2",
-                           "arith": "fp32 FMA of NF4 levels (fp32) with bf16 x, fp32 accumulation; bf16 y",
+                           "arith": "NF4 levels as bf16 (byte-pair table) x bf16 x on mma.sync, fp32 block "
+                                    "sums scaled by fp32 block constants, fp32 accumulation; bf16 y",
                            "parallelism": f"replica x{ws}"},
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": res["launches_per_step"] * args.steps, "clocks": clocks, "secondary": extra}
