@@ -430,7 +430,8 @@ def profile_case(case: str):
     """Untimed runs for ncu: `decode` / `decode16` = one layer of the decode set
     (4 calls: q/k/v, o, gate/up, down) at M = 1 / 16, three times; `prefill` =
     the prefill layer forward and backward, three times; `loftq` = one LoftQ
-    alternation (T = 1, r = 16) of a 1024 x 1024 matrix, twice; `quantize` =
+    alternation (T = 1, r = 16) of a 1024 x 1024 matrix, twice (`loftq4096`: of
+    a 4096 x 4096 matrix, once); `quantize` =
     NF4+DQ quantise and dequantise of one 11008 x 4096 bf16 matrix, three times."""
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
@@ -454,9 +455,10 @@ def profile_case(case: str):
         for _ in range(3):
             qn.qlora_linear_fwd(q, X, A, B, 32.0)
             qn.qlora_linear_bwd_dx(q, dY, A, B, 32.0)
-    elif case == "loftq":
-        W = torch.from_numpy(synth.loftq_case(seed=4, d=1024, k=1024)).to(device)
-        for _ in range(2):
+    elif case in ("loftq", "loftq4096"):
+        n = 1024 if case == "loftq" else 4096
+        W = torch.from_numpy(synth.loftq_case(seed=4, d=n, k=n)).to(device)
+        for _ in range(2 if case == "loftq" else 1):
             qn.loftq_init(W, r=16, alpha=16.0, T=1, seed=0, oversample=8, power_iters=4)
     else:
         gen = torch.Generator(device=device)
@@ -546,7 +548,7 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--quick", action="store_true", help="shorter secondary loops")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["decode", "decode16", "prefill", "quantize", "loftq"],
+    ap.add_argument("--profile", choices=["decode", "decode16", "prefill", "quantize", "loftq", "loftq4096"],
                     help="run one small case of a workload a few times, untimed (for ncu captures)")
     args = ap.parse_args()
     ws, rank, local = dist_env()

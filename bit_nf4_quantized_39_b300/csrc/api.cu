@@ -112,6 +112,9 @@ size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 // call on that workspace; every kernel that uses them returns them to zero
 // before it exits.  Every other scratch buffer lives after it.
 constexpr size_t kSemBytes = 256 * 1024;
+// Word of the zero area where the LoftQ CholeskyQR2 kernel keeps its two
+// grid-barrier counters (word 0 is the quantiser's ticket).
+constexpr int kLqBarWord = 32;
 
 qn_status check_nf4(const qn_nf4 *Q, bool need_dq_ptrs) {
   if (!Q) return fail(QN_EINVAL, "Q is NULL");
@@ -165,16 +168,42 @@ qn_status launch_quantize(const void *W, qn_dtype wdt, const qn_nf4 *Q, unsigned
     QN_LAUNCH_CHECK("nf4_quant_tail_kernel");
   }
   {
-    const int64_t bpc = (qn::kQuantThreads / 32) * 4;  // blocks per CTA-iteration (8 lanes per block)
-    int64_t grid = qn_ceil_div(nfull, bpc);
-    const int64_t cap = static_cast<int64_t>(sms) * 4;  // resident CTAs (registers, 31 KB of shared tables)
+    // Stages of 1 KiB of input, one per warp-iteration; two CTAs per SM
+    // (80 KiB of copy ring and 31 KiB of tables each).
+    const int64_t bps = (wdt == QN_F32) ? 4 : 8;
+    const int64_t nst = qn_ceil_div(nfull, bps);
+    int64_t grid = qn_ceil_div(nst, qn::kQuantWarps);
+    const int64_t cap = static_cast<int64_t>(sms) * 2;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
+    QN_TRY(cuda_check((wdt == QN_F32)
+                          ? cudaFuncSetAttribute(qn::nf4_quant_kernel<float>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, qn::kQuantSmem)
+                          : cudaFuncSetAttribute(qn::nf4_quant_kernel<__nv_bfloat16>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, qn::kQuantSmem),
+                      "cudaFuncSetAttribute(quantiser smem)"));
+    // Two CTAs of 112 KiB per SM only fit with the largest shared-memory carveout.
+    QN_TRY(cuda_check((wdt == QN_F32)
+                          ? cudaFuncSetAttribute(qn::nf4_quant_kernel<float>,
+                                                 cudaFuncAttributePreferredSharedMemoryCarveout, 100)
+                          : cudaFuncSetAttribute(qn::nf4_quant_kernel<__nv_bfloat16>,
+                                                 cudaFuncAttributePreferredSharedMemoryCarveout, 100),
+                      "cudaFuncSetAttribute(quantiser carveout)"));
+    // Size the grid to what is resident at once (the loop is grid-strided).
+    int occ = 0;
+    QN_TRY(cuda_check((wdt == QN_F32)
+                          ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, qn::nf4_quant_kernel<float>,
+                                                                          qn::kQuantThreads, qn::kQuantSmem)
+                          : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, qn::nf4_quant_kernel<__nv_bfloat16>,
+                                                                          qn::kQuantThreads, qn::kQuantSmem),
+                      "quantiser occupancy"));
+    if (occ < 1) occ = 1;
+    if (grid > static_cast<int64_t>(sms) * occ) grid = static_cast<int64_t>(sms) * occ;
     if (wdt == QN_F32)
-      qn::nf4_quant_kernel<float><<<static_cast<unsigned>(grid), qn::kQuantThreads, 0, st>>>(
+      qn::nf4_quant_kernel<float><<<static_cast<unsigned>(grid), qn::kQuantThreads, qn::kQuantSmem, st>>>(
           static_cast<const float *>(W), nfull, nblk, Q->codes, Q->absmax, b, ticket, Q->absmax_mean);
     else
-      qn::nf4_quant_kernel<__nv_bfloat16><<<static_cast<unsigned>(grid), qn::kQuantThreads, 0, st>>>(
+      qn::nf4_quant_kernel<__nv_bfloat16><<<static_cast<unsigned>(grid), qn::kQuantThreads, qn::kQuantSmem, st>>>(
           static_cast<const __nv_bfloat16 *>(W), nfull, nblk, Q->codes, Q->absmax, b, ticket, Q->absmax_mean);
     QN_LAUNCH_CHECK("nf4_quant_kernel");
   }
@@ -192,14 +221,15 @@ qn_status launch_quantize(const void *W, qn_dtype wdt, const qn_nf4 *Q, unsigned
 
 qn_status launch_dequantize(const qn_nf4 *Q, void *out, qn_dtype odt, cudaStream_t st) {
   const int64_t n = Q->d * Q->k;
-  const int64_t nchunk = n / 32;
-  int64_t grid = qn_ceil_div(nchunk > 0 ? nchunk : 1, 256);
+  // One warp-iteration per 1024 elements; eight warps per CTA, eight CTAs per SM.
+  const int64_t ntile = qn_ceil_div(n / 8, 32 * qn::kDeqWords);
+  int64_t grid = qn_ceil_div(ntile > 0 ? ntile : 1, qn::kDeqThreads / 32);
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
   if (grid > cap) grid = cap;
   if (odt == QN_BF16)
-    qn::nf4_dequant_kernel<true><<<static_cast<unsigned>(grid), 256, 0, st>>>(view_of(Q), n, out);
+    qn::nf4_dequant_kernel<true><<<static_cast<unsigned>(grid), qn::kDeqThreads, 0, st>>>(view_of(Q), n, out);
   else
-    qn::nf4_dequant_kernel<false><<<static_cast<unsigned>(grid), 256, 0, st>>>(view_of(Q), n, out);
+    qn::nf4_dequant_kernel<false><<<static_cast<unsigned>(grid), qn::kDeqThreads, 0, st>>>(view_of(Q), n, out);
   QN_LAUNCH_CHECK("nf4_dequant_kernel");
   return QN_OK;
 }
@@ -510,7 +540,7 @@ qn_status check_layer(const qn_nf4 *Q, const void *in, int64_t M, const void *A,
 }
 
 // Adapter projection C = s P Qop^T (M x N, K deep) split over K so that
-// about six CTAs per SM run, then the splits summed in order into C32 (fp32)
+// enough CTAs to fill the SMs run, then the splits summed in order into C32 (fp32)
 // or, with C2 set, its bf16 hi/lo split (each half padded to R columns, rows
 // of pitch ld2 >= 2R, zero past 2R).
 qn_status launch_lora_proj(const uint16_t *P, int64_t M, int64_t K, const uint16_t *Qm, int64_t N, int64_t qs_n,
@@ -518,7 +548,13 @@ qn_status launch_lora_proj(const uint16_t *P, int64_t M, int64_t K, const uint16
                            cudaStream_t st) {
   const int TN = N <= 16 ? 16 : 64;
   const int64_t tiles = qn_ceil_div(M, qn::kProjTM) * qn_ceil_div(N, TN);
-  int64_t S = qn_ceil_div(6 * static_cast<int64_t>(sm_count()), tiles);
+  // 16-byte aligned operands take the pipelined kernel (about four CTAs per
+  // SM, one wave); others the plain one.
+  const bool pal = (K % 8) == 0 && aligned(P, 16) && aligned(Qm, 16);
+  const bool q_rows = pal && qs_k == 1 && (qs_n % 8) == 0;                 // Qop contiguous along kk
+  const bool q_cols = pal && qs_n == 1 && (qs_k % 8) == 0 && (N % 8) == 0;  // Qop contiguous along n
+  const bool pipe = q_rows || q_cols;
+  int64_t S = qn_ceil_div((pipe ? 4 : 6) * static_cast<int64_t>(sm_count()), tiles);
   const int64_t smax = qn_ceil_div(K, 256);
   if (S > smax) S = smax;
   if (S > qn::kProjMaxSplit) S = qn::kProjMaxSplit;
@@ -527,8 +563,22 @@ qn_status launch_lora_proj(const uint16_t *P, int64_t M, int64_t K, const uint16
   S = qn_ceil_div(K, kchunk);
   dim3 grid(static_cast<unsigned>(qn_ceil_div(M, qn::kProjTM)), static_cast<unsigned>(qn_ceil_div(N, TN)),
             static_cast<unsigned>(S));
-  if (TN == 16) qn::lora_proj_kernel<16><<<grid, 128, 0, st>>>(P, M, K, Qm, N, qs_n, qs_k, s, kchunk, part);
-  else qn::lora_proj_kernel<64><<<grid, 128, 0, st>>>(P, M, K, Qm, N, qs_n, qs_k, s, kchunk, part);
+  if (pipe) {
+    auto run = [&](auto kern, int smem) -> qn_status {
+      QN_TRY(cuda_check(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
+                        "cudaFuncSetAttribute(lora_proj_pipe smem)"));
+      kern<<<grid, 128, smem, st>>>(P, M, K, Qm, N, qs_n, qs_k, s, kchunk, part);
+      return QN_OK;
+    };
+    if (TN == 16 && q_rows) QN_TRY(run(qn::lora_proj_pipe_kernel<16, false>, qn::proj_pipe_smem<16, false>()));
+    else if (TN == 16) QN_TRY(run(qn::lora_proj_pipe_kernel<16, true>, qn::proj_pipe_smem<16, true>()));
+    else if (q_rows) QN_TRY(run(qn::lora_proj_pipe_kernel<64, false>, qn::proj_pipe_smem<64, false>()));
+    else QN_TRY(run(qn::lora_proj_pipe_kernel<64, true>, qn::proj_pipe_smem<64, true>()));
+  } else if (TN == 16) {
+    qn::lora_proj_kernel<16><<<grid, 128, 0, st>>>(P, M, K, Qm, N, qs_n, qs_k, s, kchunk, part);
+  } else {
+    qn::lora_proj_kernel<64><<<grid, 128, 0, st>>>(P, M, K, Qm, N, qs_n, qs_k, s, kchunk, part);
+  }
   QN_LAUNCH_CHECK("lora_proj_kernel");
   const int64_t n = M * (C2 ? R : N);
   qn::lora_reduce_kernel<<<static_cast<unsigned>(qn_ceil_div(n, 256)), 256, 0, st>>>(part, static_cast<int>(S), M, N,
@@ -988,7 +1038,7 @@ size_t loftq_ws_bytes(int64_t d, int64_t k) {
   b += round256(prt * P * sizeof(float));                                     // product split partials
   b += round256(nb * P * P * sizeof(float));                                  // Gram partials
   b += round256(P * P * sizeof(double)) + 2 * round256(P * P * sizeof(float)) + round256(P * sizeof(float));
-  b += round256(1024 * sizeof(double)) + round256(sizeof(double));            // norm partials, norm
+  b += round256(1024 * sizeof(double)) + round256(65 * sizeof(double));       // norm partials, T + 1 norms
   b += round256(kQuantWs);
   return b;
 }
@@ -1016,7 +1066,7 @@ qn_status loftq_run_p(const float *W, int64_t d, int64_t k, int32_t r, float alp
   float *Lf = sp.take<float>(qn::kLqMaxP * qn::kLqMaxP);
   float *lam = sp.take<float>(qn::kLqMaxP);
   double *partial = sp.take<double>(1024);
-  double *norm2 = sp.take<double>(1);
+  double *norm2 = sp.take<double>(65);  // squared residual norms, copied to the host once at the end
   unsigned long long *bins = sp.take<unsigned long long>(qn::kNumBins);
 
   const float s = alpha / static_cast<float>(r);
@@ -1038,14 +1088,11 @@ qn_status loftq_run_p(const float *W, int64_t d, int64_t k, int32_t r, float alp
   QN_TRY(cuda_check(cudaMemsetAsync(A, 0, sizeof(float) * r * k, st), "memset A"));
   QN_TRY(cuda_check(cudaMemsetAsync(B, 0, sizeof(float) * d * r, st), "memset B"));
 
-  auto residual_norm = [&](int rr, double *outp) -> qn_status {
+  auto residual_norm = [&](int rr, int t) -> qn_status {  // norm2[t] = ||R - s B A||^2
     qn::resid_norm_kernel<<<red_blocks, 256, 0, st>>>(Tbuf, B, A, d, k, rr, s, partial);
     QN_LAUNCH_CHECK("resid_norm_kernel");
-    qn::sum_partials_kernel<<<1, 256, 0, st>>>(partial, red_blocks, norm2);
+    qn::sum_partials_kernel<<<1, 256, 0, st>>>(partial, red_blocks, norm2 + t);
     QN_LAUNCH_CHECK("sum_partials_kernel");
-    QN_TRY(cuda_check(cudaMemcpyAsync(outp, norm2, sizeof(double), cudaMemcpyDeviceToHost, st), "copy norm"));
-    QN_TRY(cuda_check(cudaStreamSynchronize(st), "synchronize"));
-    *outp = std::sqrt(*outp);
     return QN_OK;
   };
   auto gram = [&](const float *Ym, int64_t rows) -> qn_status {  // G = Ym^T Ym (fp64)
@@ -1057,14 +1104,34 @@ qn_status loftq_run_p(const float *W, int64_t d, int64_t k, int32_t r, float alp
     return QN_OK;
   };
   auto orth = [&](float *Ym, int64_t rows) -> qn_status {  // CholeskyQR2: Ym <- Ym L^{-T}, twice
-    for (int rep = 0; rep < 2; ++rep) {
-      QN_TRY(gram(Ym, rows));
-      qn::lq_chol_kernel<P><<<1, 256, 0, st>>>(G, p, Lf);
-      QN_LAUNCH_CHECK("lq_chol_kernel");
-      qn::lq_trsm_rows_kernel<P><<<static_cast<unsigned>(qn_ceil_div(rows, 128)), 128, 0, st>>>(Ym, rows, Lf, p);
-      QN_LAUNCH_CHECK("lq_trsm_rows_kernel");
+    if constexpr (P == 32) {  // both rounds in one cooperative launch
+      int64_t grid = qn_ceil_div(rows, 32);
+      if (grid > sms) grid = sms;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(grid));
+      cfg.blockDim = dim3(256);
+      cfg.dynamicSmemBytes = 0;
+      cfg.stream = st;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeCooperative;
+      attr[0].val.cooperative = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      QN_TRY(cuda_check(cudaLaunchKernelEx(&cfg, qn::lq_cholqr2_p32_kernel, Ym, rows, p,
+                                           reinterpret_cast<double *>(gpart), G, sem + kLqBarWord),
+                        "lq_cholqr2_p32_kernel"));
+      QN_LAUNCH_CHECK("lq_cholqr2_p32_kernel");
+      return QN_OK;
+    } else {
+      for (int rep = 0; rep < 2; ++rep) {
+        QN_TRY(gram(Ym, rows));
+        qn::lq_chol_kernel<P><<<1, 256, 0, st>>>(G, p, Lf);
+        QN_LAUNCH_CHECK("lq_chol_kernel");
+        qn::lq_trsm_rows_kernel<P><<<static_cast<unsigned>(qn_ceil_div(rows, 128)), 128, 0, st>>>(Ym, rows, Lf, p);
+        QN_LAUNCH_CHECK("lq_trsm_rows_kernel");
+      }
+      return QN_OK;
     }
-    return QN_OK;
   };
   auto reduce = [&](int S, int64_t n_out, float *out) -> qn_status {
     qn::lq_split_reduce_kernel<<<static_cast<unsigned>(qn_ceil_div(n_out, 256)), 256, 0, st>>>(ppart, S, n_out, out);
@@ -1092,7 +1159,7 @@ qn_status loftq_run_p(const float *W, int64_t d, int64_t k, int32_t r, float alp
   if (requantise) QN_TRY(launch_quantize(W, QN_F32, Q, bins, sem, st));
   qn::residual_kernel<<<sms * 8, 256, 0, st>>>(qv, W, Tbuf, n);
   QN_LAUNCH_CHECK("residual_kernel");
-  QN_TRY(residual_norm(0, &resid[0]));
+  QN_TRY(residual_norm(0, 0));
 
   for (int t = 1; t <= T; ++t) {
     if (t > 1) {  // Q-step: Q_t = NF4(W - s B A)
@@ -1123,8 +1190,12 @@ qn_status loftq_run_p(const float *W, int64_t d, int64_t k, int32_t r, float alp
     qn::lq_project_kernel<P><<<static_cast<unsigned>(qn_ceil_div(k, 256)), 256, 0, st>>>(Zt, k, V, lam, r, s, 1, A,
                                                                                          1);
     QN_LAUNCH_CHECK("lq_project_kernel(A)");
-    QN_TRY(residual_norm(r, &resid[t]));
+    QN_TRY(residual_norm(r, t));
   }
+  QN_TRY(cuda_check(cudaMemcpyAsync(resid, norm2, sizeof(double) * (T + 1), cudaMemcpyDeviceToHost, st),
+                    "copy norms"));
+  QN_TRY(cuda_check(cudaStreamSynchronize(st), "synchronize"));
+  for (int t = 0; t <= T; ++t) resid[t] = std::sqrt(resid[t]);
   return QN_OK;
 }
 

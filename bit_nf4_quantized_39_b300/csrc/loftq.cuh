@@ -370,14 +370,206 @@ lq_trsm_rows_kernel(float *__restrict__ Y, int64_t n, const float *__restrict__ 
     *reinterpret_cast<float4 *>(Y + i * P + c) = make_float4(y[c], y[c + 1], y[c + 2], y[c + 3]);
 }
 
+// ---------------------------------------------------------------------------
+// CholeskyQR2 of a 32-column panel in one launch (Fukaya, Nakatsukasa,
+// Yanagisawa, Yamamoto, "CholeskyQR2: a simple and communication-avoiding
+// algorithm for computing a tall-skinny QR factorization", ScalA 2014): two
+// rounds of  G = Y^T Y,  G = L L^T,  Y <- Y L^{-T}.  Every CTA is resident
+// at once (cooperative launch) and owns a contiguous range of rows.  A round:
+//   1. each CTA sums y y^T over its rows (fp32 within 32-row chunks, fp64
+//      across chunks) into its fp64 partial;
+//   2. grid barrier; the P*P entries of G are split over the grid's warps,
+//      each summing the CTAs' partials in a fixed order (fp64);
+//   3. grid barrier; every CTA factors G itself (one warp, lane i holding row
+//      i of the matrix in registers, fp32 as lq_chol_kernel: pivots clamped
+//      to a floor of 1e-12 times the largest diagonal entry) and solves its
+//      rows against L (as lq_trsm_rows_kernel).
+// Grid barriers are counters in the zero area with bounded waits: a wait
+// that expires records QN_DEV_TIMEOUT and the kernel carries on (the panel is
+// then wrong and the host reports the status).  The last CTA to leave resets
+// both counters.
+// ---------------------------------------------------------------------------
+constexpr unsigned kLqSpinLimit = 1u << 20;  // polls, 64 ns apart
+
+__device__ __forceinline__ void lq_grid_barrier(unsigned int *cnt, unsigned int target) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(cnt, 1u);
+    unsigned int v = 0, spins = 0;
+    for (;;) {
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+      if (v >= target) break;
+      if (++spins > kLqSpinLimit) {
+        qn_flag_timeout();
+        break;
+      }
+      __nanosleep(64);
+    }
+  }
+  __syncthreads();
+}
+
+// Step K of the one-warp Cholesky of a 32 x 32 matrix, lane i holding row i
+// in a[]: pivot from lane K, column K scaled below it, trailing lower
+// triangle updated with the shuffled column (compile-time indices only).
+template <int K>
+__device__ __forceinline__ void lq_chol_warp_step(float (&a)[32], int lane, int p, float floor_v) {
+  if constexpr (K < 32) {
+    const float dk = __shfl_sync(0xffffffffu, a[K], K);
+    const float piv = (K < p) ? sqrtf(fmaxf(dk, floor_v)) : 1.f;
+    const float inv = 1.0f / piv;
+    if (lane == K) a[K] = piv;
+    if (lane > K && lane < p) a[K] *= inv;
+    const float lik = a[K];
+#pragma unroll
+    for (int c = K + 1; c < 32; ++c) {
+      const float lck = __shfl_sync(0xffffffffu, lik, c);
+      if (lane >= c && lane < p && c < p) a[c] = fmaf(-lik, lck, a[c]);
+    }
+    lq_chol_warp_step<K + 1>(a, lane, p, floor_v);
+  }
+}
+
+__global__ void __launch_bounds__(256, 1)
+lq_cholqr2_p32_kernel(float *__restrict__ Y, int64_t n, int p, double *__restrict__ gpart,
+                      double *__restrict__ G, unsigned int *__restrict__ bar) {
+  constexpr int P = 32;
+  __shared__ __align__(16) float sY[32][P];
+  __shared__ float sL[P][P + 1];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ta = tid / 16, tb = tid % 16;  // 2 x 2 tile of G: rows 2 ta.., columns 2 tb..
+  const unsigned int nct = gridDim.x;
+  const int64_t rpc = (n + nct - 1) / nct;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * rpc;
+  const int64_t r1 = (r0 + rpc < n) ? r0 + rpc : n;
+  unsigned int nbar = 0;
+
+  for (int round = 0; round < 2; ++round) {
+    // 1. partial Gram matrix of this CTA's rows
+    double acc[2][2] = {{0.0, 0.0}, {0.0, 0.0}};
+    for (int64_t i0 = r0; i0 < r1; i0 += 32) {
+      for (int t = tid; t < 32 * P / 4; t += 256) {
+        const int rr = t / (P / 4), c4 = (t % (P / 4)) * 4;
+        const int64_t i = i0 + rr;
+        *reinterpret_cast<float4 *>(&sY[rr][c4]) =
+            (i < r1) ? __ldcg(reinterpret_cast<const float4 *>(Y + i * P + c4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      __syncthreads();
+      float f[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll 8
+      for (int ii = 0; ii < 32; ++ii) {
+        const float ya0 = sY[ii][2 * ta], ya1 = sY[ii][2 * ta + 1];
+        const float yb0 = sY[ii][2 * tb], yb1 = sY[ii][2 * tb + 1];
+        f[0][0] = fmaf(ya0, yb0, f[0][0]);
+        f[0][1] = fmaf(ya0, yb1, f[0][1]);
+        f[1][0] = fmaf(ya1, yb0, f[1][0]);
+        f[1][1] = fmaf(ya1, yb1, f[1][1]);
+      }
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) acc[a][b] += static_cast<double>(f[a][b]);
+      __syncthreads();
+    }
+    double *pp = gpart + static_cast<int64_t>(blockIdx.x) * P * P;
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int b = 0; b < 2; ++b) __stcg(pp + (2 * ta + a) * P + 2 * tb + b, acc[a][b]);
+    lq_grid_barrier(bar, ++nbar * nct);
+
+    // 2. G = sum of the partials, entries split over the grid's warps
+    for (int e = static_cast<int>(blockIdx.x) * 8 + warp; e < P * P; e += static_cast<int>(nct) * 8) {
+      double v = 0.0;
+      for (unsigned int b = lane; b < nct; b += 32) v += __ldcg(gpart + static_cast<int64_t>(b) * P * P + e);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) __stcg(G + e, v);
+    }
+    lq_grid_barrier(bar, ++nbar * nct);
+
+    // 3. Cholesky in one warp: lane i holds row i (identity past p)
+    if (warp == 0) {
+      float a[P];
+#pragma unroll
+      for (int j = 0; j < P; ++j)
+        a[j] = (lane < p && j < p) ? static_cast<float>(__ldcg(G + lane * P + j)) : ((lane == j) ? 1.f : 0.f);
+      float mx = 0.f;
+#pragma unroll
+      for (int j = 0; j < P; ++j)
+        if (j == lane && lane < p) mx = a[j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float floor_v = fmaxf(mx, 1e-30f) * 1e-12f;
+      lq_chol_warp_step<0>(a, lane, p, floor_v);
+#pragma unroll
+      for (int j = 0; j < P; ++j)
+        sL[lane][j] = (lane < p && j < p) ? ((j <= lane) ? a[j] : 0.f) : ((lane == j) ? 1.f : 0.f);
+    }
+    __syncthreads();
+    // rows of this CTA: y <- y L^{-T} (forward substitution per row)
+    for (int64_t i = r0 + tid; i < r1; i += 256) {
+      float y[P];
+#pragma unroll
+      for (int c = 0; c < P; c += 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(Y + i * P + c));
+        y[c] = v.x; y[c + 1] = v.y; y[c + 2] = v.z; y[c + 3] = v.w;
+      }
+#pragma unroll
+      for (int c = 0; c < P; ++c) {
+        float acc2 = y[c];
+#pragma unroll
+        for (int b = 0; b < c; ++b) acc2 = fmaf(-sL[c][b], y[b], acc2);
+        y[c] = (c < p) ? acc2 / sL[c][c] : 0.f;
+      }
+#pragma unroll
+      for (int c = 0; c < P; c += 4)
+        __stcg(reinterpret_cast<float4 *>(Y + i * P + c), make_float4(y[c], y[c + 1], y[c + 2], y[c + 3]));
+    }
+    // the next round reads only this CTA's own rows (after this barrier); G
+    // and the partials are rewritten only after the next grid barrier
+    __syncthreads();
+  }
+  // leave: the last CTA out resets the counters
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(bar + 1, 1u) == nct - 1u) {
+      bar[0] = 0u;
+      bar[1] = 0u;
+      __threadfence();
+    }
+  }
+}
+
 // One CTA of 256 threads: parallel cyclic Jacobi eigen-decomposition (fp32)
 // of the symmetric leading p x p block of G (accumulated in fp64), with the
-// round-robin pair ordering, so that n / 2 disjoint rotations run at once
-// (n = p rounded up to even; a padding row and column stay zero).  Outputs
-// the eigenvalues sorted descending (lam[P], zero past p) and the matching
-// eigenvectors as the columns of V (fp32 [P x P], V[row * P + col]).
+// round-robin ("circle") pair ordering, so that n / 2 disjoint rotations run
+// at once (n = p rounded up to even; a padding row and column stay zero).
+// In round t the pairs are (n-1, t) and ((t+k) mod (n-1), (t-k) mod (n-1)),
+// k = 1 .. n/2-1.  A round takes two barriers: the rotations of all pairs are
+// formed, then A <- J^T A J is applied one 2 x 2 block (a pair of rows by a
+// pair of columns) per thread, together with E <- E J.  Sweeps stop once the
+// off-diagonal mass is at the fp32 noise level.  Outputs the eigenvalues
+// sorted descending (lam[P], zero past p) and the matching eigenvectors as
+// the columns of V (fp32 [P x P], V[row * P + col]).
 template <int P>
 constexpr size_t lq_jacobi_smem() { return 2 * static_cast<size_t>(P) * (P + 1) * sizeof(float); }
+
+__device__ __forceinline__ void lq_round_pair(int t, int k, int n, int &a, int &b) {
+  const int m = n - 1;
+  int x, y;
+  if (k == 0) {
+    x = m;
+    y = t;
+  } else {
+    x = (t + k) % m;
+    y = (t - k + m) % m;
+  }
+  a = x < y ? x : y;
+  b = x < y ? y : x;
+}
 
 template <int P>
 __global__ void __launch_bounds__(256)
@@ -386,7 +578,6 @@ lq_jacobi_kernel(const double *__restrict__ G, int p, float *__restrict__ lam, f
   float (*A)[P + 1] = reinterpret_cast<float (*)[P + 1]>(lq_jac_smem);
   float (*E)[P + 1] = reinterpret_cast<float (*)[P + 1]>(lq_jac_smem + P * (P + 1));
   __shared__ float cs[P / 2][2];
-  __shared__ int pos[P];
   __shared__ int pr[P / 2][2];
   __shared__ float s_off, s_dg;
   __shared__ int order[P];
@@ -398,7 +589,6 @@ lq_jacobi_kernel(const double *__restrict__ G, int p, float *__restrict__ lam, f
     A[i][j] = (i < p && j < p) ? static_cast<float>(G[i * P + j]) : 0.f;
     E[i][j] = (i == j) ? 1.f : 0.f;
   }
-  for (int t = tid; t < P; t += 256) pos[t] = t;
   __syncthreads();
   for (int sweep = 0; sweep < 15; ++sweep) {
     if (tid < 32) {  // convergence: off-diagonal mass against the diagonal
@@ -418,10 +608,9 @@ lq_jacobi_kernel(const double *__restrict__ G, int p, float *__restrict__ lam, f
     __syncthreads();
     if (s_off <= 1e-10f * s_dg) break;  // off-diagonal mass at the fp32 noise level
     for (int step = 0; step < n - 1; ++step) {
-      // pairs of this step and their rotations
-      for (int k = tid; k < np; k += 256) {
-        int a = pos[k], b = pos[n - 1 - k];
-        if (a > b) { const int tmp = a; a = b; b = tmp; }
+      for (int k = tid; k < np; k += 256) {  // rotations of this round's pairs
+        int a, b;
+        lq_round_pair(step, k, n, a, b);
         pr[k][0] = a;
         pr[k][1] = b;
         const float aij = A[a][b];
@@ -436,44 +625,43 @@ lq_jacobi_kernel(const double *__restrict__ G, int p, float *__restrict__ lam, f
         cs[k][1] = sn;
       }
       __syncthreads();
-      // rows: A <- J^T A
-      for (int t = tid; t < np * n; t += 256) {
-        const int k = t / n, col = t % n;
-        const int a = pr[k][0], b = pr[k][1];
-        const float c = cs[k][0], sn = cs[k][1];
-        const float ra = A[a][col], rb = A[b][col];
-        A[a][col] = c * ra - sn * rb;
-        A[b][col] = sn * ra + c * rb;
-      }
-      __syncthreads();
-      // columns: A <- A J and E <- E J
-      for (int t = tid; t < np * n; t += 256) {
-        const int k = t / n, row = t % n;
-        const int a = pr[k][0], b = pr[k][1];
-        const float c = cs[k][0], sn = cs[k][1];
-        const float ca = A[row][a], cb = A[row][b];
-        A[row][a] = c * ca - sn * cb;
-        A[row][b] = sn * ca + c * cb;
-        const float ea = E[row][a], eb = E[row][b];
-        E[row][a] = c * ea - sn * eb;
-        E[row][b] = sn * ea + c * eb;
-      }
-      __syncthreads();
-      // round-robin: position 0 fixed, the others rotate by one
-      if (tid == 0) {
-        const int last = pos[n - 1];
-        for (int q = n - 1; q > 1; --q) pos[q] = pos[q - 1];
-        pos[1] = last;
+      // A <- J^T A J one 2 x 2 block at a time (rows of pair k1, columns of
+      // pair k2: rows first, then columns), and E <- E J one row of a pair.
+      for (int t = tid; t < np * np + np * n; t += 256) {
+        if (t < np * np) {
+          const int k1 = t / np, k2 = t % np;
+          const int a = pr[k1][0], b = pr[k1][1], c0 = pr[k2][0], d0 = pr[k2][1];
+          const float c1 = cs[k1][0], s1 = cs[k1][1], c2 = cs[k2][0], s2 = cs[k2][1];
+          const float ra_c = c1 * A[a][c0] - s1 * A[b][c0], ra_d = c1 * A[a][d0] - s1 * A[b][d0];
+          const float rb_c = s1 * A[a][c0] + c1 * A[b][c0], rb_d = s1 * A[a][d0] + c1 * A[b][d0];
+          A[a][c0] = c2 * ra_c - s2 * ra_d;
+          A[a][d0] = s2 * ra_c + c2 * ra_d;
+          A[b][c0] = c2 * rb_c - s2 * rb_d;
+          A[b][d0] = s2 * rb_c + c2 * rb_d;
+        } else {
+          const int u = t - np * np, k = u / n, row = u % n;
+          const int a = pr[k][0], b = pr[k][1];
+          const float c = cs[k][0], sn = cs[k][1];
+          const float ea = E[row][a], eb = E[row][b];
+          E[row][a] = c * ea - sn * eb;
+          E[row][b] = sn * ea + c * eb;
+        }
       }
       __syncthreads();
     }
   }
-  if (tid == 0) {
-    for (int i = 0; i < P; ++i) order[i] = i;
-    for (int i = 0; i < p; ++i) {
-      int best = i;
-      for (int j = i + 1; j < p; ++j) if (A[order[j]][order[j]] > A[order[best]][order[best]]) best = j;
-      const int tmp = order[i]; order[i] = order[best]; order[best] = tmp;
+  // descending order of the eigenvalues: rank of each (ties by index)
+  for (int i = tid; i < P; i += 256) {
+    if (i < p) {
+      const float di = A[i][i];
+      int rank = 0;
+      for (int j = 0; j < p; ++j) {
+        const float dj = A[j][j];
+        rank += (dj > di || (dj == di && j < i)) ? 1 : 0;
+      }
+      order[rank] = i;
+    } else {
+      order[i] = i;
     }
   }
   __syncthreads();

@@ -7,19 +7,20 @@
 // after subtracting their mean.
 //
 // Kernels
-//   nf4_quant_kernel      full 64-blocks: 128-bit loads, shuffle absmax,
+//   nf4_quant_kernel      full 64-blocks: per-warp cp.async ring, shuffle absmax,
 //                         IEEE division, threshold count, packed stores,
 //                         exact exponent-binned sum of the absmax constants.
 //   nf4_quant_tail_kernel the final partial block (n % 64 != 0).
 //   nf4_dq_kernel         per 256-group: exact mean from the bins, int8 codes.
-//   nf4_dequant_kernel    codes + constants -> fp32 / bf16, 128-bit stores.
+//   nf4_dequant_kernel    codes + constants -> fp32 / bf16, warp-contiguous
+//                         loads and 128-bit stores.
 #pragma once
 
 #include "common.cuh"
 
 namespace qn {
 
-constexpr int kQuantThreads = 256;
+constexpr int kQuantThreads = 512;
 constexpr int kNumBins = 256;  // one bin per fp32 exponent field value
 
 // Adds a block absmax to the exponent-binned exact sum: bin e' = max(e, 1)
@@ -30,6 +31,32 @@ __device__ __forceinline__ void bin_add_shared(unsigned long long *s_bins, float
   const uint32_t e = (b >> 23) & 0xFFu;
   const uint32_t sig = (b & 0x7FFFFFu) | (e ? 0x800000u : 0u);
   if (sig) atomicAdd(&s_bins[e ? e : 1u], static_cast<unsigned long long>(sig));
+}
+
+// Register-held part of the same exact sum: a lane folds the constants whose
+// bin lies within 4 of a reference bin (the first one it meets) into one
+// 64-bit integer in units of bin eref - 4 (significand << (bin - eref + 4));
+// others go to the shared bins.  flush adds the integer to bin eref - 4.  The
+// fold is used only while every bin stays below 2^63 (nblk <= 2^31).
+struct BinFold {
+  unsigned long long acc;
+  int eref;
+};
+
+__device__ __forceinline__ void bin_fold(BinFold &f, unsigned long long *s_bins, float m, bool fold) {
+  const uint32_t b = __float_as_uint(m);
+  const uint32_t e = (b >> 23) & 0xFFu;
+  const uint32_t sig = (b & 0x7FFFFFu) | (e ? 0x800000u : 0u);
+  if (!sig) return;
+  const int be = e ? static_cast<int>(e) : 1;
+  if (fold && f.eref < 0 && be >= 5) f.eref = be;
+  const int sh = be - f.eref + 4;
+  if (fold && f.eref >= 0 && sh >= 0 && sh <= 8) f.acc += static_cast<unsigned long long>(sig) << sh;
+  else atomicAdd(&s_bins[be], static_cast<unsigned long long>(sig));
+}
+
+__device__ __forceinline__ void bin_flush(const BinFold &f, unsigned long long *s_bins) {
+  if (f.acc) atomicAdd(&s_bins[f.eref - 4], f.acc);
 }
 
 // ---------------------------------------------------------------------------
@@ -297,18 +324,36 @@ __device__ __forceinline__ void quant_mean_epilogue(unsigned long long *s_bins, 
   }
 }
 
-// Lanes in groups of G = 64 / kVec own one 64-element block each per
-// iteration; the last CTA to finish derives the double-quantisation mean
-// from the exact exponent-binned sum and resets the ticket counter.
+// Quantiser main loop.  Each warp streams its own ring of kQuantRing stages
+// of 1 KiB of input (32 bytes per lane) with 16-byte cp.async, so that about
+// 128 KiB of loads are in flight per SM (two CTAs of 16 warps); a lane waits
+// only for its own copies, and a __syncwarp hands the stage to the lanes that
+// read it.  A stage holds 8 blocks of bf16 input (every lane quantises two
+// blocks with 7 other lanes, one 8-element part of each) or 4 blocks of fp32
+// input (one block per lane).  Inside a stage, the 16-byte unit u is stored
+// at unit u ^ ((u >> 3) & 1), which keeps both the cp.async writes and the
+// fp32 layout's 32-byte reads free of bank conflicts.  The last CTA to finish
+// derives the double-quantisation mean from the exact exponent-binned sum and
+// resets the ticket counter.
+constexpr int kQuantWarps = kQuantThreads / 32;
+constexpr int kQuantRing = 5;
+constexpr int kQuantStage = 1024;
+constexpr int kQuantSmem = kQuantWarps * kQuantRing * kQuantStage;  // dynamic shared memory per CTA
+
+__device__ __forceinline__ uint32_t quant_unit(uint32_t u) { return (u ^ ((u >> 3) & 1u)) * 16u; }
+
+__device__ __forceinline__ void quant_cp16(uint32_t dst, const void *src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+
 template <typename T>
-__global__ void __launch_bounds__(kQuantThreads)
+__global__ void __launch_bounds__(kQuantThreads, 2)
 nf4_quant_kernel(const T *__restrict__ x, int64_t nfull, int64_t nblk, uint8_t *__restrict__ codes,
                  float *__restrict__ absmax, unsigned long long *__restrict__ bins,
                  unsigned int *__restrict__ ticket, float *__restrict__ absmax_mean) {
-  constexpr int V = QuantVec<T>::kVec;
-  constexpr int G = 64 / V;        // lanes per block
-  constexpr int BPW = 32 / G;      // blocks per warp-iteration
-  static_assert(V == 8 && G == 8, "eight lanes of eight elements per block");
+  constexpr bool kF32 = sizeof(T) == 4;
+  constexpr int kBps = kQuantStage / (64 * static_cast<int>(sizeof(T)));  // blocks per stage: 8 or 4
+  extern __shared__ __align__(16) uint8_t q_ring[];
   __shared__ unsigned long long s_bins[kNumBins];
   __shared__ BucketEntry s_one[kBuckets];
   __shared__ BucketEntry s_tab[kBuckets * 32];
@@ -316,59 +361,104 @@ nf4_quant_kernel(const T *__restrict__ x, int64_t nfull, int64_t nblk, uint8_t *
   build_bucket_tables(s_one, s_tab);
   const int lane = threadIdx.x & 31;
   const BucketEntry *my_tab = s_tab + lane;
-  const int sub = lane / G;
-  const int li = lane % G;
-  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int li = lane & 7;
+  const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(q_ring)) +
+                        static_cast<uint32_t>((threadIdx.x >> 5) * (kQuantRing * kQuantStage));
+  const int64_t nst = (nfull + kBps - 1) / kBps;  // stages of the whole input
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kQuantWarps + (threadIdx.x >> 5);
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * kQuantWarps;
+  const char *xb = reinterpret_cast<const char *>(x);
+  BinFold fold_st = {0ull, -1};
+  const bool fold = nblk <= (int64_t(1) << 31);
 
-  // The loads of the next iteration are issued before the current block is
-  // processed (one iteration of register prefetch).
-  constexpr bool kF32 = sizeof(T) == 4;
-  uint4 na = make_uint4(0u, 0u, 0u, 0u), nb = na;  // the next block's 8 elements of this lane
-  int64_t b0 = warp * BPW;
-  if (b0 + sub < nfull) {
-    const uint4 *p = reinterpret_cast<const uint4 *>(x + (b0 + sub) * 64 + li * V);
-    na = __ldcs(p);
-    if (kF32) nb = __ldcs(p + 1);
-  }
-  for (; b0 < nfull; b0 += nwarps * BPW) {
-    const int64_t blk = b0 + sub;
-    const bool valid = blk < nfull;
-    float v[V];
-    if constexpr (kF32) {
-      const uint32_t w[8] = {na.x, na.y, na.z, na.w, nb.x, nb.y, nb.z, nb.w};
+  // Issues this lane's two 16-byte copies of stage s into ring slot `slot`
+  // (units c * 32 + lane; a unit past the last full block reads nothing and
+  // is zero-filled) and closes the copy group, which is empty past the end.
+  auto issue = [&](int64_t s, int slot) {
+    if (s < nst) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(w[i]);
+      for (int c = 0; c < 2; ++c) {
+        const uint32_t u = static_cast<uint32_t>(c * 32 + lane);
+        const int64_t blk = s * kBps + (u * 16u) / (64u * sizeof(T));
+        const bool ok = blk < nfull;
+        quant_cp16(ring + slot * kQuantStage + quant_unit(u), ok ? xb + s * kQuantStage + u * 16u : xb,
+                   ok ? 16u : 0u);
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+
+#pragma unroll
+  for (int j = 0; j < kQuantRing - 1; ++j) issue(gw + j * nw, j);
+  int slot = 0;
+  for (int64_t s = gw; s < nst; s += nw) {
+    issue(s + (kQuantRing - 1) * nw, slot == 0 ? kQuantRing - 1 : slot - 1);
+    asm volatile("cp.async.wait_group %0;" ::"n"(kQuantRing - 1) : "memory");
+    __syncwarp();
+    const uint32_t base = ring + slot * kQuantStage;
+    if constexpr (kF32) {
+      // Lane l: block l / 8 of the stage, elements 8 (l % 8) .. + 7 (units 2l, 2l + 1).
+      uint4 a, b;
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w) : "r"(base + quant_unit(2u * lane)));
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w) : "r"(base + quant_unit(2u * lane + 1u)));
+      __syncwarp();  // the slot may be refilled once every lane holds its part
+      float v[8] = {__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z), __uint_as_float(a.w),
+                    __uint_as_float(b.x), __uint_as_float(b.y), __uint_as_float(b.z), __uint_as_float(b.w)};
+      float m;
+      const uint32_t packed = nf4_quant_lane8(v, my_tab, m);
+      const int64_t blk = s * kBps + (lane >> 3);
+      if (blk < nfull) {
+        reinterpret_cast<uint32_t *>(codes + blk * 32)[li] = packed;
+        if (li == 0) {
+          absmax[blk] = m;
+          if (bins) bin_fold(fold_st, s_bins, m, fold);
+        }
+      }
     } else {
-      const uint32_t w[4] = {na.x, na.y, na.z, na.w};
+      // Lane l: blocks l / 8 and 4 + l / 8 of the stage, elements 8 (l % 8) .. + 7 of each.
+      uint4 w[2];
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[c].x), "=r"(w[c].y), "=r"(w[c].z), "=r"(w[c].w)
+                     : "r"(base + quant_unit(static_cast<uint32_t>(c * 32 + lane))));
+      __syncwarp();
+      float v0[8], v1[8];
+      const uint32_t a[4] = {w[0].x, w[0].y, w[0].z, w[0].w};
+      const uint32_t b[4] = {w[1].x, w[1].y, w[1].z, w[1].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        v[2 * i] = __uint_as_float(w[i] << 16);
-        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        v0[2 * i] = __uint_as_float(a[i] << 16);
+        v0[2 * i + 1] = __uint_as_float(a[i] & 0xFFFF0000u);
+        v1[2 * i] = __uint_as_float(b[i] << 16);
+        v1[2 * i + 1] = __uint_as_float(b[i] & 0xFFFF0000u);
+      }
+      float m0, m1;
+      const uint32_t p0 = nf4_quant_lane8(v0, my_tab, m0);
+      const uint32_t p1 = nf4_quant_lane8(v1, my_tab, m1);
+      const int64_t blk0 = s * kBps + (lane >> 3), blk1 = blk0 + 4;
+      if (blk0 < nfull) {
+        reinterpret_cast<uint32_t *>(codes + blk0 * 32)[li] = p0;
+        if (li == 0) {
+          absmax[blk0] = m0;
+          if (bins) bin_fold(fold_st, s_bins, m0, fold);
+        }
+      }
+      if (blk1 < nfull) {
+        reinterpret_cast<uint32_t *>(codes + blk1 * 32)[li] = p1;
+        if (li == 0) {
+          absmax[blk1] = m1;
+          if (bins) bin_fold(fold_st, s_bins, m1, fold);
+        }
       }
     }
-    {
-      const int64_t nblk2 = b0 + nwarps * BPW + sub;
-      if (nblk2 < nfull) {
-        const uint4 *p = reinterpret_cast<const uint4 *>(x + nblk2 * 64 + li * V);
-        na = __ldcs(p);
-        if (kF32) nb = __ldcs(p + 1);
-      } else {
-        na = make_uint4(0u, 0u, 0u, 0u);
-        nb = na;
-      }
-    }
-    float m;
-    const uint32_t packed = nf4_quant_lane8(v, my_tab, m);
-    if (valid) {
-      reinterpret_cast<uint32_t *>(codes + blk * 32)[li] = packed;
-      if (li == 0) {
-        absmax[blk] = m;
-        if (bins) bin_add_shared(s_bins, m);
-      }
-    }
+    slot = (slot + 1 == kQuantRing) ? 0 : slot + 1;
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");
   if (!bins) return;
+  bin_flush(fold_st, s_bins);
   quant_mean_epilogue(s_bins, bins, ticket, nblk, absmax_mean);
 }
 
@@ -442,59 +532,66 @@ nf4_dq_kernel(const float *__restrict__ absmax, int64_t nblk, const float *__res
 }
 
 // ---------------------------------------------------------------------------
-// Dequantisation: one thread per 32 elements (16 code bytes, one 128-bit
-// load), two such chunks per iteration.
+// Dequantisation: a lane decodes 4-byte words of codes (8 elements each).  A
+// warp-iteration covers 128 consecutive words (1024 elements): lane l takes
+// words l, l + 32, l + 64 and l + 96, so that every load of codes (128 bytes
+// per warp) and every store of results (512 bytes of bf16, or two stores of
+// 512 bytes of fp32, per warp) is contiguous.  The four code words and their
+// block constants are loaded before any is decoded.
 // ---------------------------------------------------------------------------
+constexpr int kDeqThreads = 256;
+constexpr int kDeqWords = 4;  // words per lane per warp-iteration
+
 template <bool kBf16Out>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kDeqThreads)
 nf4_dequant_kernel(QnNF4View q, int64_t n, void *__restrict__ out) {
   __shared__ float s_lut[16];
   if (threadIdx.x < 16) s_lut[threadIdx.x] = c_nf4_levels[threadIdx.x];
   __syncthreads();
-  const int64_t nchunk = n / 32;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  // Two chunks per iteration: both code loads (and both constants) are in
-  // flight before either chunk is decoded.
-  for (int64_t c0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c0 < nchunk; c0 += 2 * stride) {
-    const int64_t c1 = c0 + stride;
-    const uint4 wa = __ldcs(reinterpret_cast<const uint4 *>(q.codes) + c0);
-    const uint4 wb = (c1 < nchunk) ? __ldcs(reinterpret_cast<const uint4 *>(q.codes) + c1) : make_uint4(0u, 0u, 0u, 0u);
-    const float ma = block_scale(q, c0 >> 1);
-    const float mb = (c1 < nchunk) ? block_scale(q, c1 >> 1) : 0.f;
+  const int lane = threadIdx.x & 31;
+  const int64_t nword = n / 8;
+  const int64_t ntile = qn_ceil_div(nword, 32 * kDeqWords);
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const uint32_t *__restrict__ cw = reinterpret_cast<const uint32_t *>(q.codes);
+  const float mu = q.dq ? __ldg(q.absmax_mean) : 0.f;
+  for (int64_t t = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; t < ntile; t += nw) {
+    const int64_t w0 = t * (32 * kDeqWords) + lane;
+    uint32_t w[kDeqWords];
+    float m[kDeqWords];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-    const int64_t c = half ? c1 : c0;
-    if (c >= nchunk) break;
-    const uint4 w4 = half ? wb : wa;
-    const float m = half ? mb : ma;
-    const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-    if constexpr (kBf16Out) {
-      uint32_t o[16];
+    for (int i = 0; i < kDeqWords; ++i) {
+      const int64_t wi = w0 + 32 * i;
+      w[i] = (wi < nword) ? __ldcs(cw + wi) : 0u;
+    }
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < kDeqWords; ++i) {
+      const int64_t wi = w0 + 32 * i;
+      const int64_t j = ((wi < nword) ? wi : 0) >> 3;  // block of the word
+      m[i] = q.dq ? dq_absmax(q.absmax_q[j], q.absmax_scale[j >> 8], mu) : q.absmax[j];
+    }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t byte = (w[i] >> (8 * j)) & 0xFFu;
-          o[4 * i + j] = pack_bf16x2(__fmul_rn(s_lut[byte & 15u], m), __fmul_rn(s_lut[byte >> 4], m));
-        }
-      uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + c * 32);
+    for (int i = 0; i < kDeqWords; ++i) {
+      const int64_t wi = w0 + 32 * i;
+      if (wi >= nword) break;
+      if constexpr (kBf16Out) {
+        uint32_t o[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) __stcs(dst + i, make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]));
-    } else {
-      float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(out) + c * 32);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
+        for (int e = 0; e < 4; ++e)
+          o[e] = pack_bf16x2(__fmul_rn(s_lut[(w[i] >> (8 * e)) & 15u], m[i]),
+                             __fmul_rn(s_lut[(w[i] >> (8 * e + 4)) & 15u], m[i]));
+        __stcs(reinterpret_cast<uint4 *>(out) + wi, make_uint4(o[0], o[1], o[2], o[3]));
+      } else {
         float f[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = __fmul_rn(s_lut[(w[i] >> (4 * j)) & 15u], m);
-        __stcs(dst + 2 * i, make_float4(f[0], f[1], f[2], f[3]));
-        __stcs(dst + 2 * i + 1, make_float4(f[4], f[5], f[6], f[7]));
+        for (int e = 0; e < 8; ++e) f[e] = __fmul_rn(s_lut[(w[i] >> (4 * e)) & 15u], m[i]);
+        float4 *dst = reinterpret_cast<float4 *>(out) + 2 * wi;
+        __stcs(dst, make_float4(f[0], f[1], f[2], f[3]));
+        __stcs(dst + 1, make_float4(f[4], f[5], f[6], f[7]));
       }
     }
-    }
   }
-  // Tail: elements [nchunk*32, n), one thread each.
-  const int64_t t0 = nchunk * 32;
+  // Tail: elements [nword * 8, n), one thread each.
+  const int64_t t0 = nword * 8;
   if (blockIdx.x == 0) {
     for (int64_t e = t0 + threadIdx.x; e < n; e += blockDim.x) {
       const uint32_t byte = q.codes[e >> 1];

@@ -120,6 +120,125 @@ lora_proj_kernel(const uint16_t *__restrict__ P, int64_t M, int64_t K,
   }
 }
 
+// Pipelined variant for 16-byte aligned operands (K % 8 == 0; Qop either
+// contiguous along kk, kQT == false: Qm[n * qs_n + kk] with qs_n % 8 == 0, or
+// contiguous along n, kQT == true: Qm[kk * qs_k + n] with qs_k % 8 == 0 and
+// N % 8 == 0).  The same 64 x TN tile and split-K as lora_proj_kernel, but
+// the P and Q tiles of kProjStages K-steps are in flight at once through
+// 16-byte cp.async (zero-filled past the matrix), one CTA barrier per step.
+constexpr int kProjStages = 4;
+
+template <int TN, bool kQT>
+__host__ __device__ constexpr int proj_q_tile_bytes() {
+  return kQT ? kProjTK * (TN + 8) * 2 : TN * kProjStride * 2;
+}
+template <int TN, bool kQT>
+__host__ __device__ constexpr int proj_stage_bytes() {
+  return kProjTM * kProjStride * 2 + proj_q_tile_bytes<TN, kQT>();
+}
+template <int TN, bool kQT>
+__host__ __device__ constexpr int proj_pipe_smem() {
+  return kProjStages * proj_stage_bytes<TN, kQT>();
+}
+
+__device__ __forceinline__ void proj_cp16(uint32_t dst, const void *src, bool ok) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(ok ? 16u : 0u)
+               : "memory");
+}
+
+template <int TN, bool kQT>
+__global__ void __launch_bounds__(128)
+lora_proj_pipe_kernel(const uint16_t *__restrict__ P, int64_t M, int64_t K,
+                      const uint16_t *__restrict__ Qm, int64_t N, int64_t qs_n, int64_t qs_k,
+                      float s, int64_t kchunk, float *__restrict__ part) {
+  extern __shared__ __align__(16) uint8_t proj_smem[];
+  constexpr int NT = TN / 8;
+  constexpr int kQS = kQT ? TN + 8 : kProjStride;  // row stride of the Q tile (elements)
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kProjTM;
+  const int64_t n0 = static_cast<int64_t>(blockIdx.y) * TN;
+  const int64_t kb = static_cast<int64_t>(blockIdx.z) * kchunk;
+  const int64_t ke = (kb + kchunk < K) ? kb + kchunk : K;
+  const int nsteps = static_cast<int>((ke - kb + kProjTK - 1) / kProjTK);
+  const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(proj_smem));
+
+  auto load = [&](int slot, int64_t k0) {
+    const uint32_t sp = sbase + slot * proj_stage_bytes<TN, kQT>();
+    const uint32_t sq = sp + kProjTM * kProjStride * 2;
+#pragma unroll
+    for (int j = 0; j < kProjTM * kProjTK / 8 / 128; ++j) {  // P: 64 rows x 8 chunks
+      const int i = tid + 128 * j, r = i >> 3, c = (i & 7) * 8;
+      const int64_t gm = m0 + r, gk = k0 + c;
+      const bool ok = gm < M && gk + 8 <= ke;
+      proj_cp16(sp + (r * kProjStride + c) * 2, ok ? P + gm * K + gk : P, ok);
+    }
+    if constexpr (!kQT) {  // Q tile [n][kk]
+      for (int i = tid; i < TN * 8; i += 128) {
+        const int n = i >> 3, c = (i & 7) * 8;
+        const int64_t gn = n0 + n, gk = k0 + c;
+        const bool ok = gn < N && gk + 8 <= ke;
+        proj_cp16(sq + (n * kQS + c) * 2, ok ? Qm + gn * qs_n + gk : Qm, ok);
+      }
+    } else {  // Q tile [kk][n]
+      for (int i = tid; i < kProjTK * (TN / 8); i += 128) {
+        const int kk = i / (TN / 8), c = (i % (TN / 8)) * 8;
+        const int64_t gk = k0 + kk, gn = n0 + c;
+        const bool ok = gk < ke && gn + 8 <= N;
+        proj_cp16(sq + (kk * kQS + c) * 2, ok ? Qm + gk * qs_k + gn : Qm, ok);
+      }
+    }
+  };
+
+  float acc[NT][4] = {};
+#pragma unroll
+  for (int st = 0; st < kProjStages - 1; ++st) {
+    if (st < nsteps) load(st, kb + static_cast<int64_t>(st) * kProjTK);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  for (int step = 0; step < nsteps; ++step) {
+    asm volatile("cp.async.wait_group %0;" ::"n"(kProjStages - 2) : "memory");
+    __syncthreads();  // stage `step` visible to all; stage step - 1 no longer read
+    const int nxt = step + kProjStages - 1;
+    if (nxt < nsteps) load(nxt % kProjStages, kb + static_cast<int64_t>(nxt) * kProjTK);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    const uint8_t *stg = proj_smem + (step % kProjStages) * proj_stage_bytes<TN, kQT>();
+    const uint16_t *sP = reinterpret_cast<const uint16_t *>(stg);
+    const uint16_t *sQ = reinterpret_cast<const uint16_t *>(stg + kProjTM * kProjStride * 2);
+#pragma unroll
+    for (int kk = 0; kk < kProjTK; kk += 16) {
+      const int r = warp * 16 + g;
+      const uint32_t a0 = *reinterpret_cast<const uint32_t *>(sP + r * kProjStride + kk + 2 * t);
+      const uint32_t a1 = *reinterpret_cast<const uint32_t *>(sP + (r + 8) * kProjStride + kk + 2 * t);
+      const uint32_t a2 = *reinterpret_cast<const uint32_t *>(sP + r * kProjStride + kk + 2 * t + 8);
+      const uint32_t a3 = *reinterpret_cast<const uint32_t *>(sP + (r + 8) * kProjStride + kk + 2 * t + 8);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        uint32_t b0, b1;
+        if constexpr (!kQT) {
+          b0 = *reinterpret_cast<const uint32_t *>(sQ + (nt * 8 + g) * kQS + kk + 2 * t);
+          b1 = *reinterpret_cast<const uint32_t *>(sQ + (nt * 8 + g) * kQS + kk + 2 * t + 8);
+        } else {
+          const uint16_t *q = sQ + (kk + 2 * t) * kQS + nt * 8 + g;
+          b0 = static_cast<uint32_t>(q[0]) | (static_cast<uint32_t>(q[kQS]) << 16);
+          b1 = static_cast<uint32_t>(q[8 * kQS]) | (static_cast<uint32_t>(q[9 * kQS]) << 16);
+        }
+        mma_bf16_16816_acc(acc[nt], a0, a1, a2, a3, b0, b1);
+      }
+    }
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  float *C = part + static_cast<int64_t>(blockIdx.z) * M * N;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int64_t gm = m0 + warp * 16 + g + 8 * (e >> 1), gn = n0 + nt * 8 + 2 * t + (e & 1);
+      if (gm < M && gn < N) C[gm * N + gn] = s * acc[nt][e];
+    }
+  }
+}
+
 // C = sum over the S splits of part (in split order).  Writes the fp32 result
 // to C32 (if not null) and, if C2 is not null, its bf16 hi/lo split
 // C2[m, :] = [bf16(c) | bf16(c - bf16(c)) | 0], each half zero-padded to R

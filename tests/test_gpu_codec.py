@@ -107,6 +107,16 @@ def test_ragged_lengths(qn, n):
             assert np.array_equal(got, nf4.dequantize_bf16_bits(ref))
 
 
+@pytest.mark.parametrize("n", [1, 63, 64, 65, 64 * 8 - 1, 64 * 9, 64 * 257 + 5, 1_000_003])
+def test_ragged_lengths_bf16_input(qn, n):
+    """bf16 input: stages of 8 blocks, so a partial last stage for n/64 not a
+    multiple of 8, and fewer stages than warps for the small cases."""
+    g = np.random.default_rng(n + 7)
+    x = (g.standard_normal(n) * 0.02).astype(np.float32).reshape(1, n)
+    q, ref, _ = _quant_both(qn, x, bf16=True)
+    _check_state(q, ref)
+
+
 def test_bf16_input(qn):
     g = synth.rng(11)
     W = synth.with_outliers_exact(g, synth.normal(g, (512, 768), 0.02), 0.001, 0.2)
