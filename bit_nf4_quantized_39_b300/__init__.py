@@ -122,6 +122,9 @@ def _dev_bf16(t: torch.Tensor, name: str) -> torch.Tensor:
 _WS: dict = {}
 
 
+_ZERO_AREA = 256 * 1024  # leading bytes of every workspace that must start at zero
+
+
 def _workspace(nbytes: int, device) -> torch.Tensor | None:
     """A cached device workspace of at least ``nbytes`` bytes (256-byte aligned)."""
     if nbytes == 0:
@@ -129,7 +132,8 @@ def _workspace(nbytes: int, device) -> torch.Tensor | None:
     key = (str(device), torch.cuda.current_stream(device).cuda_stream)
     ws = _WS.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.zeros(nbytes + 512, dtype=torch.uint8, device=device)  # semaphore area starts at zero
+        ws = torch.empty(nbytes + 512, dtype=torch.uint8, device=device)
+        ws[:min(ws.numel(), _ZERO_AREA + 512)].zero_()  # the semaphore area starts at zero
         _WS[key] = ws
     return ws
 

@@ -598,8 +598,9 @@ qn_status launch_tc_bwd(const qn_nf4 *Q, const uint16_t *dY, int64_t M, const ui
   uint16_t *wt = sp.take<uint16_t>(static_cast<size_t>(ldw) * k);
   uint16_t *at2 = sp.take<uint16_t>(static_cast<size_t>(k) * qn::kTfUCols);
   {
-    dim3 grid(static_cast<unsigned>(k / 64), static_cast<unsigned>(qn_ceil_div(d, 64)));
-    qn::nf4_dequant_t_kernel<<<grid, 256, 0, st>>>(view_of(Q), ldw, wt);
+    int64_t grid = (k / 64) * qn_ceil_div(d, 64);
+    if (grid > static_cast<int64_t>(sm_count()) * 8) grid = static_cast<int64_t>(sm_count()) * 8;
+    qn::nf4_dequant_t_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(view_of(Q), ldw, wt);
     QN_LAUNCH_CHECK("nf4_dequant_t_kernel");
     qn::lora_pack_at2_kernel<<<static_cast<unsigned>(qn_ceil_div(k * qn::kTfUCols, 256)), 256, 0, st>>>(A, r, k, at2);
     QN_LAUNCH_CHECK("lora_pack_at2_kernel");
@@ -1099,29 +1100,34 @@ qn_status loftq_run_p(const float *W, int64_t d, int64_t k, int32_t r, float alp
     const int nb = static_cast<int>(qn_ceil_div(rows, qn::kLqGramRows));
     qn::lq_gram_part_kernel<P><<<nb, 256, 0, st>>>(Ym, rows, gpart);
     QN_LAUNCH_CHECK("lq_gram_part_kernel");
-    qn::lq_gram_reduce_kernel<P><<<static_cast<unsigned>(qn_ceil_div(P * P, 256)), 256, 0, st>>>(gpart, nb, G);
+    qn::lq_gram_reduce_kernel<P><<<static_cast<unsigned>(qn_ceil_div(P * P * 32, 256)), 256, 0, st>>>(gpart, nb, G);
     QN_LAUNCH_CHECK("lq_gram_reduce_kernel");
     return QN_OK;
   };
+  // P == 32: CholeskyQR2 in one cooperative launch; the panel is Ym itself
+  // (S == 0) or the sum of the S split partials in ppart, written to Ym.
+  auto cholqr2_32 = [&](const float *parts, int S, float *Ym, int64_t rows) -> qn_status {
+    int64_t grid = qn_ceil_div(rows, 32);
+    if (grid > sms) grid = sms;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    QN_TRY(cuda_check(cudaLaunchKernelEx(&cfg, qn::lq_cholqr2_p32_kernel, parts, S, Ym, rows, p,
+                                         reinterpret_cast<double *>(gpart), G, sem + kLqBarWord),
+                      "lq_cholqr2_p32_kernel"));
+    QN_LAUNCH_CHECK("lq_cholqr2_p32_kernel");
+    return QN_OK;
+  };
   auto orth = [&](float *Ym, int64_t rows) -> qn_status {  // CholeskyQR2: Ym <- Ym L^{-T}, twice
-    if constexpr (P == 32) {  // both rounds in one cooperative launch
-      int64_t grid = qn_ceil_div(rows, 32);
-      if (grid > sms) grid = sms;
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(static_cast<unsigned>(grid));
-      cfg.blockDim = dim3(256);
-      cfg.dynamicSmemBytes = 0;
-      cfg.stream = st;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeCooperative;
-      attr[0].val.cooperative = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      QN_TRY(cuda_check(cudaLaunchKernelEx(&cfg, qn::lq_cholqr2_p32_kernel, Ym, rows, p,
-                                           reinterpret_cast<double *>(gpart), G, sem + kLqBarWord),
-                        "lq_cholqr2_p32_kernel"));
-      QN_LAUNCH_CHECK("lq_cholqr2_p32_kernel");
-      return QN_OK;
+    if constexpr (P == 32) {
+      return cholqr2_32(nullptr, 0, Ym, rows);
     } else {
       for (int rep = 0; rep < 2; ++rep) {
         QN_TRY(gram(Ym, rows));
@@ -1138,7 +1144,55 @@ qn_status loftq_run_p(const float *W, int64_t d, int64_t k, int32_t r, float alp
     QN_LAUNCH_CHECK("lq_split_reduce_kernel");
     return QN_OK;
   };
+  // Splits of the register-tiled 32-column products: about three CTAs per
+  // SM, within what the partial buffer holds.
+  const size_t ppart_floats = std::max(static_cast<size_t>(Srz) * d, static_cast<size_t>(Srty) * k) * qn::kLqMaxP;
+  auto big_splits = [&](int64_t out_rows, int64_t kdim, int occ) -> int64_t {  // one wave of occ CTAs per SM
+    int64_t S = (static_cast<int64_t>(occ) * sms) / qn_ceil_div(out_rows, qn::kLqBig);
+    if (S > 16) S = 16;
+    if (S > kdim / 64) S = kdim / 64;
+    const int64_t cap = static_cast<int64_t>(ppart_floats / (static_cast<size_t>(out_rows) * 32));
+    if (S > cap) S = cap;
+    return S < 1 ? 1 : S;
+  };
+  // P == 32: the register-tiled product into the split partials; returns the
+  // number of splits.  right: R Z (d rows, K = k); otherwise R^T Y (k rows).
+  auto prod32 = [&](bool right, const float *in, int *S_out) -> qn_status {
+    const int64_t rows = right ? d : k, kdim = right ? k : d;
+    constexpr int smem_rz = qn::kLqPipe * qn::kLqRzStage, smem_rty = qn::kLqPipe * qn::kLqRtyStage;
+    int occ = 1;
+    if (right) {
+      QN_TRY(cuda_check(cudaFuncSetAttribute(qn::lq_rz32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_rz),
+                        "cudaFuncSetAttribute(rz smem)"));
+      QN_TRY(cuda_check(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, qn::lq_rz32_kernel, 256, smem_rz),
+                        "rz occupancy"));
+    } else {
+      QN_TRY(cuda_check(
+          cudaFuncSetAttribute(qn::lq_rty32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_rty),
+          "cudaFuncSetAttribute(rty smem)"));
+      QN_TRY(cuda_check(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, qn::lq_rty32_kernel, 256, smem_rty),
+                        "rty occupancy"));
+    }
+    const int64_t per = qn_ceil_div(qn_ceil_div(kdim, big_splits(rows, kdim, occ < 1 ? 1 : occ)), qn::kLqTile) *
+                        qn::kLqTile;
+    const int S = static_cast<int>(qn_ceil_div(kdim, per));
+    const dim3 grid(static_cast<unsigned>(qn_ceil_div(rows, qn::kLqBig)), static_cast<unsigned>(S));
+    if (right) {
+      qn::lq_rz32_kernel<<<grid, 256, smem_rz, st>>>(Tbuf, d, k, in, per, ppart);
+      QN_LAUNCH_CHECK("lq_rz32_kernel");
+    } else {
+      qn::lq_rty32_kernel<<<grid, 256, smem_rty, st>>>(Tbuf, d, k, in, per, ppart);
+      QN_LAUNCH_CHECK("lq_rty32_kernel");
+    }
+    *S_out = S;
+    return QN_OK;
+  };
   auto r_times = [&](const float *Z, float *Yo) -> qn_status {  // Yo = R Z   (d x P)
+    if constexpr (P == 32) {
+      int S = 1;
+      QN_TRY(prod32(true, Z, &S));
+      return reduce(S, d * P, Yo);
+    }
     const int64_t cps = qn_ceil_div(qn_ceil_div(k, Srz), qn::kLqTile) * qn::kLqTile;
     const int S = static_cast<int>(qn_ceil_div(k, cps));
     qn::lq_rz_kernel<P><<<dim3(static_cast<unsigned>(qn_ceil_div(d, qn::kLqTile)), static_cast<unsigned>(S)), 256, 0,
@@ -1147,12 +1201,24 @@ qn_status loftq_run_p(const float *W, int64_t d, int64_t k, int32_t r, float alp
     return reduce(S, d * P, Yo);
   };
   auto rt_times = [&](const float *Ym, float *Zo) -> qn_status {  // Zo = R^T Y  (k x P)
+    if constexpr (P == 32) {
+      int S = 1;
+      QN_TRY(prod32(false, Ym, &S));
+      return reduce(S, k * P, Zo);
+    }
     const int64_t rps = qn_ceil_div(qn_ceil_div(d, Srty), qn::kLqTile) * qn::kLqTile;
     const int S = static_cast<int>(qn_ceil_div(d, rps));
     qn::lq_rty_kernel<P><<<dim3(static_cast<unsigned>(k / qn::kLqTile), static_cast<unsigned>(S)), 256, 0, st>>>(
         Tbuf, d, k, Ym, rps, ppart);
     QN_LAUNCH_CHECK("lq_rty_kernel");
     return reduce(S, k * P, Zo);
+  };
+  // P == 32: out = orthonormalised (R Z or R^T Y); the split partials are
+  // summed inside the CholeskyQR2 launch.
+  auto prod_orth32 = [&](bool right, const float *in, float *out) -> qn_status {
+    int S = 1;
+    QN_TRY(prod32(right, in, &S));
+    return cholqr2_32(ppart, S, out, right ? d : k);
   };
 
   // t = 0: Q_0 = NF4(W) (or the caller's Q), residual without adapter.
@@ -1173,13 +1239,21 @@ qn_status loftq_run_p(const float *W, int64_t d, int64_t k, int32_t r, float alp
     qn::omega_kernel<<<static_cast<unsigned>(qn_ceil_div(k * P, 256)), 256, 0, st>>>(
         Om, k, p, P, seed ^ (0x9E3779B97F4A7C15ull * static_cast<uint64_t>(t)));
     QN_LAUNCH_CHECK("omega_kernel");
-    QN_TRY(r_times(Om, Y));
-    QN_TRY(orth(Y, d));
-    for (int it = 0; it < power_iters; ++it) {
-      QN_TRY(rt_times(Y, Zt));
-      QN_TRY(orth(Zt, k));
-      QN_TRY(r_times(Zt, Y));
+    if constexpr (P == 32) {
+      QN_TRY(prod_orth32(true, Om, Y));
+      for (int it = 0; it < power_iters; ++it) {
+        QN_TRY(prod_orth32(false, Y, Zt));
+        QN_TRY(prod_orth32(true, Zt, Y));
+      }
+    } else {
+      QN_TRY(r_times(Om, Y));
       QN_TRY(orth(Y, d));
+      for (int it = 0; it < power_iters; ++it) {
+        QN_TRY(rt_times(Y, Zt));
+        QN_TRY(orth(Zt, k));
+        QN_TRY(r_times(Zt, Y));
+        QN_TRY(orth(Y, d));
+      }
     }
     QN_TRY(rt_times(Y, Zt));  // Zt = R^T Y, i.e. (Y^T R)^T
     QN_TRY(gram(Zt, k));

@@ -81,30 +81,34 @@ lowrank_sub_kernel(const float *__restrict__ W, const float *__restrict__ B, con
   }
 }
 
-// R = W - deq(Q) in fp32 (the exact fp32 dequantised weight), 32 per thread.
+// R = W - deq(Q) in fp32 (the exact fp32 dequantised weight).  A lane takes
+// 4-byte words of codes (8 elements), a warp 32 consecutive words per step,
+// so code loads and the 32-byte W reads and R writes of a lane are
+// contiguous across the warp.  n % 8 == 0.
 __global__ void __launch_bounds__(256)
 residual_kernel(QnNF4View q, const float *__restrict__ W, float *__restrict__ R, int64_t n) {
   __shared__ float s_lut[16];
   if (threadIdx.x < 16) s_lut[threadIdx.x] = c_nf4_levels[threadIdx.x];
   __syncthreads();
-  const int64_t nchunk = n / 32;
-  for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < nchunk;
-       c += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const uint4 w4 = __ldg(reinterpret_cast<const uint4 *>(q.codes) + c);
-    const float m = block_scale(q, c >> 1);
-    const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-    const float4 *src = reinterpret_cast<const float4 *>(W + c * 32);
-    float4 *dst = reinterpret_cast<float4 *>(R + c * 32);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t nib = w[i / 2] >> (16 * (i & 1));
-      float4 x = __ldg(src + i);
-      x.x -= __fmul_rn(s_lut[nib & 15u], m);
-      x.y -= __fmul_rn(s_lut[(nib >> 4) & 15u], m);
-      x.z -= __fmul_rn(s_lut[(nib >> 8) & 15u], m);
-      x.w -= __fmul_rn(s_lut[(nib >> 12) & 15u], m);
-      dst[i] = x;
-    }
+  const int64_t nword = n / 8;
+  const uint32_t *__restrict__ cw = reinterpret_cast<const uint32_t *>(q.codes);
+  for (int64_t w = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; w < nword;
+       w += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const uint32_t c = __ldg(cw + w);
+    const float m = block_scale(q, w >> 3);
+    const float4 *src = reinterpret_cast<const float4 *>(W) + 2 * w;
+    float4 x0 = __ldcs(src), x1 = __ldcs(src + 1);
+    x0.x -= __fmul_rn(s_lut[c & 15u], m);
+    x0.y -= __fmul_rn(s_lut[(c >> 4) & 15u], m);
+    x0.z -= __fmul_rn(s_lut[(c >> 8) & 15u], m);
+    x0.w -= __fmul_rn(s_lut[(c >> 12) & 15u], m);
+    x1.x -= __fmul_rn(s_lut[(c >> 16) & 15u], m);
+    x1.y -= __fmul_rn(s_lut[(c >> 20) & 15u], m);
+    x1.z -= __fmul_rn(s_lut[(c >> 24) & 15u], m);
+    x1.w -= __fmul_rn(s_lut[c >> 28], m);
+    float4 *dst = reinterpret_cast<float4 *>(R) + 2 * w;
+    dst[0] = x0;
+    dst[1] = x1;
   }
 }
 
@@ -234,6 +238,154 @@ lq_rty_kernel(const float *__restrict__ R, int64_t n_rows, int64_t n_cols, const
   }
 }
 
+// Register-tiled products for 32-column panels (the common r + oversample
+// <= 32).  A thread accumulates a 4 x 4 block of the output from 16-byte
+// shared-memory reads (8 multiply-adds per read); tiles arrive through a
+// kLqPipe-deep cp.async ring (one CTA barrier per 32-deep K step).  K is
+// split over gridDim.y as in lq_rz_kernel / lq_rty_kernel.
+constexpr int kLqPipe = 3;
+constexpr int kLqBig = 128;  // output rows per CTA
+constexpr int kLqRzStage = (kLqBig * (kLqTile + 4) + kLqTile * 32) * 4;   // R tile [128][36] + Z tile [32][32]
+constexpr int kLqRtyStage = (kLqTile * (kLqBig + 4) + kLqTile * 32) * 4;  // R tile [32][132] + Y tile [32][32]
+
+__device__ __forceinline__ void lq_cp16(uint32_t dst, const void *src, bool ok) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(ok ? 16u : 0u) : "memory");
+}
+
+// part[split][i][c] = sum over the split's j of R[i, j] Z[j, c]; thread
+// (rows 4 (tid / 8) .., columns 4 (tid % 8) ..) of a 128-row tile.
+__global__ void __launch_bounds__(256)
+lq_rz32_kernel(const float *__restrict__ R, int64_t n_rows, int64_t n_cols, const float *__restrict__ Z,
+               int64_t cols_per_split, float *__restrict__ part) {
+  extern __shared__ __align__(16) float lq_pipe_smem[];
+  const int tid = threadIdx.x, rg = tid >> 3, cg = tid & 7;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kLqBig;
+  const int64_t jb = static_cast<int64_t>(blockIdx.y) * cols_per_split;
+  const int64_t je = (jb + cols_per_split < n_cols) ? jb + cols_per_split : n_cols;
+  const int nch = static_cast<int>((je - jb) / kLqTile);
+  const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(lq_pipe_smem));
+  auto load = [&](int slot, int64_t j0) {
+    const uint32_t sr = sbase + slot * kLqRzStage, sz = sr + kLqBig * (kLqTile + 4) * 4;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {  // R: 128 rows x 8 chunks
+      const int ch = tid + 256 * u, rr = ch >> 3, c4 = (ch & 7) * 4;
+      const int64_t i = i0 + rr;
+      lq_cp16(sr + (rr * (kLqTile + 4) + c4) * 4, (i < n_rows) ? R + i * n_cols + j0 + c4 : R, i < n_rows);
+    }
+    {  // Z: 32 rows x 8 chunks
+      const int rr = tid >> 3, c4 = (tid & 7) * 4;
+      lq_cp16(sz + (rr * 32 + c4) * 4, Z + (j0 + rr) * 32 + c4, true);
+    }
+  };
+  float acc[4][4] = {};
+#pragma unroll
+  for (int st = 0; st < kLqPipe - 1; ++st) {
+    if (st < nch) load(st, jb + static_cast<int64_t>(st) * kLqTile);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  for (int ch = 0; ch < nch; ++ch) {
+    asm volatile("cp.async.wait_group %0;" ::"n"(kLqPipe - 2) : "memory");
+    __syncthreads();
+    const int nx = ch + kLqPipe - 1;
+    if (nx < nch) load(nx % kLqPipe, jb + static_cast<int64_t>(nx) * kLqTile);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    const float *sR = lq_pipe_smem + (ch % kLqPipe) * (kLqRzStage / 4);
+    const float *sZ = sR + kLqBig * (kLqTile + 4);
+#pragma unroll
+    for (int kq = 0; kq < kLqTile / 4; ++kq) {
+      float4 rv[4], zv[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) rv[a] = *reinterpret_cast<const float4 *>(sR + (4 * rg + a) * (kLqTile + 4) + 4 * kq);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) zv[q] = *reinterpret_cast<const float4 *>(sZ + (4 * kq + q) * 32 + 4 * cg);
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const float r4[4] = {rv[a].x, rv[a].y, rv[a].z, rv[a].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[a][0] = fmaf(r4[q], zv[q].x, acc[a][0]);
+          acc[a][1] = fmaf(r4[q], zv[q].y, acc[a][1]);
+          acc[a][2] = fmaf(r4[q], zv[q].z, acc[a][2]);
+          acc[a][3] = fmaf(r4[q], zv[q].w, acc[a][3]);
+        }
+      }
+    }
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int64_t i = i0 + 4 * rg + a;
+    if (i < n_rows)
+      *reinterpret_cast<float4 *>(part + (static_cast<int64_t>(blockIdx.y) * n_rows + i) * 32 + 4 * cg) =
+          make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+  }
+}
+
+// part[split][j][c] = sum over the split's i of R[i, j] Y[i, c]; thread
+// (columns 4 (tid / 8) .. of a 128-column tile, panel columns 4 (tid % 8) ..).
+__global__ void __launch_bounds__(256)
+lq_rty32_kernel(const float *__restrict__ R, int64_t n_rows, int64_t n_cols, const float *__restrict__ Y,
+                int64_t rows_per_split, float *__restrict__ part) {
+  extern __shared__ __align__(16) float lq_pipe_smem[];
+  const int tid = threadIdx.x, jg = tid >> 3, cg = tid & 7;
+  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * kLqBig;
+  const int64_t ib = static_cast<int64_t>(blockIdx.y) * rows_per_split;
+  const int64_t ie = (ib + rows_per_split < n_rows) ? ib + rows_per_split : n_rows;
+  const int nch = static_cast<int>((ie - ib + kLqTile - 1) / kLqTile);
+  const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(lq_pipe_smem));
+  auto load = [&](int slot, int64_t ia) {
+    const uint32_t sr = sbase + slot * kLqRtyStage, sy = sr + kLqTile * (kLqBig + 4) * 4;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {  // R: 32 rows x 32 chunks
+      const int ch = tid + 256 * u, rr = ch >> 5, c4 = (ch & 31) * 4;
+      const int64_t i = ia + rr, j = j0 + c4;
+      const bool ok = i < ie && j < n_cols;
+      lq_cp16(sr + (rr * (kLqBig + 4) + c4) * 4, ok ? R + i * n_cols + j : R, ok);
+    }
+    {  // Y: 32 rows x 8 chunks
+      const int rr = tid >> 3, c4 = (tid & 7) * 4;
+      const int64_t i = ia + rr;
+      lq_cp16(sy + (rr * 32 + c4) * 4, (i < ie) ? Y + i * 32 + c4 : Y, i < ie);
+    }
+  };
+  float acc[4][4] = {};
+#pragma unroll
+  for (int st = 0; st < kLqPipe - 1; ++st) {
+    if (st < nch) load(st, ib + static_cast<int64_t>(st) * kLqTile);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
+  for (int ch = 0; ch < nch; ++ch) {
+    asm volatile("cp.async.wait_group %0;" ::"n"(kLqPipe - 2) : "memory");
+    __syncthreads();
+    const int nx = ch + kLqPipe - 1;
+    if (nx < nch) load(nx % kLqPipe, ib + static_cast<int64_t>(nx) * kLqTile);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    const float *sR = lq_pipe_smem + (ch % kLqPipe) * (kLqRtyStage / 4);
+    const float *sY = sR + kLqTile * (kLqBig + 4);
+#pragma unroll 8
+    for (int ii = 0; ii < kLqTile; ++ii) {
+      const float4 rv = *reinterpret_cast<const float4 *>(sR + ii * (kLqBig + 4) + 4 * jg);
+      const float4 yv = *reinterpret_cast<const float4 *>(sY + ii * 32 + 4 * cg);
+      const float r4[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        acc[a][0] = fmaf(r4[a], yv.x, acc[a][0]);
+        acc[a][1] = fmaf(r4[a], yv.y, acc[a][1]);
+        acc[a][2] = fmaf(r4[a], yv.z, acc[a][2]);
+        acc[a][3] = fmaf(r4[a], yv.w, acc[a][3]);
+      }
+    }
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int64_t j = j0 + 4 * jg + a;
+    if (j < n_cols)
+      *reinterpret_cast<float4 *>(part + (static_cast<int64_t>(blockIdx.y) * n_cols + j) * 32 + 4 * cg) =
+          make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+  }
+}
+
 // out[e] = sum over the S splits, in order, of part[split][e]   (e < n).
 __global__ void lq_split_reduce_kernel(const float *__restrict__ part, int S, int64_t n, float *__restrict__ out) {
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -289,13 +441,18 @@ lq_gram_part_kernel(const float *__restrict__ Y, int64_t n, float *__restrict__ 
     for (int b = 0; b < TW; ++b) pp[(ta * TW + a) * P + tb * TW + b] = acc[a][b];
 }
 
+// G[e] = sum over the blocks of part[block][e] in fp64: one warp per entry
+// (lane-strided partial sums, then a fixed shuffle tree).
 template <int P>
 __global__ void lq_gram_reduce_kernel(const float *__restrict__ part, int nblocks, double *__restrict__ G) {
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= P * P) return;
-  double s = 0.0;
-  for (int b = 0; b < nblocks; ++b) s += static_cast<double>(part[static_cast<int64_t>(b) * P * P + e]);
-  G[e] = s;
+  const int e = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (e >= P * P) return;  // uniform over the warp
+  double v = 0.0;
+  for (int b = lane; b < nblocks; b += 32) v += static_cast<double>(part[static_cast<int64_t>(b) * P * P + e]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) G[e] = v;
 }
 
 // One CTA of 256 threads: Cholesky G = L L^T of the leading p x p block (G
@@ -375,15 +532,19 @@ lq_trsm_rows_kernel(float *__restrict__ Y, int64_t n, const float *__restrict__ 
 // Yanagisawa, Yamamoto, "CholeskyQR2: a simple and communication-avoiding
 // algorithm for computing a tall-skinny QR factorization", ScalA 2014): two
 // rounds of  G = Y^T Y,  G = L L^T,  Y <- Y L^{-T}.  Every CTA is resident
-// at once (cooperative launch) and owns a contiguous range of rows.  A round:
+// at once (cooperative launch) and owns a contiguous range of rows.  With
+// S > 0 the panel is first formed as the sum, in split order, of the S
+// split-K partials of the product that made it (part[z][n][32], the sums
+// lq_split_reduce_kernel forms) and written to Y.  A round:
 //   1. each CTA sums y y^T over its rows (fp32 within 32-row chunks, fp64
 //      across chunks) into its fp64 partial;
 //   2. grid barrier; the P*P entries of G are split over the grid's warps,
 //      each summing the CTAs' partials in a fixed order (fp64);
 //   3. grid barrier; every CTA factors G itself (one warp, lane i holding row
-//      i of the matrix in registers, fp32 as lq_chol_kernel: pivots clamped
-//      to a floor of 1e-12 times the largest diagonal entry) and solves its
-//      rows against L (as lq_trsm_rows_kernel).
+//      i of the matrix in registers, fp32: pivots clamped to a floor of
+//      1e-12 times the largest diagonal entry, as lq_chol_kernel, but with
+//      the hardware reciprocal square root) and solves its rows against L
+//      by forward substitution (multiplying by the reciprocal pivots).
 // Grid barriers are counters in the zero area with bounded waits: a wait
 // that expires records QN_DEV_TIMEOUT and the kernel carries on (the panel is
 // then wrong and the host reports the status).  The last CTA to leave resets
@@ -411,32 +572,43 @@ __device__ __forceinline__ void lq_grid_barrier(unsigned int *cnt, unsigned int 
 }
 
 // Step K of the one-warp Cholesky of a 32 x 32 matrix, lane i holding row i
-// in a[]: pivot from lane K, column K scaled below it, trailing lower
-// triangle updated with the shuffled column (compile-time indices only).
+// in a[] (compile-time indices only): pivot from lane K (hardware reciprocal
+// square root), column K scaled below it, the scaled column published in
+// shared memory (col, 16-byte aligned) and read back four entries at a time
+// for the trailing update.  Updates of entries right of a lane's diagonal are
+// harmless (never read) and are not masked; rows past p stay identity rows.
 template <int K>
-__device__ __forceinline__ void lq_chol_warp_step(float (&a)[32], int lane, int p, float floor_v) {
+__device__ __forceinline__ void lq_chol_warp_step(float (&a)[32], int lane, int p, float floor_v, float *col) {
   if constexpr (K < 32) {
     const float dk = __shfl_sync(0xffffffffu, a[K], K);
-    const float piv = (K < p) ? sqrtf(fmaxf(dk, floor_v)) : 1.f;
-    const float inv = 1.0f / piv;
-    if (lane == K) a[K] = piv;
-    if (lane > K && lane < p) a[K] *= inv;
+    const float x = fmaxf(dk, floor_v);
+    const float rs = rsqrtf(x);  // hardware reciprocal square root
+    if (lane == K) a[K] = (K < p) ? x * rs : 1.f;
+    if (lane > K && lane < p) a[K] *= rs;
     const float lik = a[K];
+    col[lane] = lik;
+    __syncwarp();
 #pragma unroll
-    for (int c = K + 1; c < 32; ++c) {
-      const float lck = __shfl_sync(0xffffffffu, lik, c);
-      if (lane >= c && lane < p && c < p) a[c] = fmaf(-lik, lck, a[c]);
+    for (int g = (K + 1) / 4; g < 8; ++g) {
+      const float4 v = reinterpret_cast<const float4 *>(col)[g];
+      const float cv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (4 * g + e > K) a[4 * g + e] = fmaf(-lik, cv[e], a[4 * g + e]);
     }
-    lq_chol_warp_step<K + 1>(a, lane, p, floor_v);
+    __syncwarp();
+    lq_chol_warp_step<K + 1>(a, lane, p, floor_v, col);
   }
 }
 
 __global__ void __launch_bounds__(256, 1)
-lq_cholqr2_p32_kernel(float *__restrict__ Y, int64_t n, int p, double *__restrict__ gpart,
-                      double *__restrict__ G, unsigned int *__restrict__ bar) {
+lq_cholqr2_p32_kernel(const float *__restrict__ part, int S, float *__restrict__ Y, int64_t n, int p,
+                      double *__restrict__ gpart, double *__restrict__ G, unsigned int *__restrict__ bar) {
   constexpr int P = 32;
   __shared__ __align__(16) float sY[32][P];
   __shared__ float sL[P][P + 1];
+  __shared__ float sRinv[P];
+  __shared__ __align__(16) float sCol[P];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int ta = tid / 16, tb = tid % 16;  // 2 x 2 tile of G: rows 2 ta.., columns 2 tb..
   const unsigned int nct = gridDim.x;
@@ -452,8 +624,21 @@ lq_cholqr2_p32_kernel(float *__restrict__ Y, int64_t n, int p, double *__restric
       for (int t = tid; t < 32 * P / 4; t += 256) {
         const int rr = t / (P / 4), c4 = (t % (P / 4)) * 4;
         const int64_t i = i0 + rr;
-        *reinterpret_cast<float4 *>(&sY[rr][c4]) =
-            (i < r1) ? __ldcg(reinterpret_cast<const float4 *>(Y + i * P + c4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < r1) {
+          if (round == 0 && S > 0) {  // the panel is the sum of the S partials, in split order
+            const float *src = part + i * P + c4;
+            v = __ldcg(reinterpret_cast<const float4 *>(src));
+            for (int z = 1; z < S; ++z) {
+              const float4 w = __ldcg(reinterpret_cast<const float4 *>(src + static_cast<int64_t>(z) * n * P));
+              v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+            }
+            __stcg(reinterpret_cast<float4 *>(Y + i * P + c4), v);
+          } else {
+            v = __ldcg(reinterpret_cast<const float4 *>(Y + i * P + c4));
+          }
+        }
+        *reinterpret_cast<float4 *>(&sY[rr][c4]) = v;
       }
       __syncthreads();
       float f[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
@@ -502,10 +687,15 @@ lq_cholqr2_p32_kernel(float *__restrict__ Y, int64_t n, int p, double *__restric
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       const float floor_v = fmaxf(mx, 1e-30f) * 1e-12f;
-      lq_chol_warp_step<0>(a, lane, p, floor_v);
+      lq_chol_warp_step<0>(a, lane, p, floor_v, sCol);
 #pragma unroll
       for (int j = 0; j < P; ++j)
         sL[lane][j] = (lane < p && j < p) ? ((j <= lane) ? a[j] : 0.f) : ((lane == j) ? 1.f : 0.f);
+      float dgl = 1.f;  // L[lane][lane]
+#pragma unroll
+      for (int j = 0; j < P; ++j)
+        if (j == lane && lane < p) dgl = a[j];
+      sRinv[lane] = 1.0f / dgl;
     }
     __syncthreads();
     // rows of this CTA: y <- y L^{-T} (forward substitution per row)
@@ -521,7 +711,7 @@ lq_cholqr2_p32_kernel(float *__restrict__ Y, int64_t n, int p, double *__restric
         float acc2 = y[c];
 #pragma unroll
         for (int b = 0; b < c; ++b) acc2 = fmaf(-sL[c][b], y[b], acc2);
-        y[c] = (c < p) ? acc2 / sL[c][c] : 0.f;
+        y[c] = (c < p) ? acc2 * sRinv[c] : 0.f;
       }
 #pragma unroll
       for (int c = 0; c < P; c += 4)
@@ -715,28 +905,75 @@ lq_project_kernel(const float *__restrict__ in, int64_t n, const float *__restri
   }
 }
 
-// partial[block] = sum over its elements of (R - s * B A)^2 in fp64.
+// partial[block] = sum over its elements of (R - s * B A)^2.  Tiles of 64
+// rows x 128 columns (grid-strided); thread (8 rows 8 (tid / 32) .., 4 columns
+// 4 (tid % 32) ..): B A in fp32 from shared-memory tiles of 16 adapter
+// columns at a time, the 32 squared differences summed in fp32, tiles and the
+// CTA's threads summed in fp64.
+constexpr int kRnRows = 64, kRnCols = 128;
+
 __global__ void __launch_bounds__(256)
 resid_norm_kernel(const float *__restrict__ R, const float *__restrict__ B, const float *__restrict__ A,
                   int64_t d, int64_t k, int r, float s, double *__restrict__ partial) {
+  __shared__ __align__(16) float sA[16][kRnCols];
+  __shared__ __align__(16) float sB[kRnRows][16 + 4];
   __shared__ double red[256];
-  double acc = 0.0;
-  const int64_t n = d * k;
-  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n;
-       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t row = e / k, col = e % k;
-    float lr = 0.f;
-    for (int q = 0; q < r; ++q) lr = fmaf(__ldg(B + row * r + q), __ldg(A + q * k + col), lr);
-    const double diff = static_cast<double>(R[e]) - static_cast<double>(s) * static_cast<double>(lr);
-    acc += diff * diff;
+  const int tid = threadIdx.x, rg = tid >> 5, cg = tid & 31;
+  const int64_t tiles_c = (k + kRnCols - 1) / kRnCols, tiles = tiles_c * ((d + kRnRows - 1) / kRnRows);
+  double total = 0.0;
+  for (int64_t tl = blockIdx.x; tl < tiles; tl += gridDim.x) {
+    const int64_t r0 = (tl / tiles_c) * kRnRows, c0 = (tl % tiles_c) * kRnCols;
+    float acc[8][4] = {};
+    for (int q0 = 0; q0 < r; q0 += 16) {
+      for (int t = tid; t < 16 * kRnCols; t += 256) {
+        const int q = t / kRnCols, c = t % kRnCols;
+        sA[q][c] = (q0 + q < r && c0 + c < k) ? __ldg(A + static_cast<int64_t>(q0 + q) * k + c0 + c) : 0.f;
+      }
+      for (int t = tid; t < kRnRows * 16; t += 256) {
+        const int i = t / 16, q = t % 16;
+        sB[i][q] = (q0 + q < r && r0 + i < d) ? __ldg(B + (r0 + i) * r + q0 + q) : 0.f;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const float4 av = *reinterpret_cast<const float4 *>(&sA[q][4 * cg]);
+#pragma unroll
+        for (int a = 0; a < 8; ++a) {
+          const float bv = sB[8 * rg + a][q];
+          acc[a][0] = fmaf(bv, av.x, acc[a][0]);
+          acc[a][1] = fmaf(bv, av.y, acc[a][1]);
+          acc[a][2] = fmaf(bv, av.z, acc[a][2]);
+          acc[a][3] = fmaf(bv, av.w, acc[a][3]);
+        }
+      }
+      __syncthreads();
+    }
+    float sq = 0.f;
+    const int64_t col = c0 + 4 * cg;
+    if (col < k) {
+#pragma unroll
+      for (int a = 0; a < 8; ++a) {
+        const int64_t row = r0 + 8 * rg + a;
+        if (row < d) {
+          const float4 rv = __ldcs(reinterpret_cast<const float4 *>(R + row * k + col));
+          const float e0 = fmaf(-s, acc[a][0], rv.x), e1 = fmaf(-s, acc[a][1], rv.y);
+          const float e2 = fmaf(-s, acc[a][2], rv.z), e3 = fmaf(-s, acc[a][3], rv.w);
+          sq = fmaf(e0, e0, sq);
+          sq = fmaf(e1, e1, sq);
+          sq = fmaf(e2, e2, sq);
+          sq = fmaf(e3, e3, sq);
+        }
+      }
+    }
+    total += static_cast<double>(sq);
   }
-  red[threadIdx.x] = acc;
+  red[tid] = total;
   __syncthreads();
   for (int w = 128; w > 0; w >>= 1) {
-    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    if (tid < w) red[tid] += red[tid + w];
     __syncthreads();
   }
-  if (threadIdx.x == 0) partial[blockIdx.x] = red[0];
+  if (tid == 0) partial[blockIdx.x] = red[0];
 }
 
 __global__ void sum_partials_kernel(const double *__restrict__ partial, int count, double *__restrict__ out) {

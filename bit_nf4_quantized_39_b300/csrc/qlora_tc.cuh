@@ -310,48 +310,59 @@ struct TbBars {
   int abort;
 };
 
-// W^T[c, r] = bf16(level[code(r, c)] * m(r, c / 64)) for a 64 x 64 tile; W^T
-// has row stride ldw (d rounded up to a multiple of 8).
+// W^T[c, r] = bf16(level[code(r, c)] * m(r, c / 64)), 64 x 64 tiles of W
+// (grid-strided); W^T has row stride ldw (d rounded up to a multiple of 8).
+// A thread decodes rows r, r + 1 of W at 8 columns (two 4-byte code words;
+// a warp reads 8 rows x 32 contiguous bytes) into 8 words, each the pair
+// (W[r][c], W[r+1][c]), of a shared tile T[c][r / 2] (row stride 36 words;
+// word column xor 4 * (c / 8 mod 8), so neither these stores nor the 16-byte
+// reads below conflict).  Then 8 threads write one 128-byte row of W^T.
+constexpr int kDtStride = 36;
+
 __global__ void __launch_bounds__(256) nf4_dequant_t_kernel(QnNF4View q, int64_t ldw, uint16_t *__restrict__ wt) {
   __shared__ float lv[16];
-  __shared__ uint16_t tile[64][64 + 2];  // [column of W][row of W]
+  __shared__ __align__(16) uint32_t tile[64][kDtStride];
   const int tid = threadIdx.x;
   if (tid < 16) lv[tid] = c_nf4_levels[tid];
-  const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64, c0 = static_cast<int64_t>(blockIdx.x) * 64;
-  const int rr = tid >> 2, part = tid & 3;  // row of the tile, 16-column quarter
-  const int64_t row = r0 + rr;
-  uint2 w = make_uint2(0u, 0u);
-  float m = 0.f;
-  if (row < q.d) {
-    w = __ldg(reinterpret_cast<const uint2 *>(q.codes + row * (q.k >> 1) + (c0 >> 1)) + part);
-    m = block_scale(q, row * (q.k >> 6) + (c0 >> 6));
-  }
   __syncthreads();
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const uint32_t word = (i < 8) ? w.x : w.y;
-    const uint32_t code = (word >> (4 * (i & 7))) & 15u;
-    tile[part * 16 + i][rr] = f32_to_bf16_bits(__fmul_rn(lv[code], m));
-  }
-  __syncthreads();
-  // 64 rows of W^T (columns c0 ..) x 64 entries (rows r0 ..): 16 threads per row, 4 entries each
-  const int oc = tid >> 2, seg = tid & 3;
-  const int64_t col = c0 + oc;
-  if (col < q.k) {
+  const int cg = tid & 7, rp = tid >> 3;  // 8 columns 8 cg .. ; rows 2 rp, 2 rp + 1
+  const int64_t tiles_c = (q.k + 63) / 64, tiles = tiles_c * ((q.d + 63) / 64);
+  for (int64_t tl = blockIdx.x; tl < tiles; tl += gridDim.x) {
+    const int64_t r0 = (tl / tiles_c) * 64, c0 = (tl % tiles_c) * 64;
+    uint32_t w[2] = {0u, 0u};
+    float m[2] = {0.f, 0.f};
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int e0 = seg * 16 + h * 8;
-      if (r0 + e0 + 8 <= q.d) {
-        uint4 v;
-        v.x = tile[oc][e0] | (static_cast<uint32_t>(tile[oc][e0 + 1]) << 16);
-        v.y = tile[oc][e0 + 2] | (static_cast<uint32_t>(tile[oc][e0 + 3]) << 16);
-        v.z = tile[oc][e0 + 4] | (static_cast<uint32_t>(tile[oc][e0 + 5]) << 16);
-        v.w = tile[oc][e0 + 6] | (static_cast<uint32_t>(tile[oc][e0 + 7]) << 16);
-        *reinterpret_cast<uint4 *>(wt + col * ldw + r0 + e0) = v;
-      } else {
-        for (int e = e0; e < e0 + 8 && r0 + e < q.d; ++e) wt[col * ldw + r0 + e] = tile[oc][e];
+      const int64_t row = r0 + 2 * rp + h;
+      if (row < q.d && c0 + 8 * cg < q.k) {
+        w[h] = __ldg(reinterpret_cast<const uint32_t *>(q.codes + row * (q.k >> 1) + (c0 >> 1)) + cg);
+        m[h] = block_scale(q, row * (q.k >> 6) + (c0 >> 6));
       }
     }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t lo = f32_to_bf16_bits(__fmul_rn(lv[(w[0] >> (4 * j)) & 15u], m[0]));
+      const uint32_t hi = f32_to_bf16_bits(__fmul_rn(lv[(w[1] >> (4 * j)) & 15u], m[1]));
+      tile[8 * cg + j][rp ^ (4 * cg)] = lo | (hi << 16);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int ch = tid + 256 * h, oc = ch >> 3, qd = ch & 7;  // row oc of the tile, rows 8 qd .. of W
+      const int64_t col = c0 + oc;
+      const int64_t rr = r0 + 8 * qd;
+      if (col < q.k && rr < q.d) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(&tile[oc][(4 * qd) ^ (4 * ((oc >> 3) & 7))]);
+        if (rr + 8 <= q.d) {
+          *reinterpret_cast<uint4 *>(wt + col * ldw + rr) = v;
+        } else {
+          const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+          for (int e = 0; e < 8 && rr + e < q.d; ++e)
+            wt[col * ldw + rr + e] = static_cast<uint16_t>(vv[e >> 1] >> (16 * (e & 1)));
+        }
+      }
+    }
+    __syncthreads();
   }
 }
 
