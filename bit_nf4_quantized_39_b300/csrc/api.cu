@@ -539,6 +539,41 @@ qn_status check_layer(const qn_nf4 *Q, const void *in, int64_t M, const void *A,
   return QN_OK;
 }
 
+// A second stream per device and calling thread, for side kernels that are
+// independent of the caller's stream work until a join: fork records an
+// event on `st` that the side stream waits for; join makes `st` wait for
+// everything issued on the side stream since.  Both are plain event
+// dependencies, so the pattern is also valid inside a stream capture.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+qn_status side_stream(SideStream **out) {
+  thread_local SideStream tab[64];
+  int dev = 0;
+  QN_TRY(cuda_check(cudaGetDevice(&dev), "cudaGetDevice"));
+  if (dev < 0 || dev >= 64) return fail(QN_EUNSUPPORTED, "device ordinal out of range");
+  SideStream &ss = tab[dev];
+  if (!ss.s) {
+    QN_TRY(cuda_check(cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking), "side stream"));
+    QN_TRY(cuda_check(cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming), "side stream event"));
+    QN_TRY(cuda_check(cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming), "side stream event"));
+  }
+  *out = &ss;
+  return QN_OK;
+}
+
+qn_status side_fork(SideStream *ss, cudaStream_t st) {
+  QN_TRY(cuda_check(cudaEventRecord(ss->fork, st), "fork record"));
+  return cuda_check(cudaStreamWaitEvent(ss->s, ss->fork, 0), "fork wait");
+}
+
+qn_status side_join(SideStream *ss, cudaStream_t st) {
+  QN_TRY(cuda_check(cudaEventRecord(ss->join, ss->s), "join record"));
+  return cuda_check(cudaStreamWaitEvent(st, ss->join, 0), "join wait");
+}
+
 // Adapter projection C = s P Qop^T (M x N, K deep) split over K so that
 // enough CTAs to fill the SMs run, then the splits summed in order into C32 (fp32)
 // or, with C2 set, its bf16 hi/lo split (each half padded to R columns, rows
@@ -592,7 +627,7 @@ qn_status launch_lora_proj(const uint16_t *P, int64_t M, int64_t K, const uint16
 // columns of W x 256 tokens (qlora_bwd_tc_kernel); v2 is the bf16 hi/lo split
 // of v = s dY B in the U2 layout of the forward.
 qn_status launch_tc_bwd(const qn_nf4 *Q, const uint16_t *dY, int64_t M, const uint16_t *v2, const uint16_t *A,
-                        int32_t r, uint16_t *dX, Span &sp, cudaStream_t st) {
+                        int32_t r, uint16_t *dX, Span &sp, cudaStream_t st, SideStream *side) {
   const int64_t d = Q->d, k = Q->k;
   const int64_t ldw = qn::tb_ldw(d);
   uint16_t *wt = sp.take<uint16_t>(static_cast<size_t>(ldw) * k);
@@ -602,7 +637,9 @@ qn_status launch_tc_bwd(const qn_nf4 *Q, const uint16_t *dY, int64_t M, const ui
     if (grid > static_cast<int64_t>(sm_count()) * 8) grid = static_cast<int64_t>(sm_count()) * 8;
     qn::nf4_dequant_t_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(view_of(Q), ldw, wt);
     QN_LAUNCH_CHECK("nf4_dequant_t_kernel");
-    qn::lora_pack_at2_kernel<<<static_cast<unsigned>(qn_ceil_div(k * qn::kTfUCols, 256)), 256, 0, st>>>(A, r, k, at2);
+    // AT2 on the side stream (when there is one), next to the adapter projection
+    qn::lora_pack_at2_kernel<<<static_cast<unsigned>(qn_ceil_div(k * qn::kTfUCols, 256)), 256, 0,
+                               side ? side->s : st>>>(A, r, k, at2);
     QN_LAUNCH_CHECK("lora_pack_at2_kernel");
   }
   CUtensorMap amap, bmap, atmap, vmap;
@@ -621,6 +658,7 @@ qn_status launch_tc_bwd(const qn_nf4 *Q, const uint16_t *dY, int64_t M, const ui
   QN_TRY(cuda_check(cudaFuncSetAttribute(qn::qlora_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(qn::kTbSmemBytes)),
                     "tcgen05 backward shared-memory limit"));
+  if (side) QN_TRY(side_join(side, st));  // v2 and AT2 come from the side stream
   dim3 grid(static_cast<unsigned>(qn_ceil_div(k, qn::kTcBN)), static_cast<unsigned>(qn_ceil_div(M, qn::kTcBM)));
   qn::qlora_bwd_tc_kernel<<<grid, qn::kTbThreads, qn::kTbSmemBytes, st>>>(amap, bmap, atmap, vmap, M, d, k, dX);
   QN_LAUNCH_CHECK("qlora_bwd_tc_kernel");
@@ -632,7 +670,7 @@ qn_status launch_tc_bwd(const qn_nf4 *Q, const uint16_t *dY, int64_t M, const ui
 // tokens (qlora_fwd_tc_kernel); u2 is the bf16 hi/lo split of u = s X A^T,
 // rows [hi | lo] of kTfUCols columns, each half zero-padded to 64.
 qn_status launch_tc_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M, const uint16_t *u2, const uint16_t *B,
-                        int32_t r, uint16_t *Y, Span &sp, cudaStream_t st) {
+                        int32_t r, uint16_t *Y, Span &sp, cudaStream_t st, SideStream *side) {
   const int64_t d = Q->d, k = Q->k, kp = qn::tf_scale_pitch(k);
   float *scales = sp.take<float>(static_cast<size_t>(d) * kp);
   qn::nf4_block_scale_kernel<<<static_cast<unsigned>(qn_ceil_div(d * kp, 256)), 256, 0, st>>>(view_of(Q), kp, scales);
@@ -646,6 +684,7 @@ qn_status launch_tc_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M, const uin
   QN_TRY(cuda_check(cudaFuncSetAttribute(qn::qlora_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(qn::kTfSmemBytes)),
                     "tcgen05 forward shared-memory limit"));
+  if (side) QN_TRY(side_join(side, st));  // u2 comes from the side stream
   dim3 grid(static_cast<unsigned>(qn_ceil_div(d, qn::kTcBN)), static_cast<unsigned>(qn_ceil_div(M, qn::kTcBM)));
   qn::qlora_fwd_tc_kernel<<<grid, qn::kTfThreads, qn::kTfSmemBytes, st>>>(
       xmap, umap, static_cast<const uint8_t *>(Q->codes), scales, d, k, M, B, r, Y);
@@ -820,8 +859,12 @@ qn_status qlora_linear_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M, const 
   float *part = sp.take<float>(static_cast<size_t>(qn::kProjMaxSplit) * M * r);
   if (qn::tc_supported(M, d, k, r)) {
     uint16_t *u2 = sp.take<uint16_t>(static_cast<size_t>(M) * qn::kTfUCols);
-    QN_TRY(launch_lora_proj(X, M, k, A, r, k, 1, s, part, nullptr, qn::kTfUCols / 2, u2, qn::kTfUCols, st));
-    return launch_tc_fwd(Q, X, M, u2, B, r, Y, sp, st);
+    // u2 on the side stream while the block constants are formed on st
+    SideStream *side = nullptr;
+    QN_TRY(side_stream(&side));
+    QN_TRY(side_fork(side, st));
+    QN_TRY(launch_lora_proj(X, M, k, A, r, k, 1, s, part, nullptr, qn::kTfUCols / 2, u2, qn::kTfUCols, side->s));
+    return launch_tc_fwd(Q, X, M, u2, B, r, Y, sp, st, side);
   }
   QN_TRY(launch_lora_proj(X, M, k, A, r, k, 1, s, part, u, 0, nullptr, 0, st));
   dim3 grid(static_cast<unsigned>(qn_ceil_div(d, qn::kTileN)), static_cast<unsigned>(qn_ceil_div(M, qn::kTileM)));
@@ -881,8 +924,12 @@ qn_status qlora_linear_bwd_dx(const qn_nf4 *Q, const uint16_t *dY, int64_t M, co
   // v[m, q] = s * sum_i dY[m, i] B[i, q]: Qop(n = q, kk = i) = B[i * r + q].
   if (qn::tc_bwd_supported(M, d, k, r)) {
     uint16_t *v2 = sp.take<uint16_t>(static_cast<size_t>(M) * qn::kTfUCols);
-    QN_TRY(launch_lora_proj(dY, M, d, B, r, 1, r, s, part, nullptr, qn::kTfUCols / 2, v2, qn::kTfUCols, st));
-    return launch_tc_bwd(Q, dY, M, v2, A, r, dX, sp, st);
+    // v2 on the side stream while W^T and AT2 are formed on st
+    SideStream *side = nullptr;
+    QN_TRY(side_stream(&side));
+    QN_TRY(side_fork(side, st));
+    QN_TRY(launch_lora_proj(dY, M, d, B, r, 1, r, s, part, nullptr, qn::kTfUCols / 2, v2, qn::kTfUCols, side->s));
+    return launch_tc_bwd(Q, dY, M, v2, A, r, dX, sp, st, side);
   }
   QN_TRY(launch_lora_proj(dY, M, d, B, r, 1, r, s, part, v, 0, nullptr, 0, st));
   dim3 grid(static_cast<unsigned>(qn_ceil_div(k, qn::kTileN)), static_cast<unsigned>(qn_ceil_div(M, qn::kTileM)));
@@ -1257,7 +1304,7 @@ qn_status loftq_run_p(const float *W, int64_t d, int64_t k, int32_t r, float alp
     }
     QN_TRY(rt_times(Y, Zt));  // Zt = R^T Y, i.e. (Y^T R)^T
     QN_TRY(gram(Zt, k));
-    qn::lq_jacobi_kernel<P><<<1, 256, qn::lq_jacobi_smem<P>(), st>>>(G, p, lam, V);
+    qn::lq_jacobi_kernel<P><<<1, qn::kLqJacThreads, qn::lq_jacobi_smem<P>(), st>>>(G, p, lam, V);
     QN_LAUNCH_CHECK("lq_jacobi_kernel");
     qn::lq_project_kernel<P><<<static_cast<unsigned>(qn_ceil_div(d, 256)), 256, 0, st>>>(Y, d, V, lam, r, s, 0, B, 0);
     QN_LAUNCH_CHECK("lq_project_kernel(B)");

@@ -733,51 +733,67 @@ lq_cholqr2_p32_kernel(const float *__restrict__ part, int S, float *__restrict__
   }
 }
 
-// One CTA of 256 threads: parallel cyclic Jacobi eigen-decomposition (fp32)
-// of the symmetric leading p x p block of G (accumulated in fp64), with the
-// round-robin ("circle") pair ordering, so that n / 2 disjoint rotations run
-// at once (n = p rounded up to even; a padding row and column stay zero).
-// In round t the pairs are (n-1, t) and ((t+k) mod (n-1), (t-k) mod (n-1)),
-// k = 1 .. n/2-1.  A round takes two barriers: the rotations of all pairs are
-// formed, then A <- J^T A J is applied one 2 x 2 block (a pair of rows by a
-// pair of columns) per thread, together with E <- E J.  Sweeps stop once the
-// off-diagonal mass is at the fp32 noise level.  Outputs the eigenvalues
-// sorted descending (lam[P], zero past p) and the matching eigenvectors as
-// the columns of V (fp32 [P x P], V[row * P + col]).
-template <int P>
-constexpr size_t lq_jacobi_smem() { return 2 * static_cast<size_t>(P) * (P + 1) * sizeof(float); }
+// One CTA of kLqJacThreads threads: parallel cyclic Jacobi eigen-
+// decomposition (fp32) of the symmetric leading p x p block of G (accumulated
+// in fp64), with the round-robin ("circle") pair ordering, so that n / 2
+// disjoint rotations run at once (n = p rounded up to even; a padding row and
+// column stay zero).  In round t the pairs are (n-1, t) and ((t+k) mod (n-1),
+// (t-k) mod (n-1)), k = 1 .. n/2-1; the whole schedule is tabulated once.  A
+// round takes two barriers: the rotations of all pairs are formed (the
+// reciprocal square root for the cosine), then A <- J^T A J is applied one
+// 2 x 2 block (a pair of rows by a pair of columns, rows first) per item,
+// together with E <- E J; each thread's items are the same in every round.
+// Sweeps stop once the off-diagonal mass is at the fp32 noise level.  Outputs
+// the eigenvalues sorted descending (lam[P], zero past p) and the matching
+// eigenvectors as the columns of V (fp32 [P x P], V[row * P + col]).
+constexpr int kLqJacThreads = 512;
 
-__device__ __forceinline__ void lq_round_pair(int t, int k, int n, int &a, int &b) {
-  const int m = n - 1;
-  int x, y;
-  if (k == 0) {
-    x = m;
-    y = t;
-  } else {
-    x = (t + k) % m;
-    y = (t - k + m) % m;
-  }
-  a = x < y ? x : y;
-  b = x < y ? y : x;
+template <int P>
+constexpr size_t lq_jacobi_smem() {
+  return 2 * static_cast<size_t>(P) * (P + 1) * sizeof(float) + static_cast<size_t>(P - 1) * (P / 2) * 2;
 }
 
 template <int P>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kLqJacThreads)
 lq_jacobi_kernel(const double *__restrict__ G, int p, float *__restrict__ lam, float *__restrict__ V) {
-  extern __shared__ float lq_jac_smem[];  // A then E, P x (P + 1) each
+  extern __shared__ float lq_jac_smem[];  // A, E (P x (P + 1) each), then the pair schedule
   float (*A)[P + 1] = reinterpret_cast<float (*)[P + 1]>(lq_jac_smem);
   float (*E)[P + 1] = reinterpret_cast<float (*)[P + 1]>(lq_jac_smem + P * (P + 1));
+  unsigned char (*sched)[P / 2][2] = reinterpret_cast<unsigned char (*)[P / 2][2]>(lq_jac_smem + 2 * P * (P + 1));
   __shared__ float cs[P / 2][2];
-  __shared__ int pr[P / 2][2];
   __shared__ float s_off, s_dg;
   __shared__ int order[P];
   const int tid = threadIdx.x;
   const int n = p + (p & 1);
   const int np = n / 2;
-  for (int t = tid; t < P * P; t += 256) {
+  for (int t = tid; t < P * P; t += kLqJacThreads) {
     const int i = t / P, j = t % P;
     A[i][j] = (i < p && j < p) ? static_cast<float>(G[i * P + j]) : 0.f;
     E[i][j] = (i == j) ? 1.f : 0.f;
+  }
+  for (int t = tid; t < (n - 1) * np; t += kLqJacThreads) {
+    const int step = t / np, k = t % np, m = n - 1;
+    const int x = (k == 0) ? m : (step + k) % m;
+    const int y = (k == 0) ? step : (step - k + m) % m;
+    sched[step][k][0] = static_cast<unsigned char>(x < y ? x : y);
+    sched[step][k][1] = static_cast<unsigned char>(x < y ? y : x);
+  }
+  // this thread's items (the same every round): blocks (k1, k2), then E rows
+  constexpr int kIpt = ((P / 2) * (P / 2) + (P / 2) * P + kLqJacThreads - 1) / kLqJacThreads;  // items per thread
+  const int items = np * np + np * n;
+  int it_k1[kIpt], it_k2[kIpt], it_row[kIpt];
+#pragma unroll
+  for (int u = 0; u < kIpt; ++u) {
+    const int t = tid + u * kLqJacThreads;
+    if (t < np * np) {
+      it_k1[u] = t / np;
+      it_k2[u] = t % np;
+      it_row[u] = -1;
+    } else {
+      const int v = t - np * np;
+      it_k1[u] = it_k2[u] = v / n;
+      it_row[u] = v % n;
+    }
   }
   __syncthreads();
   for (int sweep = 0; sweep < 15; ++sweep) {
@@ -798,30 +814,29 @@ lq_jacobi_kernel(const double *__restrict__ G, int p, float *__restrict__ lam, f
     __syncthreads();
     if (s_off <= 1e-10f * s_dg) break;  // off-diagonal mass at the fp32 noise level
     for (int step = 0; step < n - 1; ++step) {
-      for (int k = tid; k < np; k += 256) {  // rotations of this round's pairs
-        int a, b;
-        lq_round_pair(step, k, n, a, b);
-        pr[k][0] = a;
-        pr[k][1] = b;
+      if (tid < np) {  // rotation of pair tid
+        const int a = sched[step][tid][0], b = sched[step][tid][1];
         const float aij = A[a][b];
         float c = 1.f, sn = 0.f;
         if (fabsf(aij) > 1e-30f * (fabsf(A[a][a]) + fabsf(A[b][b]))) {
           const float theta = (A[b][b] - A[a][a]) / (2.f * aij);
           const float tt = copysignf(1.f, theta) / (fabsf(theta) + sqrtf(theta * theta + 1.f));
-          c = 1.f / sqrtf(tt * tt + 1.f);
+          c = rsqrtf(tt * tt + 1.f);
           sn = tt * c;
         }
-        cs[k][0] = c;
-        cs[k][1] = sn;
+        cs[tid][0] = c;
+        cs[tid][1] = sn;
       }
       __syncthreads();
-      // A <- J^T A J one 2 x 2 block at a time (rows of pair k1, columns of
-      // pair k2: rows first, then columns), and E <- E J one row of a pair.
-      for (int t = tid; t < np * np + np * n; t += 256) {
-        if (t < np * np) {
-          const int k1 = t / np, k2 = t % np;
-          const int a = pr[k1][0], b = pr[k1][1], c0 = pr[k2][0], d0 = pr[k2][1];
-          const float c1 = cs[k1][0], s1 = cs[k1][1], c2 = cs[k2][0], s2 = cs[k2][1];
+#pragma unroll
+      for (int u = 0; u < kIpt; ++u) {
+        if (tid + u * kLqJacThreads >= items) break;
+        const int k1 = it_k1[u], k2 = it_k2[u];
+        const int a = sched[step][k1][0], b = sched[step][k1][1];
+        const float c1 = cs[k1][0], s1 = cs[k1][1];
+        if (it_row[u] < 0) {
+          const int c0 = sched[step][k2][0], d0 = sched[step][k2][1];
+          const float c2 = cs[k2][0], s2 = cs[k2][1];
           const float ra_c = c1 * A[a][c0] - s1 * A[b][c0], ra_d = c1 * A[a][d0] - s1 * A[b][d0];
           const float rb_c = s1 * A[a][c0] + c1 * A[b][c0], rb_d = s1 * A[a][d0] + c1 * A[b][d0];
           A[a][c0] = c2 * ra_c - s2 * ra_d;
@@ -829,19 +844,17 @@ lq_jacobi_kernel(const double *__restrict__ G, int p, float *__restrict__ lam, f
           A[b][c0] = c2 * rb_c - s2 * rb_d;
           A[b][d0] = s2 * rb_c + c2 * rb_d;
         } else {
-          const int u = t - np * np, k = u / n, row = u % n;
-          const int a = pr[k][0], b = pr[k][1];
-          const float c = cs[k][0], sn = cs[k][1];
+          const int row = it_row[u];
           const float ea = E[row][a], eb = E[row][b];
-          E[row][a] = c * ea - sn * eb;
-          E[row][b] = sn * ea + c * eb;
+          E[row][a] = c1 * ea - s1 * eb;
+          E[row][b] = s1 * ea + c1 * eb;
         }
       }
       __syncthreads();
     }
   }
   // descending order of the eigenvalues: rank of each (ties by index)
-  for (int i = tid; i < P; i += 256) {
+  for (int i = tid; i < P; i += kLqJacThreads) {
     if (i < p) {
       const float di = A[i][i];
       int rank = 0;
@@ -855,8 +868,8 @@ lq_jacobi_kernel(const double *__restrict__ G, int p, float *__restrict__ lam, f
     }
   }
   __syncthreads();
-  for (int i = tid; i < P; i += 256) lam[i] = (i < p) ? A[order[i]][order[i]] : 0.f;
-  for (int t = tid; t < P * P; t += 256) {
+  for (int i = tid; i < P; i += kLqJacThreads) lam[i] = (i < p) ? A[order[i]][order[i]] : 0.f;
+  for (int t = tid; t < P * P; t += kLqJacThreads) {
     const int row = t / P, col = t % P;
     V[t] = (col < p) ? E[row][order[col]] : 0.f;
   }

@@ -32,8 +32,9 @@
 //    the block's dot products, scaled by the block constants in fp32.  The
 //    row group's block constants (int8 codes, or fp32 absmax) arrive with its
 //    first stage as one bulk copy into a shared-memory tile; the group scale
-//    sigma comes through L1.  The
-//    MMA's k order is a permutation of the block's elements, the same one for
+//    sigma comes through L1.  Without X staged in shared memory, the X
+//    fragments of the next stage are loaded (through L2) while the current
+//    stage is decoded.  The MMA's k order is a permutation of the block's elements, the same one for
 //    A and X, so the sum is unchanged.  At the end of a row group each warp
 //    writes its partial sums to a shared-memory ring slot and arrives on the
 //    slot's mbarrier; the group's finisher warp (group index mod 8) sums the
@@ -368,8 +369,30 @@ skinny_kernel(const __grid_constant__ SkGroup g) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
 
-    // ---- the group's stages: this warp takes blocks s*16 + cw and s*16 + cw + 8
+    // ---- the group's stages: this warp takes blocks s*16 + cw and s*16 + cw + 8.
+    // Without staged X (XS false) the X fragments come from global memory
+    // through L2; those of stage s + 1 are loaded while stage s is decoded.
+    uint4 xc[2][MT][2], xn[2][MT][2];
+    auto load_x = [&](int s2, uint4 (&xo)[2][MT][2]) {
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int b = s2 * kSkStageBlocks + cw + 8 * t;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const int tok = gq + 8 * mt;
+          xo[t][mt][0] = make_uint4(0u, 0u, 0u, 0u);
+          xo[t][mt][1] = xo[t][mt][0];
+          if (!XS && s2 < nst && b < nb && tok < M) {
+            const int64_t e = static_cast<int64_t>(tok) * k + static_cast<int64_t>(b) * 64 + tq * 16;
+            xo[t][mt][0] = __ldcg(reinterpret_cast<const uint4 *>(g.X + e));
+            xo[t][mt][1] = __ldcg(reinterpret_cast<const uint4 *>(g.X + e + 8));
+          }
+        }
+      }
+    };
+    if (!XS) load_x(0, xc);
     for (int s = 0; s < nst; ++s, ++q) {
+      if (!XS) load_x(s + 1, xn);
       const uint32_t slot = q % kSkStages;
       ok = mbar_wait(smem_u32(&st_full[slot]), (q / kSkStages) & 1, abort);
       ok = __all_sync(0xffffffffu, ok);
@@ -424,17 +447,12 @@ skinny_kernel(const __grid_constant__ SkGroup g) {
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           // X fragment: token gq + 8 mt, elements 16 tq .. 16 tq + 15 of block b
-          uint4 x0 = make_uint4(0u, 0u, 0u, 0u), x1 = x0;
+          uint4 x0 = xc[t][mt][0], x1 = xc[t][mt][1];
           const int tok = gq + 8 * mt;
-          if (tok < M) {
+          if (XS && tok < M) {
             const int64_t e = static_cast<int64_t>(tok) * k + static_cast<int64_t>(b) * 64 + tq * 16;
-            if (XS) {
-              x0 = *reinterpret_cast<const uint4 *>(xs + e);
-              x1 = *reinterpret_cast<const uint4 *>(xs + e + 8);
-            } else {
-              x0 = *reinterpret_cast<const uint4 *>(g.X + e);
-              x1 = *reinterpret_cast<const uint4 *>(g.X + e + 8);
-            }
+            x0 = *reinterpret_cast<const uint4 *>(xs + e);
+            x1 = *reinterpret_cast<const uint4 *>(xs + e + 8);
           }
           const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
           float dsum[4] = {0.f, 0.f, 0.f, 0.f};
@@ -447,6 +465,15 @@ skinny_kernel(const __grid_constant__ SkGroup g) {
           acc[mt][2] = fmaf(dsum[2], m[t][1], acc[mt][2]);
           acc[mt][3] = fmaf(dsum[3], m[t][1], acc[mt][3]);
         }
+      }
+      if (!XS) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            xc[t][mt][0] = xn[t][mt][0];
+            xc[t][mt][1] = xn[t][mt][1];
+          }
       }
     }
     if (!ok) break;
