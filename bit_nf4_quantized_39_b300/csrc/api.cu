@@ -256,9 +256,10 @@ size_t lg_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
   const int64_t Rp = qn::lg_rp(r), Mp = qn::lg_round(M, qn::kLgTK);
   const int64_t Nmax = d > k ? d : k;
   const int Smax = qn::lg_splits(M, d, r) > qn::lg_splits(M, k, r) ? qn::lg_splits(M, d, r) : qn::lg_splits(M, k, r);
-  return kSemBytes + 2 * round256(static_cast<size_t>(M) * r * sizeof(float)) + proj_ws_bytes(M, r) +
+  // two independent chains (dB from u, dA from v), each with its own split partials
+  return kSemBytes + 2 * round256(static_cast<size_t>(M) * r * sizeof(float)) + 2 * proj_ws_bytes(M, r) +
          2 * round256(static_cast<size_t>(2) * Rp * Mp * sizeof(uint16_t)) +
-         round256(static_cast<size_t>(Smax) * Rp * Nmax * sizeof(float));
+         2 * round256(static_cast<size_t>(Smax) * Rp * Nmax * sizeof(float));
 }
 
 size_t loftq_ws_bytes(int64_t d, int64_t k);  // LoftQ workspace (defined with the LoftQ loop)
@@ -960,25 +961,31 @@ qn_status qlora_linear_bwd_lora(const uint16_t *X, const uint16_t *dY, int64_t M
   const float s = alpha / static_cast<float>(r);
   float *u = sp.take<float>(static_cast<size_t>(M) * r);
   float *v = sp.take<float>(static_cast<size_t>(M) * r);
-  float *part = sp.take<float>(static_cast<size_t>(qn::kProjMaxSplit) * M * r);
+  float *part_u = sp.take<float>(static_cast<size_t>(qn::kProjMaxSplit) * M * r);
+  float *part_v = sp.take<float>(static_cast<size_t>(qn::kProjMaxSplit) * M * r);
   const int64_t Rp = qn::lg_rp(r), Mp = qn::lg_round(M, qn::kLgTK);
   uint16_t *ut2 = sp.take<uint16_t>(static_cast<size_t>(2) * Rp * Mp);
   uint16_t *vt2 = sp.take<uint16_t>(static_cast<size_t>(2) * Rp * Mp);
   const int Sd = qn::lg_splits(M, d, r), Sk = qn::lg_splits(M, k, r);
   const size_t gpart_n = std::max(static_cast<size_t>(Sd) * Rp * d, static_cast<size_t>(Sk) * Rp * k);
-  float *gpart = sp.take<float>(gpart_n);
-  // u = s X A^T (Qop(n = q, kk = j) = A[q * k + j]);  v = s dY B (Qop(n = q, kk = i) = B[i * r + q])
-  QN_TRY(launch_lora_proj(X, M, k, A, r, k, 1, s, part, u, 0, nullptr, 0, st));
-  QN_TRY(launch_lora_proj(dY, M, d, B, r, 1, r, s, part, v, 0, nullptr, 0, st));
+  float *gpart_u = sp.take<float>(gpart_n);
+  float *gpart_v = sp.take<float>(gpart_n);
   const unsigned pg = static_cast<unsigned>(qn_ceil_div(Rp * Mp, 256));
-  qn::lora_vt_pack_kernel<<<pg, 256, 0, st>>>(u, M, r, Rp, Mp, ut2);
+  // Two independent chains, the first on a side stream:
+  //   u = s X A^T (Qop(n = q, kk = j) = A[q * k + j]);  dB^T[q, i] = sum_m u[m, q] dY[m, i]  (written as dB, d x r)
+  //   v = s dY B (Qop(n = q, kk = i) = B[i * r + q]);   dA[q, j] = sum_m v[m, q] X[m, j]
+  SideStream *side = nullptr;
+  QN_TRY(side_stream(&side));
+  QN_TRY(side_fork(side, st));
+  QN_TRY(launch_lora_proj(X, M, k, A, r, k, 1, s, part_u, u, 0, nullptr, 0, side->s));
+  qn::lora_vt_pack_kernel<<<pg, 256, 0, side->s>>>(u, M, r, Rp, Mp, ut2);
   QN_LAUNCH_CHECK("lora_vt_pack_kernel(u)");
+  QN_TRY(launch_lora_grad(dY, M, d, ut2, r, gpart_u, 1, dB, side->s));
+  QN_TRY(launch_lora_proj(dY, M, d, B, r, 1, r, s, part_v, v, 0, nullptr, 0, st));
   qn::lora_vt_pack_kernel<<<pg, 256, 0, st>>>(v, M, r, Rp, Mp, vt2);
   QN_LAUNCH_CHECK("lora_vt_pack_kernel(v)");
-  // dB^T[q, i] = sum_m u[m, q] dY[m, i]  (written as dB, d x r);  dA[q, j] = sum_m v[m, q] X[m, j]
-  QN_TRY(launch_lora_grad(dY, M, d, ut2, r, gpart, 1, dB, st));
-  QN_TRY(launch_lora_grad(X, M, k, vt2, r, gpart, 0, dA, st));
-  return QN_OK;
+  QN_TRY(launch_lora_grad(X, M, k, vt2, r, gpart_v, 0, dA, st));
+  return side_join(side, st);
 }
 
 qn_status qlora_linear_fwd_f32(const qn_nf4 *Q, const float *X, int64_t M, const float *A, const float *B, int32_t r,

@@ -46,7 +46,9 @@ nf4_merge_kernel(QnNF4View qin, const uint16_t *__restrict__ A, const uint16_t *
   unsigned long long *s_bins = reinterpret_cast<unsigned long long *>(sB + kMgRows * (kMgRChunk + 1));
   BucketEntry *s_one = reinterpret_cast<BucketEntry *>(s_bins + kNumBins);
   BucketEntry *s_tab = s_one + kBuckets;
+  __shared__ float s_lv[16];  // the levels, indexed per lane (a constant-bank read would serialise)
   for (int i = threadIdx.x; i < kNumBins; i += blockDim.x) s_bins[i] = 0ull;
+  if (threadIdx.x < 16) s_lv[threadIdx.x] = c_nf4_levels[threadIdx.x];
   build_bucket_tables(s_one, s_tab);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const BucketEntry *my_tab = s_tab + lane;
@@ -54,6 +56,8 @@ nf4_merge_kernel(QnNF4View qin, const uint16_t *__restrict__ A, const uint16_t *
   const int64_t row0 = static_cast<int64_t>(blockIdx.y) * kMgRows + warp * 8;
   const int64_t col = static_cast<int64_t>(blockIdx.x) * kMgCols + lane * 8;
   const bool col_ok = col < k;  // k is a multiple of 64: a block is valid or not as a whole
+  BinFold fold_st = {0ull, -1};
+  const bool fold = d * nb <= (int64_t(1) << 31);
 
   // The input codes and block constants of this thread's 8 rows x 8 columns.
   uint32_t win[8];
@@ -123,7 +127,7 @@ nf4_merge_kernel(QnNF4View qin, const uint16_t *__restrict__ A, const uint16_t *
     float x[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const float base = __fmul_rn(c_nf4_levels[(win[rr] >> (4 * j)) & 15u], min_[rr]);
+      const float base = __fmul_rn(s_lv[(win[rr] >> (4 * j)) & 15u], min_[rr]);
       const float t = __fmul_rn(s, acc[rr][j]);
       x[j] = (sign > 0) ? __fadd_rn(base, t) : __fsub_rn(base, t);
     }
@@ -134,11 +138,12 @@ nf4_merge_kernel(QnNF4View qin, const uint16_t *__restrict__ A, const uint16_t *
       *reinterpret_cast<uint32_t *>(codes_out + (e >> 1)) = packed;
       if ((lane & 7) == 0) {
         absmax_out[e >> 6] = m;
-        if (bins) bin_add_shared(s_bins, m);
+        if (bins) bin_fold(fold_st, s_bins, m, fold);
       }
     }
   }
   if (!bins) return;
+  bin_flush(fold_st, s_bins);
   quant_mean_epilogue(s_bins, bins, ticket, d * nb, absmax_mean_out);
 }
 

@@ -61,7 +61,10 @@ f32_gemm_kernel(const F32Gemm gp) {
   constexpr int TM = BM / 16;  // rows per thread
   __shared__ float sP[kF32BK][BM + 4];
   __shared__ float sO[kF32BK][kF32BN + 4];
+  __shared__ float s_lv[16];  // the levels, indexed per lane (a constant-bank read would serialise)
   const int tid = threadIdx.x;
+  if (tid < 16) s_lv[tid] = c_nf4_levels[tid];
+  __syncthreads();
   const int ty = tid / 16, tx = tid % 16;  // thread tile: rows ty*TM.., columns tx*8..
   const int64_t m0 = static_cast<int64_t>(blockIdx.y) * BM;
   const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kF32BN;
@@ -96,7 +99,7 @@ f32_gemm_kernel(const F32Gemm gp) {
         const uint32_t w = *reinterpret_cast<const uint32_t *>(q.codes + (e >> 1));
         const float m = block_scale(q, e >> 6);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) sO[kk][nn + j] = __fmul_rn(c_nf4_levels[(w >> (4 * j)) & 15u], m);
+        for (int j = 0; j < 8; ++j) sO[kk][nn + j] = __fmul_rn(s_lv[(w >> (4 * j)) & 15u], m);
       } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j) sO[kk][nn + j] = 0.f;
@@ -111,7 +114,7 @@ f32_gemm_kernel(const F32Gemm gp) {
         const uint32_t w = *reinterpret_cast<const uint32_t *>(q.codes + (e >> 1));
         const float m = block_scale(q, e >> 6);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) sO[kh + j][nn] = __fmul_rn(c_nf4_levels[(w >> (4 * j)) & 15u], m);
+        for (int j = 0; j < 8; ++j) sO[kh + j][nn] = __fmul_rn(s_lv[(w >> (4 * j)) & 15u], m);
       } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j) sO[kh + j][nn] = 0.f;
