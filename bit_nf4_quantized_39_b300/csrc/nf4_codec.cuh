@@ -224,23 +224,19 @@ __device__ __forceinline__ void build_bucket_entry(int idx, BucketEntry *tab) {
 
 // `tab` is the lane's column of the per-lane replicated table: entry b of
 // lane l sits at tab[b * 32 + l], so the 32 lanes of a warp never conflict on
-// a bank whatever buckets they hit.
+// a bank whatever buckets they hit.  The key comes from max(|v|, 2^-6) (every
+// value below 2^-5 in magnitude has code 7, so the clamp is exact; a NaN maps
+// to the smallest bucket), the sign picks the half of the table, and the
+// decision v > thr is read off the sign of the fp32 difference thr - v (which
+// is +0 only for v = thr and negative exactly when v > thr), so that most of
+// the work runs on the multiply-add pipe rather than the integer/logic one.
 __device__ __forceinline__ uint32_t bucket_code(float v, const BucketEntry *tab) {
-  const uint32_t bits = __float_as_uint(v);
-  uint32_t ek;  // exponent and top 3 significand bits: bits 20 .. 30
-  asm("bfe.u32 %0, %1, 20, 11;" : "=r"(ek) : "r"(bits));
-  // |v| <= 1 gives key <= 48; the upper clamp only keeps non-finite inputs
-  // (outside the method's domain) inside the table.
-  const uint32_t key = min(max(ek, kBucketKeyMin) - kBucketKeyMin, 55u);
-  const BucketEntry en = tab[(key + ((bits >> 31) ? 56u : 0u)) * 32u];
-  return en.base + ((v > en.thr) ? 1u : 0u);
-}
-
-// w with bits [4 i, 4 i + 4) replaced by the low 4 bits of c.
-__device__ __forceinline__ uint32_t put_nibble(uint32_t w, uint32_t c, int i) {
-  uint32_t r;
-  asm("bfi.b32 %0, %1, %2, %3, 4;" : "=r"(r) : "r"(c), "r"(w), "r"(4 * i));
-  return r;
+  const float qc = fmaxf(fabsf(v), 0x1.0p-6f);
+  const uint32_t key = (__float_as_uint(qc) >> 20) - kBucketKeyMin;  // 0 .. 48 for |v| <= 1
+  const uint32_t half = (__float_as_uint(v) >> 31) * 56u;
+  const BucketEntry en = tab[(key + half) * 32u];
+  const float d = en.thr - v;
+  return en.base + (__float_as_uint(d) >> 31);
 }
 
 // IEEE-correct x / m for |x| <= m with m in [2^-125, 2^125], from the
@@ -284,7 +280,10 @@ __device__ __forceinline__ uint32_t nf4_quant_lane8(float (&v)[8], const BucketE
   }
   uint32_t packed = 0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) packed = put_nibble(packed, bucket_code(v[i], tab), i);
+  for (int i = 0; i < 8; ++i) {  // packed += code << 4 i, as a multiply-add
+    const uint32_t c = bucket_code(v[i], tab);
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(packed) : "r"(c), "r"(1u << (4 * i)), "r"(packed));
+  }
   m_out = m;
   return packed;
 }
