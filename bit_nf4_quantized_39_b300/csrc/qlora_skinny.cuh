@@ -21,8 +21,8 @@
 //    of 16 rows of one projection (the M side of an m16n8k16 MMA).  A
 //    producer warp streams each row group's codes with TMA in stages of 16
 //    rows x 16 blocks (8 KiB, four 128-byte boxes with the 128-byte swizzle)
-//    through a 12-stage shared-memory ring (96 KiB in flight per SM).  Eight
-//    consumer warps take two 64-blocks of every stage each.  A lane (group g, thread t) reads 8 code
+//    through a 10-stage shared-memory ring (80 KiB in flight per SM).
+//    Sixteen consumer warps take one 64-block of every stage each.  A lane (group g, thread t) reads 8 code
 //    bytes of rows g and g+8 (elements 16t .. 16t+15 of its block; the
 //    swizzle makes the reads conflict-free); every byte becomes one bf16x2
 //    A-fragment register with one byte permute (address) and one shared-
@@ -56,14 +56,15 @@
 
 namespace qn {
 
-constexpr int kSkConsumers = 8;                      // consumer warps (two 64-blocks of each stage)
+constexpr int kSkConsumers = 16;                     // consumer warps (one 64-block of each stage each)
+constexpr int kSkItems = 16 / kSkConsumers;          // 64-blocks per consumer warp and stage
 constexpr int kSkProducer = kSkConsumers;            // the TMA producer warp
 constexpr int kSkThreads = (kSkConsumers + 1) * 32;
 constexpr int kSkRows = 16;                          // rows per row group (MMA M)
 constexpr int kSkStageBlocks = 16;                   // 64-blocks per stage
 constexpr int kSkStageBytes = kSkRows * kSkStageBlocks * 32;  // 8 KiB of codes
 constexpr int kSkBoxBytes = 128;                     // TMA box width: one swizzle span, 4 blocks
-constexpr int kSkStages = 12;                        // stage ring depth (96 KiB in flight)
+constexpr int kSkStages = 10;                        // stage ring depth (80 KiB in flight)
 constexpr int kSkMaxNb = 256;                        // 64-blocks per row (k <= 16384)
 constexpr int kSkCTiles = 3;                         // int8 block-constant tiles (row groups in flight)
 constexpr int kSkCTileBytes = kSkRows * kSkMaxNb;    // one group's int8 constants
@@ -307,21 +308,18 @@ skinny_kernel(const __grid_constant__ SkGroup g) {
 
   // ================================= consumers ==================================
   const int gq = lane >> 2, tq = lane & 3;  // MMA group id, thread in group
-  const int cw = warp;                      // takes blocks cw and cw + 8 of every stage
+  const int cw = warp;                      // takes block cw of every stage
   const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
   {
     // entry b of lane l: bf16(level[b & 15]) | bf16(level[b >> 4]) << 16.
-    // Thread tid writes the words of entries b = (tid >> 5) + 8 n of lane tid & 31.
+    // Thread tid writes the words of entries b = (tid >> 5) + 16 n of lane
+    // tid & 31 (16 consumer warps: b & 15 = tid >> 5, b >> 4 = n).
+    static_assert(kSkConsumers == 16, "table build assumes 16 consumer warps");
     const int b0 = tid >> 5, l = tid & 31;
-    uint32_t lv[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) lv[i] = f32_to_bf16_bits(c_nf4_levels[i]);
+    const uint32_t lo = f32_to_bf16_bits(c_nf4_levels[b0]);
     uint32_t *lw = reinterpret_cast<uint32_t *>(lut);
 #pragma unroll
-    for (int n = 0; n < 32; ++n) {
-      const int b = b0 + 8 * n;  // b & 15 = b0 + 8 (n & 1), b >> 4 = n >> 1
-      lw[b * 64 + l] = lv[b0 + 8 * (n & 1)] | (lv[n >> 1] << 16);
-    }
+    for (int n = 0; n < 16; ++n) lw[(b0 + 16 * n) * 64 + l] = lo | (f32_to_bf16_bits(c_nf4_levels[n]) << 16);
   }
   pdl_wait();  // X and u are written by the kernels before this one
   const int64_t nu = static_cast<int64_t>(M) * g.rtot;
@@ -369,14 +367,14 @@ skinny_kernel(const __grid_constant__ SkGroup g) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
 
-    // ---- the group's stages: this warp takes blocks s*16 + cw and s*16 + cw + 8.
+    // ---- the group's stages: this warp takes block s*16 + cw.
     // Without staged X (XS false) the X fragments come from global memory
     // through L2; those of stage s + 1 are loaded while stage s is decoded.
-    uint4 xc[2][MT][2], xn[2][MT][2];
-    auto load_x = [&](int s2, uint4 (&xo)[2][MT][2]) {
+    uint4 xc[kSkItems][MT][2], xn[kSkItems][MT][2];
+    auto load_x = [&](int s2, uint4 (&xo)[kSkItems][MT][2]) {
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int b = s2 * kSkStageBlocks + cw + 8 * t;
+      for (int t = 0; t < kSkItems; ++t) {
+        const int b = s2 * kSkStageBlocks + cw + kSkConsumers * t;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           const int tok = gq + 8 * mt;
@@ -398,12 +396,12 @@ skinny_kernel(const __grid_constant__ SkGroup g) {
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       const unsigned char *stage = ring + slot * kSkStageBytes;
-      uint32_t a[2][2][8];  // [item][row half][byte]: bf16 pair of elements 16 tq + 2 byte, +1
-      float m[2][2];        // [item][row half]: block constants
-      int bi[2];
+      uint32_t a[kSkItems][2][8];  // [item][row half][byte]: bf16 pair of elements 16 tq + 2 byte, +1
+      float m[kSkItems][2];        // [item][row half]: block constants
+      int bi[kSkItems];
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int cb = cw + 8 * t;  // block of the stage
+      for (int t = 0; t < kSkItems; ++t) {
+        const int cb = cw + kSkConsumers * t;  // block of the stage
         const int b = s * kSkStageBlocks + cb;
         bi[t] = b;
         // Code bytes 8 tq .. 8 tq + 7 of block b for rows gq and gq + 8: box
@@ -441,7 +439,7 @@ skinny_kernel(const __grid_constant__ SkGroup g) {
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&st_empty[slot]));  // codes are in registers now
 #pragma unroll
-      for (int t = 0; t < 2; ++t) {
+      for (int t = 0; t < kSkItems; ++t) {
         const int b = bi[t];
         if (b >= nb) continue;
 #pragma unroll
@@ -468,7 +466,7 @@ skinny_kernel(const __grid_constant__ SkGroup g) {
       }
       if (!XS) {
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
+        for (int t = 0; t < kSkItems; ++t)
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
             xc[t][mt][0] = xn[t][mt][0];

@@ -218,7 +218,7 @@ def test_chain_reads_previous_output(qn, M):
     qn.device_status()
 
 
-@pytest.mark.parametrize("M", [1, 3])
+@pytest.mark.parametrize("M", [1, 3, 12])
 def test_group_of_projections(qn, M):
     """Projections of one input in one call (query/key/value style), with
     different d and r per member, against the oracle one by one."""
