@@ -368,10 +368,13 @@ skinny_kernel(const __grid_constant__ SkGroup g) {
       for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
 
     // ---- the group's stages: this warp takes block s*16 + cw.
-    // Without staged X (XS false) the X fragments come from global memory
-    // through L2; those of stage s + 1 are loaded while stage s is decoded.
+    // What comes from global memory through L2 is loaded one stage ahead,
+    // while the stage before is decoded: the X fragments (without staged X)
+    // and the per-block value behind the block constant (the DQ group scale,
+    // or the fp32 absmax).
     uint4 xc[kSkItems][MT][2], xn[kSkItems][MT][2];
-    auto load_x = [&](int s2, uint4 (&xo)[kSkItems][MT][2]) {
+    float sc[kSkItems][2], sn[kSkItems][2];
+    auto prefetch = [&](int s2, uint4 (&xo)[kSkItems][MT][2], float (&so)[kSkItems][2]) {
 #pragma unroll
       for (int t = 0; t < kSkItems; ++t) {
         const int b = s2 * kSkStageBlocks + cw + kSkConsumers * t;
@@ -386,11 +389,20 @@ skinny_kernel(const __grid_constant__ SkGroup g) {
             xo[t][mt][1] = __ldcg(reinterpret_cast<const uint4 *>(g.X + e + 8));
           }
         }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float v = 0.f;
+          if (s2 < nst && row_ok[h] && b < nb) {
+            const int64_t blk = static_cast<int64_t>(row0 + gq + 8 * h) * nb + b;
+            v = dq ? __ldcg(qv.absmax_scale + (blk >> 8)) : __ldcg(qv.absmax + blk);
+          }
+          so[t][h] = v;
+        }
       }
     };
-    if (!XS) load_x(0, xc);
+    prefetch(0, xc, sc);
     for (int s = 0; s < nst; ++s, ++q) {
-      if (!XS) load_x(s + 1, xn);
+      prefetch(s + 1, xn, sn);
       const uint32_t slot = q % kSkStages;
       ok = mbar_wait(smem_u32(&st_full[slot]), (q / kSkStages) & 1, abort);
       ok = __all_sync(0xffffffffu, ok);
@@ -428,9 +440,9 @@ skinny_kernel(const __grid_constant__ SkGroup g) {
             const int64_t blk = static_cast<int64_t>(row0 + lr) * nb + b;
             if (dq) {
               const int qc = (o < cbytes) ? static_cast<int>(ct[o]) : static_cast<int>(__ldg(qv.absmax_q + blk));
-              mm = dq_absmax(static_cast<int8_t>(qc), __ldg(qv.absmax_scale + (blk >> 8)), mu);
+              mm = dq_absmax(static_cast<int8_t>(qc), sc[t][h], mu);
             } else {
-              mm = __ldg(qv.absmax + blk);
+              mm = sc[t][h];
             }
           }
           m[t][h] = mm;
@@ -464,14 +476,15 @@ skinny_kernel(const __grid_constant__ SkGroup g) {
           acc[mt][3] = fmaf(dsum[3], m[t][1], acc[mt][3]);
         }
       }
-      if (!XS) {
 #pragma unroll
-        for (int t = 0; t < kSkItems; ++t)
+      for (int t = 0; t < kSkItems; ++t) {
+        sc[t][0] = sn[t][0];
+        sc[t][1] = sn[t][1];
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            xc[t][mt][0] = xn[t][mt][0];
-            xc[t][mt][1] = xn[t][mt][1];
-          }
+        for (int mt = 0; mt < MT; ++mt) {
+          xc[t][mt][0] = xn[t][mt][0];
+          xc[t][mt][1] = xn[t][mt][1];
+        }
       }
     }
     if (!ok) break;
