@@ -94,3 +94,39 @@ def test_tc_backward_exact_absmax_and_degenerate(qn):
     assert layer.rel_fro(dX, ref) < TOL
     dX, ref = _bwd(qn, np.zeros((384, 320), np.float32), c["dY"], c["A"], c["B"], c["alpha"])  # adapter only
     assert layer.rel_fro(dX, ref) < TOL
+
+
+def test_prefill_calls_in_a_graph_match_eager(qn):
+    """The large-M forward, backward dX and adapter gradients run part of
+    their work on a second stream (event fork / join).  Captured in a CUDA
+    graph and replayed, they must give the same bits as the eager calls."""
+    c = synth.layer_case(seed=11, d=1000, k=256, M=600, r=16, alpha=32.0)
+    q = qn.nf4_quantize(torch.from_numpy(c["W"]).cuda())
+    X, dY = c["X"].cuda(), c["dY"].cuda()
+    A, B = c["A"].cuda(), c["B"].cuda()
+    Y0 = qn.qlora_linear_fwd(q, X, A, B, c["alpha"])
+    dX0 = qn.qlora_linear_bwd_dx(q, dY, A, B, c["alpha"])
+    dA0, dB0 = qn.qlora_linear_bwd_lora(X, dY, A, B, c["alpha"])
+    torch.cuda.synchronize()
+    Y1, dX1 = torch.empty_like(Y0), torch.empty_like(dX0)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up on the capture stream (workspace allocation)
+        qn.qlora_linear_fwd(q, X, A, B, c["alpha"], out=Y1)
+        qn.qlora_linear_bwd_dx(q, dY, A, B, c["alpha"], out=dX1)
+        qn.qlora_linear_bwd_lora(X, dY, A, B, c["alpha"])
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        qn.qlora_linear_fwd(q, X, A, B, c["alpha"], out=Y1)
+        qn.qlora_linear_bwd_dx(q, dY, A, B, c["alpha"], out=dX1)
+        dA1, dB1 = qn.qlora_linear_bwd_lora(X, dY, A, B, c["alpha"])
+    Y1.zero_(); dX1.zero_()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    qn.device_status()
+    assert torch.equal(Y1, Y0)
+    assert torch.equal(dX1, dX0)
+    assert torch.equal(dA1, dA0) and torch.equal(dB1, dB0)
