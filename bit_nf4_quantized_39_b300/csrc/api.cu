@@ -590,7 +590,9 @@ qn_status launch_lora_proj(const uint16_t *P, int64_t M, int64_t K, const uint16
   const bool q_rows = pal && qs_k == 1 && (qs_n % 8) == 0;                 // Qop contiguous along kk
   const bool q_cols = pal && qs_n == 1 && (qs_k % 8) == 0 && (N % 8) == 0;  // Qop contiguous along n
   const bool pipe = q_rows || q_cols;
-  int64_t S = qn_ceil_div((pipe ? 4 : 6) * static_cast<int64_t>(sm_count()), tiles);
+  // one wave: the pipelined kernel holds four CTAs per SM
+  int64_t S = pipe ? (4 * static_cast<int64_t>(sm_count())) / tiles
+                   : qn_ceil_div(6 * static_cast<int64_t>(sm_count()), tiles);
   const int64_t smax = qn_ceil_div(K, 256);
   if (S > smax) S = smax;
   if (S > qn::kProjMaxSplit) S = qn::kProjMaxSplit;
@@ -617,6 +619,12 @@ qn_status launch_lora_proj(const uint16_t *P, int64_t M, int64_t K, const uint16
   }
   QN_LAUNCH_CHECK("lora_proj_kernel");
   const int64_t n = M * (C2 ? R : N);
+  if ((N % 4) == 0 && (R % 4) == 0 && (ld2 % 4) == 0 && aligned(C32, 16) && aligned(C2, 8)) {
+    qn::lora_reduce4_kernel<<<static_cast<unsigned>(qn_ceil_div(n / 4, 256)), 256, 0, st>>>(
+        part, static_cast<int>(S), M, N, C32, R, C2, ld2);
+    QN_LAUNCH_CHECK("lora_reduce4_kernel");
+    return QN_OK;
+  }
   qn::lora_reduce_kernel<<<static_cast<unsigned>(qn_ceil_div(n, 256)), 256, 0, st>>>(part, static_cast<int>(S), M, N,
                                                                                       C32, R, C2, ld2);
   QN_LAUNCH_CHECK("lora_reduce_kernel");

@@ -261,6 +261,39 @@ __global__ void lora_reduce_kernel(const float *__restrict__ part, int S, int64_
   }
 }
 
+// lora_reduce_kernel four columns at a time (N, R and ld2 multiples of 4, C32
+// and C2 16- and 8-byte aligned): thread (m, c4) sums columns 4 c4 .. + 3 of
+// row m over the splits in split order (the same sums) and writes them, or
+// the zero padding of C2 when 4 c4 >= N.
+__global__ void lora_reduce4_kernel(const float *__restrict__ part, int S, int64_t M, int64_t N,
+                                    float *__restrict__ C32, int R, uint16_t *__restrict__ C2, int64_t ld2) {
+  const int64_t cols4 = (C2 ? R : N) / 4;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= M * cols4) return;
+  const int64_t m = i / cols4, j = (i % cols4) * 4;
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (j < N)
+    for (int z = 0; z < S; ++z) {
+      const float4 w = *reinterpret_cast<const float4 *>(part + (static_cast<int64_t>(z) * M + m) * N + j);
+      v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+    }
+  if (C32 && j < N) *reinterpret_cast<float4 *>(C32 + m * N + j) = v;
+  if (C2) {
+    const float f[4] = {v.x, v.y, v.z, v.w};
+    uint32_t hi[2], lo[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const uint16_t h0 = f32_to_bf16_bits(f[2 * e]), h1 = f32_to_bf16_bits(f[2 * e + 1]);
+      hi[e] = h0 | (static_cast<uint32_t>(h1) << 16);
+      lo[e] = f32_to_bf16_bits(f[2 * e] - bf16_bits_to_f32(h0)) |
+              (static_cast<uint32_t>(f32_to_bf16_bits(f[2 * e + 1] - bf16_bits_to_f32(h1))) << 16);
+    }
+    *reinterpret_cast<uint2 *>(C2 + m * ld2 + j) = make_uint2(hi[0], hi[1]);
+    *reinterpret_cast<uint2 *>(C2 + m * ld2 + R + j) = make_uint2(lo[0], lo[1]);
+    for (int64_t q = 2 * R + j; q < ld2; q += R) *reinterpret_cast<uint2 *>(C2 + m * ld2 + q) = make_uint2(0u, 0u);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Tiled fused GEMM on CUDA cores (any M; fallback path).
 //   kTrans == false (forward):  C[m, c] = sum_j P[m, j] W'[c, j] + sum_q L[m, q] Bm[c, q]
