@@ -17,6 +17,7 @@
 #include "qlora_simt.cuh"
 #include "qlora_decode.cuh"
 #include "qlora_skinny.cuh"
+#include "qlora_m16.cuh"
 #include "qlora_gemv.cuh"
 #include "qlora_tc.cuh"
 #include "lora_grad.cuh"
@@ -527,6 +528,55 @@ qn_status launch_skinny_group(int n, const qn_nf4 *const *Q, const uint16_t *X, 
   return xs ? launch_skinny_variant<2, true>(g, smem, st) : launch_skinny_variant<2, false>(g, smem, st);
 }
 
+// Forward of a group of projections of one input with 8 < M <= 16 tokens on
+// the K-slice kernel: the adapter down-projection u (skinny_u_kernel), then
+// the weights (qlora_m16_kernel), both PDL-launched.  `taken` is false (and
+// nothing is launched) when the shapes or alignments do not suit it: k a
+// multiple of 256, the int8 block constants 4-byte aligned.
+qn_status launch_m16_group(int n, const qn_nf4 *const *Q, const uint16_t *X, int64_t M, const uint16_t *const *A,
+                           const uint16_t *const *B, const int32_t *r, const float *alpha, uint16_t *const *Y,
+                           Span &sp, cudaStream_t st, bool *taken) {
+  *taken = false;
+  const int64_t k = Q[0]->k;
+  if (M <= 8 || M > 16 || (k % 256) != 0) return QN_OK;
+  for (int i = 0; i < n; ++i)
+    if (Q[i]->dq && !aligned(Q[i]->absmax_q, 4)) return QN_OK;
+  qn::SkGroup g = {};
+  g.n = n;
+  g.M = static_cast<int>(M);
+  g.k = k;
+  g.X = X;
+  int64_t tiles = 0, us = 0;
+  for (int i = 0; i < n; ++i) {
+    qn::SkProj &p = g.p[i];
+    p.q = view_of(Q[i]);
+    p.A = A[i];
+    p.B = B[i];
+    p.Y = Y[i];
+    p.r = r[i];
+    p.s = alpha[i] / static_cast<float>(r[i]);
+    p.group_off = tiles;
+    p.u_off = us;
+    tiles += qn_ceil_div(Q[i]->d, 16);
+    us += r[i];
+  }
+  if (tiles > (int64_t{1} << 30)) return QN_OK;
+  g.ngroups = tiles;
+  g.rtot = us;
+  g.u = sp.take<float>(static_cast<size_t>(M) * us);
+  QN_TRY(launch_pdl(qn::skinny_u_kernel, dim3(static_cast<unsigned>(us), static_cast<unsigned>(M)),
+                    dim3(qn::kSkUThreads), 0, st, "skinny_u_kernel", g));
+  QN_TRY(cuda_check(cudaFuncSetAttribute(qn::qlora_m16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(qn::kM16SmemBytes)),
+                    "cudaFuncSetAttribute(m16 smem)"));
+  int64_t grid = sm_count();
+  if (grid > tiles) grid = tiles;
+  QN_TRY(launch_pdl(qn::qlora_m16_kernel, dim3(static_cast<unsigned>(grid)), dim3(qn::kM16Threads),
+                    qn::kM16SmemBytes, st, "qlora_m16_kernel", g));
+  *taken = true;
+  return QN_OK;
+}
+
 qn_status check_layer(const qn_nf4 *Q, const void *in, int64_t M, const void *A, const void *B, int32_t r,
                       float alpha, const void *out) {
   QN_TRY(check_nf4(Q, true));
@@ -863,7 +913,12 @@ qn_status qlora_linear_fwd(const qn_nf4 *Q, const uint16_t *X, int64_t M, const 
     if (taken) return QN_OK;
   }
   if (use_decode(M, k)) return launch_decode_group(1, &Q, X, &A, &B, &r, &alpha, &Y, sem, sp, st);
-  if (use_skinny(M, k)) return launch_skinny_group(1, &Q, X, M, &A, &B, &r, &alpha, &Y, sp, st);
+  if (use_skinny(M, k)) {
+    bool taken = false;
+    QN_TRY(launch_m16_group(1, &Q, X, M, &A, &B, &r, &alpha, &Y, sp, st, &taken));
+    if (taken) return QN_OK;
+    return launch_skinny_group(1, &Q, X, M, &A, &B, &r, &alpha, &Y, sp, st);
+  }
   float *u = sp.take<float>(static_cast<size_t>(M) * r);
   float *part = sp.take<float>(static_cast<size_t>(qn::kProjMaxSplit) * M * r);
   if (qn::tc_supported(M, d, k, r)) {
@@ -908,6 +963,8 @@ qn_status qlora_linear_fwd_group(int32_t n, const qn_nf4 *const *Q, const uint16
     QN_TRY(launch_gemv_group(n, Q, X, M, A, B, r, alpha, Y, sem, sp, st, &taken));
     if (taken) return QN_OK;
     if (use_decode(M, k)) return launch_decode_group(n, Q, X, A, B, r, alpha, Y, sem, sp, st);
+    QN_TRY(launch_m16_group(n, Q, X, M, A, B, r, alpha, Y, sp, st, &taken));
+    if (taken) return QN_OK;
     return launch_skinny_group(n, Q, X, M, A, B, r, alpha, Y, sp, st);
   }
   for (int i = 0; i < n; ++i)
