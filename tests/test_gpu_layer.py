@@ -66,6 +66,12 @@ def test_layer_case(qn):
 @pytest.mark.parametrize("M,d,k,r", [
     (1, 256, 512, 8), (2, 200, 192, 3), (5, 384, 1024, 64), (16, 320, 256, 16),
     (17, 192, 320, 8), (100, 330, 256, 24), (300, 128, 640, 64), (129, 1000, 128, 1),
+    # 8 < M <= 16: the K-slice kernel (k a multiple of 256, ragged rows and
+    # tokens, one and several tiles per CTA, a second batch of tiles per CTA)
+    # and the row-group kernel (k not)
+    (12, 1000, 512, 8), (9, 3000, 768, 24), (12, 200, 320, 8), (12, 30000, 256, 8),
+    # M <= 8 with x too large for the few-token kernel: the row-group kernel
+    (6, 256, 4096, 16),
 ])
 def test_shapes_with_ragged_tails(qn, M, d, k, r):
     c = synth.layer_case(seed=M * 7 + d, d=d, k=k, M=M, r=r, alpha=2.0 * r)
