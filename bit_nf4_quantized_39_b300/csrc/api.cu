@@ -145,9 +145,35 @@ QnNF4View view_of(const qn_nf4 *Q) {
   return v;
 }
 
-constexpr size_t kQuantWs = kSemBytes + qn::kNumBins * sizeof(unsigned long long);
+// Launch with programmatic stream serialisation (PDL): the kernel may start
+// before the previous kernel on the stream has finished; the kernels
+// themselves call griddepcontrol.wait before touching anything that the
+// previous kernel may write.
+template <typename... KArgs, typename... Args>
+qn_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     const char *what, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  QN_TRY(cuda_check(cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...), what));
+  QN_LAUNCH_CHECK(what);
+  return QN_OK;
+}
 
-// Quantise n elements (internal; arguments already checked).  `bins` (2 KiB)
+constexpr size_t kQuantWs = kSemBytes + qn::kNumBins * sizeof(unsigned long long);
+// Byte offset in the zero area of the quantiser's exponent bins (2 KiB); the
+// kernels return them to zero.
+constexpr size_t kBinsOffset = 64 * 1024;
+
+// Quantise n elements (internal; arguments already checked).  `bins` (2 KiB,
+// zero on entry, zero again on exit)
 // and `ticket` (one word, zero on entry, zero again on exit) are scratch.
 qn_status launch_quantize(const void *W, qn_dtype wdt, const qn_nf4 *Q, unsigned long long *bins,
                           unsigned int *ticket, cudaStream_t st) {
@@ -155,7 +181,6 @@ qn_status launch_quantize(const void *W, qn_dtype wdt, const qn_nf4 *Q, unsigned
   const int64_t nfull = n / 64;
   const int64_t nblk = qn_ceil_div(n, 64);
   unsigned long long *b = Q->dq ? bins : nullptr;
-  if (b) QN_TRY(cuda_check(cudaMemsetAsync(b, 0, qn::kNumBins * sizeof(unsigned long long), st), "memset bins"));
   const int sms = sm_count();
   // The partial last block goes first: its constant must be in the bins
   // before the main kernel's last CTA forms the mean.
@@ -213,9 +238,9 @@ qn_status launch_quantize(const void *W, qn_dtype wdt, const qn_nf4 *Q, unsigned
     int64_t grid = qn_ceil_div(ngrp, qn::kDqWarps);
     const int64_t cap = static_cast<int64_t>(sms) * 4;
     if (grid > cap) grid = cap;
-    qn::nf4_dq_kernel<<<static_cast<unsigned>(grid), qn::kDqWarps * 32, 0, st>>>(
-        Q->absmax, nblk, Q->absmax_mean, Q->absmax_q, Q->absmax_scale);
-    QN_LAUNCH_CHECK("nf4_dq_kernel");
+    QN_TRY(launch_pdl(qn::nf4_dq_kernel, dim3(static_cast<unsigned>(grid)), dim3(qn::kDqWarps * 32), 0, st,
+                      "nf4_dq_kernel", static_cast<const float *>(Q->absmax), nblk,
+                      static_cast<const float *>(Q->absmax_mean), Q->absmax_q, Q->absmax_scale));
   }
   return QN_OK;
 }
@@ -273,27 +298,6 @@ size_t bwd_ws_bytes(int64_t M, int64_t d, int64_t k, int32_t r) {
          qn::tc_bwd_ws_bytes(M, d, k, r);
 }
 
-// Launch with programmatic stream serialisation (PDL): the kernel may start
-// before the previous kernel on the stream has finished; the kernels
-// themselves call griddepcontrol.wait before touching anything that the
-// previous kernel may write.
-template <typename... KArgs, typename... Args>
-qn_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                     const char *what, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  QN_TRY(cuda_check(cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...), what));
-  QN_LAUNCH_CHECK(what);
-  return QN_OK;
-}
 
 // Single-token forward of a group of projections of one input: one
 // persistent kernel (every CTA resident, at least one per SM); its two
@@ -881,7 +885,7 @@ qn_status nf4_quantize(const void *W, qn_dtype wdt, const qn_nf4 *Q, void *ws, s
     if (ws_bytes < kQuantWs) return fail(QN_ENOMEM, "workspace %zu < %zu bytes", ws_bytes, kQuantWs);
     if (!aligned(ws, 16)) return fail(QN_EALIGN, "workspace not 16-byte aligned");
   }
-  return launch_quantize(W, wdt, Q, reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kSemBytes),
+  return launch_quantize(W, wdt, Q, reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kBinsOffset),
                          static_cast<unsigned int *>(ws), static_cast<cudaStream_t>(stream));
 }
 
@@ -1115,7 +1119,9 @@ qn_status nf4_quantize_noalloc(const void *W, qn_dtype wdt, const qn_nf4 *Q, voi
   QN_TRY(noalloc_bins(&bins));
   unsigned int *ticket = reinterpret_cast<unsigned int *>(bins + qn::kNumBins);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  QN_TRY(cuda_check(cudaMemsetAsync(ticket, 0, sizeof(unsigned int), st), "clear scratch ticket"));
+  // bins and ticket start from zero on every call (the kernels also leave them zero)
+  QN_TRY(cuda_check(cudaMemsetAsync(bins, 0, (qn::kNumBins + 32) * sizeof(unsigned long long), st),
+                    "clear scratch"));
   return launch_quantize(W, wdt, Q, bins, ticket, st);
 }
 
@@ -1187,7 +1193,7 @@ qn_status loftq_run_p(const float *W, int64_t d, int64_t k, int32_t r, float alp
   float *lam = sp.take<float>(qn::kLqMaxP);
   double *partial = sp.take<double>(1024);
   double *norm2 = sp.take<double>(65);  // squared residual norms, copied to the host once at the end
-  unsigned long long *bins = sp.take<unsigned long long>(qn::kNumBins);
+  unsigned long long *bins = reinterpret_cast<unsigned long long *>(reinterpret_cast<char *>(sem) + kBinsOffset);
 
   const float s = alpha / static_cast<float>(r);
   const int sms = sm_count();
@@ -1457,10 +1463,9 @@ qn_status nf4_merge_lora(const qn_nf4 *Q, const uint16_t *A, const uint16_t *B, 
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t d = Q->d, k = Q->k, nblk = d * (k >> 6);
-  unsigned long long *bins = Qout->dq ? reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kSemBytes)
+  unsigned long long *bins = Qout->dq ? reinterpret_cast<unsigned long long *>(static_cast<char *>(ws) + kBinsOffset)
                                       : nullptr;
   unsigned int *ticket = static_cast<unsigned int *>(ws);
-  if (bins) QN_TRY(cuda_check(cudaMemsetAsync(bins, 0, qn::kNumBins * sizeof(unsigned long long), st), "memset bins"));
   static int attr_set[64] = {0};
   int dev = 0;
   QN_TRY(cuda_check(cudaGetDevice(&dev), "cudaGetDevice"));

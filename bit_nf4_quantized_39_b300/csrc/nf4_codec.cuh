@@ -300,7 +300,8 @@ __device__ __forceinline__ void build_bucket_tables(BucketEntry *s_one, BucketEn
 // End of a quantising kernel with double quantisation (every thread of the
 // CTA calls it): the CTA's exponent bins go to the global bins; the last CTA
 // of the whole grid (1-D or not) to finish forms the exact mean of all nblk
-// block constants, stores it and returns the ticket to zero.
+// block constants, stores it and returns the ticket and the bins to zero
+// (both are zero on entry: they live in a zero area).
 __device__ __forceinline__ void quant_mean_epilogue(unsigned long long *s_bins, unsigned long long *bins,
                                                     unsigned int *ticket, int64_t nblk, float *absmax_mean) {
   __shared__ bool s_last;
@@ -321,6 +322,8 @@ __device__ __forceinline__ void quant_mean_epilogue(unsigned long long *s_bins, 
       *ticket = 0u;
     }
   }
+  __syncthreads();  // the bins are read; return them to zero for the next call
+  for (int i = threadIdx.x; i < kNumBins; i += blockDim.x) bins[i] = 0ull;
 }
 
 // Quantiser main loop.  Each warp streams its own ring of kQuantRing stages
@@ -498,6 +501,7 @@ __global__ void __launch_bounds__(kDqWarps * 32)
 nf4_dq_kernel(const float *__restrict__ absmax, int64_t nblk, const float *__restrict__ absmax_mean,
               int8_t *__restrict__ absmax_q, float *__restrict__ absmax_scale) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the constants and the mean come from the quantiser
   const float mu = __ldcg(absmax_mean);
   const int64_t ngrp = qn_ceil_div(nblk, 256);
   for (int64_t g = static_cast<int64_t>(blockIdx.x) * kDqWarps + warp; g < ngrp;
@@ -508,7 +512,7 @@ nf4_dq_kernel(const float *__restrict__ absmax, int64_t nblk, const float *__res
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int64_t j = base + i;
-      c[i] = (j < nblk) ? __fsub_rn(absmax[j], mu) : 0.f;
+      c[i] = (j < nblk) ? __fsub_rn(__ldcg(absmax + j), mu) : 0.f;
       S = fmaxf(S, fabsf(c[i]));
     }
 #pragma unroll
