@@ -69,7 +69,7 @@ def test_layer_case(qn):
     # 8 < M <= 16: the K-slice kernel (k a multiple of 256, ragged rows and
     # tokens, one and several tiles per CTA, a second batch of tiles per CTA)
     # and the row-group kernel (k not)
-    (12, 1000, 512, 8), (9, 3000, 768, 24), (12, 200, 320, 8), (12, 30000, 256, 8),
+    (12, 1000, 512, 8), (9, 3000, 768, 24), (12, 200, 320, 8), (12, 30000, 256, 8), (12, 1000, 1024, 8),
     # M <= 8 with x too large for the few-token kernel: the row-group kernel
     (6, 256, 4096, 16),
 ])
