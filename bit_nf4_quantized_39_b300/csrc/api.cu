@@ -429,7 +429,7 @@ qn_status launch_gemv_group(int n, const qn_nf4 *const *Q, const uint16_t *X, in
     p.s = alpha[i] / static_cast<float>(r[i]);
     p.row_off = rows;
     p.u_off = us;
-    if (!aligned(p.consts, 16) || !aligned(p.A, 16) || !aligned(p.B, 16) ||
+    if (!aligned(p.codes, 16) || !aligned(p.consts, 16) || !aligned(p.A, 16) || !aligned(p.B, 16) ||
         (p.dq && !aligned(p.absmax_scale, 16)))
       return QN_OK;
     rows += Q[i]->d;

@@ -7,42 +7,43 @@
 // weight is 4-bit NF4 with blockwise constants.)  The call is bound by the
 // bytes of the packed weights (8-50 MB at decode sizes).  On this part an SM
 // needs ~100 KB of reads in flight to cover HBM latency under load, and
-// shared-memory copies with cp.async carry that with no registers, so:
+// asynchronous copies into shared memory carry that with no registers, so:
 //
 // * the group's rows form one list, cut into equal contiguous ranges, one
-//   per CTA (one CTA per SM, 16 warps); a range is cut into 16-row tiles and
-//   each tile into stages of 16 rows x 2048 columns (16 KiB of codes);
-// * all threads copy stages with 16-byte cp.async (whole 128-byte lines,
-//   xor-swizzled in shared memory) into a kGvRing-deep ring: kGvRing - 1
-//   stages (80 KiB) in flight while one is consumed; one barrier per stage
-//   both publishes the stage and frees the slot of the previous one;
-// * warp w takes 64-blocks w and w + 16 of each stage: a lane (group g,
-//   thread t) reads 8 code bytes of rows g and g + 8, turns each byte into a
-//   bf16x2 pair through a per-lane replicated byte-pair table (one byte
-//   permute and one shared load with an immediate base per byte),
-//   multiplies on mma.sync m16n8k16 (tokens are the N columns) against x,
-//   which is staged as bf16 in the unused half of every table row, and
-//   scales each block's dot products by its block constant in fp32.  The
-//   MMA's k order is a permutation of the block's elements, the same for
-//   both operands.  Each lane decodes one block constant per stage (row
-//   lane mod 16, block w + 16 (lane / 16)) from the DQ codes and scales
-//   copied to shared memory at the start;
-// * at the end of a tile the warps' partial sums go to a double-buffered
-//   area; during the next stage one warp adds them in warp order;
+//   per CTA (one CTA per SM); a range is cut into 16-row tiles and each tile
+//   into stages of 16 rows x 4096 columns (32 KiB of codes);
+// * a producer warp brings each stage into a ring of 2..8 slots (what the
+//   shared memory leaves) with one bulk copy (TMA) per row, counted on
+//   the slot's full barrier; rows sit 2080 bytes apart, so the consumers'
+//   8-byte reads are conflict-free.  Bulk copies keep the stage traffic out
+//   of the load/store pipe that the table lookups need;
+// * 16 consumer warps: warp w takes 64-blocks w, w + 16, w + 32, w + 48 of
+//   each stage: a lane (group g, thread t) reads 8 code bytes of rows g and
+//   g + 8, turns each byte into a bf16x2 pair through a per-lane replicated
+//   byte-pair table (one byte permute and one shared load with an immediate
+//   base per byte), multiplies on mma.sync m16n8k16 (tokens are the N
+//   columns) against x, which is staged as bf16 in the unused half of every
+//   table row, and scales each block's dot products by its fp32 block
+//   constant (decoded once per CTA into shared memory).  The MMA's k order
+//   is a permutation of the block's elements, the same for both operands.
+//   A warp arrives on the slot's empty barrier when it is done with it;
+// * at the end of a tile each warp writes its partial sums; the output
+//   phase adds them in warp order;
 // * the adapter rows u = s X A^T are spread over the CTAs (row j by CTA
 //   j mod G, split over the 16 warps) before the weight loop and published
-//   through a ready counter; after the loop one thread per CTA waits
-//   (bounded) for all of them, then thread i adds u . B[row i] and writes
-//   bf16 Y = row sum + adapter term.
+//   through a ready counter by the second producer warp; after its copies
+//   the first producer warp waits (bounded) for all of them and stages u;
+//   then thread i adds u . B[row i] and writes bf16 Y = row sum + adapter
+//   term.
 //
 // Programmatic dependent launch: the kernel lets the next call launch at
 // entry; before griddepcontrol.wait a CTA only builds its tables and
 // prefetches its first stages into L2 (a prefetch cannot return stale data).
 // Everything a kernel may have written -- codes, constants, X, A, B, u, Y,
 // the counters -- is read after the wait, through L2 (ld.global.cg,
-// cp.async.cg).  Every CTA of the grid is resident at once (one per SM), so
-// the wait for u always ends; it is bounded all the same (QN_DEV_TIMEOUT).
-// The last CTA to leave returns both counters to zero.
+// cp.async.cg, bulk copies).  Every CTA of the grid is resident at once (one
+// per SM), so the wait for u always ends; it is bounded all the same
+// (QN_DEV_TIMEOUT).  The last CTA to leave returns both counters to zero.
 #pragma once
 
 #include "common.cuh"
@@ -51,12 +52,14 @@
 namespace qn {
 
 constexpr int kGvWarps = 16;                        // consumer warps (MMA)
-constexpr int kGvProducers = 64;                    // producer threads (two warps: stage copies)
+constexpr int kGvProducers = 64;                    // producer threads (two warps: stage copies, u)
 constexpr int kGvThreads = kGvWarps * 32 + kGvProducers;
 constexpr int kGvMaxRing = 8;                       // stage slots at most (the plan picks what fits)
 constexpr int kGvStageBlocks = 64;                  // 64-blocks per stage (4096 columns)
-constexpr uint32_t kGvStageRow = kGvStageBlocks * 32;  // bytes of one row in a stage
-constexpr uint32_t kGvStageBytes = 16 * kGvStageRow;  // 32 KiB of codes
+constexpr uint32_t kGvStageRow = kGvStageBlocks * 32;  // code bytes of one row in a stage
+constexpr uint32_t kGvRowPitch = kGvStageRow + 32;    // shared-memory bytes per row: 32 bytes of padding
+constexpr uint32_t kGvStageBytes = 16 * kGvRowPitch;  // 32 KiB of codes + padding
+static_assert(kGvStageBlocks % 32 == 0, "a warp takes blocks w + 16 j in pairs");
 constexpr int kGvMaxM = 8;
 constexpr int kGvMaxGroup = 8;
 constexpr int kGvMaxXElems = 16384;                 // M * k staged in the table rows
@@ -176,11 +179,6 @@ __device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
 }
-// Arrives on the mbarrier once this thread's earlier cp.async copies have
-// landed (the barrier's count includes this arrival).
-__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
 __device__ __forceinline__ uint2 lds_v2(uint32_t a) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
@@ -188,9 +186,10 @@ __device__ __forceinline__ uint2 lds_v2(uint32_t a) {
 }
 __device__ __forceinline__ uint2 lds_v2_off8r(uint32_t a) {  // 8 rows of a stage further
   uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2+16384];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2+16640];" : "=r"(v.x), "=r"(v.y) : "r"(a));
   return v;
 }
+static_assert(8 * kGvRowPitch == 16640, "immediate offset of lds_v2_off8r");
 __device__ __forceinline__ uint4 lds_v4(uint32_t a) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
@@ -274,13 +273,10 @@ inline bool gv_plan(GvGroup &g, int grid, int esz_max, bool any_dq) {
   return true;
 }
 
-// Shared-memory offset of byte x (0..2047) of row r (0..15) of a stage: the
-// 16-byte pieces of each 128-byte span are xor-swizzled by r mod 8, so the
-// 8-byte reads of rows g (and g + 8) of one column by eight lane groups hit
-// different banks.
-__device__ __forceinline__ uint32_t gv_stage_off(uint32_t r, uint32_t x) {
-  return r * kGvStageRow + (x & ~127u) + ((((x >> 4) & 7u) ^ (r & 7u)) << 4) + (x & 15u);
-}
+// A stage holds row r (0..15) at r * kGvRowPitch.  The 32 bytes of padding
+// per row shift consecutive rows by eight banks, so the 8-byte reads of rows
+// g = 0..3 (and 4..7) by the four lanes of each group cover all 32 banks once
+// per half-warp: conflict-free.
 
 // Copies [g0, g0 + len) of an array of `size` bytes to shared memory (16-byte
 // pieces, the piece that crosses the end of the array zero-filled).
@@ -407,7 +403,7 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
   }
   if (warp == 9 && lane == 0) {
     for (int i = 0; i < kGvMaxRing; ++i) {
-      mbar_init(smem_u32(&full[i]), kGvProducers);
+      mbar_init(smem_u32(&full[i]), 1);
       mbar_init(smem_u32(&empty[i]), kGvWarps);
     }
     mbar_init(smem_u32(upart), 1);
@@ -455,6 +451,23 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
     rows[lr] = rw;
   }
   __syncthreads();
+  if (warp == kGvWarps) {
+    // The codes of the first stages into L2 while the kernel before this one
+    // finishes (a prefetch changes no data, so it may run before the wait):
+    // lane r takes row r of each tile.
+    const int npre = nst < g.ring ? nst : g.ring;
+    int tl = 0, ch = 0;
+    for (int s = 0; s < npre; ++s) {
+      const int cbl = (nb - ch * kGvStageBlocks) < kGvStageBlocks ? nb - ch * kGvStageBlocks : kGvStageBlocks;
+      if (lane < 16 && 16 * tl + lane < nrows)
+        prefetch_l2_bulk(rows[16 * tl + lane].code + static_cast<int64_t>(ch) * kGvStageRow,
+                         static_cast<uint32_t>(cbl) * 32u);
+      if (++ch == nch) {
+        ch = 0;
+        ++tl;
+      }
+    }
+  }
   pdl_wait_grid();
 
   // ---- after the wait -----------------------------------------------------------
@@ -463,62 +476,58 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
   const int R = g.ring;
   if (warp >= kGvWarps) {
     // ================================ producers =================================
-    // Stages in order (tile, chunk) into slots 0, 1, ... R - 1, 0, ...: thread
-    // p copies the 16-byte columns 16 p and 16 p + 1024 of the chunk's 2048
-    // bytes of all 16 rows, then arrives on the slot's full barrier once its
-    // copies land.
-    const uint32_t x = static_cast<uint32_t>(tid - kGvWarps * 32) << 4;
-    // The second producer warp adds the consumers' parts of this CTA's
-    // adapter rows (in warp order) and publishes them once the ring is full;
-    // its fence then stalls no consumer.
-    bool published = warp != kGvWarps + 1 || nu == 0;
-    auto publish = [&]() {
-      published = true;
-      if (!mbar_wait(smem_u32(upart), 0, abort)) return;
-      if (lane < nu * M) {
-        const int iu = lane / M, t = lane - iu * M;
-        const int64_t j = blockIdx.x + static_cast<int64_t>(G) * iu;
-        int pi = 0;
-        for (int i = 1; i < g.n; ++i)
-          if (j >= mt.p[i].u_off) pi = i;
-        float v = 0.f;
-        for (int w = 0; w < kGvWarps; ++w) v += ured[(iu * kGvWarps + w) * M + t];
-        g.u[t * rtot + j] = mt.p[pi].s * v;
-      }
-      __syncwarp();
-      if (lane == 0) {
-        __threadfence();
-        atomicAdd(&g.zero_area[kGvFlagReady], static_cast<unsigned>(nu));
-      }
-    };
-    int tl = 0, ch = 0;
-    for (int s = 0; s < nst; ++s) {
-      if (s == R && !published) publish();
-      const int slot = s % R;
-      if (s >= R && !mbar_wait(smem_u32(&empty[slot]), ((s / R) - 1) & 1, abort)) break;
-      const int cbl = (nb - ch * kGvStageBlocks) < kGvStageBlocks ? nb - ch * kGvStageBlocks : kGvStageBlocks;
-      const uint32_t dst = ring + static_cast<uint32_t>(slot) * kGvStageBytes;
-      const int64_t co = static_cast<int64_t>(ch) * kGvStageRow;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t xh = x + 1024u * h;
-        if (xh < static_cast<uint32_t>(cbl) * 32u) {
-#pragma unroll 4
-          for (int r = 0; r < 16; ++r) cp_async16(dst + gv_stage_off(r, xh), rows[tl * 16 + r].code + co + xh);
+    if (warp == kGvWarps + 1) {
+      // The second producer warp adds the consumers' parts of this CTA's
+      // adapter rows (in warp order) and publishes them.
+      if (nu > 0 && mbar_wait(smem_u32(upart), 0, abort)) {
+        if (lane < nu * M) {
+          const int iu = lane / M, t = lane - iu * M;
+          const int64_t j = blockIdx.x + static_cast<int64_t>(G) * iu;
+          int pi = 0;
+          for (int i = 1; i < g.n; ++i)
+            if (j >= mt.p[i].u_off) pi = i;
+          float v = 0.f;
+          for (int w = 0; w < kGvWarps; ++w) v += ured[(iu * kGvWarps + w) * M + t];
+          g.u[t * rtot + j] = mt.p[pi].s * v;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          atomicAdd(&g.zero_area[kGvFlagReady], static_cast<unsigned>(nu));
         }
       }
-      cp_async_mbar_arrive(smem_u32(&full[slot]));
-      if (++ch == nch) {
-        ch = 0;
-        ++tl;
+    } else {
+      // Stages in order (tile, chunk) into slots 0, 1, ... R - 1, 0, ...: lane r
+      // issues the bulk copy of row r of the tile (padding rows are not copied:
+      // their block constants are 0), counted on the slot's full barrier after
+      // lane 0 has announced the stage's bytes.
+      int tl = 0, ch = 0, s = 0;
+      const uint8_t *rowp = lane < 16 && lane < nrows ? rows[lane].code : nullptr;
+      for (; s < nst; ++s) {
+        const int slot = s % R;
+        if (s >= R && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[slot]), ((s / R) - 1) & 1, abort))) break;
+        const int cbl = (nb - ch * kGvStageBlocks) < kGvStageBlocks ? nb - ch * kGvStageBlocks : kGvStageBlocks;
+        const uint32_t bytes = static_cast<uint32_t>(cbl) * 32u;
+        const int nv = (nrows - 16 * tl) < 16 ? nrows - 16 * tl : 16;
+        const uint32_t fb = smem_u32(&full[slot]);
+        if (lane == 0) mbar_arrive_expect_tx(fb, bytes * static_cast<uint32_t>(nv));
+        __syncwarp();
+        if (lane < nv)
+          bulk_load(ring + static_cast<uint32_t>(slot) * kGvStageBytes + static_cast<uint32_t>(lane) * kGvRowPitch,
+                    rowp + static_cast<int64_t>(ch) * kGvStageRow, bytes, fb);
+        if (++ch == nch) {
+          ch = 0;
+          ++tl;
+          if (lane < 16 && 16 * tl + lane < nrows) rowp = rows[16 * tl + lane].code;
+        }
       }
-    }
-    if (!published) publish();
-    cp_async_wait_all();
-    if (warp == kGvWarps) {
-      // While the consumers finish: wait (bounded) until every CTA has
-      // published its rows of u, then stage u; the final barrier hands it over.
       if (lane == 0) {
+        // After an abort the copies still in flight target this CTA's shared
+        // memory: wait (bounded) for the last one of every slot.
+        if (s < nst)
+          for (int q = s > R ? s - R : 0; q < s; ++q) mbar_wait_drain(smem_u32(&full[q % R]), (q / R) & 1);
+        // While the consumers finish: wait (bounded) until every CTA has
+        // published its rows of u, then stage u; the final barrier hands it over.
         unsigned int spins = 0;
         while (gv_ld_acquire(&g.zero_area[kGvFlagReady]) < static_cast<unsigned>(rtot)) {
           if (++spins > kGvSpinLimit) {
@@ -664,7 +673,7 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
   // ---- weight loop: wait for a stage, consume blocks warp + 16 j, j = 0..3 ---------
   const uint32_t lane4 = static_cast<uint32_t>(lane) << 2;
   // this lane's code bytes of block `warp`, row gq (block warp + 16 j: +512 j; row gq + 8: +16384)
-  const uint32_t cofs = gv_stage_off(static_cast<uint32_t>(gq), static_cast<uint32_t>(warp * 32 + tq * 8));
+  const uint32_t cofs = static_cast<uint32_t>(gq) * kGvRowPitch + static_cast<uint32_t>(warp * 32 + tq * 8);
   // x of token gq, elements 64 warp + 16 tq .. + 15 (block warp + 16 j: +4096 j bytes)
   const uint32_t xw0 = sb + gv_x_chunk(gq * kc + 2u * tq, gq) + (static_cast<uint32_t>(warp) << 8);
   const uint32_t xw1 = sb + gv_x_chunk(gq * kc + 2u * tq + 1u, gq) + (static_cast<uint32_t>(warp) << 8);
@@ -691,10 +700,10 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
     if (ok) {
       const int cbl = (nb - ch * kGvStageBlocks) < kGvStageBlocks ? nb - ch * kGvStageBlocks : kGvStageBlocks;
       const uint32_t ca = ring + static_cast<uint32_t>(slot) * kGvStageBytes + cofs;
-      const uint32_t xo = static_cast<uint32_t>(ch) << 14;  // 64 blocks of 256 bytes per chunk
+      const uint32_t xo = static_cast<uint32_t>(ch * kGvStageBlocks) << 8;  // 256 bytes of table row per block
       const uint32_t mo = static_cast<uint32_t>(ch * kGvStageBlocks) * 4u;
 #pragma unroll
-      for (int jp = 0; jp < 4; jp += 2) {
+      for (int jp = 0; jp < kGvStageBlocks / 16; jp += 2) {
         // blocks warp + 16 jp and warp + 16 (jp + 1) side by side; a block past
         // the chunk's end reads in-bounds leftovers of the slot with x = 0, m = 0
         const bool v0 = warp + 16 * jp < cbl, v1 = warp + 16 * (jp + 1) < cbl;
