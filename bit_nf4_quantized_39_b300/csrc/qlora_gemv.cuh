@@ -288,6 +288,8 @@ __device__ __forceinline__ void gv_copy(uint32_t dst, const void *base, int64_t 
     cp_async16_zfill(dst + c, src + c, static_cast<uint32_t>(left < 16 ? left : 16));
   }
 }
+// Bulk L2 prefetch of [g0, g0 + len) of an array of `size` bytes (g0 and len
+// multiples of 16; the range is cut at the last whole 16 bytes of the array).
 __device__ __forceinline__ void gv_prefetch(const void *base, int64_t g0, int64_t len, int64_t size) {
   int64_t end = g0 + len;
   if (end > (size & ~int64_t{15})) end = size & ~int64_t{15};
@@ -427,6 +429,15 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
     for (int i = 1; i < mt.nseg; ++i)
       if (j >= mt.p[i].u_off) pi = i;
     gv_prefetch(mt.p[pi].A, (j - mt.p[pi].u_off) * k * 2, k * 2, static_cast<int64_t>(mt.p[pi].r) * k * 2);
+  }
+  if (tid >= 64 && tid < 64 + mt.nseg) {  // B rows of this CTA's rows into L2 (read by the output phase)
+    const GvSeg &sg = mt.seg[tid - 64];
+    if (sg.lr0 < sg.lr1) {
+      const GvProj &p = mt.p[sg.p];
+      const int64_t b0 = sg.ra * p.r * 2, b1 = (sg.ra + (sg.lr1 - sg.lr0)) * p.r * 2;
+      const int64_t a0 = b0 & ~int64_t{15};  // 16-byte aligned start and length
+      gv_prefetch(p.B, a0, ((b1 + 15) & ~int64_t{15}) - a0, p.d * p.r * 2);
+    }
   }
   for (int lr = tid; lr < ntl * 16; lr += kGvThreads) {
     // padding rows of the last tile read the first row's codes (their block
