@@ -38,7 +38,7 @@
 //
 // Programmatic dependent launch: the kernel lets the next call launch at
 // entry; before griddepcontrol.wait a CTA only builds its tables and
-// prefetches its first stages into L2 (a prefetch cannot return stale data).
+// prefetches its A and B rows into L2 (a prefetch cannot return stale data).
 // Everything a kernel may have written -- codes, constants, X, A, B, u, Y,
 // the counters -- is read after the wait, through L2 (ld.global.cg,
 // cp.async.cg, bulk copies).  Every CTA of the grid is resident at once (one
@@ -462,23 +462,6 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
     rows[lr] = rw;
   }
   __syncthreads();
-  if (warp == kGvWarps) {
-    // The codes of the first stages into L2 while the kernel before this one
-    // finishes (a prefetch changes no data, so it may run before the wait):
-    // lane r takes row r of each tile.
-    const int npre = nst < g.ring ? nst : g.ring;
-    int tl = 0, ch = 0;
-    for (int s = 0; s < npre; ++s) {
-      const int cbl = (nb - ch * kGvStageBlocks) < kGvStageBlocks ? nb - ch * kGvStageBlocks : kGvStageBlocks;
-      if (lane < 16 && 16 * tl + lane < nrows)
-        prefetch_l2_bulk(rows[16 * tl + lane].code + static_cast<int64_t>(ch) * kGvStageRow,
-                         static_cast<uint32_t>(cbl) * 32u);
-      if (++ch == nch) {
-        ch = 0;
-        ++tl;
-      }
-    }
-  }
   pdl_wait_grid();
 
   // ---- after the wait -----------------------------------------------------------
@@ -490,7 +473,10 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
     if (warp == kGvWarps + 1) {
       // The second producer warp adds the consumers' parts of this CTA's
       // adapter rows (in warp order) and publishes them.
-      if (nu > 0 && mbar_wait(smem_u32(upart), 0, abort)) {
+      bool got = false;
+      if (nu > 0 && lane == 0) got = mbar_wait(smem_u32(upart), 0, abort);
+      __syncwarp();
+      if (__shfl_sync(0xffffffffu, got, 0)) {
         if (lane < nu * M) {
           const int iu = lane / M, t = lane - iu * M;
           const int64_t j = blockIdx.x + static_cast<int64_t>(G) * iu;
@@ -514,9 +500,16 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
       // lane 0 has announced the stage's bytes.
       int tl = 0, ch = 0, s = 0;
       const uint8_t *rowp = lane < 16 && lane < nrows ? rows[lane].code : nullptr;
+      // The consumers' small copies (x, block constants, A) go out first.
+      asm volatile("bar.sync 2, %0;" ::"n"((kGvWarps + 1) * 32) : "memory");
       for (; s < nst; ++s) {
         const int slot = s % R;
-        if (s >= R && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[slot]), ((s / R) - 1) & 1, abort))) break;
+        if (s >= R) {
+          bool free_ = false;
+          if (lane == 0) free_ = mbar_wait(smem_u32(&empty[slot]), ((s / R) - 1) & 1, abort);
+          __syncwarp();
+          if (!__shfl_sync(0xffffffffu, free_, 0)) break;
+        }
         const int cbl = (nb - ch * kGvStageBlocks) < kGvStageBlocks ? nb - ch * kGvStageBlocks : kGvStageBlocks;
         const uint32_t bytes = static_cast<uint32_t>(cbl) * 32u;
         const int nv = (nrows - 16 * tl) < 16 ? nrows - 16 * tl : 16;
@@ -566,6 +559,7 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
     if (p.dq) gv_copy(s.sig_off, p.absmax_scale, s.sig_g0, s.sig_len, ((p.d * nb + 255) >> 8) * 4);
   }
   cp_async_commit();
+  asm volatile("bar.arrive 2, %0;" ::"n"((kGvWarps + 1) * 32) : "memory");  // the stage copies may start
   // adapter rows of this CTA: warp slice [v0, v1) of the k / 8 vectors
   const int v0 = static_cast<int>(kc * warp / kGvWarps), v1 = static_cast<int>(kc * (warp + 1) / kGvWarps);
   uint4 av0[kGvUVec], av1[kGvUVec];  // A pieces of two adapter rows
@@ -586,47 +580,48 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
   if (tid < g.n) mt.mu[tid] = mt.p[tid].dq ? ld_cg_f32(mt.p[tid].absmax_mean) : 0.f;
   cp_async_wait_all();  // the small copies
   asm volatile("bar.sync 1, %0;" ::"n"(kGvWarps * 32) : "memory");
-  // block constants of the range, decoded once into mconst[lr * ms + b]: warp
-  // w takes rows w, w + 16, ...; when nb is a multiple of 4, lane c takes
-  // blocks 4c .. 4c + 3 of the row (one 32-bit read of DQ codes: a row starts
-  // at a multiple of 4 blocks, so the four share one 256-block DQ group; or
-  // one 16-byte read of fp32 constants), else one block at a time.
-  const bool by4 = (nb & 3) == 0;
-#pragma unroll 4
-  for (int lr = warp; lr < ntl * 16; lr += kGvWarps) {
-    const GvRow &rw = rows[lr];
-    float *mr = mconst + lr * g.ms;
-    if (!by4) {
-      for (int b = lane; b < nb; b += 32) {
+  // block constants of the range, decoded once into mconst[lr * ms + b], one
+  // item per consumer thread in turn: when nb is a multiple of 4, item (row
+  // lr, c) is blocks 4c .. 4c + 3 of the row (one 32-bit read of DQ codes: a
+  // row starts at a multiple of 4 blocks, so the four share one 256-block DQ
+  // group; or one 16-byte read of fp32 constants), else item (lr, b) is
+  // block b.
+  {
+    const bool by4 = (nb & 3) == 0;
+    const int per = by4 ? nb >> 2 : nb;  // items per row
+    const int items = ntl * 16 * per;
+    for (int it = tid; it < items; it += kGvWarps * 32) {
+      const int lr = it / per, c = it - lr * per;
+      const GvRow rw = rows[lr];
+      float *mr = mconst + lr * g.ms;
+      if (by4) {
+        float m[4] = {0.f, 0.f, 0.f, 0.f};
+        if (rw.dq > 0) {
+          const uint32_t wq = *reinterpret_cast<const uint32_t *>(base + (rw.raw - kGvSmemBase) + 4 * c);
+          const float sg = *reinterpret_cast<const float *>(base + (rw.sig - kGvSmemBase) + ((rw.e0 + 4 * c) >> 8) * 4);
+          const float mu = mt.mu[rw.p];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) m[j] = dq_absmax(static_cast<int8_t>((wq >> (8 * j)) & 0xFFu), sg, mu);
+        } else if (rw.dq == 0) {
+          const uint4 wf = *reinterpret_cast<const uint4 *>(base + (rw.raw - kGvSmemBase) + 16 * c);
+          m[0] = __uint_as_float(wf.x);
+          m[1] = __uint_as_float(wf.y);
+          m[2] = __uint_as_float(wf.z);
+          m[3] = __uint_as_float(wf.w);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mr[4 * c + j] = m[j];
+      } else {
         float m = 0.f;
         if (rw.dq > 0) {
-          const int8_t q = *reinterpret_cast<const int8_t *>(base + (rw.raw - kGvSmemBase) + b);
-          const float sg = *reinterpret_cast<const float *>(base + (rw.sig - kGvSmemBase) + ((rw.e0 + b) >> 8) * 4);
+          const int8_t q = *reinterpret_cast<const int8_t *>(base + (rw.raw - kGvSmemBase) + c);
+          const float sg = *reinterpret_cast<const float *>(base + (rw.sig - kGvSmemBase) + ((rw.e0 + c) >> 8) * 4);
           m = dq_absmax(q, sg, mt.mu[rw.p]);
         } else if (rw.dq == 0) {
-          m = *reinterpret_cast<const float *>(base + (rw.raw - kGvSmemBase) + b * 4);
+          m = *reinterpret_cast<const float *>(base + (rw.raw - kGvSmemBase) + c * 4);
         }
-        mr[b] = m;
+        mr[c] = m;
       }
-      continue;
-    }
-    for (int c = lane; 4 * c < nb; c += 32) {
-      float m[4] = {0.f, 0.f, 0.f, 0.f};
-      if (rw.dq > 0) {
-        const uint32_t wq = *reinterpret_cast<const uint32_t *>(base + (rw.raw - kGvSmemBase) + 4 * c);
-        const float sg = *reinterpret_cast<const float *>(base + (rw.sig - kGvSmemBase) + ((rw.e0 + 4 * c) >> 8) * 4);
-        const float mu = mt.mu[rw.p];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) m[j] = dq_absmax(static_cast<int8_t>((wq >> (8 * j)) & 0xFFu), sg, mu);
-      } else if (rw.dq == 0) {
-        const uint4 wf = *reinterpret_cast<const uint4 *>(base + (rw.raw - kGvSmemBase) + 16 * c);
-        m[0] = __uint_as_float(wf.x);
-        m[1] = __uint_as_float(wf.y);
-        m[2] = __uint_as_float(wf.z);
-        m[3] = __uint_as_float(wf.w);
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) mr[4 * c + j] = m[j];
     }
   }
 
