@@ -412,8 +412,6 @@ qn_status launch_gemv_group(int n, const qn_nf4 *const *Q, const uint16_t *X, in
   g.X = X;
   g.zero_area = zero_area;
   int64_t rows = 0, us = 0;
-  int esz = 1;
-  bool any_dq = false;
   for (int i = 0; i < n; ++i) {
     qn::GvProj &p = g.p[i];
     p.codes = Q[i]->codes;
@@ -434,14 +432,12 @@ qn_status launch_gemv_group(int n, const qn_nf4 *const *Q, const uint16_t *X, in
       return QN_OK;
     rows += Q[i]->d;
     us += r[i];
-    if (!p.dq) esz = 4;
-    any_dq = any_dq || p.dq;
   }
   g.rows = rows;
   g.rtot = us;
   for (int i = 0; i < 16; ++i) g.lev16[i] = bf16_bits_rne(kNF4Levels[i]);
   const int grid = static_cast<int>(sm_count());
-  if (!qn::gv_plan(g, grid, esz, any_dq)) return QN_OK;
+  if (!qn::gv_plan(g, grid)) return QN_OK;
   g.u = sp.take<float>(static_cast<size_t>(M) * us);
   bool base_ok = false;  // the u buffer is scratch for the one-time probe
   QN_TRY(smem_base_matches(reinterpret_cast<unsigned int *>(g.u), st, &base_ok));

@@ -94,7 +94,7 @@ struct GvGroup {  // the kernel's parameter block (copied to shared memory at en
   float *u;                    // M x rtot fp32 (workspace)
   unsigned int *zero_area;     // ready and exit counters, zero between calls
   // shared-memory layout: byte offsets from the start of dynamic shared memory (gv_plan)
-  uint32_t off_ring, off_raw, off_sig, off_rows, off_m, off_part, off_us, off_ured, off_meta, off_bar, smem;
+  uint32_t off_ring, off_rows, off_m, off_part, off_us, off_ured, off_meta, off_bar, smem;
   int rows_cta;                // largest row range of a CTA
   int ring;                    // stage slots
   int ms;                      // row stride (floats, odd) of the decoded block constants
@@ -104,32 +104,25 @@ struct GvGroup {  // the kernel's parameter block (copied to shared memory at en
 
 static_assert(sizeof(GvGroup) % 8 == 0, "parameter block copied in 8-byte pieces");
 
-// A CTA's rows of one projection, with where its block constants and DQ
-// scales sit in shared memory.  Each copy covers the 16-byte-aligned superset
-// of the bytes it needs: [g0, g0 + len) of the source array.
+// A CTA's rows of one projection.
 struct GvSeg {
   int p, lr0, lr1;             // projection; CTA-local rows [lr0, lr1)
   int64_t ra;                  // projection row of lr0
-  int64_t raw_g0, sig_g0;
-  uint32_t raw_off, sig_off, raw_len, sig_len;  // shared addresses and byte counts
 };
 // One row of a CTA's range, or a padding row of its last tile (dq == -1; it
 // points at the range's first row).
 struct GvRow {
   const uint8_t *code;         // the row's packed codes
-  uint32_t raw;                // shared address of the row's first block constant
-  uint32_t sig;                // shared address of the DQ scale of the row's first block
   int prow;                    // row within its projection
-  short e0;                    // (first block of the row) mod 256: its place in its DQ group
   signed char p;               // projection
   signed char dq;              // 1: DQ constants, 0: fp32 constants, -1: padding row
 };
 struct GvMeta {
   GvSeg seg[kGvMaxGroup];
   GvProj p[kGvMaxGroup];
-  float mu[kGvMaxGroup];
   int nseg;
 };
+constexpr int kGvDecRows = 4;  // rows whose block constants a thread loads at once
 
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -151,6 +144,16 @@ __device__ __forceinline__ float ld_cg_f32(const float *p) {
   float v;
   asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
   return v;
+}
+__device__ __forceinline__ uint32_t ld_cg_u32(const void *p) {
+  uint32_t v;
+  asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_cg_s8(const void *p) {  // sign-extended
+  int v;
+  asm volatile("ld.global.cg.s8 %0, [%1];" : "=r"(v) : "l"(p));
+  return static_cast<uint32_t>(v);
 }
 __device__ __forceinline__ uint32_t ld_cg_u16(const uint16_t *p) {
   unsigned short v;
@@ -232,7 +235,7 @@ __device__ __forceinline__ uint32_t gv_x_chunk(uint32_t c, uint32_t t) {
 // Layout of one launch (host side): the stage ring gets what the rest
 // leaves of the shared memory, 2..kGvMaxRing slots.  False if the group does
 // not fit.
-inline bool gv_plan(GvGroup &g, int grid, int esz_max, bool any_dq) {
+inline bool gv_plan(GvGroup &g, int grid) {
   const int64_t k = g.k, nb = k >> 6;
   const int64_t rows_cta = qn_ceil_div(g.rows, grid);
   const int64_t ntl = qn_ceil_div(rows_cta, 16);
@@ -245,10 +248,6 @@ inline bool gv_plan(GvGroup &g, int grid, int esz_max, bool any_dq) {
   auto a16 = [](int64_t v) { return (v + 15) & ~int64_t{15}; };
   g.ms = static_cast<int>(nb | 1);
   int64_t off = kGvLutBytes + a16(sizeof(GvGroup));  // the table, then a copy of this block
-  g.off_raw = static_cast<uint32_t>(off);
-  off += a16(rows_cta * nb * esz_max + 32 * n);
-  g.off_sig = static_cast<uint32_t>(off);
-  off += any_dq ? a16((rows_cta * nb / 256 + 2 + 8) * 4 * n) : 0;
   g.off_rows = static_cast<uint32_t>(off);
   off += a16(ntl * 16 * static_cast<int64_t>(sizeof(GvRow)));
   g.off_m = static_cast<uint32_t>(off);
@@ -278,16 +277,6 @@ inline bool gv_plan(GvGroup &g, int grid, int esz_max, bool any_dq) {
 // g = 0..3 (and 4..7) by the four lanes of each group cover all 32 banks once
 // per half-warp: conflict-free.
 
-// Copies [g0, g0 + len) of an array of `size` bytes to shared memory (16-byte
-// pieces, the piece that crosses the end of the array zero-filled).
-__device__ __forceinline__ void gv_copy(uint32_t dst, const void *base, int64_t g0, uint32_t len, int64_t size) {
-  const char *src = static_cast<const char *>(base) + g0;
-  const int64_t avail = size - g0;
-  for (uint32_t c = threadIdx.x * 16u; c < len; c += kGvWarps * 32 * 16u) {  // consumer threads
-    const int64_t left = avail - c;
-    cp_async16_zfill(dst + c, src + c, static_cast<uint32_t>(left < 16 ? left : 16));
-  }
-}
 // Bulk L2 prefetch of [g0, g0 + len) of an array of `size` bytes (g0 and len
 // multiples of 16; the range is cut at the last whole 16 bytes of the array).
 __device__ __forceinline__ void gv_prefetch(const void *base, int64_t g0, int64_t len, int64_t size) {
@@ -364,42 +353,18 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
     GvSeg s;
     s.p = pj;
     s.lr0 = s.lr1 = 0x7fffffff;  // no rows in this CTA
-    s.ra = s.raw_g0 = s.sig_g0 = 0;
-    s.raw_len = s.sig_len = 0;
+    s.ra = 0;
     int64_t a = 0, e = 0;
     if (pj < g.n) {
       mt.p[pj] = p;
       a = R0 > p.row_off ? R0 : p.row_off;
       e = R1 < p.row_off + p.d ? R1 : p.row_off + p.d;
     }
-    const bool has = a < e;
-    if (has) {
+    if (a < e) {
       s.lr0 = static_cast<int>(a - R0);
       s.lr1 = static_cast<int>(e - R0);
       s.ra = a - p.row_off;
-      const int64_t nr = e - a;
-      const int esz = p.dq ? 1 : 4;
-      const int64_t b0 = s.ra * nb * esz, b1 = (s.ra + nr) * nb * esz;
-      s.raw_g0 = b0 & ~int64_t{15};
-      s.raw_len = static_cast<uint32_t>(((b1 + 15) & ~int64_t{15}) - s.raw_g0);
-      if (p.dq) {  // DQ group scales: floats [f0, f1]
-        const int64_t f0 = (s.ra * nb) >> 8, f1 = ((s.ra + nr) * nb - 1) >> 8;
-        s.sig_g0 = (f0 * 4) & ~int64_t{15};
-        s.sig_len = static_cast<uint32_t>((((f1 + 1) * 4 + 15) & ~int64_t{15}) - s.sig_g0);
-      }
     }
-    // shared-memory places of the copies: exclusive prefix sums over projections
-    uint32_t rx = 0, sx = 0;
-#pragma unroll
-    for (int j = 0; j < kGvMaxGroup; ++j) {
-      const uint32_t rl = __shfl_sync(0xffu, s.raw_len, j), sl = __shfl_sync(0xffu, s.sig_len, j);
-      if (j < pj) {
-        rx += rl;
-        sx += sl;
-      }
-    }
-    s.raw_off = sb + g.off_raw + rx;
-    s.sig_off = sb + g.off_sig + sx;
     mt.seg[pj] = s;
     if (pj == 0) mt.nseg = g.n;
   }
@@ -450,15 +415,11 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
     const GvSeg &s = mt.seg[si];
     const GvProj &p = mt.p[s.p];
     const int prow = static_cast<int>(s.ra) + (lq - s.lr0);
-    const int64_t e0 = static_cast<int64_t>(prow) * nb;  // first block of the row
     GvRow rw;
     rw.code = p.codes + prow * kh;
     rw.prow = prow;
     rw.p = static_cast<signed char>(s.p);
     rw.dq = pad ? static_cast<signed char>(-1) : static_cast<signed char>(p.dq);
-    rw.e0 = static_cast<short>(e0 & 255);
-    rw.raw = s.raw_off + static_cast<uint32_t>(e0 * (p.dq ? 1 : 4) - s.raw_g0);
-    rw.sig = p.dq ? s.sig_off + static_cast<uint32_t>((e0 >> 8) * 4 - s.sig_g0) : 0u;
     rows[lr] = rw;
   }
   __syncthreads();
@@ -547,17 +508,10 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
     }
   } else {
   // ================================ consumers ===================================
-  // small copies: X (swizzled into the table rows), block constants, DQ scales
+  // X into the odd halves of the table rows (swizzled by token)
   for (int t = 0; t < M; ++t)
     for (uint32_t v = tid; v < kc; v += kGvWarps * 32)
       cp_async16(sb + gv_x_chunk(t * kc + v, t), g.X + static_cast<int64_t>(t) * k + v * 8);
-  for (int i = 0; i < mt.nseg; ++i) {
-    const GvSeg &s = mt.seg[i];
-    if (s.lr0 >= s.lr1) continue;
-    const GvProj &p = mt.p[s.p];
-    gv_copy(s.raw_off, p.consts, s.raw_g0, s.raw_len, p.d * nb * (p.dq ? 1 : 4));
-    if (p.dq) gv_copy(s.sig_off, p.absmax_scale, s.sig_g0, s.sig_len, ((p.d * nb + 255) >> 8) * 4);
-  }
   cp_async_commit();
   asm volatile("bar.arrive 2, %0;" ::"n"((kGvWarps + 1) * 32) : "memory");  // the stage copies may start
   // adapter rows of this CTA: warp slice [v0, v1) of the k / 8 vectors
@@ -577,53 +531,83 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
   };
   if (nu > 0) load_a(av0, 0, 0);
   if (nu > 1) load_a(av1, 1, 0);
-  if (tid < g.n) mt.mu[tid] = mt.p[tid].dq ? ld_cg_f32(mt.p[tid].absmax_mean) : 0.f;
-  cp_async_wait_all();  // the small copies
-  asm volatile("bar.sync 1, %0;" ::"n"(kGvWarps * 32) : "memory");
-  // block constants of the range, decoded once into mconst[lr * ms + b], one
-  // item per consumer thread in turn: when nb is a multiple of 4, item (row
-  // lr, c) is blocks 4c .. 4c + 3 of the row (one 32-bit read of DQ codes: a
-  // row starts at a multiple of 4 blocks, so the four share one 256-block DQ
-  // group; or one 16-byte read of fp32 constants), else item (lr, b) is
-  // block b.
+  // Block constants of the range, decoded once into mconst[lr * ms + b]
+  // straight from global memory (through L2): thread (r0, c) takes item c of
+  // rows r0, r0 + rpp, ..., loading kGvDecRows rows' inputs before it decodes
+  // any.  When nb is a multiple of 4, item c is blocks 4c .. 4c + 3 (one
+  // 32-bit read of DQ codes: a row starts at a multiple of 4 blocks, so the
+  // four share one 256-block DQ group; or one 16-byte read of fp32
+  // constants), else item c is block c.  k <= 16384, so a row has at most
+  // 256 items and rpp >= 2.
   {
     const bool by4 = (nb & 3) == 0;
-    const int per = by4 ? nb >> 2 : nb;  // items per row
-    const int items = ntl * 16 * per;
-    for (int it = tid; it < items; it += kGvWarps * 32) {
-      const int lr = it / per, c = it - lr * per;
-      const GvRow rw = rows[lr];
-      float *mr = mconst + lr * g.ms;
-      if (by4) {
-        float m[4] = {0.f, 0.f, 0.f, 0.f};
-        if (rw.dq > 0) {
-          const uint32_t wq = *reinterpret_cast<const uint32_t *>(base + (rw.raw - kGvSmemBase) + 4 * c);
-          const float sg = *reinterpret_cast<const float *>(base + (rw.sig - kGvSmemBase) + ((rw.e0 + 4 * c) >> 8) * 4);
-          const float mu = mt.mu[rw.p];
+    const int per = by4 ? nb >> 2 : nb;          // items per row
+    const int rpp = (kGvWarps * 32) / per;       // rows per pass
+    const int c = tid % per, r0 = tid / per;
+    const int nrt = ntl * 16, ms = g.ms;
+    const int64_t eb = by4 ? 4 * c : c;          // first block of the item within its row
+    for (int lb = r0; r0 < rpp && lb < nrt; lb += kGvDecRows * rpp) {
+      uint4 v[kGvDecRows];
+      float sgv[kGvDecRows], muv[kGvDecRows];
+      int dqv[kGvDecRows];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) m[j] = dq_absmax(static_cast<int8_t>((wq >> (8 * j)) & 0xFFu), sg, mu);
-        } else if (rw.dq == 0) {
-          const uint4 wf = *reinterpret_cast<const uint4 *>(base + (rw.raw - kGvSmemBase) + 16 * c);
-          m[0] = __uint_as_float(wf.x);
-          m[1] = __uint_as_float(wf.y);
-          m[2] = __uint_as_float(wf.z);
-          m[3] = __uint_as_float(wf.w);
+      for (int i = 0; i < kGvDecRows; ++i) {
+        const int lr = lb + i * rpp;
+        dqv[i] = -1;
+        v[i] = make_uint4(0u, 0u, 0u, 0u);
+        sgv[i] = muv[i] = 0.f;
+        if (lr < nrt) {
+          const GvRow rw = rows[lr];
+          dqv[i] = rw.dq;
+          if (rw.dq >= 0) {
+            const GvProj &p = mt.p[rw.p];
+            const int64_t e = static_cast<int64_t>(rw.prow) * nb + eb;  // the item's first block
+            if (rw.dq > 0) {
+              const int8_t *q = static_cast<const int8_t *>(p.consts) + e;
+              v[i].x = by4 ? ld_cg_u32(q) : ld_cg_s8(q);
+              sgv[i] = ld_cg_f32(p.absmax_scale + (e >> 8));
+              muv[i] = ld_cg_f32(p.absmax_mean);
+            } else {
+              const float *f = static_cast<const float *>(p.consts) + e;
+              if (by4)
+                v[i] = ld_cg_v4(f);
+              else
+                v[i].x = __float_as_uint(ld_cg_f32(f));
+            }
+          }
         }
+      }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) mr[4 * c + j] = m[j];
-      } else {
-        float m = 0.f;
-        if (rw.dq > 0) {
-          const int8_t q = *reinterpret_cast<const int8_t *>(base + (rw.raw - kGvSmemBase) + c);
-          const float sg = *reinterpret_cast<const float *>(base + (rw.sig - kGvSmemBase) + ((rw.e0 + c) >> 8) * 4);
-          m = dq_absmax(q, sg, mt.mu[rw.p]);
-        } else if (rw.dq == 0) {
-          m = *reinterpret_cast<const float *>(base + (rw.raw - kGvSmemBase) + c * 4);
+      for (int i = 0; i < kGvDecRows; ++i) {
+        const int lr = lb + i * rpp;
+        if (lr >= nrt) break;
+        float *mr = mconst + lr * ms;
+        if (by4) {
+          float m[4] = {0.f, 0.f, 0.f, 0.f};
+          if (dqv[i] > 0) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) m[j] = dq_absmax(static_cast<int8_t>((v[i].x >> (8 * j)) & 0xFFu), sgv[i], muv[i]);
+          } else if (dqv[i] == 0) {
+            m[0] = __uint_as_float(v[i].x);
+            m[1] = __uint_as_float(v[i].y);
+            m[2] = __uint_as_float(v[i].z);
+            m[3] = __uint_as_float(v[i].w);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mr[4 * c + j] = m[j];
+        } else {
+          float m = 0.f;
+          if (dqv[i] > 0)
+            m = dq_absmax(static_cast<int8_t>(v[i].x & 0xFFu), sgv[i], muv[i]);
+          else if (dqv[i] == 0)
+            m = __uint_as_float(v[i].x);
+          mr[c] = m;
         }
-        mr[c] = m;
       }
     }
   }
+  cp_async_wait_all();  // X
+  asm volatile("bar.sync 1, %0;" ::"n"(kGvWarps * 32) : "memory");
 
   {
     const int span = v1 - v0;
