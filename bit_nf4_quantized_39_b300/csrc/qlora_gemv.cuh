@@ -94,7 +94,7 @@ struct GvGroup {  // the kernel's parameter block (copied to shared memory at en
   float *u;                    // M x rtot fp32 (workspace)
   unsigned int *zero_area;     // ready and exit counters, zero between calls
   // shared-memory layout: byte offsets from the start of dynamic shared memory (gv_plan)
-  uint32_t off_ring, off_rows, off_m, off_part, off_us, off_ured, off_meta, off_bar, smem;
+  uint32_t off_ring, off_rows, off_m, off_part, off_us, off_ured, off_bar, smem;
   int rows_cta;                // largest row range of a CTA
   int ring;                    // stage slots
   int ms;                      // row stride (floats, odd) of the decoded block constants
@@ -104,11 +104,6 @@ struct GvGroup {  // the kernel's parameter block (copied to shared memory at en
 
 static_assert(sizeof(GvGroup) % 8 == 0, "parameter block copied in 8-byte pieces");
 
-// A CTA's rows of one projection.
-struct GvSeg {
-  int p, lr0, lr1;             // projection; CTA-local rows [lr0, lr1)
-  int64_t ra;                  // projection row of lr0
-};
 // One row of a CTA's range, or a padding row of its last tile (dq == -1; it
 // points at the range's first row).
 struct GvRow {
@@ -116,11 +111,6 @@ struct GvRow {
   int prow;                    // row within its projection
   signed char p;               // projection
   signed char dq;              // 1: DQ constants, 0: fp32 constants, -1: padding row
-};
-struct GvMeta {
-  GvSeg seg[kGvMaxGroup];
-  GvProj p[kGvMaxGroup];
-  int nseg;
 };
 constexpr int kGvDecRows = 4;  // rows whose block constants a thread loads at once
 
@@ -258,8 +248,6 @@ inline bool gv_plan(GvGroup &g, int grid) {
   off += a16(g.rtot * M * 4);
   g.off_ured = static_cast<uint32_t>(off);
   off += a16(static_cast<int64_t>(kGvMaxURows) * kGvWarps * M * 4);
-  g.off_meta = static_cast<uint32_t>(off);
-  off += a16(sizeof(GvMeta));
   g.off_bar = static_cast<uint32_t>(off);
   off += a16(2 * kGvMaxRing * 8 + 16);
   off = (off + 1023) & ~int64_t{1023};
@@ -303,27 +291,46 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
   }
   unsigned char *base = gv_raw;
   const uint32_t sb = kGvSmemBase;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint64_t *full = reinterpret_cast<uint64_t *>(base + gp.off_bar);  // [kGvMaxRing]: a stage has landed
+  uint64_t *empty = full + kGvMaxRing;                                // [kGvMaxRing]: every warp is done with it
+  uint64_t *upart = empty + kGvMaxRing;                               // the consumers' parts of u are written
+  volatile int *abort = reinterpret_cast<volatile int *>(upart + 1);
   {
     // The parameter block into shared memory: one parallel read instead of a
-    // chain of constant-cache misses over its ~900 bytes.
+    // chain of constant-cache misses over its ~900 bytes.  The level table and
+    // the barriers need none of it and are set up meanwhile.
     const uint2 *src = reinterpret_cast<const uint2 *>(&gp);
     uint2 *dst = reinterpret_cast<uint2 *>(base + kGvLutBytes);
-    for (int i = threadIdx.x; i < static_cast<int>(sizeof(GvGroup) / 8); i += kGvThreads) dst[i] = src[i];
+    for (int i = tid; i < static_cast<int>(sizeof(GvGroup) / 8); i += kGvThreads) dst[i] = src[i];
+  }
+  if (tid < 256) {
+    // table entry b: bf16(level[b & 15]) | bf16(level[b >> 4]) << 16, written by
+    // thread b into all 32 lane slots of row b (16-byte stores in a rotated
+    // order, so that eight neighbouring threads hit different banks)
+    const uint32_t lv = gp.lev16[lane & 15];
+    const uint32_t v = __shfl_sync(0xffffffffu, lv, tid & 15) | (__shfl_sync(0xffffffffu, lv, tid >> 4) << 16);
+    const uint4 v4 = make_uint4(v, v, v, v);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4 *>(base + tid * 256 + 16 * ((q + tid) & 7)) = v4;
+  }
+  if (warp == 9 && lane == 0) {
+    for (int i = 0; i < kGvMaxRing; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), kGvWarps);
+    }
+    mbar_init(smem_u32(upart), 1);
+    *abort = 0;
+    mbar_fence_init();
   }
   __syncthreads();
   const GvGroup &g = *reinterpret_cast<const GvGroup *>(base + kGvLutBytes);
-  GvMeta &mt = *reinterpret_cast<GvMeta *>(base + g.off_meta);
   GvRow *rows = reinterpret_cast<GvRow *>(base + g.off_rows);
   float *part = reinterpret_cast<float *>(base + g.off_part);
   float *mconst = reinterpret_cast<float *>(base + g.off_m);
-  uint64_t *full = reinterpret_cast<uint64_t *>(base + g.off_bar);  // [kGvMaxRing]: a stage has landed
-  uint64_t *empty = full + kGvMaxRing;                               // [kGvMaxRing]: every warp is done with it
-  uint64_t *upart = empty + kGvMaxRing;                              // the consumers' parts of u are written
-  volatile int *abort = reinterpret_cast<volatile int *>(upart + 1);
   float *us = reinterpret_cast<float *>(base + g.off_us);
   float *ured = reinterpret_cast<float *>(base + g.off_ured);
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
   const int64_t k = g.k, kh = k >> 1;
   const int nb = static_cast<int>(k >> 6);
@@ -345,80 +352,38 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
   const int64_t rtot = g.rtot;
   const int nu = static_cast<int>((rtot - blockIdx.x + G - 1) / G);  // adapter rows of this CTA (j = blockIdx + G i)
 
-  // ---- before the wait: projections and segments (thread i: projection i),
-  // L2 prefetch, level table, row table --------------------------------------------
-  if (warp == 8 && lane < kGvMaxGroup) {
-    const int pj = lane;  // projection
-    const GvProj p = g.p[pj];
-    GvSeg s;
-    s.p = pj;
-    s.lr0 = s.lr1 = 0x7fffffff;  // no rows in this CTA
-    s.ra = 0;
-    int64_t a = 0, e = 0;
-    if (pj < g.n) {
-      mt.p[pj] = p;
-      a = R0 > p.row_off ? R0 : p.row_off;
-      e = R1 < p.row_off + p.d ? R1 : p.row_off + p.d;
-    }
-    if (a < e) {
-      s.lr0 = static_cast<int>(a - R0);
-      s.lr1 = static_cast<int>(e - R0);
-      s.ra = a - p.row_off;
-    }
-    mt.seg[pj] = s;
-    if (pj == 0) mt.nseg = g.n;
-  }
-  if (warp == 9 && lane == 0) {
-    for (int i = 0; i < kGvMaxRing; ++i) {
-      mbar_init(smem_u32(&full[i]), 1);
-      mbar_init(smem_u32(&empty[i]), kGvWarps);
-    }
-    mbar_init(smem_u32(upart), 1);
-    *abort = 0;
-    mbar_fence_init();
-  }
-  if (tid < 256) {
-    // table entry b: bf16(level[b & 15]) | bf16(level[b >> 4]) << 16, written by
-    // thread b into all 32 lane slots of row b (16-byte stores in a rotated
-    // order, so that eight neighbouring threads hit different banks)
-    const uint32_t lv = g.lev16[lane & 15];
-    const uint32_t v = __shfl_sync(0xffffffffu, lv, tid & 15) | (__shfl_sync(0xffffffffu, lv, tid >> 4) << 16);
-    const uint4 v4 = make_uint4(v, v, v, v);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4 *>(base + tid * 256 + 16 * ((q + tid) & 7)) = v4;
-  }
-  __syncthreads();
+  // ---- before the wait: row table, L2 prefetch of A and B -----------------------------
   if (tid >= 32 && tid < 32 + nu) {  // A rows of this CTA's adapter rows into L2
     const int64_t j = blockIdx.x + static_cast<int64_t>(G) * (tid - 32);
     int pi = 0;
-    for (int i = 1; i < mt.nseg; ++i)
-      if (j >= mt.p[i].u_off) pi = i;
-    gv_prefetch(mt.p[pi].A, (j - mt.p[pi].u_off) * k * 2, k * 2, static_cast<int64_t>(mt.p[pi].r) * k * 2);
+    for (int i = 1; i < g.n; ++i)
+      if (j >= g.p[i].u_off) pi = i;
+    gv_prefetch(g.p[pi].A, (j - g.p[pi].u_off) * k * 2, k * 2, static_cast<int64_t>(g.p[pi].r) * k * 2);
   }
-  if (tid >= 64 && tid < 64 + mt.nseg) {  // B rows of this CTA's rows into L2 (read by the output phase)
-    const GvSeg &sg = mt.seg[tid - 64];
-    if (sg.lr0 < sg.lr1) {
-      const GvProj &p = mt.p[sg.p];
-      const int64_t b0 = sg.ra * p.r * 2, b1 = (sg.ra + (sg.lr1 - sg.lr0)) * p.r * 2;
+  if (tid >= 64 && tid < 64 + g.n) {  // B rows of this CTA's rows into L2 (read by the output phase)
+    const GvProj &p = g.p[tid - 64];
+    const int64_t a = R0 > p.row_off ? R0 : p.row_off, e = R1 < p.row_off + p.d ? R1 : p.row_off + p.d;
+    if (a < e) {
+      const int64_t b0 = (a - p.row_off) * p.r * 2, b1 = (e - p.row_off) * p.r * 2;
       const int64_t a0 = b0 & ~int64_t{15};  // 16-byte aligned start and length
       gv_prefetch(p.B, a0, ((b1 + 15) & ~int64_t{15}) - a0, p.d * p.r * 2);
     }
   }
   for (int lr = tid; lr < ntl * 16; lr += kGvThreads) {
-    // padding rows of the last tile read the first row's codes (their block
-    // constants are 0)
+    // a padding row of the last tile points at the range's first row (its
+    // codes are not copied and its block constants are 0)
     const bool pad = lr >= nrows;
-    const int lq = pad ? 0 : lr;
-    int si = 0;
-    for (int i = 0; i < mt.nseg; ++i)
-      if (lq >= mt.seg[i].lr0 && lq < mt.seg[i].lr1) si = i;
-    const GvSeg &s = mt.seg[si];
-    const GvProj &p = mt.p[s.p];
-    const int prow = static_cast<int>(s.ra) + (lq - s.lr0);
+    const int64_t R = R0 + (pad ? 0 : lr);
+    int pi = 0;
+#pragma unroll
+    for (int i = 1; i < kGvMaxGroup; ++i)
+      if (i < g.n && R >= g.p[i].row_off) pi = i;
+    const GvProj &p = g.p[pi];
+    const int prow = static_cast<int>(R - p.row_off);
     GvRow rw;
     rw.code = p.codes + prow * kh;
     rw.prow = prow;
-    rw.p = static_cast<signed char>(s.p);
+    rw.p = static_cast<signed char>(pi);
     rw.dq = pad ? static_cast<signed char>(-1) : static_cast<signed char>(p.dq);
     rows[lr] = rw;
   }
@@ -443,10 +408,10 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
           const int64_t j = blockIdx.x + static_cast<int64_t>(G) * iu;
           int pi = 0;
           for (int i = 1; i < g.n; ++i)
-            if (j >= mt.p[i].u_off) pi = i;
+            if (j >= g.p[i].u_off) pi = i;
           float v = 0.f;
           for (int w = 0; w < kGvWarps; ++w) v += ured[(iu * kGvWarps + w) * M + t];
-          g.u[t * rtot + j] = mt.p[pi].s * v;
+          g.u[t * rtot + j] = g.p[pi].s * v;
         }
         __syncwarp();
         if (lane == 0) {
@@ -521,8 +486,8 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
     const int64_t j = blockIdx.x + static_cast<int64_t>(G) * iu;
     int pi = 0;
     for (int i = 1; i < g.n; ++i)
-      if (j >= mt.p[i].u_off) pi = i;
-    const uint16_t *arow = mt.p[pi].A + (j - mt.p[pi].u_off) * k;
+      if (j >= g.p[i].u_off) pi = i;
+    const uint16_t *arow = g.p[pi].A + (j - g.p[pi].u_off) * k;
 #pragma unroll
     for (int i = 0; i < kGvUVec; ++i) {
       const int v = v0 + lane + 32 * (bt * kGvUVec + i);
@@ -560,7 +525,7 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
           const GvRow rw = rows[lr];
           dqv[i] = rw.dq;
           if (rw.dq >= 0) {
-            const GvProj &p = mt.p[rw.p];
+            const GvProj &p = g.p[rw.p];
             const int64_t e = static_cast<int64_t>(rw.prow) * nb + eb;  // the item's first block
             if (rw.dq > 0) {
               const int8_t *q = static_cast<const int8_t *>(p.consts) + e;
@@ -762,7 +727,7 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
   uint4 bq[8];
   if (bvec && tid < nrows) {
     const GvRow &rw = rows[tid];
-    const GvProj &p = mt.p[rw.p];
+    const GvProj &p = g.p[rw.p];
     const uint16_t *br = p.B + static_cast<int64_t>(rw.prow) * p.r;
 #pragma unroll
     for (int c = 0; c < 8; ++c) bq[c] = (8 * c < p.r) ? ld_cg_v4(br + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
@@ -771,7 +736,7 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
   // Y = (partial sums of the warps, in warp order) + u . B[row]
   for (int lr = tid; lr < nrows; lr += kGvThreads) {
     const GvRow &rw = rows[lr];
-    const GvProj &p = mt.p[rw.p];
+    const GvProj &p = g.p[rw.p];
     const uint16_t *br = p.B + static_cast<int64_t>(rw.prow) * p.r;
     const float *ur = us + p.u_off;
     float a[MT][2];
@@ -789,12 +754,17 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
           if (q0 + 8 * c >= p.r) break;
           const uint32_t bw[4] = {bq[c].x, bq[c].y, bq[c].z, bq[c].w};
 #pragma unroll
-          for (int h = 0; h < 8; ++h) {
-            const float b = (h & 1) ? __uint_as_float(bw[h >> 1] & 0xFFFF0000u) : __uint_as_float(bw[h >> 1] << 16);
-            const int q = q0 + 8 * c + h;
+          for (int t = 0; t < MT; ++t) {
+            if (t >= M) break;
+            // u[t, q0 + 8c ..] in two 16-byte reads (every r and u_off is a multiple of 8)
+            const float4 ua = *reinterpret_cast<const float4 *>(ur + t * rtot + q0 + 8 * c);
+            const float4 ub = *reinterpret_cast<const float4 *>(ur + t * rtot + q0 + 8 * c + 4);
+            const float uv[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
 #pragma unroll
-            for (int t = 0; t < MT; ++t)
-              if (t < M) a[t][h & 1] = fmaf(ur[t * rtot + q], b, a[t][h & 1]);
+            for (int h = 0; h < 8; ++h) {
+              const float b = (h & 1) ? __uint_as_float(bw[h >> 1] & 0xFFFF0000u) : __uint_as_float(bw[h >> 1] << 16);
+              a[t][h & 1] = fmaf(uv[h], b, a[t][h & 1]);
+            }
           }
         }
       } else {
