@@ -38,7 +38,7 @@
 //
 // Programmatic dependent launch: the kernel lets the next call launch at
 // entry; before griddepcontrol.wait a CTA only builds its tables and
-// prefetches its A and B rows into L2 (a prefetch cannot return stale data).
+// prefetches its A rows into L2 (a prefetch cannot return stale data).
 // Everything a kernel may have written -- codes, constants, X, A, B, u, Y,
 // the counters -- is read after the wait, through L2 (ld.global.cg,
 // cp.async.cg, bulk copies).  Every CTA of the grid is resident at once (one
@@ -112,7 +112,7 @@ struct GvRow {
   signed char p;               // projection
   signed char dq;              // 1: DQ constants, 0: fp32 constants, -1: padding row
 };
-constexpr int kGvDecRows = 4;  // rows whose block constants a thread loads at once
+constexpr int kGvDecRows = 6;  // rows whose block constants a thread loads at once
 
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -352,22 +352,13 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
   const int64_t rtot = g.rtot;
   const int nu = static_cast<int>((rtot - blockIdx.x + G - 1) / G);  // adapter rows of this CTA (j = blockIdx + G i)
 
-  // ---- before the wait: row table, L2 prefetch of A and B -----------------------------
+  // ---- before the wait: row table, L2 prefetch of A ------------------------------------
   if (tid >= 32 && tid < 32 + nu) {  // A rows of this CTA's adapter rows into L2
     const int64_t j = blockIdx.x + static_cast<int64_t>(G) * (tid - 32);
     int pi = 0;
     for (int i = 1; i < g.n; ++i)
       if (j >= g.p[i].u_off) pi = i;
     gv_prefetch(g.p[pi].A, (j - g.p[pi].u_off) * k * 2, k * 2, static_cast<int64_t>(g.p[pi].r) * k * 2);
-  }
-  if (tid >= 64 && tid < 64 + g.n) {  // B rows of this CTA's rows into L2 (read by the output phase)
-    const GvProj &p = g.p[tid - 64];
-    const int64_t a = R0 > p.row_off ? R0 : p.row_off, e = R1 < p.row_off + p.d ? R1 : p.row_off + p.d;
-    if (a < e) {
-      const int64_t b0 = (a - p.row_off) * p.r * 2, b1 = (e - p.row_off) * p.r * 2;
-      const int64_t a0 = b0 & ~int64_t{15};  // 16-byte aligned start and length
-      gv_prefetch(p.B, a0, ((b1 + 15) & ~int64_t{15}) - a0, p.d * p.r * 2);
-    }
   }
   for (int lr = tid; lr < ntl * 16; lr += kGvThreads) {
     // a padding row of the last tile points at the range's first row (its
@@ -451,6 +442,17 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
           if (lane < 16 && 16 * tl + lane < nrows) rowp = rows[16 * tl + lane].code;
         }
       }
+      // The CTA's rows of B into L2 for the output phase, a few stages before
+      // the end (an earlier prefetch would be evicted by the stream of codes).
+      if (lane < g.n) {
+        const GvProj &p = g.p[lane];
+        const int64_t a = R0 > p.row_off ? R0 : p.row_off, e = R1 < p.row_off + p.d ? R1 : p.row_off + p.d;
+        if (a < e) {
+          const int64_t b0 = (a - p.row_off) * p.r * 2, b1 = (e - p.row_off) * p.r * 2;
+          const int64_t a0 = b0 & ~int64_t{15};  // 16-byte aligned start and length
+          gv_prefetch(p.B, a0, ((b1 + 15) & ~int64_t{15}) - a0, p.d * p.r * 2);
+        }
+      }
       if (lane == 0) {
         // After an abort the copies still in flight target this CTA's shared
         // memory: wait (bounded) for the last one of every slot.
@@ -478,6 +480,82 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
     for (uint32_t v = tid; v < kc; v += kGvWarps * 32)
       cp_async16(sb + gv_x_chunk(t * kc + v, t), g.X + static_cast<int64_t>(t) * k + v * 8);
   cp_async_commit();
+  // Block constants of the range, decoded once into mconst[lr * ms + b]
+  // straight from global memory (through L2): thread (r0, c) takes item c of
+  // rows r0, r0 + rpp, ..., loading kGvDecRows rows' inputs before it decodes
+  // any; the first batch goes out before the stage copies.  When nb is a
+  // multiple of 4, item c is blocks 4c .. 4c + 3 (one 32-bit read of DQ
+  // codes: a row starts at a multiple of 4 blocks, so the four share one
+  // 256-block DQ group; or one 16-byte read of fp32 constants), else item c
+  // is block c.  k <= 16384, so a row has at most 256 items and rpp >= 2.
+  const bool by4 = (nb & 3) == 0;
+  const int dper = by4 ? nb >> 2 : nb;          // items per row
+  const int rpp = (kGvWarps * 32) / dper;       // rows per pass
+  const int dc = tid % dper, dr0 = tid / dper;
+  const int nrt = ntl * 16;
+  const int64_t eb = by4 ? 4 * dc : dc;         // first block of the item within its row
+  // per row: DQ {codes, scale, mean} or fp32 constants, in .x .. .w; dq flag
+  uint4 dv[kGvDecRows];
+  int dqv[kGvDecRows];
+  auto dec_load = [&](int lb) {
+#pragma unroll
+    for (int i = 0; i < kGvDecRows; ++i) {
+      const int lr = lb + i * rpp;
+      dqv[i] = -1;
+      dv[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (dr0 < rpp && lr < nrt) {
+        const GvRow rw = rows[lr];
+        dqv[i] = rw.dq;
+        if (rw.dq >= 0) {
+          const GvProj &p = g.p[rw.p];
+          const int64_t e = static_cast<int64_t>(rw.prow) * nb + eb;  // the item's first block
+          if (rw.dq > 0) {
+            const int8_t *q = static_cast<const int8_t *>(p.consts) + e;
+            dv[i].x = by4 ? ld_cg_u32(q) : ld_cg_s8(q);
+            dv[i].y = __float_as_uint(ld_cg_f32(p.absmax_scale + (e >> 8)));
+            dv[i].z = __float_as_uint(ld_cg_f32(p.absmax_mean));
+          } else {
+            const float *f = static_cast<const float *>(p.consts) + e;
+            if (by4)
+              dv[i] = ld_cg_v4(f);
+            else
+              dv[i].x = __float_as_uint(ld_cg_f32(f));
+          }
+        }
+      }
+    }
+  };
+  auto dec_store = [&](int lb) {
+#pragma unroll
+    for (int i = 0; i < kGvDecRows; ++i) {
+      const int lr = lb + i * rpp;
+      if (dr0 >= rpp || lr >= nrt) break;
+      float *mr = mconst + lr * g.ms;
+      const float sg = __uint_as_float(dv[i].y), mu = __uint_as_float(dv[i].z);
+      if (by4) {
+        float m[4] = {0.f, 0.f, 0.f, 0.f};
+        if (dqv[i] > 0) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) m[j] = dq_absmax(static_cast<int8_t>((dv[i].x >> (8 * j)) & 0xFFu), sg, mu);
+        } else if (dqv[i] == 0) {
+          m[0] = __uint_as_float(dv[i].x);
+          m[1] = __uint_as_float(dv[i].y);
+          m[2] = __uint_as_float(dv[i].z);
+          m[3] = __uint_as_float(dv[i].w);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mr[4 * dc + j] = m[j];
+      } else {
+        float m = 0.f;
+        if (dqv[i] > 0)
+          m = dq_absmax(static_cast<int8_t>(dv[i].x & 0xFFu), sg, mu);
+        else if (dqv[i] == 0)
+          m = __uint_as_float(dv[i].x);
+        mr[dc] = m;
+      }
+    }
+  };
+  dec_load(dr0);
   asm volatile("bar.arrive 2, %0;" ::"n"((kGvWarps + 1) * 32) : "memory");  // the stage copies may start
   // adapter rows of this CTA: warp slice [v0, v1) of the k / 8 vectors
   const int v0 = static_cast<int>(kc * warp / kGvWarps), v1 = static_cast<int>(kc * (warp + 1) / kGvWarps);
@@ -496,80 +574,10 @@ qlora_gemv_kernel(const __grid_constant__ GvGroup gp) {
   };
   if (nu > 0) load_a(av0, 0, 0);
   if (nu > 1) load_a(av1, 1, 0);
-  // Block constants of the range, decoded once into mconst[lr * ms + b]
-  // straight from global memory (through L2): thread (r0, c) takes item c of
-  // rows r0, r0 + rpp, ..., loading kGvDecRows rows' inputs before it decodes
-  // any.  When nb is a multiple of 4, item c is blocks 4c .. 4c + 3 (one
-  // 32-bit read of DQ codes: a row starts at a multiple of 4 blocks, so the
-  // four share one 256-block DQ group; or one 16-byte read of fp32
-  // constants), else item c is block c.  k <= 16384, so a row has at most
-  // 256 items and rpp >= 2.
-  {
-    const bool by4 = (nb & 3) == 0;
-    const int per = by4 ? nb >> 2 : nb;          // items per row
-    const int rpp = (kGvWarps * 32) / per;       // rows per pass
-    const int c = tid % per, r0 = tid / per;
-    const int nrt = ntl * 16, ms = g.ms;
-    const int64_t eb = by4 ? 4 * c : c;          // first block of the item within its row
-    for (int lb = r0; r0 < rpp && lb < nrt; lb += kGvDecRows * rpp) {
-      uint4 v[kGvDecRows];
-      float sgv[kGvDecRows], muv[kGvDecRows];
-      int dqv[kGvDecRows];
-#pragma unroll
-      for (int i = 0; i < kGvDecRows; ++i) {
-        const int lr = lb + i * rpp;
-        dqv[i] = -1;
-        v[i] = make_uint4(0u, 0u, 0u, 0u);
-        sgv[i] = muv[i] = 0.f;
-        if (lr < nrt) {
-          const GvRow rw = rows[lr];
-          dqv[i] = rw.dq;
-          if (rw.dq >= 0) {
-            const GvProj &p = g.p[rw.p];
-            const int64_t e = static_cast<int64_t>(rw.prow) * nb + eb;  // the item's first block
-            if (rw.dq > 0) {
-              const int8_t *q = static_cast<const int8_t *>(p.consts) + e;
-              v[i].x = by4 ? ld_cg_u32(q) : ld_cg_s8(q);
-              sgv[i] = ld_cg_f32(p.absmax_scale + (e >> 8));
-              muv[i] = ld_cg_f32(p.absmax_mean);
-            } else {
-              const float *f = static_cast<const float *>(p.consts) + e;
-              if (by4)
-                v[i] = ld_cg_v4(f);
-              else
-                v[i].x = __float_as_uint(ld_cg_f32(f));
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kGvDecRows; ++i) {
-        const int lr = lb + i * rpp;
-        if (lr >= nrt) break;
-        float *mr = mconst + lr * ms;
-        if (by4) {
-          float m[4] = {0.f, 0.f, 0.f, 0.f};
-          if (dqv[i] > 0) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) m[j] = dq_absmax(static_cast<int8_t>((v[i].x >> (8 * j)) & 0xFFu), sgv[i], muv[i]);
-          } else if (dqv[i] == 0) {
-            m[0] = __uint_as_float(v[i].x);
-            m[1] = __uint_as_float(v[i].y);
-            m[2] = __uint_as_float(v[i].z);
-            m[3] = __uint_as_float(v[i].w);
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) mr[4 * c + j] = m[j];
-        } else {
-          float m = 0.f;
-          if (dqv[i] > 0)
-            m = dq_absmax(static_cast<int8_t>(v[i].x & 0xFFu), sgv[i], muv[i]);
-          else if (dqv[i] == 0)
-            m = __uint_as_float(v[i].x);
-          mr[c] = m;
-        }
-      }
-    }
+  dec_store(dr0);
+  for (int lb = dr0 + kGvDecRows * rpp; lb < nrt; lb += kGvDecRows * rpp) {
+    dec_load(lb);
+    dec_store(lb);
   }
   cp_async_wait_all();  // X
   asm volatile("bar.sync 1, %0;" ::"n"(kGvWarps * 32) : "memory");
