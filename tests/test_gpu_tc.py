@@ -65,6 +65,16 @@ def test_tc_forward_degenerate_terms(qn):
     assert layer.rel_fro(Y, ref) < TOL
 
 
+# W = 0 isolates the adapter term s (X A^T) B^T; ranks up to 16 take the
+# single-pass projection (one CTA per 16 tokens over all of K), including a
+# ragged last token block, K shorter than one 256-column stage, and odd ranks.
+@pytest.mark.parametrize("M,d,k,r", [(1000, 512, 1024, 16), (33, 128, 4096, 3), (129, 256, 64, 11)])
+def test_tc_forward_adapter_only(qn, M, d, k, r):
+    c = synth.layer_case(seed=M + d + k + r, d=d, k=k, M=M, r=r, alpha=2.0 * r)
+    Y, ref = _fwd(qn, np.zeros((d, k), np.float32), c["X"], c["A"], c["B"], c["alpha"])
+    assert layer.rel_fro(Y, ref) < TOL, (M, d, k, r)
+
+
 def _bwd(qn, W, dY, A, B, alpha, dq=True):
     q = qn.nf4_quantize(torch.from_numpy(W).cuda(), dq=dq)
     Wd = nf4.dequantize(nf4.quantize(W, 64, dq=dq)).reshape(W.shape)
