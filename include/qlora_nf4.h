@@ -247,7 +247,7 @@ qn_status qlora_linear_bwd_dx(const qn_nf4 *Q, const uint16_t *dY, int64_t M,
  *   A device fp32 [r x k], B device fp32 [d x r],
  *   resid host fp64[T+1]: resid[t] = ||W - deq(Q_t) - s B_t A_t||_F, with
  *   resid[0] the plain QLoRA residual ||W - deq(NF4(W))||_F.
- *   1 <= r, r + oversample <= 32, 0 <= T <= 64, d, k multiples of 64 and >= r + oversample.
+ *   1 <= r, r + oversample <= 96, 0 <= T <= 64, d, k multiples of 64 and >= r + oversample.
  *   Block size 64 and the DQ setting are taken from Q (Q->dq); the rank-r
  *   step is always the randomised one.
  */
