@@ -334,3 +334,38 @@ def test_small_m_adapter_term_on_its_own(qn, M):
         Y = qn.qlora_linear_fwd(q, X.cuda(), A, B, 16.0)
         qn.device_status()
         assert tile_max_rel(_f64(Y), ref, 16, 16) < TOL
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_few_token_exact_and_mixed_block_constants(qn, M):
+    """The M <= 8 kernel decodes the block constants straight from global
+    memory: fp32 absmax (dq = False) four blocks at a time when the number of
+    blocks per row is a multiple of 4 and one at a time otherwise, and a
+    grouped call whose projections mix fp32 and double-quantised constants."""
+    g = np.random.default_rng(90 + M)
+
+    def proj(d, k, dq, r):
+        W = (g.standard_normal((d, k)) * 0.02).astype(np.float32)
+        A = synth.to_bf16((g.standard_normal((r, k)) / np.sqrt(k)).astype(np.float32))
+        B = synth.to_bf16((g.standard_normal((d, r)) * 0.05).astype(np.float32))
+        q = qn.nf4_quantize(torch.from_numpy(W).cuda(), dq=dq)
+        Wd = nf4.dequantize(nf4.quantize(W, 64, dq=dq)).reshape(d, k)
+        return q, A, B, Wd
+
+    for d, k in ((300, 512), (200, 192)):  # 8 and 3 blocks per row
+        X = synth.to_bf16(g.standard_normal((M, k), dtype=np.float32))
+        q, A, B, Wd = proj(d, k, False, 8)
+        Y = qn.qlora_linear_fwd(q, X.cuda(), A.cuda(), B.cuda(), 16.0)
+        qn.device_status()
+        ref = layer.linear_fwd(_f64(X), Wd, _f64(A), _f64(B), 16.0, 8)
+        assert tile_max_rel(_f64(Y), ref, 16, 16) < TOL, (d, k)
+    k = 512
+    X = synth.to_bf16(g.standard_normal((M, k), dtype=np.float32))
+    parts = [proj(256, k, True, 16), proj(130, k, False, 8), proj(70, k, True, 4)]
+    Ys = qn.qlora_linear_fwd_group([p[0] for p in parts], X.cuda(), [p[1].cuda() for p in parts],
+                                   [p[2].cuda() for p in parts], [16.0] * 3)
+    qn.device_status()
+    for Y, (q, A, B, Wd) in zip(Ys, parts):
+        ref = layer.linear_fwd(_f64(X), Wd, _f64(A), _f64(B), 16.0, A.shape[0])
+        assert tile_max_rel(_f64(Y), ref, 16, 16) < TOL
+
