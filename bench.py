@@ -54,7 +54,7 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
 # regex:qlora_gemv -s 4 -c 4 python bench.py --profile decode`).  They hold
 # for the kernel source they were taken on (its sha256); for any other source
 # the bench reports traffic as null.
-GEMV_TRAFFIC_SHA256 = "5378d45dacf4fd8b699e74224b1c8525ba02419c7b8907b9e3afc437668fdf4e"
+GEMV_TRAFFIC_SHA256 = "27ae316811226d4aa612fe6ba3790093755e205b5cb5c181514abc29149d2729"
 GEMV_TRAFFIC = {"qkv": 29197056, "o": 9789696, "gate_up": 50473728 + 69120, "down": 25294080}
 
 

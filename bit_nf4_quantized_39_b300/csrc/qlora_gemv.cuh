@@ -125,11 +125,6 @@ __device__ __forceinline__ uint4 ld_cg_v4(const void *p) {
   asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
 }
-__device__ __forceinline__ uint2 ld_cg_v2(const void *p) {
-  uint2 v;
-  asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
-}
 __device__ __forceinline__ float ld_cg_f32(const float *p) {
   float v;
   asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
@@ -155,10 +150,6 @@ __device__ __forceinline__ unsigned int gv_ld_acquire(const unsigned int *p) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-// 16-byte cp.async that reads `src_bytes` (1..16) and zero-fills the rest.
-__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void *src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
 __device__ __forceinline__ void gv_mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                        uint32_t b1) {
   asm volatile(
@@ -166,11 +157,6 @@ __device__ __forceinline__ void gv_mma(float (&d)[4], uint32_t a0, uint32_t a1, 
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
-  return v;
 }
 __device__ __forceinline__ uint2 lds_v2(uint32_t a) {
   uint2 v;
@@ -200,11 +186,6 @@ __device__ __forceinline__ uint32_t lds_lut(uint32_t off) {
 __device__ __forceinline__ float lds_f32(uint32_t a) {
   float v;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ float lds_f32_off32(uint32_t a) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1+32];" : "=f"(v) : "r"(a));
   return v;
 }
 // Table offset of byte `sel` of `w` for this lane: (byte << 8) | (lane << 2).
